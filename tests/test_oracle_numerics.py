@@ -1,0 +1,44 @@
+"""Pins for the oracle's bf16 rounding: hand cases from the IEEE layout and
+agreement with torch's float32 -> bfloat16 conversion (a library routine)."""
+import numpy as np
+import torch
+
+from oracle.numerics import Arith, round_bf16
+
+
+def f(bits):
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def test_hand_cases():
+    one = 1.0
+    ulp = 2.0 ** -7                       # bf16 spacing in [1, 2)
+    assert round_bf16(one)[()] == one
+    assert round_bf16(one + ulp / 2)[()] == one              # tie -> even (1.0)
+    assert round_bf16(one + 3 * ulp / 2)[()] == one + 2 * ulp  # tie -> even (1 + 2ulp)
+    assert round_bf16(one + ulp / 2 + 2.0 ** -20)[()] == one + ulp
+    assert round_bf16(-(one + ulp / 4))[()] == -one
+    assert np.isinf(round_bf16(f(0x7F7FFFFF))[()])           # rounds up past max bf16
+    assert np.isnan(round_bf16(np.float32(np.nan))[()])
+    assert round_bf16(np.float32(np.inf))[()] == np.inf
+
+
+def test_matches_torch_bfloat16():
+    g = np.random.default_rng(0)
+    x = np.concatenate([
+        g.standard_normal(200000).astype(np.float32) * 10.0,
+        # exact ties: low 16 bits = 0x8000 on finite values
+        ((g.standard_normal(20000).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000))
+         | np.uint32(0x8000)).view(np.float32),
+        np.float32([0.0, -0.0, 1e-40, -1e-40, 3.0e38]),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    got = round_bf16(x)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_arith_points():
+    a32 = Arith(np.float32, bf16_points=True)
+    assert a32.r(1.0 + 2.0 ** -9) == 1.0
+    a64 = Arith(np.float64)
+    assert a64.r(1.0 + 2.0 ** -30) == 1.0 + 2.0 ** -30
