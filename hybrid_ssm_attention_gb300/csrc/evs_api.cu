@@ -1,0 +1,784 @@
+// C ABI of libevs: model / state ownership, the verify sequence, CUDA-graph
+// capture, accept / commit entry points and the single-operator entry points.
+//
+// The verify sequence is the EvSpark block-verification forward pass
+// (preprint abstract, contribution (i); discussion post, "What we
+// implemented"): one pass over n = gamma'+1 tokens through every layer, each
+// mixer writing the state after every block position to its spare bank.
+// Commit (same passages: "sliced directly to the accepted boundary") flips
+// banks on the device; nothing is recomputed or copied.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "evs_internal.cuh"
+
+using namespace evs;
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<long long> g_launches{0};
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CUDA_TRY(x)                                                                                 \
+  do {                                                                                              \
+    cudaError_t e_ = (x);                                                                           \
+    if (e_ != cudaSuccess)                                                                          \
+      return fail(EVS_ERR_CUDA, "%s failed: %s (%s:%d)", #x, cudaGetErrorString(e_), __FILE__, __LINE__); \
+  } while (0)
+
+#define EVS_TRY(x)          \
+  do {                      \
+    int r_ = (x);           \
+    if (r_ != EVS_OK) return r_; \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int num_sms_current(int* out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev));
+  return EVS_OK;
+}
+
+struct LayerW {
+  int kind, param;
+  const void *w_in, *w_out, *w_gu, *w_down;
+  const float *taps, *lam, *res;
+  CUtensorMap m_in, m_out, m_gu, m_down;
+};
+
+struct LayerS {
+  float* ext[2];
+  float* st[2];
+  void* kc;
+  void* vc;
+};
+
+struct GraphEntry {
+  // key
+  int n, mode, top_k;
+  float T;
+  const void *tok, *logits, *p, *q, *u, *acc, *otok;
+  bool round;
+  // value
+  cudaGraphExec_t exec;
+  int kernels;
+  unsigned long long last_use;
+};
+
+}  // namespace
+
+void evs::count_launch(int k) { g_launches += k; }
+
+struct evs_model {
+  evs_config cfg;
+  std::vector<int> kind, param;
+  int num_sms;
+  bool tc;  // bf16 storage: tensor-core GEMMs
+  const void* embed;
+  const void* head;
+  CUtensorMap m_head;
+  std::vector<LayerW> L;
+  Partials p_in, p_out, p_gu, p_down, p_head;
+  bool has_attn;
+  int n_max;
+};
+
+struct evs_state {
+  evs_model* m;
+  long long ctx_max;
+  evs_book* book;
+  int host_pos;
+  bool host_pos_known;
+  int host_pending;
+  float* X;
+  void *xn, *g, *h;
+  float* ws[2];
+  void* attn_scratch;
+  AttnBufs ab;
+  std::vector<LayerS> S;
+  CUtensorMap m_xn, m_g, m_h;
+  bool use_graphs, pdl;
+  cudaStream_t cap;
+  std::vector<GraphEntry> graphs;
+  unsigned long long tick;
+  std::vector<void*> allocs;
+};
+
+namespace {
+
+size_t esize(int dtype) { return dtype == EVS_BF16 ? 2 : 4; }
+
+int dmalloc(evs_state* s, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(EVS_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  s->allocs.push_back(*p);
+  return EVS_OK;
+}
+
+// ------------------------------------------------------------------ verify sequence
+int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc) {
+  evs_model* m = s->m;
+  const evs_config& c = m->cfg;
+  const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
+  const float eps = c.norm_eps;
+  int wsi = 0;
+  auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const void* W, const CUtensorMap& xm,
+                  const void* X, int K, Partials* out) -> int {
+    Partials P = plan;
+    P.ws = s->ws[(wsi++) & 1];
+    if (m->tc)
+      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, &s->book->status));
+    else
+      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, n, P, K));
+    *out = P;
+    return EVS_OK;
+  };
+  CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, n, d, V, eps, s->X, s->xn, s->book));
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    const LayerW& w = m->L[i];
+    LayerS& st = s->S[i];
+    Partials P;
+    EVS_TRY(gemm(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, d, &P));
+    MixSrc src{&P, nullptr, 0};
+    if (w.kind == EVS_LAYER_FIR) {
+      CUDA_TRY(launch_fir(Lc, dt, src, d, n, w.param, w.taps, st.ext[0], st.ext[1], s->book, s->g));
+    } else if (w.kind == EVS_LAYER_IIR) {
+      CUDA_TRY(launch_iir(Lc, dt, src, d, n, w.param, w.lam, w.res, st.st[0], st.st[1], s->book, s->g));
+    } else {
+      CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk, c.rope_base,
+                                st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
+    }
+    EVS_TRY(gemm(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, &P));
+    CUDA_TRY(launch_residual_norm(Lc, dt, P, s->X, n, d, eps, s->xn));
+    EVS_TRY(gemm(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, d, &P));
+    CUDA_TRY(launch_mlp_act(Lc, dt, P, n, F, s->h));
+    EVS_TRY(gemm(m->p_down, w.m_down, w.w_down, s->m_h, s->h, F, &P));
+    CUDA_TRY(launch_residual_norm(Lc, dt, P, s->X, n, d, eps, s->xn));
+  }
+  Partials P;
+  EVS_TRY(gemm(m->p_head, m->m_head, m->head, s->m_xn, s->xn, d, &P));
+  CUDA_TRY(launch_logits(Lc, P, n, V, logits));
+  return EVS_OK;
+}
+
+struct RoundArgs {
+  float* p;
+  const float* q;
+  const int32_t* drafts;  // = tokens + 1
+  const float* u;
+  float T;
+  int top_k, mode;
+  int32_t *acc, *otok;
+};
+
+int enqueue_round(evs_state* s, const int32_t* tokens, int n, float* logits, const RoundArgs& r,
+                  const LaunchCtx& Lc) {
+  EVS_TRY(enqueue_verify(s, tokens, n, logits, Lc));
+  const int V = s->m->cfg.vocab;
+  const float* P = logits;
+  if (r.mode == EVS_SAMPLE) {
+    CUDA_TRY(launch_probs(Lc, logits, n, V, r.T, r.top_k, r.p));
+    P = r.p;
+  }
+  CUDA_TRY(launch_accept(Lc, P, r.q, r.drafts, r.u, n, V, r.mode, r.acc, r.otok));
+  CUDA_TRY(launch_commit(Lc, s->book, 0, r.acc, 0));
+  return EVS_OK;
+}
+
+GraphEntry* find_graph(evs_state* s, const GraphEntry& key) {
+  for (auto& g : s->graphs)
+    if (g.round == key.round && g.n == key.n && g.tok == key.tok && g.logits == key.logits &&
+        g.mode == key.mode && g.top_k == key.top_k && g.T == key.T && g.p == key.p && g.q == key.q &&
+        g.u == key.u && g.acc == key.acc && g.otok == key.otok)
+      return &g;
+  return nullptr;
+}
+
+template <typename F>
+int run_captured(evs_state* s, GraphEntry key, cudaStream_t stream, F&& body) {
+  if (!s->use_graphs) {
+    LaunchCtx Lc{stream, s->pdl};
+    return body(Lc);
+  }
+  GraphEntry* g = find_graph(s, key);
+  if (!g) {
+    if (s->graphs.size() >= 16) {  // evict the least recently used
+      size_t victim = 0;
+      for (size_t i = 1; i < s->graphs.size(); ++i)
+        if (s->graphs[i].last_use < s->graphs[victim].last_use) victim = i;
+      cudaGraphExecDestroy(s->graphs[victim].exec);
+      s->graphs.erase(s->graphs.begin() + victim);
+    }
+    const long long before = g_launches.load();
+    CUDA_TRY(cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeRelaxed));
+    LaunchCtx Lc{s->cap, s->pdl};
+    int r = body(Lc);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(s->cap, &graph);
+    if (r != EVS_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return r;
+    }
+    if (e != cudaSuccess) return fail(EVS_ERR_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(EVS_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+    key.exec = exec;
+    key.kernels = (int)(g_launches.load() - before);
+    g_launches -= key.kernels;  // counted again at each launch
+    s->graphs.push_back(key);
+    g = &s->graphs.back();
+  }
+  g->last_use = ++s->tick;
+  CUDA_TRY(cudaGraphLaunch(g->exec, stream));
+  count_launch(g->kernels);
+  return EVS_OK;
+}
+
+int check_cfg(const evs_config* c) {
+  if (!c) return fail(EVS_ERR_ARG, "null config");
+  if (c->vocab <= 0 || c->d_model <= 0 || c->n_layers <= 0 || c->d_ffn <= 0)
+    return fail(EVS_ERR_ARG, "vocab, d_model, n_layers, d_ffn must be positive");
+  if (c->gamma_max < 0 || c->gamma_max + 1 > NTOK) return fail(EVS_ERR_ARG, "gamma_max must be in [0, %d]", NTOK - 1);
+  if (c->dtype != EVS_BF16 && c->dtype != EVS_F32) return fail(EVS_ERR_ARG, "dtype must be EVS_BF16 or EVS_F32");
+  if (!c->layer_kind_host || !c->layer_param_host) return fail(EVS_ERR_ARG, "null layer arrays");
+  if (c->d_model % 32) return fail(EVS_ERR_UNSUPPORTED, "d_model must be a multiple of 32");
+  if (!(c->norm_eps >= 0.f)) return fail(EVS_ERR_ARG, "norm_eps must be >= 0");
+  if (c->dtype == EVS_BF16) {
+    if (c->d_model % 128 || (2 * c->d_ffn) % 128 || c->vocab % 128 || c->d_ffn % 64)
+      return fail(EVS_ERR_UNSUPPORTED, "bf16 path needs d_model, 2*d_ffn, vocab multiples of 128 and d_ffn of 64");
+  }
+  for (int i = 0; i < c->n_layers; ++i) {
+    const int k = c->layer_kind_host[i], p = c->layer_param_host[i];
+    if (k == EVS_LAYER_FIR) {
+      if (p < 1 || p > 1024) return fail(EVS_ERR_UNSUPPORTED, "layer %d: FIR length must be in [1, 1024]", i);
+    } else if (k == EVS_LAYER_IIR) {
+      if (p < 1 || p > 32 || (p & (p - 1))) return fail(EVS_ERR_UNSUPPORTED, "layer %d: IIR poles must be a power of two <= 32", i);
+      if (c->d_model % (256 / p)) return fail(EVS_ERR_UNSUPPORTED, "layer %d: d_model * poles must be a multiple of 256", i);
+    } else if (k == EVS_LAYER_ATTN) {
+      if (c->n_heads * c->head_dim != c->d_model) return fail(EVS_ERR_ARG, "n_heads * head_dim != d_model");
+      if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+        return fail(EVS_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+      if (c->attn_chunk < 32 || c->attn_chunk % 32 || c->attn_chunk > 1024)
+        return fail(EVS_ERR_UNSUPPORTED, "attn_chunk must be a multiple of 32 in [32, 1024]");
+      if (!(c->rope_base > 0.f)) return fail(EVS_ERR_ARG, "rope_base must be > 0");
+    } else {
+      return fail(EVS_ERR_ARG, "layer %d: unknown kind %d", i, k);
+    }
+  }
+  return EVS_OK;
+}
+
+}  // namespace
+
+// =================================================================== model
+extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs_model** out) {
+  if (!out) return fail(EVS_ERR_ARG, "null out");
+  *out = nullptr;
+  EVS_TRY(check_cfg(cfg));
+  if (!w || !w->embed || !w->lm_head || !w->layers_host) return fail(EVS_ERR_ARG, "null weights");
+  evs_model* m = new evs_model();
+  m->cfg = *cfg;
+  m->kind.assign(cfg->layer_kind_host, cfg->layer_kind_host + cfg->n_layers);
+  m->param.assign(cfg->layer_param_host, cfg->layer_param_host + cfg->n_layers);
+  m->cfg.layer_kind_host = m->kind.data();
+  m->cfg.layer_param_host = m->param.data();
+  int r = num_sms_current(&m->num_sms);
+  if (r != EVS_OK) {
+    delete m;
+    return r;
+  }
+  m->tc = cfg->dtype == EVS_BF16;
+  m->embed = w->embed;
+  m->head = w->lm_head;
+  m->n_max = cfg->gamma_max + 1;
+  m->has_attn = false;
+  const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;
+  char err[256] = {0};
+  auto enc = [&](CUtensorMap* map, const void* base, int N, int K) -> bool {
+    if (!m->tc) return true;
+    if (!aligned16(base)) {
+      snprintf(err, sizeof err, "weight pointer not 16-byte aligned");
+      return false;
+    }
+    return encode_tmap_2d(map, base, (uint64_t)K, (uint64_t)N, TILE_K, TILE_M, err, sizeof err);
+  };
+  for (int i = 0; i < cfg->n_layers; ++i) {
+    const evs_layer_weights& lw = w->layers_host[i];
+    LayerW L{};
+    L.kind = m->kind[i];
+    L.param = m->param[i];
+    L.w_in = lw.w_in;
+    L.w_out = lw.w_out;
+    L.w_gu = lw.w_gu;
+    L.w_down = lw.w_down;
+    L.taps = lw.fir_taps;
+    L.lam = lw.iir_lambda;
+    L.res = lw.iir_residue;
+    if (!L.w_in || !L.w_out || !L.w_gu || !L.w_down ||
+        (L.kind == EVS_LAYER_FIR && !L.taps) || (L.kind == EVS_LAYER_IIR && (!L.lam || !L.res))) {
+      delete m;
+      return fail(EVS_ERR_ARG, "layer %d: null weight pointer", i);
+    }
+    if (L.kind == EVS_LAYER_ATTN) m->has_attn = true;
+    if (!enc(&L.m_in, L.w_in, 3 * d, d) || !enc(&L.m_out, L.w_out, d, d) || !enc(&L.m_gu, L.w_gu, 2 * F, d) ||
+        !enc(&L.m_down, L.w_down, d, F)) {
+      delete m;
+      return fail(EVS_ERR_CUDA, "layer %d: %s", i, err);
+    }
+    m->L.push_back(L);
+  }
+  if (!enc(&m->m_head, m->head, V, d)) {
+    delete m;
+    return fail(EVS_ERR_CUDA, "head: %s", err);
+  }
+  m->p_in = plan_gemm(3 * d, d, m->num_sms);
+  m->p_out = plan_gemm(d, d, m->num_sms);
+  m->p_gu = plan_gemm(2 * F, d, m->num_sms);
+  m->p_down = plan_gemm(d, F, m->num_sms);
+  m->p_head = plan_gemm(V, d, m->num_sms);
+  *out = m;
+  return EVS_OK;
+}
+
+extern "C" int evs_model_destroy(evs_model* m) {
+  delete m;
+  return EVS_OK;
+}
+
+// =================================================================== state
+static void state_free(evs_state* s) {
+  if (!s) return;
+  for (auto& g : s->graphs) cudaGraphExecDestroy(g.exec);
+  if (s->cap) cudaStreamDestroy(s->cap);
+  for (void* p : s->allocs) cudaFree(p);
+  delete s;
+}
+
+static evs_book initial_book() {
+  evs_book b{};
+  b.iir_slot = -1;
+  return b;
+}
+
+extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) {
+  if (!m || !out) return fail(EVS_ERR_ARG, "null argument");
+  if (ctx_max < 1 || ctx_max > (1ll << 30)) return fail(EVS_ERR_ARG, "ctx_max out of range");
+  *out = nullptr;
+  evs_state* s = new evs_state();
+  s->m = m;
+  s->ctx_max = ctx_max;
+  s->use_graphs = true;
+  const char* pdl_env = getenv("EVS_PDL");
+  s->pdl = !(pdl_env && pdl_env[0] == '0');
+  const evs_config& c = m->cfg;
+  const int d = c.d_model, F = c.d_ffn, nm = m->n_max;
+  const size_t es = esize(c.dtype);
+  int r = EVS_OK;
+#define ALLOC(ptr, bytes)                                              \
+  do {                                                                 \
+    void* p_ = nullptr;                                                \
+    r = dmalloc(s, &p_, (bytes));                                      \
+    if (r != EVS_OK) { state_free(s); return r; }                      \
+    ptr = reinterpret_cast<decltype(ptr)>(p_);                         \
+  } while (0)
+  ALLOC(s->book, sizeof(evs_book));
+  ALLOC(s->X, sizeof(float) * NTOK * d);
+  ALLOC(s->xn, es * NTOK * d);
+  ALLOC(s->g, es * NTOK * d);
+  ALLOC(s->h, es * NTOK * F);
+  size_t wsb = 0;
+  for (const Partials* P : {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head})
+    wsb = std::max(wsb, partials_bytes(*P));
+  ALLOC(s->ws[0], wsb);
+  ALLOC(s->ws[1], wsb);
+  if (m->has_attn) {
+    const size_t ab = attn_scratch_bytes(c.n_heads, c.head_dim, ctx_max, c.attn_chunk);
+    ALLOC(s->attn_scratch, ab);
+    attn_bufs_from_scratch(s->attn_scratch, c.n_heads, c.head_dim, ctx_max, c.attn_chunk, &s->ab);
+  }
+  s->S.resize(m->L.size());
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    LayerS& st = s->S[i];
+    st = LayerS{};
+    const LayerW& L = m->L[i];
+    if (L.kind == EVS_LAYER_FIR) {
+      for (int b = 0; b < 2; ++b) ALLOC(st.ext[b], sizeof(float) * (size_t)(L.param - 1 + nm) * d);
+    } else if (L.kind == EVS_LAYER_IIR) {
+      for (int b = 0; b < 2; ++b) ALLOC(st.st[b], sizeof(float) * 2 * (size_t)nm * d * L.param);
+    } else {
+      ALLOC(st.kc, es * (size_t)c.n_heads * ctx_max * c.head_dim);
+      ALLOC(st.vc, es * (size_t)c.n_heads * ctx_max * c.head_dim);
+    }
+  }
+#undef ALLOC
+  if (m->tc) {
+    char err[256] = {0};
+    if (!encode_tmap_2d(&s->m_xn, s->xn, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
+        !encode_tmap_2d(&s->m_g, s->g, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
+        !encode_tmap_2d(&s->m_h, s->h, F, NTOK, TILE_K, NTOK, err, sizeof err)) {
+      state_free(s);
+      return fail(EVS_ERR_CUDA, "activation tensor map: %s", err);
+    }
+  }
+  cudaError_t e = cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    state_free(s);
+    return fail(EVS_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
+  }
+  // zero activations once (rows beyond a block's n are read but never used)
+  cudaMemset(s->xn, 0, es * NTOK * d);
+  cudaMemset(s->g, 0, es * NTOK * d);
+  cudaMemset(s->h, 0, es * NTOK * F);
+  r = evs_state_reset(s, 0);
+  if (r == EVS_OK) {
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) r = fail(EVS_ERR_CUDA, "state init: %s", cudaGetErrorString(e));
+  }
+  if (r != EVS_OK) {
+    state_free(s);
+    return r;
+  }
+  *out = s;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_destroy(evs_state* s) {
+  if (s) cudaDeviceSynchronize();
+  state_free(s);
+  return EVS_OK;
+}
+
+extern "C" int evs_state_reset(evs_state* s, cudaStream_t stream) {
+  if (!s) return fail(EVS_ERR_ARG, "null state");
+  const evs_model* m = s->m;
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    const LayerW& L = m->L[i];
+    if (L.kind == EVS_LAYER_FIR)
+      for (int b = 0; b < 2; ++b)
+        CUDA_TRY(cudaMemsetAsync(s->S[i].ext[b], 0, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * m->cfg.d_model, stream));
+  }
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_book_set(Lc, s->book, initial_book()));
+  s->host_pos = 0;
+  s->host_pos_known = true;
+  s->host_pending = 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_layer_view(const evs_state* s, int32_t layer, evs_layer_view* out) {
+  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
+  if (layer < 0 || layer >= (int)s->S.size()) return fail(EVS_ERR_ARG, "layer out of range");
+  const LayerS& st = s->S[layer];
+  out->kind = s->m->L[layer].kind;
+  out->param = s->m->L[layer].param;
+  out->fir_ext[0] = st.ext[0];
+  out->fir_ext[1] = st.ext[1];
+  out->iir_all[0] = st.st[0];
+  out->iir_all[1] = st.st[1];
+  out->k_cache = st.kc;
+  out->v_cache = st.vc;
+  out->ctx_max = s->ctx_max;
+  out->n_max = s->m->n_max;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_book_dev(const evs_state* s, evs_book** out) {
+  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
+  *out = s->book;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_book_read(const evs_state* s, evs_book* out, cudaStream_t stream) {
+  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
+  CUDA_TRY(cudaMemcpyAsync(out, s->book, sizeof(evs_book), cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  return EVS_OK;
+}
+
+extern "C" int evs_state_book_write(evs_state* s, const evs_book* in, cudaStream_t stream) {
+  if (!s || !in) return fail(EVS_ERR_ARG, "null argument");
+  if (in->pos < 0 || in->pos > s->ctx_max || (in->fir_bank & ~1) || (in->iir_bank & ~1) ||
+      in->iir_slot < -1 || in->iir_slot >= s->m->n_max || in->fir_off < 0 || in->fir_off > s->m->n_max ||
+      in->pending_n < 0 || in->pending_n > s->m->n_max)
+    return fail(EVS_ERR_ARG, "book field out of range");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_book_set(Lc, s->book, *in));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  s->host_pos = in->pos;
+  s->host_pos_known = true;
+  s->host_pending = in->pending_n;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_check(evs_state* s, cudaStream_t stream, int32_t* status) {
+  evs_book b;
+  EVS_TRY(evs_state_book_read(s, &b, stream));
+  if (status) *status = b.status;
+  if (b.status) return fail(EVS_ERR_DEVICE, "device status 0x%x", b.status);
+  return EVS_OK;
+}
+
+extern "C" int evs_state_use_graphs(evs_state* s, int32_t enable) {
+  if (!s) return fail(EVS_ERR_ARG, "null state");
+  s->use_graphs = enable != 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_clone(const evs_state* src, evs_state* dst, cudaStream_t stream) {
+  if (!src || !dst) return fail(EVS_ERR_ARG, "null state");
+  if (src->m != dst->m || src->ctx_max != dst->ctx_max) return fail(EVS_ERR_ARG, "clone needs the same model and ctx_max");
+  evs_book b;
+  EVS_TRY(evs_state_book_read(src, &b, stream));
+  const evs_model* m = src->m;
+  const evs_config& c = m->cfg;
+  const size_t es = esize(c.dtype);
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    const LayerW& L = m->L[i];
+    const LayerS &a = src->S[i], &z = dst->S[i];
+    if (L.kind == EVS_LAYER_FIR) {
+      for (int k = 0; k < 2; ++k)
+        CUDA_TRY(cudaMemcpyAsync(z.ext[k], a.ext[k], sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
+                                 cudaMemcpyDeviceToDevice, stream));
+    } else if (L.kind == EVS_LAYER_IIR) {
+      for (int k = 0; k < 2; ++k)
+        CUDA_TRY(cudaMemcpyAsync(z.st[k], a.st[k], sizeof(float) * 2 * (size_t)m->n_max * c.d_model * L.param,
+                                 cudaMemcpyDeviceToDevice, stream));
+    } else if (b.pos + b.pending_n > 0) {
+      const size_t rowb = es * c.head_dim, pitch = rowb * src->ctx_max;
+      const size_t rows = (size_t)std::min<long long>(src->ctx_max, (long long)b.pos + b.pending_n);
+      CUDA_TRY(cudaMemcpy2DAsync(z.kc, pitch, a.kc, pitch, rows * rowb, c.n_heads, cudaMemcpyDeviceToDevice, stream));
+      CUDA_TRY(cudaMemcpy2DAsync(z.vc, pitch, a.vc, pitch, rows * rowb, c.n_heads, cudaMemcpyDeviceToDevice, stream));
+    }
+  }
+  CUDA_TRY(cudaMemcpyAsync(dst->book, src->book, sizeof(evs_book), cudaMemcpyDeviceToDevice, stream));
+  dst->host_pos = b.pos;
+  dst->host_pos_known = true;
+  dst->host_pending = b.pending_n;
+  return EVS_OK;
+}
+
+// =================================================================== path
+static int check_block(evs_state* s, int n) {
+  if (n < 1 || n > s->m->n_max) return fail(EVS_ERR_ARG, "n=%d outside [1, gamma_max+1=%d]", n, s->m->n_max);
+  if (s->host_pending) return fail(EVS_ERR_STATE, "a verified block of %d tokens awaits commit", s->host_pending);
+  if (s->host_pos_known && (long long)s->host_pos + n > s->ctx_max)
+    return fail(EVS_ERR_CAPACITY, "position %d + %d exceeds ctx_max %lld", s->host_pos, n, s->ctx_max);
+  return EVS_OK;
+}
+
+extern "C" int evs_verify_block(evs_state* s, const int32_t* tokens, int32_t n, float* logits, cudaStream_t stream) {
+  if (!s || !tokens || !logits) return fail(EVS_ERR_ARG, "null argument");
+  EVS_TRY(check_block(s, n));
+  GraphEntry key{};
+  key.n = n;
+  key.tok = tokens;
+  key.logits = logits;
+  EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) { return enqueue_verify(s, tokens, n, logits, Lc); }));
+  s->host_pending = n;
+  return EVS_OK;
+}
+
+extern "C" int evs_probs(const float* logits, int32_t n, int32_t V, float T, int32_t top_k, float* p,
+                         cudaStream_t stream) {
+  if (!logits || !p) return fail(EVS_ERR_ARG, "null argument");
+  if (n < 1 || n > 4096 || V < 1 || V > 8192) return fail(EVS_ERR_ARG, "n or V out of range");
+  if (!(T > 0.f)) return fail(EVS_ERR_ARG, "temperature must be > 0");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_probs(Lc, logits, n, V, T, top_k, p));
+  return EVS_OK;
+}
+
+extern "C" int evs_accept(const float* p, const float* q, const int32_t* drafts, const float* u, int32_t n,
+                          int32_t V, int32_t mode, int32_t* acc, int32_t* tok, cudaStream_t stream) {
+  if (!p || !acc || !tok) return fail(EVS_ERR_ARG, "null argument");
+  if (n < 1 || V < 1 || V > 8192) return fail(EVS_ERR_ARG, "n or V out of range");
+  if (mode != EVS_GREEDY && mode != EVS_SAMPLE) return fail(EVS_ERR_ARG, "mode must be EVS_GREEDY or EVS_SAMPLE");
+  if (n > 1 && !drafts) return fail(EVS_ERR_ARG, "null drafts");
+  if (mode == EVS_SAMPLE && (!u || (n > 1 && !q))) return fail(EVS_ERR_ARG, "sample mode needs q and u");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_accept(Lc, p, q, drafts, u, n, V, mode, acc, tok));
+  return EVS_OK;
+}
+
+extern "C" int evs_commit(evs_state* s, int32_t keep, cudaStream_t stream) {
+  if (!s) return fail(EVS_ERR_ARG, "null state");
+  if (!s->host_pending) return fail(EVS_ERR_STATE, "commit without a pending verify");
+  if (keep < 0 || keep > s->host_pending) return fail(EVS_ERR_ARG, "keep=%d outside [0, %d]", keep, s->host_pending);
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_commit(Lc, s->book, keep, nullptr, 0));
+  s->host_pos += keep;
+  s->host_pending = 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_commit_dev(evs_state* s, const int32_t* accepted, cudaStream_t stream) {
+  if (!s || !accepted) return fail(EVS_ERR_ARG, "null argument");
+  if (!s->host_pending) return fail(EVS_ERR_STATE, "commit without a pending verify");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_commit(Lc, s->book, 0, accepted, 0));
+  s->host_pos_known = false;
+  s->host_pending = 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_round(evs_state* s, const int32_t* tokens, int32_t n, float* logits, float* p, const float* q,
+                         const float* u, float T, int32_t top_k, int32_t mode, int32_t* acc, int32_t* otok,
+                         cudaStream_t stream) {
+  if (!s || !tokens || !logits || !acc || !otok) return fail(EVS_ERR_ARG, "null argument");
+  if (mode != EVS_GREEDY && mode != EVS_SAMPLE) return fail(EVS_ERR_ARG, "bad mode");
+  if (mode == EVS_SAMPLE && (!p || !u || (n > 1 && !q) || !(T > 0.f)))
+    return fail(EVS_ERR_ARG, "sample mode needs p, q, u and T > 0");
+  EVS_TRY(check_block(s, n));
+  RoundArgs r{p, q, tokens + 1, u, T, top_k, mode, acc, otok};
+  GraphEntry key{};
+  key.round = true;
+  key.n = n;
+  key.tok = tokens;
+  key.logits = logits;
+  key.p = p;
+  key.q = q;
+  key.u = u;
+  key.T = T;
+  key.top_k = top_k;
+  key.mode = mode;
+  key.acc = acc;
+  key.otok = otok;
+  EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) { return enqueue_round(s, tokens, n, logits, r, Lc); }));
+  s->host_pos_known = false;
+  s->host_pending = 0;
+  return EVS_OK;
+}
+
+// =================================================================== operators
+extern "C" int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_t dtype, const void* abv,
+                          const float* taps, float* e0, float* e1, const evs_book* book, void* g,
+                          cudaStream_t stream) {
+  if (!abv || !taps || !e0 || !e1 || !book || !g) return fail(EVS_ERR_ARG, "null argument");
+  if (L < 1 || L > 1024 || d < 32 || d % 32 || n < 1 || n > NTOK || n > n_max)
+    return fail(EVS_ERR_ARG, "bad FIR shape");
+  if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{nullptr, abv, 3 * d}, d, n, L, taps, e0, e1, book, g));
+  return EVS_OK;
+}
+
+extern "C" int evs_op_iir(int32_t M, int32_t d, int32_t n, int32_t n_max, int32_t dtype, const void* abv,
+                          const float* lam, const float* res, float* s0, float* s1, const evs_book* book, void* g,
+                          cudaStream_t stream) {
+  if (!abv || !lam || !res || !s0 || !s1 || !book || !g) return fail(EVS_ERR_ARG, "null argument");
+  if (M < 1 || M > 32 || (M & (M - 1)) || d % (256 / M) || n < 1 || n > NTOK || n > n_max)
+    return fail(EVS_ERR_ARG, "bad IIR shape");
+  if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_iir(Lc, dtype, MixSrc{nullptr, abv, 3 * d}, d, n, M, lam, res, s0, s1, book, g));
+  return EVS_OK;
+}
+
+extern "C" size_t evs_op_attention_scratch_bytes(int32_t H, int32_t Dh, int64_t ctx_max, int32_t chunk, int32_t n_max) {
+  (void)n_max;
+  if (H < 1 || Dh < 2 || ctx_max < 1 || chunk < 1) return 0;
+  return attn_scratch_bytes(H, Dh, ctx_max, chunk);
+}
+
+extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max, int64_t ctx_max, int32_t chunk,
+                                float base, int32_t dtype, const void* qkv, void* kc, void* vc, evs_book* book,
+                                void* g, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  if (!qkv || !kc || !vc || !book || !g || !scratch) return fail(EVS_ERR_ARG, "null argument");
+  if (H < 1 || (Dh != 32 && Dh != 64 && Dh != 128) || n < 1 || n > NTOK || n > n_max || ctx_max < 1 ||
+      chunk < 32 || chunk % 32 || chunk > 1024)
+    return fail(EVS_ERR_ARG, "bad attention shape");
+  if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
+  if (scratch_bytes < attn_scratch_bytes(H, Dh, ctx_max, chunk)) return fail(EVS_ERR_ARG, "scratch too small");
+  int sms = 0;
+  EVS_TRY(num_sms_current(&sms));
+  AttnBufs B;
+  attn_bufs_from_scratch(scratch, H, Dh, ctx_max, chunk, &B);
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{nullptr, qkv, 3 * H * Dh}, H, Dh, n, ctx_max, chunk, base, kc, vc, book,
+                            B, g, sms));
+  return EVS_OK;
+}
+
+extern "C" int evs_op_commit(evs_book* book, int32_t keep, int32_t n, cudaStream_t stream) {
+  if (!book) return fail(EVS_ERR_ARG, "null book");
+  if (n < 1 || keep < 0 || keep > n) return fail(EVS_ERR_ARG, "keep=%d outside [0, n=%d]", keep, n);
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_commit(Lc, book, keep, nullptr, n));
+  return EVS_OK;
+}
+
+static int gemm_plan_op(int32_t N, int32_t K, Partials* P) {
+  int sms = 0;
+  EVS_TRY(num_sms_current(&sms));
+  *P = plan_gemm(N, K, sms);
+  return EVS_OK;
+}
+
+extern "C" size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype) {
+  (void)dtype;
+  if (N < 1 || K < 1) return 0;
+  Partials P;
+  if (gemm_plan_op(N, K, &P) != EVS_OK) return 0;
+  return partials_bytes(P) + 256;
+}
+
+extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, int32_t n, int32_t dtype, float* Y,
+                           void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  if (!W || !X || !Y || !scratch) return fail(EVS_ERR_ARG, "null argument");
+  if (N < 1 || K < 1 || n < 1 || n > NTOK) return fail(EVS_ERR_ARG, "bad GEMM shape");
+  if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
+  Partials P;
+  EVS_TRY(gemm_plan_op(N, K, &P));
+  if (scratch_bytes < partials_bytes(P) + 256) return fail(EVS_ERR_ARG, "scratch too small");
+  P.ws = (float*)scratch;
+  int* err_flag = (int*)((char*)scratch + partials_bytes(P));
+  LaunchCtx Lc{stream, false};
+  if (dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X)) {
+    CUtensorMap wm, xm;
+    char err[256] = {0};
+    if (!encode_tmap_2d(&wm, W, K, N, TILE_K, TILE_M, err, sizeof err) ||
+        !encode_tmap_2d(&xm, X, K, n, TILE_K, NTOK, err, sizeof err))
+      return fail(EVS_ERR_CUDA, "%s", err);
+    CUDA_TRY(cudaMemsetAsync(err_flag, 0, sizeof(int), stream));
+    CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, err_flag));
+  } else {
+    CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, n, P, K));
+  }
+  CUDA_TRY(launch_logits(Lc, P, n, N, Y));
+  return EVS_OK;
+}
+
+// =================================================================== misc
+extern "C" const char* evs_last_error(void) { return g_err.c_str(); }
+extern "C" const char* evs_version(void) { return "evs 0.1 (sm_103a)"; }
+extern "C" int64_t evs_kernel_launches(void) { return g_launches.load(); }
+extern "C" int32_t evs_verify_kernel_count(const evs_state* s, int32_t n) {
+  (void)n;
+  if (!s) return -1;
+  int k = 1 + 2;  // embed, head GEMM, logits
+  for (const auto& L : s->m->L) k += 7 + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
+  return k;
+}

@@ -1,0 +1,411 @@
+// Skinny weight-streaming GEMM: partials of Y[tok][col] = sum_k X[tok][k] W[col][k]
+// for a verify block of n <= 16 tokens against a [N][K] weight matrix.
+//
+// The verify step is bound by reading the weights once (the discussion
+// post's reply, "Regime overlap": ~80% of a native step is the weight read).
+// So the kernel is a weight stream: one persistent CTA per SM walks a
+// contiguous range of 128x64 weight units (stream-K order), TMA brings each
+// unit into a 128-byte-swizzled shared-memory ring, and one thread issues
+// tcgen05.mma with the weight tile as A (M = 128 output columns) and the
+// block's activations as B (N = 16 tokens), accumulating in TMEM.  Each tile
+// segment's 128x16 fp32 accumulator is drained by four epilogue warps into a
+// partial slot; the consumer of the GEMM sums the slots in CTA order.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+#include "evs_internal.cuh"
+
+namespace evs {
+
+Partials plan_gemm(int N, int K, int num_sms) {
+  Partials P{};
+  P.N = N;
+  const int T = (N + TILE_M - 1) / TILE_M;
+  P.KB = (K + TILE_K - 1) / TILE_K;
+  P.U = (long long)T * P.KB;
+  P.G = (int)std::min<long long>(num_sms, P.U);
+  int ms = 1;
+  for (int c = 0; c < P.G; ++c) {
+    const long long b = unit_begin(P.U, P.G, c), e = unit_begin(P.U, P.G, c + 1);
+    ms = std::max(ms, (int)((e - 1) / P.KB - b / P.KB + 1));
+  }
+  P.maxseg = ms;
+  return P;
+}
+
+size_t partials_bytes(const Partials& P) {
+  return (size_t)P.G * P.maxseg * NTOK * TILE_M * sizeof(float);
+}
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint32_t box_inner, uint32_t box_outer, char* err, size_t errlen) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+      snprintf(err, errlen, "cuTensorMapEncodeTiled entry point unavailable");
+      return false;
+    }
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(err, errlen, "cuTensorMapEncodeTiled failed (%d) for [%llu][%llu]", (int)r,
+             (unsigned long long)outer, (unsigned long long)inner);
+    return false;
+  }
+  return true;
+}
+
+namespace {
+
+constexpr int STAGES = 8;
+constexpr int A_BYTES = TILE_M * TILE_K * 2;  // 16 KB weight tile
+constexpr int B_BYTES = NTOK * TILE_K * 2;    // 2 KB activation tile
+constexpr int GEMM_THREADS = 192;             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr uint64_t WAIT_NS = 4000000000ull;   // upper bound on any pipeline wait
+constexpr int NBARS = 2 * STAGES + 5;         // full, empty, acc_full[2], acc_empty[2], drain
+constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + NBARS * 8 + 16;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false once WAIT_NS elapsed (the abort flag is then raised)
+// or another role already aborted.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > WAIT_NS) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
+// layout TMA writes: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
+// N = 16 (bits 17-22 hold N/8), M = 128 (bits 24-28 hold M/16).
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NTOK >> 3) << 17) |
+                           ((uint32_t)(TILE_M >> 4) << 24);
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   Partials P, int* err_flag) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto acc_full = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
+  auto acc_empty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const long long ub = unit_begin(P.U, P.G, c), ue = unit_begin(P.U, P.G, c + 1);
+  const long long nunits = ue - ub;
+  const int first_tile = (int)(ub / P.KB);
+  const int nseg = (int)((ue - 1) / P.KB) - first_tile + 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    const int pre = (int)std::min<long long>(STAGES, nunits);
+    // weight tiles do not depend on the preceding kernel: start streaming now
+    for (int i = 0; i < pre; ++i) {
+      const long long u = ub + i;
+      mbar_expect_tx(full(i), A_BYTES + B_BYTES);
+      tma_load_2d(smem_u32(sA + i * A_BYTES), &wmap, full(i), (int)(u % P.KB) * TILE_K,
+                  (int)(u / P.KB) * TILE_M, pol_w);
+    }
+    pdl_wait();  // activations are written by the preceding kernel
+    for (int i = 0; i < pre; ++i) {
+      const long long u = ub + i;
+      tma_load_2d(smem_u32(sB + i * B_BYTES), &xmap, full(i), (int)(u % P.KB) * TILE_K, 0, pol_x);
+    }
+    long long i = pre;
+    for (; i < nunits; ++i) {
+      const int s = (int)(i % STAGES);
+      const uint32_t round = (uint32_t)(i / STAGES);
+      if (!mbar_wait(empty(s), (round - 1) & 1, abort_flag)) break;
+      const long long u = ub + i;
+      mbar_expect_tx(full(s), A_BYTES + B_BYTES);
+      tma_load_2d(smem_u32(sA + s * A_BYTES), &wmap, full(s), (int)(u % P.KB) * TILE_K,
+                  (int)(u / P.KB) * TILE_M, pol_w);
+      tma_load_2d(smem_u32(sB + s * B_BYTES), &xmap, full(s), (int)(u % P.KB) * TILE_K, 0, pol_x);
+    }
+    // make sure no copy into this CTA's shared memory is still in flight
+    for (long long j = std::max<long long>(0, i - STAGES); j < i; ++j) {
+      volatile int local_abort = 0;
+      mbar_wait(full((int)(j % STAGES)), (uint32_t)(j / STAGES) & 1, &local_abort);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    long long i = 0;
+    bool ok = true;
+    for (int seg = 0; seg < nseg && ok; ++seg) {
+      const int tile = first_tile + seg;
+      const long long seg_end = std::min<long long>(ue, (long long)(tile + 1) * P.KB);
+      const int b = seg & 1;
+      if (seg >= 2 && !mbar_wait(acc_empty(b), (uint32_t)((seg >> 1) - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem + (uint32_t)(b * NTOK);
+      bool first = true;
+      for (; ub + i < seg_end; ++i) {
+        const int s = (int)(i % STAGES);
+        if (!mbar_wait(full(s), (uint32_t)(i / STAGES) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(smem_u32(sA + s * A_BYTES));
+        const uint64_t bd = sw128_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+        for (int k = 0; k < TILE_K / 16; ++k)  // 16 bf16 = 32 bytes per MMA step along K
+          mma_bf16(dt, ad + 2 * k, bd + 2 * k, IDESC, (first && k == 0) ? 0u : 1u);
+        first = false;
+        mma_commit(empty(s));
+      }
+      if (ok) mma_commit(acc_full(b));
+    }
+    // wait for every issued MMA before TMEM is released
+    mma_commit(drain);
+    volatile int local_abort = 0;
+    mbar_wait(drain, 0, &local_abort);
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> partial slots
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    for (int seg = 0; seg < nseg; ++seg) {
+      const int b = seg & 1;
+      if (!warp_wait(acc_full(b), (uint32_t)(seg >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      float v[NTOK];
+      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NTOK), v);
+      tc_fence_before();
+      mbar_arrive(acc_empty(b));
+      const long long slot = (long long)c * P.maxseg + seg;
+      float* dst = P.ws + slot * NTOK * TILE_M + row;
+#pragma unroll
+      for (int j = 0; j < NTOK; ++j) __stcg(dst + j * TILE_M, v[j]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
+}
+
+// SIMT variant with the same unit schedule and partial layout (float32
+// storage, or shapes the tensor-core path does not take).
+template <typename T>
+__global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, int ldx, int n,
+                                                        Partials P, int K) {
+  __shared__ float xs[NTOK][TILE_K];
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x;
+  const long long ub = unit_begin(P.U, P.G, c), ue = unit_begin(P.U, P.G, c + 1);
+  const int first_tile = (int)(ub / P.KB);
+  long long u = ub;
+  while (u < ue) {
+    const int tile = (int)(u / P.KB);
+    const long long seg_end = std::min<long long>(ue, (long long)(tile + 1) * P.KB);
+    const int row = tile * TILE_M + threadIdx.x;
+    float acc[NTOK];
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) acc[t] = 0.f;
+    for (; u < seg_end; ++u) {
+      const int k0 = (int)(u % P.KB) * TILE_K;
+      const int kn = min(TILE_K, K - k0);
+      __syncthreads();
+      for (int e = threadIdx.x; e < NTOK * TILE_K; e += blockDim.x) {
+        const int t = e / TILE_K, k = e % TILE_K;
+        xs[t][k] = (t < n && k < kn) ? to_f(X[(size_t)t * ldx + k0 + k]) : 0.f;
+      }
+      __syncthreads();
+      if (row < P.N) {
+        const T* wr = W + (size_t)row * K + k0;
+        for (int k = 0; k < kn; ++k) {
+          const float w = to_f(wr[k]);
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t) acc[t] = fmaf(w, xs[t][k], acc[t]);
+        }
+      }
+    }
+    const long long slot = (long long)c * P.maxseg + (tile - first_tile);
+    float* dst = P.ws + slot * NTOK * TILE_M + threadIdx.x;
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) dst[t * TILE_M] = acc[t];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                           const Partials& P, int K, int* err_flag) {
+  (void)K;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)GEMM_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch(L, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), GEMM_SMEM, wmap, xmap, P, err_flag);
+}
+
+cudaError_t launch_gemm_simt(const LaunchCtx& L, int dtype, const void* W, const void* X, int ldx,
+                             int n, const Partials& P, int K) {
+  if (dtype == EVS_BF16)
+    return launch(L, gemm_simt_kernel<bf16>, dim3(P.G), dim3(128), 0, (const bf16*)W, (const bf16*)X,
+                  ldx, n, P, K);
+  return launch(L, gemm_simt_kernel<float>, dim3(P.G), dim3(128), 0, (const float*)W, (const float*)X,
+                ldx, n, P, K);
+}
+
+}  // namespace evs

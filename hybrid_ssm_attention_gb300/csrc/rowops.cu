@@ -1,0 +1,335 @@
+// Row kernels of the verify step and the accept / commit kernels.
+//
+//  embed_norm     X[t] = E[token_t]; xn[t] = RMSNorm(X[t]) in storage dtype
+//  residual_norm  X[t] += (GEMM partials)[t]; xn[t] = RMSNorm(X[t])
+//  mlp_act        h[t][j] = silu(gate) * up from the gate/up GEMM partials
+//  logits         logits[t][j] = head GEMM partials
+//  probs          temperature / top-k softmax of each logits row (model card,
+//                 "Library" example: T = 1.0, top_k = 4)
+//  accept         the exact accept rule of speculative sampling (EvSpark
+//                 preprint abstract; discussion post, "What we implemented"):
+//                 greedy match or u*q < p, residual / bonus resampling
+//  commit         per-position state slicing by bank flips (abstract, (i))
+//
+// Reductions run in a fixed order (per-thread strided partials, then a
+// butterfly), so results are reproducible and independent of the block size.
+#include "evs_internal.cuh"
+
+namespace evs {
+namespace {
+
+template <typename V, typename Op>
+__device__ V block_reduce(V v, Op op, V* scratch /* >= 32 */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  V r = scratch[0];
+  for (int w = 1; w < nw; ++w) r = op(r, scratch[w]);
+  __syncthreads();
+  return r;
+}
+
+struct AddF { __device__ float operator()(float a, float b) const { return a + b; } };
+struct MaxF { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
+struct AddU { __device__ unsigned long long operator()(unsigned long long a, unsigned long long b) const { return a + b; } };
+
+// RMSNorm of row t of X (already final in X) into xn
+template <typename T>
+__device__ void norm_row(const float* x, int d, float eps, T* xo, float* scratch) {
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  ss = block_reduce(ss, AddF(), scratch);
+  const float den = sqrtf(ss / (float)d + eps);
+  for (int c = threadIdx.x; c < d; c += blockDim.x) xo[c] = from_f<T>(x[c] / den);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) embed_norm_kernel(const T* E, const int32_t* tokens, int n, int d,
+                                                         int V, float eps, float* X, T* xn, evs_book* book) {
+  __shared__ float scratch[32];
+  const int t = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  if (t == 0 && threadIdx.x == 0) book->pending_n = n;
+  const int tok = tokens[t];
+  const bool ok = tok >= 0 && tok < V;
+  if (!ok && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
+  float* x = X + (size_t)t * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) x[c] = ok ? to_f(E[(size_t)tok * d + c]) : 0.f;
+  __syncthreads();
+  norm_row<T>(x, d, eps, xn + (size_t)t * d, scratch);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) residual_norm_kernel(Partials P, float* X, int d, float eps, T* xn) {
+  __shared__ float scratch[32];
+  const int t = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  float* x = X + (size_t)t * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) x[c] += partial_sum(P, t, c);
+  __syncthreads();
+  norm_row<T>(x, d, eps, xn + (size_t)t * d, scratch);
+}
+
+template <typename T>
+__global__ void mlp_act_kernel(Partials P, int F, T* h) {
+  const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  if (j >= F) return;
+  const float gt = partial_sum(P, t, j), up = partial_sum(P, t, F + j);
+  const float s = gt / (1.f + expf(-gt));
+  h[(size_t)t * F + j] = from_f<T>(s * up);
+}
+
+__global__ void logits_kernel(Partials P, int V, float* logits) {
+  const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  if (j < V) logits[(size_t)t * V + j] = partial_sum(P, t, j);
+}
+
+// One CTA per row.  top-k by rank: entry j is kept iff fewer than k entries
+// beat it (larger value, or equal value at a lower index).
+__global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, float T, int k, float* p) {
+  extern __shared__ float sm[];
+  __shared__ float scratch[32];
+  float* l_s = sm;        // [V]
+  float* w_s = sm + V;    // [V]
+  const int t = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  for (int j = threadIdx.x; j < V; j += blockDim.x) l_s[j] = logits[(size_t)t * V + j];
+  __syncthreads();
+  const bool use_k = k > 0 && k < V;
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+    bool keep = true;
+    if (use_k) {
+      const float lj = l_s[j];
+      int rank = 0;
+      for (int l = 0; l < V; ++l) rank += (l_s[l] > lj) || (l_s[l] == lj && l < j);
+      keep = rank < k;
+    }
+    w_s[j] = keep ? 1.f : 0.f;
+    if (keep) mx = fmaxf(mx, l_s[j]);
+  }
+  mx = block_reduce(mx, MaxF(), scratch);
+  float sum = 0.f;
+  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+    const float w = w_s[j] != 0.f ? expf((l_s[j] - mx) / T) : 0.f;
+    w_s[j] = w;
+    sum += w;
+  }
+  sum = block_reduce(sum, AddF(), scratch);
+  for (int j = threadIdx.x; j < V; j += blockDim.x) p[(size_t)t * V + j] = w_s[j] / sum;
+}
+
+// argmax over a row, ties to the lowest index
+__device__ int block_argmax(const float* row, int V, float* fs, int* is) {
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+    const float v = row[j];
+    if (v > bv || (v == bv && j < bi)) { bv = v; bi = j; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) { fs[warp] = bv; is[warp] = bi; }
+  __syncthreads();
+  bv = fs[0];
+  bi = is[0];
+  for (int w = 1; w < nw; ++w)
+    if (fs[w] > bv || (fs[w] == bv && is[w] < bi)) { bv = fs[w]; bi = is[w]; }
+  __syncthreads();
+  return bi == 0x7fffffff ? 0 : bi;
+}
+
+__device__ __forceinline__ unsigned int ladder_weight(float w) {
+  // floor(w * 2^24): the scaling is exact in float32, the conversion truncates
+  return (unsigned int)(fmaxf(w, 0.f) * 16777216.0f);
+}
+
+// Inverse CDF on integer weights: smallest j with prefix_j > thr.
+// Thread i owns the contiguous slice [i*seg, (i+1)*seg).
+__device__ int ladder_find(const unsigned int* W, int V, unsigned long long thr, unsigned long long* us,
+                           int* found) {
+  const int seg = (V + blockDim.x - 1) / blockDim.x;
+  const int j0 = min(V, (int)threadIdx.x * seg), j1 = min(V, j0 + seg);
+  unsigned long long local = 0;
+  for (int j = j0; j < j1; ++j) local += W[j];
+  // exclusive scan of the per-thread sums, in thread order
+  us[threadIdx.x] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long run = 0;
+    for (int i = 0; i < (int)blockDim.x; ++i) {
+      const unsigned long long x = us[i];
+      us[i] = run;
+      run += x;
+    }
+    *found = -1;
+  }
+  __syncthreads();
+  unsigned long long pre = us[threadIdx.x];
+  if (pre <= thr && thr < pre + local) {
+    for (int j = j0; j < j1; ++j) {
+      pre += W[j];
+      if (pre > thr) { *found = j; break; }
+    }
+  }
+  __syncthreads();
+  return *found;
+}
+
+__global__ void __launch_bounds__(256) accept_kernel(const float* p, const float* q, const int32_t* drafts,
+                                                     const float* u, int n, int V, int mode, int32_t* out_a,
+                                                     int32_t* out_tok) {
+  extern __shared__ unsigned int Wsm[];  // [V]
+  __shared__ float fs[32];
+  __shared__ int is[32];
+  __shared__ unsigned long long us[256];
+  __shared__ int found;
+  pdl_trigger();
+  pdl_wait();
+  const int gamma = n - 1;
+  int a = gamma;
+  for (int i = 1; i <= gamma; ++i) {
+    const int d = drafts[i - 1];
+    bool ok;
+    if (mode == EVS_GREEDY) {
+      ok = d == block_argmax(p + (size_t)(i - 1) * V, V, fs, is);
+    } else {
+      ok = d >= 0 && d < V && __fmul_rn(u[i - 1], q[(size_t)(i - 1) * V + d]) < p[(size_t)(i - 1) * V + d];
+    }
+    if (!ok) { a = i - 1; break; }
+  }
+  int token;
+  if (mode == EVS_GREEDY) {
+    token = block_argmax(p + (size_t)a * V, V, fs, is);
+  } else {
+    const float* pa = p + (size_t)a * V;
+    unsigned long long S = 0;
+    if (a < gamma) {
+      const float* qa = q + (size_t)a * V;
+      unsigned long long loc = 0;
+      for (int j = threadIdx.x; j < V; j += blockDim.x) {
+        Wsm[j] = ladder_weight(__fsub_rn(pa[j], qa[j]));
+        loc += Wsm[j];
+      }
+      S = block_reduce(loc, AddU(), us);
+    }
+    if (S == 0) {
+      unsigned long long loc = 0;
+      for (int j = threadIdx.x; j < V; j += blockDim.x) {
+        Wsm[j] = ladder_weight(pa[j]);
+        loc += Wsm[j];
+      }
+      S = block_reduce(loc, AddU(), us);
+    }
+    __syncthreads();
+    const unsigned long long U = (unsigned long long)(unsigned int)(u[gamma] * 16777216.0f);
+    const unsigned long long thr = (U * S) >> 24;
+    token = ladder_find(Wsm, V, thr, us, &found);
+  }
+  if (threadIdx.x == 0) {
+    out_a[0] = a;
+    out_tok[0] = token;
+  }
+}
+
+// Commit: keep = *acc_dev + 1 when acc_dev is given, else keep_host.
+// n_explicit > 0 replaces book->pending_n (bare-book operator use).
+__global__ void commit_kernel(evs_book* book, int keep_host, const int32_t* acc_dev, int n_explicit) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x != 0) return;
+  const int keep = acc_dev ? acc_dev[0] + 1 : keep_host;
+  const int n = n_explicit > 0 ? n_explicit : book->pending_n;
+  if (n <= 0 || keep < 0 || keep > n) {
+    set_status(book, EVS_DEV_BAD_KEEP);
+    book->pending_n = 0;
+    return;
+  }
+  book->fir_bank ^= 1;
+  book->fir_off = keep;
+  if (keep > 0) {
+    book->iir_bank ^= 1;
+    book->iir_slot = keep - 1;
+  }
+  book->pos += keep;
+  book->pending_n = 0;
+}
+
+__global__ void book_set_kernel(evs_book* book, evs_book v) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) *book = v;
+}
+
+}  // namespace
+
+cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, const int32_t* tokens, int n,
+                              int d, int V, float eps, float* X, void* xn, evs_book* book) {
+  if (dtype == EVS_BF16)
+    return launch(L, embed_norm_kernel<bf16>, dim3(n), dim3(512), 0, (const bf16*)E, tokens, n, d, V, eps, X,
+                  (bf16*)xn, book);
+  return launch(L, embed_norm_kernel<float>, dim3(n), dim3(512), 0, (const float*)E, tokens, n, d, V, eps, X,
+                (float*)xn, book);
+}
+
+cudaError_t launch_residual_norm(const LaunchCtx& L, int dtype, const Partials& P, float* X, int n, int d,
+                                 float eps, void* xn) {
+  if (dtype == EVS_BF16)
+    return launch(L, residual_norm_kernel<bf16>, dim3(n), dim3(512), 0, P, X, d, eps, (bf16*)xn);
+  return launch(L, residual_norm_kernel<float>, dim3(n), dim3(512), 0, P, X, d, eps, (float*)xn);
+}
+
+cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const Partials& P, int n, int F, void* h) {
+  const dim3 g((F + 255) / 256, n);
+  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, P, F, (bf16*)h);
+  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, P, F, (float*)h);
+}
+
+cudaError_t launch_logits(const LaunchCtx& L, const Partials& P, int n, int V, float* logits) {
+  return launch(L, logits_kernel, dim3((V + 255) / 256, n), dim3(256), 0, P, V, logits);
+}
+
+cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, float T, int top_k, float* p) {
+  const size_t smem = sizeof(float) * 2 * V;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(probs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch(L, probs_kernel, dim3(n), dim3(256), smem, logits, V, T, top_k, p);
+}
+
+cudaError_t launch_accept(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
+                          const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok) {
+  const size_t smem = sizeof(unsigned int) * V;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch(L, accept_kernel, dim3(1), dim3(256), smem, p, q, drafts, u, n, V, mode, acc, tok);
+}
+
+cudaError_t launch_commit(const LaunchCtx& L, evs_book* book, int keep, const int32_t* acc_dev, int n_explicit) {
+  return launch(L, commit_kernel, dim3(1), dim3(32), 0, book, keep, acc_dev, n_explicit);
+}
+
+cudaError_t launch_book_set(const LaunchCtx& L, evs_book* book, evs_book v) {
+  return launch(L, book_set_kernel, dim3(1), dim3(32), 0, book, v);
+}
+
+}  // namespace evs

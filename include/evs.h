@@ -1,0 +1,301 @@
+/*
+ * evs.h - C ABI of the block-verify / accept / commit path of lossless
+ * speculative decoding for StripedHyena2-style hybrid models (EvSpark).
+ *
+ * Sources (cited by page and passage):
+ *  [abstract]    "EvSpark: Lossless Speculative Decoding for Hybrid DNA
+ *                Foundation Models", preprint abstract, contribution (i):
+ *                block-verification forward pass + per-position state-slicing
+ *                rollback over FIR windows, IIR recurrences and KV caches,
+ *                with zero recomputation; exact rejection-sampling verify.
+ *  [systems]     GitHub discussion "EvSpark: ~3x lossless speculative decoding
+ *                for Evo2 7B with hybrid-state rollback", "The systems
+ *                problem": KV caches append-only, FIR states fixed-length
+ *                sliding windows, IIR states recurrent over the whole prefix.
+ *  [implemented] same post, "What we implemented": keep the intermediate
+ *                state of every block position, slice to the accepted
+ *                boundary once the verifier decides.
+ *  [prereq1]     same discussion, author's reply, prerequisite 1: the
+ *                per-position FIR/IIR state of all gamma+1 candidates.
+ *  [library]     model card "EvSpark - lossless speculative decoding for
+ *                Evo2", "Library" / "Quickstart": generate / generate_native,
+ *                greedy, T = 1.0, top_k = 4, decode-time gamma' <= gamma.
+ *
+ * Conventions
+ *  - Every function returns EVS_OK (0) or an EVS_ERR_* code; the message of
+ *    the last failure on the calling thread is evs_last_error().
+ *  - Pointers named *_dev are device pointers (cudaMalloc'd or equivalent,
+ *    16-byte aligned); *_host are host pointers.  Inputs and outputs are
+ *    owned by the caller; evs_model / evs_state buffers by the library.
+ *  - Work is enqueued on the caller's stream and returns without waiting,
+ *    unless a function says "synchronous".
+ *  - Storage dtype (EVS_BF16 / EVS_F32) applies to weights, GEMM inputs and
+ *    the KV cache; residual stream, filter state, logits and probabilities
+ *    are always float32.
+ *  - In-kernel checks never trap: they set bits of the state's device status
+ *    word (EVS_DEV_*), skip the offending access, and evs_state_check()
+ *    reports them.
+ */
+#ifndef EVS_H
+#define EVS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes */
+enum {
+  EVS_OK = 0,
+  EVS_ERR_ARG = 1,         /* bad argument (null, range, alignment, shape) */
+  EVS_ERR_STATE = 2,       /* protocol misuse: commit without a pending verify, verify while one is pending */
+  EVS_ERR_CAPACITY = 3,    /* committed length + n > ctx_max */
+  EVS_ERR_OOM = 4,         /* device allocation failed */
+  EVS_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed */
+  EVS_ERR_DEVICE = 6,      /* an in-kernel check fired (see EVS_DEV_*) */
+  EVS_ERR_UNSUPPORTED = 7  /* shape the kernels do not handle (message says why) */
+};
+
+/* bits of evs_book.status */
+enum {
+  EVS_DEV_BAD_TOKEN = 1,   /* a token id outside [0, vocab) */
+  EVS_DEV_KV_OVERFLOW = 2, /* an append past ctx_max */
+  EVS_DEV_BAD_KEEP = 4,    /* commit keep outside [0, pending n] */
+  EVS_DEV_TIMEOUT = 8      /* a bounded pipeline wait gave up */
+};
+
+enum { EVS_F32 = 0, EVS_BF16 = 1 };
+enum { EVS_LAYER_FIR = 0, EVS_LAYER_IIR = 1, EVS_LAYER_ATTN = 2 };
+enum { EVS_GREEDY = 0, EVS_SAMPLE = 1 };
+
+/* ---------------------------------------------------------------- model */
+/* Shape of the hybrid stack.  Layer i is
+ *   EVS_LAYER_FIR  : Hyena mixer with an explicit causal filter of length
+ *                    layer_param[i] (short / medium FIR, [systems]);
+ *   EVS_LAYER_IIR  : Hyena mixer with a modal IIR filter of layer_param[i]
+ *                    diagonal complex poles (1..32) ([systems]);
+ *   EVS_LAYER_ATTN : multi-head attention with rotary embedding over an
+ *                    append-only KV cache; layer_param ignored.
+ * Each layer is  x += Mixer(RMSNorm(x)); x += MLP(RMSNorm(x)), with
+ * Hyena  [a|b|v] = W_in xn, z = b*v, y = h (*) z, out = W_out (a*y);
+ * MLP    W_down (silu(W_gate xn) * W_up xn); head logits = W_lm RMSNorm(x).
+ * bf16 storage needs d_model, 2*d_ffn, vocab multiples of 128 and
+ * d_model, d_ffn multiples of 64; f32 storage has no such limit.        */
+typedef struct evs_config {
+  int32_t vocab;
+  int32_t d_model;
+  int32_t n_layers;
+  int32_t n_heads;
+  int32_t head_dim;       /* even; n_heads * head_dim == d_model when any attention layer exists */
+  int32_t d_ffn;
+  int32_t gamma_max;      /* verify blocks hold n <= gamma_max + 1 <= 16 tokens */
+  int32_t dtype;          /* EVS_BF16 or EVS_F32 */
+  int32_t attn_chunk;     /* keys per split-KV chunk, multiple of 32 (e.g. 256) */
+  float rope_base;        /* e.g. 10000 */
+  float norm_eps;         /* e.g. 1e-6 */
+  const int32_t* layer_kind_host;   /* [n_layers] EVS_LAYER_* */
+  const int32_t* layer_param_host;  /* [n_layers] */
+} evs_config;
+
+/* Device weights, row-major [out][in] in the storage dtype; caller-owned,
+ * must stay valid until evs_model_destroy.
+ *  w_in   [3*d][d]   rows a|b|v (Hyena) or q|k|v (attention, heads contiguous)
+ *  w_out  [d][d]
+ *  w_gu   [2*F][d]   rows 0..F-1 gate, F..2F-1 up
+ *  w_down [d][F]
+ *  fir_taps    float32 [L][d]; tap j multiplies z_{t-j}
+ *  iir_lambda  float32 [d][M][2] complex poles (re, im)
+ *  iir_residue float32 [d][M][2] complex residues                          */
+typedef struct evs_layer_weights {
+  const void* w_in;
+  const void* w_out;
+  const void* w_gu;
+  const void* w_down;
+  const float* fir_taps;
+  const float* iir_lambda;
+  const float* iir_residue;
+} evs_layer_weights;
+
+typedef struct evs_weights {
+  const void* embed;                  /* [vocab][d] */
+  const void* lm_head;                /* [vocab][d] */
+  const evs_layer_weights* layers_host; /* [n_layers], read during create only */
+} evs_weights;
+
+typedef struct evs_model evs_model;
+typedef struct evs_state evs_state;
+
+/* Creates a model on the current device; builds TMA descriptors for the
+ * bf16 weights.  Returns EVS_ERR_UNSUPPORTED for shapes the kernels lack. */
+int evs_model_create(const evs_config* cfg, const evs_weights* w, evs_model** out);
+int evs_model_destroy(evs_model* m);
+
+/* ---------------------------------------------------------------- state */
+/* Device-resident bookkeeping of one decoding state.  FIR windows and IIR
+ * states live in two banks per layer: a verify reads the current bank and
+ * writes its per-position results to the other; commit flips banks and
+ * moves offsets, so slicing copies nothing ([implemented]).              */
+typedef struct evs_book {
+  int32_t pos;        /* committed tokens = valid KV rows = next position */
+  int32_t fir_bank;   /* bank holding the current FIR windows */
+  int32_t fir_off;    /* window = rows [fir_off, fir_off + L - 1) of that bank */
+  int32_t iir_bank;   /* bank holding the current IIR states */
+  int32_t iir_slot;   /* slot within that bank, -1 = the zero initial state */
+  int32_t pending_n;  /* block size awaiting commit, 0 if none */
+  int32_t status;     /* EVS_DEV_* bits */
+  int32_t reserved;
+} evs_book;
+
+/* Per-layer state buffers (device pointers owned by the state):
+ *  FIR : fir_ext[b]  float32 [L-1+n_max][d]  - window followed by block z
+ *  IIR : iir_all[b]  float32 [n_max][d][M][2] - state after each block position
+ *  ATTN: k_cache, v_cache [H][ctx_max][Dh] storage dtype (head-major, so a
+ *        head's keys stream contiguously)                               */
+typedef struct evs_layer_view {
+  int32_t kind, param;
+  float* fir_ext[2];
+  float* iir_all[2];
+  void* k_cache;
+  void* v_cache;
+  int64_t ctx_max;
+  int32_t n_max;
+} evs_layer_view;
+
+/* Allocates all state for up to ctx_max positions (KV caches for attention
+ * layers, two FIR / IIR banks per Hyena layer, activations, workspaces) and
+ * resets it.  Synchronous. */
+int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out);
+int evs_state_destroy(evs_state* s);
+/* Zero windows / states, empty caches, position 0.  Enqueued on stream. */
+int evs_state_reset(evs_state* s, cudaStream_t stream);
+/* Copies every buffer and the bookkeeping of src into dst (same model and
+ * ctx_max): the snapshot of snapshot-and-replay rollback ([abstract]). */
+int evs_state_clone(const evs_state* src, evs_state* dst, cudaStream_t stream);
+int evs_state_layer_view(const evs_state* s, int32_t layer, evs_layer_view* out);
+/* Device address of the bookkeeping (for graph-captured callers). */
+int evs_state_book_dev(const evs_state* s, evs_book** out);
+/* Synchronous read / write of the bookkeeping (tests, synthesised states).
+ * A write also updates the host's copy of pos and pending_n. */
+int evs_state_book_read(const evs_state* s, evs_book* out_host, cudaStream_t stream);
+int evs_state_book_write(evs_state* s, const evs_book* in_host, cudaStream_t stream);
+/* Synchronous: waits for the stream, returns EVS_ERR_DEVICE if any
+ * EVS_DEV_* bit is set (status copied to *status_host when non-null). */
+int evs_state_check(evs_state* s, cudaStream_t stream, int32_t* status_host);
+/* Capture verify / commit sequences in CUDA graphs (default on). */
+int evs_state_use_graphs(evs_state* s, int32_t enable);
+
+/* ---------------------------------------------------------------- path */
+/* Block verify ([abstract] (i); [implemented]; [prereq1]).
+ * tokens_dev int32 [n]: the pending token followed by n-1 drafts.
+ * Writes logits_dev float32 [n][vocab], row i scoring the token after
+ * tokens[i].  Every layer keeps the state after each block position:
+ * FIR ext rows, IIR per-position states, KV rows pos..pos+n-1.  n = 1 is
+ * native decoding.  1 <= n <= gamma_max+1; EVS_ERR_STATE if a verify is
+ * pending; EVS_ERR_CAPACITY if pos + n > ctx_max (pos as known to the host:
+ * after evs_commit_dev the device checks and sets EVS_DEV_KV_OVERFLOW). */
+int evs_verify_block(evs_state* s, const int32_t* tokens_dev, int32_t n,
+                     float* logits_dev, cudaStream_t stream);
+
+/* Target distribution ([library]: T, top_k).  logits_dev [n][V] ->
+ * p_dev [n][V]: softmax of logits / T over the top_k largest entries of each
+ * row (ties to the lower index), zero elsewhere; top_k <= 0 or >= V keeps
+ * all.  T > 0. */
+int evs_probs(const float* logits_dev, int32_t n, int32_t V, float T,
+              int32_t top_k, float* p_dev, cudaStream_t stream);
+
+/* Accept rule ([abstract]: exact rejection-sampling verification; greedy
+ * equality with native decoding).  n = gamma + 1 >= 1 block rows.
+ *  p_dev  [n][V]   target rows (greedy: any scores, e.g. logits)
+ *  q_dev  [n-1][V] drafter distributions (unused in greedy mode)
+ *  drafts_dev int32 [n-1], u_dev float32 [n] uniforms in [0,1) (unused greedy)
+ * Draft i (1-based) is accepted iff  greedy: d_i == argmax p_{i-1} (lowest
+ * index on ties); sample: u_{i-1} * q_i(d_i) < p_{i-1}(d_i) in float32.
+ * At the first rejection a = i-1 and the output token is argmax p_a /
+ * sample((p_a - q_{a+1})^+, u_{n-1}) (falls back to p_a if that residual has
+ * no integer mass); if all accepted a = n-1 and the token is argmax p_a /
+ * sample(p_a, u_{n-1}).  sample(w,u) is the inverse CDF over integer weights
+ * floor(w_j 2^24): exact and independent of summation order.
+ * Writes out_accepted_dev[0] = a and out_token_dev[0] = token. */
+int evs_accept(const float* p_dev, const float* q_dev, const int32_t* drafts_dev,
+               const float* u_dev, int32_t n, int32_t V, int32_t mode,
+               int32_t* out_accepted_dev, int32_t* out_token_dev, cudaStream_t stream);
+
+/* Commit ([abstract] (i): per-position state slicing with zero
+ * recomputation).  keep in [0, n] tokens of the pending block are consumed:
+ * FIR window <- ext rows [keep, keep+L-1); IIR state <- state after block
+ * position keep-1 (keep = 0: unchanged); KV length, position += keep.
+ * Bank flips only - no data is copied.  EVS_ERR_STATE without a pending
+ * verify; EVS_ERR_ARG if keep is out of range. */
+int evs_commit(evs_state* s, int32_t keep, cudaStream_t stream);
+/* Same with keep = accepted_dev[0] + 1 read on the device (the output of
+ * evs_accept), so a verify-accept-commit round needs no host round trip and
+ * can be graph-captured.  A keep outside [0, n] sets EVS_DEV_BAD_KEEP and
+ * leaves the state as before the verify. */
+int evs_commit_dev(evs_state* s, const int32_t* accepted_dev, cudaStream_t stream);
+
+/* One round as a single graph launch: verify(tokens) -> logits; probs (if
+ * mode == EVS_SAMPLE) -> p; accept -> accepted, token; commit_dev.  p_dev
+ * may be null in greedy mode. */
+int evs_round(evs_state* s, const int32_t* tokens_dev, int32_t n, float* logits_dev,
+              float* p_dev, const float* q_dev, const float* u_dev, float T, int32_t top_k,
+              int32_t mode, int32_t* out_accepted_dev, int32_t* out_token_dev,
+              cudaStream_t stream);
+
+/* ---------------------------------------------------------------- operators
+ * Single-operator entry points over caller-owned buffers: the same kernels
+ * the model path runs, with the mixer input given as a plain matrix instead
+ * of GEMM partial sums.  For operator-level parity and timing.            */
+
+/* Hyena FIR mixer for one block ([systems], [prereq1]).
+ * abv_dev [n][3d] storage dtype (a|b|v), taps [L][d], ext banks
+ * [L-1+n_max][d] float32, book_dev: fir_bank / fir_off / pos are read,
+ * nothing written.  Writes g_dev [n][d] storage dtype = a * (h (*) (b*v))
+ * and ext rows [0, L-1+n) of bank 1-fir_bank.  Needs d % 32 == 0. */
+int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_t dtype,
+               const void* abv_dev, const float* taps_dev, float* ext0_dev, float* ext1_dev,
+               const evs_book* book_dev, void* g_dev, cudaStream_t stream);
+/* Hyena modal IIR mixer for one block.  State banks [n_max][d][M][2];
+ * reads the state at (iir_bank, iir_slot), writes the n per-position states
+ * to slots 0..n-1 of bank 1-iir_bank.  M must be a power of two <= 32 and
+ * d * M a multiple of 256. */
+int evs_op_iir(int32_t M, int32_t d, int32_t n, int32_t n_max, int32_t dtype,
+               const void* abv_dev, const float* lambda_dev, const float* residue_dev,
+               float* st0_dev, float* st1_dev, const evs_book* book_dev, void* g_dev,
+               cudaStream_t stream);
+/* Block-causal attention for one block: qkv_dev [n][3*H*Dh] (q|k|v, heads
+ * contiguous) storage dtype; caches [H][ctx_max][Dh]; Dh in {32, 64, 128};
+ * rotary embedding at positions pos..pos+n-1,
+ * k/v appended to the caches at those rows, query i attends rows
+ * 0..pos+i.  Writes g_dev [n][H*Dh].  scratch: evs_op_attention_scratch_bytes. */
+size_t evs_op_attention_scratch_bytes(int32_t H, int32_t Dh, int64_t ctx_max, int32_t chunk, int32_t n_max);
+int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max, int64_t ctx_max,
+                     int32_t chunk, float rope_base, int32_t dtype, const void* qkv_dev,
+                     void* k_cache_dev, void* v_cache_dev, evs_book* book_dev, void* g_dev,
+                     void* scratch_dev, size_t scratch_bytes, cudaStream_t stream);
+/* Commit on a bare book after an operator call on a block of n tokens:
+ * keep in [0, n]; flips the FIR / IIR banks and advances pos as evs_commit
+ * does. */
+int evs_op_commit(evs_book* book_dev, int32_t keep, int32_t n, cudaStream_t stream);
+/* Skinny GEMM Y[n][N] = X[n][K] W^T (weight-streaming path; tensor cores
+ * for bf16).  W [N][K], X [n][K] storage dtype, n <= 16; Y float32.
+ * scratch: evs_op_gemm_scratch_bytes. */
+size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype);
+int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
+                int32_t dtype, float* y_dev, void* scratch_dev, size_t scratch_bytes,
+                cudaStream_t stream);
+
+/* ---------------------------------------------------------------- misc */
+const char* evs_last_error(void);
+const char* evs_version(void);
+/* Number of kernels the library enqueued since load (all entry points). */
+int64_t evs_kernel_launches(void);
+/* Kernels one evs_verify_block(n) enqueues on this state (graph nodes). */
+int32_t evs_verify_kernel_count(const evs_state* s, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EVS_H */

@@ -283,6 +283,25 @@ def synth_state(shape: ModelShape, seed: int, P: int, ctx_max: Optional[int] = N
     return out
 
 
+def mixer_params(seed: int, kind: str, param: int, d: int, pole_mag=(0.9, 0.999),
+                 residue_std: float = 0.25) -> dict:
+    """Filter parameters of one Hyena layer with the recipe of make_weights:
+    FIR taps [L][d] ~ N(0, 1/sqrt(L)); IIR poles / residues [d][M] complex64."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 8])))
+    if kind in (SE, MR):
+        return {"taps": _normal_f32(g, (param, d), 1.0 / np.sqrt(param))}
+    lam, res = _poles(g, d, param, pole_mag, residue_std)
+    return {"lam": lam, "res": res}
+
+
+def layer_state(seed: int, kind: str, param: int, d: int, P: int = 0, n_heads: int = 0,
+                head_dim: int = 0, dtype: str = "bf16") -> dict:
+    """Synthesised state of one layer with the recipe of synth_state."""
+    shape = ModelShape(name="one", vocab=1, d_model=d, layers=[(kind, param)], n_heads=n_heads,
+                       head_dim=head_dim, d_ffn=1, gamma=0, dtype=dtype)
+    return synth_state(shape, seed, P)["layers"][0]
+
+
 def abv_block(seed: int, n: int, d: int, dtype: str = "bf16") -> np.ndarray:
     """Mixer inputs for an operator-level test: [n][3d] ~ N(0, 1) (a | b | v)."""
     ss = np.random.SeedSequence([seed, 7])

@@ -1,0 +1,52 @@
+"""Helpers for the -m gpu parity tests (no test functions here)."""
+import numpy as np
+
+BF16 = "<i2"
+
+
+def torch():
+    import torch as t
+    return t
+
+
+class _CAI:
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def wrap(ptr, shape, typestr="<f4"):
+    """Zero-copy torch view of library-owned device memory."""
+    t = torch()
+    return t.as_tensor(_CAI(ptr, shape, typestr), device="cuda")
+
+
+def to_np(t_):
+    t = torch()
+    if t_.dtype == t.bfloat16:
+        return (t_.contiguous().view(t.int16).cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return t_.detach().cpu().numpy()
+
+
+def up(a, dtype=None):
+    """numpy -> cuda tensor; uint16 arrays are bf16 bit patterns."""
+    t = torch()
+    if a.dtype == np.uint16:
+        return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(t.bfloat16)
+    if np.iscomplexobj(a):
+        return t.from_numpy(np.ascontiguousarray(a.astype(np.complex64)).view(np.float32)).cuda()
+    return t.from_numpy(np.ascontiguousarray(a, dtype=dtype or a.dtype)).cuda()
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+def book_zero(t):
+    """A device evs_book at position 0 (iir_slot = -1)."""
+    b = t.zeros(8, dtype=t.int32, device="cuda")
+    b[4] = -1
+    return b
