@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of the block-verify / accept / commit round at gamma = 12.
+
+Workload: the 7B-shaped random-init hybrid stack (32 layers, d_model 4096,
+gated MLP 11008, FIR-short / FIR-medium / IIR with attention every 6th
+layer, vocab 512, bf16 weights ~13 GB), a 1024-token ACGT prompt, greedy
+decoding with the identity drafter (drafts = the target's own native greedy
+continuation, precomputed on the GPU outside the timed region, as in the
+identity-drafter measurement of the EvSpark discussion post).
+
+One step = one round: block verify of 13 tokens (pending + 12 drafts),
+accept, commit - all in one CUDA graph on one stream.  Metric: accepted
+tokens per second (emitted tokens / summed round time; drafter excluded),
+plus verify-round latency and HBM bandwidth against the roofline.
+
+Inputs (weights 13 GB, KV) are larger than L2, so no flush is needed.
+Under torchrun every rank runs an independent replica (the path does not
+shard); value = all ranks' tokens / the slowest rank's time.
+
+--impl reference times the CPU oracle (test infrastructure) on the host
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "accepted tok/s at gamma=12 (block verify + accept + commit, identity drafter, greedy)"
+UNIT = "tok/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="evs", choices=["evs", "reference"])
+    ap.add_argument("--prompt", type=int, default=1024)
+    ap.add_argument("--seed", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ ranks
+def dist_setup(gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.lines, self.proc = gpu, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def step_bytes(shape, P, n):
+    """Bytes one verify round must move: weights once, each mixer's state
+    read + retained per-position state written, KV read + append, logits."""
+    d, F, V, es = shape.d_model, shape.d_ffn, shape.vocab, 2
+    H, Dh = shape.n_heads, shape.head_dim
+    b = (4 * d * d + 3 * d * F) * es * len(shape.layers) + V * d * es + n * d * es + n * V * 4
+    for kind, prm in shape.layers:
+        if kind in ("SE", "MR"):
+            b += (prm - 1) * d * 4 + (prm - 1 + n) * d * 4 + prm * d * 4
+        elif kind == "LI":
+            b += prm * d * 8 * 3 + n * prm * d * 8
+        else:
+            b += (P + n) * H * Dh * es * 2 + n * H * Dh * es * 2
+    return b
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_tokens_per_s(shape, W, seed, P, steps, warm=1):
+    """The CPU oracle (fp32 with bf16 storage points) on a bounded sample:
+    `steps` native steps from a synthesised state at context P."""
+    import synth
+    from oracle.model import Model as OModel
+    from oracle.numerics import Arith
+    om = OModel(shape, synth.weights_f32(W), Arith(np.float32, bf16_points=True))
+    S = synth.synth_state(shape, seed, P)
+    S["layers"] = [dict(L, k=None if L["k"] is None else synth.bf16_bits_to_f32(L["k"]),
+                        v=None if L["v"] is None else synth.bf16_bits_to_f32(L["v"])) for L in S["layers"]]
+    st = om.state_from(S, P + warm + steps + 1)
+    toks = [int(x) for x in synth.prompt(shape, seed, warm + steps)]
+    for t in toks[:warm]:
+        om.step(st, t)
+    t0 = time.perf_counter()
+    for t in toks[warm:]:
+        om.step(st, t)
+    dt = time.perf_counter() - t0
+    return steps / dt, dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import synth
+    shape = synth.stack_7b()
+    W = synth.make_weights(shape, args.seed)
+    tps, dt = oracle_tokens_per_s(shape, W, args.seed, args.prompt, args.steps, warm=args.warmup)
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "7B-shaped hybrid stack, gamma=12, context 1024",
+                       "note": "one step = one oracle native step (1 of a round's 13 positions)"},
+            "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} oracle native steps after {args.warmup} warm-up, "
+                                       f"fp32 with bf16 storage points, context {args.prompt}"},
+            "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_evs(args, rank, world, local):
+    import torch
+
+    import hybrid_ssm_attention_gb300 as evs
+    import synth
+    from hybrid_ssm_attention_gb300 import build as _build
+    _build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    shape = synth.stack_7b()
+    n = shape.n_block
+    P0 = args.prompt
+    rounds = args.warmup + args.steps
+    ctx = P0 + n * rounds + 2 * n
+    W = synth.make_weights(shape, args.seed)
+    model = evs.Model(shape, W)
+    st = evs.State(model, ctx)
+    prompt = [int(x) for x in synth.prompt(shape, args.seed, P0)]
+
+    # prefill prompt[:-1] in blocks of n, committing each block
+    lg = torch.empty((n, shape.vocab), dtype=torch.float32, device=dev)
+    for s0 in range(0, P0 - 1, n):
+        blk = torch.tensor(prompt[s0:min(s0 + n, P0 - 1)], dtype=torch.int32, device=dev)
+        evs.evs_verify_block(st, blk, blk.numel(), lg[:blk.numel()])
+        evs.evs_commit(st, blk.numel())
+    snap = evs.State(model, ctx)
+    st.clone_into(snap)
+    torch.cuda.synchronize()
+
+    # native greedy decoding (n = 1 rounds): the identity drafter's tokens
+    n_nat = n * rounds + 1
+    y = torch.empty(n_nat + 1, dtype=torch.int32, device=dev)
+    y[0] = prompt[-1]
+    tok1 = torch.empty(1, dtype=torch.int32, device=dev)
+    lg1 = torch.empty((1, shape.vocab), dtype=torch.float32, device=dev)
+    acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    otok = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok1.copy_(y[:1])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(n_nat):
+        if i == 16:
+            e0.record()
+        evs.evs_round(st, tok1, 1, lg1, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
+        tok1.copy_(otok)
+        y[i + 1:i + 2].copy_(otok)
+    e1.record()
+    torch.cuda.synchronize()
+    native_step_ms = e0.elapsed_time(e1) / (n_nat - 16)
+
+    # speculative rounds from the post-prompt state: block r = y[n r : n r + n]
+    snap.clone_into(st)
+    blocks = y[: n * rounds].view(rounds, n).contiguous()
+    tokens = torch.empty(n, dtype=torch.int32, device=dev)
+    acc_log = torch.zeros(rounds, dtype=torch.int32, device=dev)
+    launches0 = None
+    clocks = ClockSampler(local).start()
+    for r in range(rounds):
+        if r == args.warmup:
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            launches0 = evs.evs_kernel_launches()
+            torch.cuda.nvtx.range_push("timed")
+            e0.record()
+        tokens.copy_(blocks[r])
+        evs.evs_round(st, tokens, n, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
+        acc_log[r:r + 1].copy_(acc)
+    e1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    launches = evs.evs_kernel_launches() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    t_ms = e0.elapsed_time(e1)
+    t_max_ms = reduce_max(t_ms, world)
+    accepted = acc_log.cpu().numpy()
+    book = st.book()
+    ok = bool((accepted == n - 1).all()) and book["pos"] == P0 - 1 + n * rounds
+    emitted = float(np.sum(accepted[args.warmup:] + 1))
+    total_tokens = reduce_sum(emitted, world)
+    value = total_tokens / (t_max_ms / 1e3)
+    ms_per_step = t_ms / args.steps
+
+    # dominant kernel: the weight-streaming GEMM, every launch of one step timed alone
+    ms, by = evs.evs_profile_gemms(st, n)
+    peak, peak_src = load_peaks()
+    g_bytes, g_ms = float(sum(by)), float(sum(ms))
+    achieved = g_bytes / (g_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "gemm_tc_kernel", "launches": len(ms),
+                "avg_launch_us": 1e3 * g_ms / len(ms), "bytes_per_launch": g_bytes / len(ms),
+                "peak_source": peak_src}
+    sb = step_bytes(shape, P0 - 1 + n * (args.warmup + args.steps // 2), n)
+
+    # end to end through the C ABI with host buffers (pinned), result read back every round
+    e2e = None
+    if not args.no_e2e:
+        snap.clone_into(st)
+        host_blocks = blocks.cpu().pin_memory()
+        acc_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+        tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+        emitted_e2e = 0
+        for r in range(rounds):
+            if r == args.warmup:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            tokens.copy_(host_blocks[r], non_blocking=True)
+            evs.evs_round(st, tokens, n, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
+            acc_h.copy_(acc, non_blocking=True)
+            tok_h.copy_(otok, non_blocking=True)
+            stream.synchronize()
+            if r >= args.warmup:
+                emitted_e2e += int(acc_h.item()) + 1
+        dt = time.perf_counter() - t0
+        e2e = {"value": reduce_sum(emitted_e2e, world) / reduce_max(dt, world), "unit": UNIT,
+               "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 8}
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        st.close()
+        snap.close()
+        model.close()
+        torch.cuda.empty_cache()
+        tps, dt = oracle_tokens_per_s(shape, W, args.seed, P0, args.cpu_steps)
+        cpu = {"value": tps, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{args.cpu_steps} oracle native steps (1 token each) of the same stack at context "
+                         f"{P0}, fp32 with bf16 storage points, after 1 warm-up step"}
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "7B-shaped hybrid stack: 32 layers (FIR7/FIR128/IIR16, attention every 6th), "
+                                   "d_model 4096, MLP 11008, vocab 512, bf16 weights 12.96 GB; 1024-token ACGT "
+                                   "prompt; gamma=12; identity drafter, greedy",
+                       "gamma": 12, "context_start": P0, "generated_tokens": n * rounds,
+                       "l2": "inputs larger than L2 (13 GB of weights per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "verify_round_us": 1e3 * ms_per_step,
+            "native_step_us": 1e3 * native_step_ms,
+            "identity_overhead": ms_per_step / (n * native_step_ms),
+            "all_accepted": ok,
+            "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms_per_step / 1e3) / 1e9,
+                         "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_evs(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

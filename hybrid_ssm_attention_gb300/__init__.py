@@ -18,7 +18,7 @@ from . import _abi
 from ._abi import (EVS_BF16, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN, EVS_LAYER_FIR,  # noqa: F401
                    EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
 
-__all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_probs", "evs_accept",
+__all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
            "evs_commit", "evs_commit_dev", "evs_round", "evs_op_fir", "evs_op_iir",
            "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_kernel_launches"]
 
@@ -194,6 +194,11 @@ def evs_verify_block(state: State, tokens, n: int, logits, stream=None):
            "evs_verify_block")
 
 
+def evs_verify_block_trace(state: State, tokens, n: int, logits, x_trace, stream=None):
+    _check(lib().evs_verify_block_trace(state.handle, _ptr(tokens), int(n), _ptr(logits), _ptr(x_trace),
+                                        _stream(stream)), "evs_verify_block_trace")
+
+
 def evs_probs(logits, n: int, V: int, T: float, top_k: int, p, stream=None):
     _check(lib().evs_probs(_ptr(logits), int(n), int(V), float(T), int(top_k), _ptr(p), _stream(stream)),
            "evs_probs")
@@ -256,3 +261,18 @@ def evs_op_gemm(w, x, N, K, n, dtype, y, scratch, stream=None):
 
 def evs_kernel_launches() -> int:
     return int(lib().evs_kernel_launches())
+
+
+def evs_verify_kernel_count(state: State, n: int) -> int:
+    return int(lib().evs_verify_kernel_count(state.handle, int(n)))
+
+
+def evs_profile_gemms(state: State, n: int, stream=None):
+    """Per-launch (ms, algorithmic bytes) of one verify step's weight GEMMs."""
+    cap = 4 * len(state.model.shape.layers) + 1
+    ms = (C.c_float * cap)()
+    by = (C.c_int64 * cap)()
+    cnt = C.c_int32()
+    _check(lib().evs_profile_gemms(state.handle, int(n), ms, by, cap, C.byref(cnt), _stream(stream)),
+           "evs_profile_gemms")
+    return [float(ms[i]) for i in range(cnt.value)], [int(by[i]) for i in range(cnt.value)]

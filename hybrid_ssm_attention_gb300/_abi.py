@@ -68,6 +68,7 @@ PROTOTYPES = {
     "evs_state_check": (i32, [vp, vp, C.POINTER(i32)]),
     "evs_state_use_graphs": (i32, [vp, i32]),
     "evs_verify_block": (i32, [vp, vp, i32, vp, vp]),
+    "evs_verify_block_trace": (i32, [vp, vp, i32, vp, vp, vp]),
     "evs_probs": (i32, [vp, i32, i32, f32, i32, vp, vp]),
     "evs_accept": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]),
     "evs_commit": (i32, [vp, i32, vp]),
@@ -80,6 +81,7 @@ PROTOTYPES = {
     "evs_op_commit": (i32, [vp, i32, i32, vp]),
     "evs_op_gemm_scratch_bytes": (sz, [i32, i32, i32]),
     "evs_op_gemm": (i32, [vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]),
+    "evs_profile_gemms": (i32, [vp, i32, C.POINTER(C.c_float), C.POINTER(i64), i32, C.POINTER(i32), vp]),
     "evs_last_error": (C.c_char_p, []),
     "evs_version": (C.c_char_p, []),
     "evs_kernel_launches": (i64, []),

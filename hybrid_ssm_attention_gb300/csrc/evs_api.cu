@@ -137,7 +137,8 @@ int dmalloc(evs_state* s, void** p, size_t bytes) {
 }
 
 // ------------------------------------------------------------------ verify sequence
-int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc) {
+int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc,
+                   float* trace = nullptr) {
   evs_model* m = s->m;
   const evs_config& c = m->cfg;
   const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
@@ -154,7 +155,9 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     *out = P;
     return EVS_OK;
   };
+  const size_t xbytes = sizeof(float) * (size_t)n * d;
   CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, n, d, V, eps, s->X, s->xn, s->book));
+  if (trace) CUDA_TRY(cudaMemcpyAsync(trace, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
     LayerS& st = s->S[i];
@@ -175,6 +178,8 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     CUDA_TRY(launch_mlp_act(Lc, dt, P, n, F, s->h));
     EVS_TRY(gemm(m->p_down, w.m_down, w.w_down, s->m_h, s->h, F, &P));
     CUDA_TRY(launch_residual_norm(Lc, dt, P, s->X, n, d, eps, s->xn));
+    if (trace)
+      CUDA_TRY(cudaMemcpyAsync(trace + (i + 1) * (size_t)n * d, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   }
   Partials P;
   EVS_TRY(gemm(m->p_head, m->m_head, m->head, s->m_xn, s->xn, d, &P));
@@ -601,6 +606,16 @@ extern "C" int evs_verify_block(evs_state* s, const int32_t* tokens, int32_t n, 
   return EVS_OK;
 }
 
+extern "C" int evs_verify_block_trace(evs_state* s, const int32_t* tokens, int32_t n, float* logits,
+                                      float* x_trace, cudaStream_t stream) {
+  if (!s || !tokens || !logits || !x_trace) return fail(EVS_ERR_ARG, "null argument");
+  EVS_TRY(check_block(s, n));
+  LaunchCtx Lc{stream, false};
+  EVS_TRY(enqueue_verify(s, tokens, n, logits, Lc, x_trace));
+  s->host_pending = n;
+  return EVS_OK;
+}
+
 extern "C" int evs_probs(const float* logits, int32_t n, int32_t V, float T, int32_t top_k, float* p,
                          cudaStream_t stream) {
   if (!logits || !p) return fail(EVS_ERR_ARG, "null argument");
@@ -769,6 +784,57 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
   }
   CUDA_TRY(launch_logits(Lc, P, n, N, Y));
   return EVS_OK;
+}
+
+// =================================================================== profiling
+extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host, int32_t max_launches,
+                                 int32_t* count, cudaStream_t stream) {
+  if (!s || !ms_host || !bytes_host || !count) return fail(EVS_ERR_ARG, "null argument");
+  if (n < 1 || n > s->m->n_max) return fail(EVS_ERR_ARG, "n out of range");
+  const evs_model* m = s->m;
+  const int nl = (int)m->L.size();
+  const int total = 4 * nl + 1;
+  if (max_launches < total) return fail(EVS_ERR_ARG, "need room for %d launches", total);
+  const evs_config& c = m->cfg;
+  const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
+  const size_t es = esize(dt);
+  std::vector<cudaEvent_t> ev(total + 1);
+  for (auto& e : ev) CUDA_TRY(cudaEventCreate(&e));
+  LaunchCtx Lc{stream, false};
+  // keep the GPU busy while the host enqueues, so events time only the GEMMs
+  CUDA_TRY(launch_busy(Lc, 2000000));
+  int k = 0;
+  int r = EVS_OK;
+  auto one = [&](const Partials& plan, const CUtensorMap& wm, const void* W, const CUtensorMap& xm, const void* X,
+                 int N, int K) -> int {
+    Partials P = plan;
+    P.ws = s->ws[k & 1];
+    CUDA_TRY(cudaEventRecord(ev[k], stream));
+    if (m->tc)
+      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, &s->book->status));
+    else
+      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, n, P, K));
+    bytes_host[k] = (int64_t)N * K * es + (int64_t)n * K * es + (int64_t)n * N * 4;
+    ++k;
+    return EVS_OK;
+  };
+  for (int i = 0; i < nl && r == EVS_OK; ++i) {
+    const LayerW& w = m->L[i];
+    r = one(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, 3 * d, d);
+    if (r == EVS_OK) r = one(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, d);
+    if (r == EVS_OK) r = one(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d);
+    if (r == EVS_OK) r = one(m->p_down, w.m_down, w.w_down, s->m_h, s->h, d, F);
+  }
+  if (r == EVS_OK) r = one(m->p_head, m->m_head, m->head, s->m_xn, s->xn, V, d);
+  if (r == EVS_OK) {
+    cudaError_t e = cudaEventRecord(ev[k], stream);
+    if (e == cudaSuccess) e = cudaEventSynchronize(ev[k]);
+    for (int j = 0; j < k && e == cudaSuccess; ++j) e = cudaEventElapsedTime(&ms_host[j], ev[j], ev[j + 1]);
+    if (e != cudaSuccess) r = fail(EVS_ERR_CUDA, "profiling events: %s", cudaGetErrorString(e));
+  }
+  for (auto& e : ev) cudaEventDestroy(e);
+  *count = k;
+  return r;
 }
 
 // =================================================================== misc

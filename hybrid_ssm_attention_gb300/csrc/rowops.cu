@@ -271,6 +271,14 @@ __global__ void commit_kernel(evs_book* book, int keep_host, const int32_t* acc_
   book->pending_n = 0;
 }
 
+// Fixed amount of arithmetic (no memory, no waits) that occupies the stream
+// for a few milliseconds; ends after `iters` iterations whatever happens.
+__global__ void busy_kernel(long long iters, float* sink) {
+  float x = threadIdx.x;
+  for (long long i = 0; i < iters; ++i) x = fmaf(x, 0.999999f, 1e-7f);
+  if (x == -1.f) sink[0] = x;  // never true; keeps the loop
+}
+
 __global__ void book_set_kernel(evs_book* book, evs_book v) {
   pdl_trigger();
   pdl_wait();
@@ -330,6 +338,10 @@ cudaError_t launch_commit(const LaunchCtx& L, evs_book* book, int keep, const in
 
 cudaError_t launch_book_set(const LaunchCtx& L, evs_book* book, evs_book v) {
   return launch(L, book_set_kernel, dim3(1), dim3(32), 0, book, v);
+}
+
+cudaError_t launch_busy(const LaunchCtx& L, long long iters) {
+  return launch(L, busy_kernel, dim3(1), dim3(32), 0, iters, (float*)nullptr);
 }
 
 }  // namespace evs

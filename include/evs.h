@@ -199,6 +199,13 @@ int evs_state_use_graphs(evs_state* s, int32_t enable);
 int evs_verify_block(evs_state* s, const int32_t* tokens_dev, int32_t n,
                      float* logits_dev, cudaStream_t stream);
 
+/* Block verify that also copies the residual stream after the embedding
+ * and after every layer to x_trace_dev float32 [n_layers+1][n][d_model]
+ * (layer-by-layer validation and tracing; runs without graph capture).
+ * Same contract as evs_verify_block otherwise. */
+int evs_verify_block_trace(evs_state* s, const int32_t* tokens_dev, int32_t n,
+                           float* logits_dev, float* x_trace_dev, cudaStream_t stream);
+
 /* Target distribution ([library]: T, top_k).  logits_dev [n][V] ->
  * p_dev [n][V]: softmax of logits / T over the top_k largest entries of each
  * row (ties to the lower index), zero elsewhere; top_k <= 0 or >= V keeps
@@ -286,6 +293,17 @@ size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype);
 int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
                 int32_t dtype, float* y_dev, void* scratch_dev, size_t scratch_bytes,
                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------- profiling */
+/* Times every weight GEMM of one verify step of n tokens (per layer: in,
+ * out, gate/up, down; then the head) with CUDA events around each launch,
+ * on stream; synchronous.  A short fixed-length busy kernel runs ahead so
+ * the events see only GPU time.  ms_host[i] = launch i's duration,
+ * bytes_host[i] = its algorithmic bytes (weights + activations in +
+ * outputs); *count = number of launches (4 * n_layers + 1 <= max_launches).
+ * Uses the state's workspaces; leaves the decoding state unchanged. */
+int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host,
+                      int32_t max_launches, int32_t* count, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- misc */
 const char* evs_last_error(void);

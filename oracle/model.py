@@ -195,32 +195,43 @@ class Model:
         return o.reshape(d)
 
     # ------------------------------------------------------------------ step
+    def embed_token(self, token: int):
+        if not (0 <= int(token) < self.shape.vocab):
+            raise ValueError("token out of range")
+        return self.embed[int(token)].astype(self.ar.dt).copy()
+
+    def layer_forward(self, M, L: LayerState, x, pos: int):
+        """One layer for one token: x + Mixer(RMSNorm(x)), then + MLP(RMSNorm(.)).
+        Updates the layer's state L in place."""
+        sh, ar = self.shape, self.ar
+        d, F, eps = sh.d_model, sh.d_ffn, sh.norm_eps
+        xn = ar.r(rmsnorm(x, eps, ar))
+        u = ar.r(M["w_in"] @ xn)
+        if M["kind"] == ATT:
+            g = ar.r(self.attn_step(M, L, u, pos))
+        else:
+            a, b, v = u[:d], u[d:2 * d], u[2 * d:]
+            z = b * v
+            y = self.fir_step(M, L, z) if M["kind"] in (SE, MR) else self.iir_step(M, L, z)
+            g = ar.r(a * y)
+        x = x + M["w_out"] @ g
+        xn = ar.r(rmsnorm(x, eps, ar))
+        gu = M["w_gu"] @ xn
+        h = ar.r(silu(gu[:F], ar) * gu[F:])
+        return x + M["w_down"] @ h
+
+    def head(self, x):
+        """Final RMSNorm and LM head."""
+        return self.lm_head @ self.ar.r(rmsnorm(x, self.shape.norm_eps, self.ar))
+
     def step(self, st: State, token: int):
         """One native decode step: consumes ``token`` at position st.pos,
         updates every layer's state in place, returns the logits."""
-        sh, ar = self.shape, self.ar
-        d, F, eps = sh.d_model, sh.d_ffn, sh.norm_eps
-        if not (0 <= int(token) < sh.vocab):
-            raise ValueError("token out of range")
-        x = self.embed[int(token)].astype(ar.dt).copy()
+        x = self.embed_token(token)
         for M, L in zip(self.layers, st.layers):
-            xn = ar.r(rmsnorm(x, eps, ar))
-            u = ar.r(M["w_in"] @ xn)
-            if M["kind"] == ATT:
-                g = ar.r(self.attn_step(M, L, u, st.pos))
-            else:
-                a, b, v = u[:d], u[d:2 * d], u[2 * d:]
-                z = b * v
-                y = self.fir_step(M, L, z) if M["kind"] in (SE, MR) else self.iir_step(M, L, z)
-                g = ar.r(a * y)
-            x = x + M["w_out"] @ g
-            xn = ar.r(rmsnorm(x, eps, ar))
-            gu = M["w_gu"] @ xn
-            h = ar.r(silu(gu[:F], ar) * gu[F:])
-            x = x + M["w_down"] @ h
-        xn = ar.r(rmsnorm(x, eps, ar))
+            x = self.layer_forward(M, L, x, st.pos)
         st.pos += 1
-        return self.lm_head @ xn
+        return self.head(x)
 
     # ------------------------------------------------------------------ block
     def verify(self, st: State, tokens):

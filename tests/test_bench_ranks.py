@@ -1,0 +1,55 @@
+"""Host-side logic of bench.py's multi-replica mode on CPU (gloo, world size 2):
+the step time is the max over ranks, the token count the sum over ranks, and
+rank 0 alone prints."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.reduce_max(10.0 + rank, world)
+    s = bench.reduce_sum(13.0 * (rank + 1), world)
+    bench.barrier(world)
+    q.put((rank, t, s))
+    dist.destroy_process_group()
+
+
+def test_replica_aggregation_gloo():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [11.0, 11.0]
+    assert [r[2] for r in res] == [39.0, 39.0]
+
+
+def test_step_bytes_counts_weights_once():
+    import bench
+    import synth
+    sh = synth.stack_7b()
+    b = bench.step_bytes(sh, 1024, 13)
+    w = 32 * (4 * 4096 * 4096 + 3 * 4096 * 11008) * 2
+    assert w == 12952010752
+    assert 13.0e9 < b < 13.3e9

@@ -133,23 +133,60 @@ def _load_synth_state(evs, shape, st, S, P):
     st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
 
 
+def _retained_np(shape, st, P, n):
+    """Copies of the per-position state a verify left in the spare banks."""
+    t = torch()
+    book = st.book()
+    out = {}
+    for li, (kind, param) in enumerate(shape.layers):
+        v = st.view(li)
+        d = shape.d_model
+        if kind in ("SE", "MR"):
+            out[li] = to_np(wrap(v.fir_ext[1 - book["fir_bank"]], (param - 1 + v.n_max, d)))
+        elif kind == "LI":
+            out[li] = to_np(wrap(v.iir_all[1 - book["iir_bank"]], (v.n_max, d, param, 2)))
+        else:
+            H, Dh = shape.n_heads, shape.head_dim
+            kc = wrap(v.k_cache, (H, v.ctx_max, Dh), "<i2").view(t.bfloat16)
+            vc = wrap(v.v_cache, (H, v.ctx_max, Dh), "<i2").view(t.bfloat16)
+            out[li] = (to_np(kc[:, P:P + n]).transpose(1, 0, 2), to_np(vc[:, P:P + n]).transpose(1, 0, 2))
+    return out
+
+
 @pytest.mark.gpu
 def test_7b_block_verify_full_size():
+    """Full-size 7B-shaped block verify (n = 13, context 1024).
+
+    Teacher-forced layer by layer: oracle layer l applied to the GPU's own
+    residual stream entering layer l must reproduce the GPU's layer update
+    (X_{l+1} - X_l) within 2e-2 of its max, and the per-position state the
+    layer retained (FIR windows, IIR states, appended K/V) within 2e-2; the
+    head applied to the GPU's final stream reproduces the GPU logits.  The
+    free-running comparison (oracle's own 32 layers) compounds bf16 rounding
+    flips through depth (a 1e-6 input perturbation alone moves the oracle's
+    logits by ~2e-3), so it is held to 5e-2 and to identical greedy choices
+    wherever the oracle's top-2 gap exceeds 4x the observed error."""
     import hybrid_ssm_attention_gb300 as evs
     from oracle.model import Model as OModel
     from oracle.numerics import Arith
+    t = torch()
     shape = synth.stack_7b()
-    P = 1024
+    P, n = 1024, shape.n_block
     W = synth.make_weights(shape, 3)
     S = synth.synth_state(shape, 3, P)
     m = evs.Model(shape, W)
     st = evs.State(m, P + 64)
     _load_synth_state(evs, shape, st, S, P)
-    toks = [int(x) for x in synth.prompt(shape, 3, shape.n_block)]
-    lg, _ = _verify(evs, st, toks, shape.vocab)
-    got = to_np(lg)
+    toks = [int(x) for x in synth.prompt(shape, 3, n)]
+    tt = t.tensor(np.asarray(toks, np.int32), device="cuda")
+    lg = t.empty((n, shape.vocab), dtype=t.float32, device="cuda")
+    trace = t.empty((len(shape.layers) + 1, n, shape.d_model), dtype=t.float32, device="cuda")
+    evs.evs_verify_block_trace(st, tt, n, lg, trace)
+    got, X = to_np(lg), to_np(trace)
+    retained = _retained_np(shape, st, P, n)
     assert st.check() == 0
-    del m.tensors[:]   # free device weights before the host oracle runs
+    st.close()
+    m.close()
     Wf = synth.weights_f32(W)
     del W
     om = OModel(shape, Wf, Arith(np.float32, bf16_points=True))
@@ -158,11 +195,33 @@ def test_7b_block_verify_full_size():
     Sf["layers"] = [dict(L, k=None if L["k"] is None else synth.bf16_bits_to_f32(L["k"]),
                          v=None if L["v"] is None else synth.bf16_bits_to_f32(L["v"])) for L in S["layers"]]
     ost = om.state_from(Sf, P + 64)
+    worst = []
+    for li, (M, L) in enumerate(zip(om.layers, ost.layers)):
+        d_ref, d_gpu = [], []
+        for i in range(n):
+            x_out = om.layer_forward(M, L, X[li][i].copy(), P + i)
+            d_ref.append(x_out - X[li][i])
+            d_gpu.append(X[li + 1][i] - X[li][i])
+            kind = M["kind"]
+            if kind in ("SE", "MR"):
+                assert rel_err(retained[li][i + 1:i + M["param"]], L.window) <= TOL, (li, i)
+            elif kind == "LI":
+                R = retained[li][i]
+                assert rel_err(R[..., 0], L.s.real) <= TOL and rel_err(R[..., 1], L.s.imag) <= TOL, (li, i)
+        if M["kind"] == "ATT":
+            assert rel_err(retained[li][0], L.K[P:P + n]) <= TOL and rel_err(retained[li][1], L.V[P:P + n]) <= TOL
+        e = rel_err(np.stack(d_gpu), np.stack(d_ref))
+        worst.append(e)
+        assert e <= TOL, (li, M["kind"], e)
+    head = np.stack([om.head(X[-1][i]) for i in range(n)])
+    assert rel_err(got, head) <= 1e-3
+    ost = om.state_from(Sf, P + 64)
     ref, _ = om.verify(ost, toks)
     err = rel_err(got, ref)
-    assert err <= TOL, err
+    print(f"per-layer teacher-forced max err {max(worst):.3e}; free-running logits err {err:.3e}")
+    assert err <= 5e-2, err
     gap_tol = 4 * np.abs(got - ref).max()
-    for i in range(len(toks)):
+    for i in range(n):
         srt = np.sort(ref[i])
         if srt[-1] - srt[-2] > gap_tol:
             assert int(np.argmax(got[i])) == int(np.argmax(ref[i])), i
