@@ -95,7 +95,9 @@ struct evs_model {
   const void* head;
   CUtensorMap m_head;
   std::vector<LayerW> L;
-  Partials p_in, p_out, p_gu, p_down, p_head;
+  Partials p_in, p_out, p_gu, p_down, p_head;  // with device slot tables
+  int4* tab_dev;                               // the five slot tables
+  size_t ws_bytes;                             // largest partial workspace
   bool has_attn;
   int n_max;
 };
@@ -169,7 +171,7 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     } else if (w.kind == EVS_LAYER_IIR) {
       CUDA_TRY(launch_iir(Lc, dt, src, d, n, w.param, w.lam, w.res, st.st[0], st.st[1], s->book, s->g));
     } else {
-      CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk, c.rope_base,
+      CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk,
                                 st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
     }
     EVS_TRY(gemm(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, &P));
@@ -359,16 +361,45 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     delete m;
     return fail(EVS_ERR_CUDA, "head: %s", err);
   }
-  m->p_in = plan_gemm(3 * d, d, m->num_sms);
-  m->p_out = plan_gemm(d, d, m->num_sms);
-  m->p_gu = plan_gemm(2 * F, d, m->num_sms);
-  m->p_down = plan_gemm(d, F, m->num_sms);
-  m->p_head = plan_gemm(V, d, m->num_sms);
+  {
+    std::vector<GemmPlan> plans(5);
+    const int shapes[5][2] = {{3 * d, d}, {d, d}, {2 * F, d}, {d, F}, {V, d}};
+    Partials* dst[5] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head};
+    size_t tb = 0;
+    m->ws_bytes = 0;
+    for (int k = 0; k < 5; ++k) {
+      if (!plan_gemm(shapes[k][0], shapes[k][1], m->num_sms, &plans[k])) {
+        delete m;
+        return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d has too many column tiles", shapes[k][0], shapes[k][1]);
+      }
+      tb += table_bytes(plans[k]);
+      m->ws_bytes = std::max(m->ws_bytes, partials_bytes(plans[k]));
+    }
+    cudaError_t e = cudaMalloc(&m->tab_dev, tb);
+    if (e != cudaSuccess) {
+      delete m;
+      return fail(EVS_ERR_OOM, "cudaMalloc(slot tables): %s", cudaGetErrorString(e));
+    }
+    size_t off = 0;
+    for (int k = 0; k < 5; ++k) {
+      const int T = (int)(table_bytes(plans[k]) / sizeof(int4));
+      e = cudaMemcpy(m->tab_dev + off, plans[k].tab, table_bytes(plans[k]), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        cudaFree(m->tab_dev);
+        delete m;
+        return fail(EVS_ERR_CUDA, "upload slot tables: %s", cudaGetErrorString(e));
+      }
+      *dst[k] = plans[k].P;
+      dst[k]->tab = m->tab_dev + off;
+      off += T;
+    }
+  }
   *out = m;
   return EVS_OK;
 }
 
 extern "C" int evs_model_destroy(evs_model* m) {
+  if (m && m->tab_dev) cudaFree(m->tab_dev);
   delete m;
   return EVS_OK;
 }
@@ -415,14 +446,18 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   ALLOC(s->g, es * NTOK * d);
   ALLOC(s->h, es * NTOK * F);
   size_t wsb = 0;
-  for (const Partials* P : {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head})
-    wsb = std::max(wsb, partials_bytes(*P));
+  wsb = m->ws_bytes;
   ALLOC(s->ws[0], wsb);
   ALLOC(s->ws[1], wsb);
   if (m->has_attn) {
     const size_t ab = attn_scratch_bytes(c.n_heads, c.head_dim, ctx_max, c.attn_chunk);
     ALLOC(s->attn_scratch, ab);
     attn_bufs_from_scratch(s->attn_scratch, c.n_heads, c.head_dim, ctx_max, c.attn_chunk, &s->ab);
+    cudaError_t e = fill_rope_table(s->ab, c.head_dim, c.rope_base, 0);
+    if (e != cudaSuccess) {
+      state_free(s);
+      return fail(EVS_ERR_CUDA, "rotary table: %s", cudaGetErrorString(e));
+    }
   }
   s->S.resize(m->L.size());
   for (size_t i = 0; i < m->L.size(); ++i) {
@@ -732,7 +767,8 @@ extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max,
   AttnBufs B;
   attn_bufs_from_scratch(scratch, H, Dh, ctx_max, chunk, &B);
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{nullptr, qkv, 3 * H * Dh}, H, Dh, n, ctx_max, chunk, base, kc, vc, book,
+  CUDA_TRY(fill_rope_table(B, Dh, base, stream));
+  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{nullptr, qkv, 3 * H * Dh}, H, Dh, n, ctx_max, chunk, kc, vc, book,
                             B, g, sms));
   return EVS_OK;
 }
@@ -745,19 +781,23 @@ extern "C" int evs_op_commit(evs_book* book, int32_t keep, int32_t n, cudaStream
   return EVS_OK;
 }
 
-static int gemm_plan_op(int32_t N, int32_t K, Partials* P) {
+// Operator GEMM scratch: [partial slots][slot table, 256-aligned][error flag, 256 bytes]
+static int gemm_plan_op(int32_t N, int32_t K, GemmPlan* g, size_t* table_off, size_t* total) {
   int sms = 0;
   EVS_TRY(num_sms_current(&sms));
-  *P = plan_gemm(N, K, sms);
+  if (!plan_gemm(N, K, sms, g)) return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d unsupported", N, K);
+  *table_off = (partials_bytes(*g) + 255) & ~(size_t)255;
+  *total = *table_off + ((table_bytes(*g) + 255) & ~(size_t)255) + 256;
   return EVS_OK;
 }
 
 extern "C" size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype) {
   (void)dtype;
   if (N < 1 || K < 1) return 0;
-  Partials P;
-  if (gemm_plan_op(N, K, &P) != EVS_OK) return 0;
-  return partials_bytes(P) + 256;
+  static thread_local GemmPlan g;
+  size_t toff = 0, total = 0;
+  if (gemm_plan_op(N, K, &g, &toff, &total) != EVS_OK) return 0;
+  return total;
 }
 
 extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, int32_t n, int32_t dtype, float* Y,
@@ -765,11 +805,16 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
   if (!W || !X || !Y || !scratch) return fail(EVS_ERR_ARG, "null argument");
   if (N < 1 || K < 1 || n < 1 || n > NTOK) return fail(EVS_ERR_ARG, "bad GEMM shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
-  Partials P;
-  EVS_TRY(gemm_plan_op(N, K, &P));
-  if (scratch_bytes < partials_bytes(P) + 256) return fail(EVS_ERR_ARG, "scratch too small");
+  static thread_local GemmPlan g;
+  size_t toff = 0, total = 0;
+  EVS_TRY(gemm_plan_op(N, K, &g, &toff, &total));
+  if (scratch_bytes < total) return fail(EVS_ERR_ARG, "scratch too small (%zu < %zu)", scratch_bytes, total);
+  Partials P = g.P;
   P.ws = (float*)scratch;
-  int* err_flag = (int*)((char*)scratch + partials_bytes(P));
+  P.tab = (const int4*)((char*)scratch + toff);
+  int* err_flag = (int*)((char*)scratch + total - 256);
+  CUDA_TRY(cudaMemcpyAsync((void*)P.tab, g.tab, table_bytes(g), cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));  // g is reused by the next call
   LaunchCtx Lc{stream, false};
   if (dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X)) {
     CUtensorMap wm, xm;

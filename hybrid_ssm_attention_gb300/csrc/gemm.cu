@@ -20,24 +20,24 @@
 
 namespace evs {
 
-Partials plan_gemm(int N, int K, int num_sms) {
-  Partials P{};
+bool plan_gemm(int N, int K, int num_sms, GemmPlan* g) {
+  Partials& P = g->P;
+  P = Partials{};
   P.N = N;
   const int T = (N + TILE_M - 1) / TILE_M;
+  if (T > 1024 || N < 1 || K < 1 || num_sms < 1) return false;
   P.KB = (K + TILE_K - 1) / TILE_K;
   P.U = (long long)T * P.KB;
   P.G = (int)std::min<long long>(num_sms, P.U);
-  int ms = 1;
-  for (int c = 0; c < P.G; ++c) {
-    const long long b = unit_begin(P.U, P.G, c), e = unit_begin(P.U, P.G, c + 1);
-    ms = std::max(ms, (int)((e - 1) / P.KB - b / P.KB + 1));
+  int base = 0;
+  for (int t = 0; t < T; ++t) {
+    const int c0 = unit_owner(P.U, P.G, (long long)t * P.KB);
+    const int c1 = unit_owner(P.U, P.G, (long long)t * P.KB + P.KB - 1);
+    g->tab[t] = make_int4(base, c1 - c0 + 1, c0, 0);
+    base += c1 - c0 + 1;
   }
-  P.maxseg = ms;
-  return P;
-}
-
-size_t partials_bytes(const Partials& P) {
-  return (size_t)P.G * P.maxseg * NTOK * TILE_M * sizeof(float);
+  g->slots = base;
+  return true;
 }
 
 bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NTOK), v);
       tc_fence_before();
       mbar_arrive(acc_empty(b));
-      const long long slot = (long long)c * P.maxseg + seg;
+      const int4 e = __ldg(P.tab + first_tile + seg);
+      const long long slot = e.x + (c - e.z);
       float* dst = P.ws + slot * NTOK * TILE_M + row;
 #pragma unroll
       for (int j = 0; j < NTOK; ++j) __stcg(dst + j * TILE_M, v[j]);
@@ -350,7 +351,6 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
   pdl_wait();
   const int c = blockIdx.x;
   const long long ub = unit_begin(P.U, P.G, c), ue = unit_begin(P.U, P.G, c + 1);
-  const int first_tile = (int)(ub / P.KB);
   long long u = ub;
   while (u < ue) {
     const int tile = (int)(u / P.KB);
@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
         }
       }
     }
-    const long long slot = (long long)c * P.maxseg + (tile - first_tile);
+    const int4 e = __ldg(P.tab + tile);
+    const long long slot = e.x + (c - e.z);
     float* dst = P.ws + slot * NTOK * TILE_M + threadIdx.x;
 #pragma unroll
     for (int t = 0; t < NTOK; ++t) dst[t * TILE_M] = acc[t];

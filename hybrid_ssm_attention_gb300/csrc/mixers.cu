@@ -14,6 +14,7 @@
 // Every mixer first forms its inputs from the in-projection (GEMM partials
 // or a plain matrix) with the storage rounding of the path.
 #include <algorithm>
+#include <cmath>
 
 #include "evs_internal.cuh"
 
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const f
 // ------------------------------------------------------------------ attention
 // (1) rotary embedding + append: grid (n, H), Dh/2 threads, one rotation pair each.
 template <typename T, typename Src>
-__global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max, float base, T* kc,
+__global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max, const double* inv_freq, T* kc,
                                 T* vc, float* qbuf, evs_book* book) {
   const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = Dh >> 1;
   const int d = H * Dh;
@@ -127,11 +128,14 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   const float q1 = stored<T>(src.get(t, col)), q2 = stored<T>(src.get(t, col + half));
   const float k1 = stored<T>(src.get(t, d + col)), k2 = stored<T>(src.get(t, d + col + half));
   const float v1 = stored<T>(src.get(t, 2 * d + col)), v2 = stored<T>(src.get(t, 2 * d + col + half));
-  // angle pos * base^(-2i/Dh), evaluated in double, rounded once to float
-  const double inv_freq = pow((double)base, -2.0 * (double)i / (double)Dh);
-  double sd, cd;
-  sincos((double)pos * inv_freq, &sd, &cd);
-  const float cs = (float)cd, sn = (float)sd;
+  // angle pos * base^(-2i/Dh) in double (table built on the host in
+  // double), reduced to [-pi, pi] in double, then sin / cos in float
+  const double TWO_PI = 6.283185307179586476925287;
+  const double ang = (double)pos * inv_freq[i];
+  const double turns = rint(ang * (1.0 / TWO_PI));
+  const float red = (float)fma(-turns, TWO_PI, ang);
+  float sn, cs;
+  sincosf(red, &sn, &cs);
   const float rq1 = q1 * cs - q2 * sn, rq2 = q1 * sn + q2 * cs;
   const float rk1 = k1 * cs - k2 * sn, rk2 = k1 * sn + k2 * cs;
   const size_t row = ((size_t)h * ctx_max + pos) * Dh;
@@ -354,10 +358,9 @@ cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, int n, long long ctx_
 
 template <typename T, typename Src>
 cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, int n, long long ctx_max, int chunk,
-                        float base, void* kc, void* vc, evs_book* book, const AttnBufs& B, void* g,
-                        int num_sms) {
+                        void* kc, void* vc, evs_book* book, const AttnBufs& B, void* g, int num_sms) {
   cudaError_t e = launch(L, qkv_rope_kernel<T, Src>, dim3(n, H), dim3(Dh / 2), 0, s, H, Dh, n, ctx_max,
-                         base, (T*)kc, (T*)vc, B.qbuf, book);
+                         (const double*)B.inv_freq, (T*)kc, (T*)vc, B.qbuf, book);
   if (e != cudaSuccess) return e;
   switch (Dh) {
     case 32: e = attn_split_dispatch<T, 32>(L, H, n, ctx_max, chunk, book, B, kc, vc, num_sms); break;
@@ -403,14 +406,16 @@ cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, 
 size_t attn_scratch_bytes(int H, int Dh, long long ctx_max, int chunk) {
   const long long nchunk = (ctx_max + chunk - 1) / chunk;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al(sizeof(float) * NTOK * H * Dh) + al(sizeof(float) * H * nchunk * NTOK * Dh) +
-         al(sizeof(float) * H * nchunk * NTOK * 2);
+  return al(sizeof(double) * (Dh / 2)) + al(sizeof(float) * NTOK * H * Dh) +
+         al(sizeof(float) * H * nchunk * NTOK * Dh) + al(sizeof(float) * H * nchunk * NTOK * 2);
 }
 
 void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int chunk, AttnBufs* out) {
   const long long nchunk = (ctx_max + chunk - 1) / chunk;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* p = (char*)scratch;
+  out->inv_freq = (double*)p;
+  p += al(sizeof(double) * (Dh / 2));
   out->qbuf = (float*)p;
   p += al(sizeof(float) * NTOK * H * Dh);
   out->part_o = (float*)p;
@@ -419,20 +424,29 @@ void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int
   out->nchunk_max = (int)nchunk;
 }
 
+cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStream_t stream) {
+  double tab[512];
+  if (Dh / 2 > 512) return cudaErrorInvalidValue;
+  for (int i = 0; i < Dh / 2; ++i) tab[i] = std::pow((double)rope_base, -2.0 * (double)i / (double)Dh);
+  cudaError_t e = cudaMemcpyAsync(B.inv_freq, tab, sizeof(double) * (Dh / 2), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);  // tab lives on this stack frame
+}
+
 cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, int n,
-                             long long ctx_max, int chunk, float rope_base, void* kc, void* vc,
+                             long long ctx_max, int chunk, void* kc, void* vc,
                              evs_book* book, const AttnBufs& B, void* g, int num_sms) {
   if (src.part) {
     SrcPartials s{*src.part};
     return dtype == EVS_BF16
-               ? attention_t<bf16>(L, s, H, Dh, n, ctx_max, chunk, rope_base, kc, vc, book, B, g, num_sms)
-               : attention_t<float>(L, s, H, Dh, n, ctx_max, chunk, rope_base, kc, vc, book, B, g, num_sms);
+               ? attention_t<bf16>(L, s, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms)
+               : attention_t<float>(L, s, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms);
   }
   if (dtype == EVS_BF16)
     return attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.plain, src.ld}, H, Dh, n, ctx_max, chunk,
-                             rope_base, kc, vc, book, B, g, num_sms);
+                             kc, vc, book, B, g, num_sms);
   return attention_t<float>(L, SrcPlain<float>{(const float*)src.plain, src.ld}, H, Dh, n, ctx_max, chunk,
-                            rope_base, kc, vc, book, B, g, num_sms);
+                            kc, vc, book, B, g, num_sms);
 }
 
 }  // namespace evs

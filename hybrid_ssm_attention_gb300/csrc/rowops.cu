@@ -13,7 +13,11 @@
 //
 // Reductions run in a fixed order (per-thread strided partials, then a
 // butterfly), so results are reproducible and independent of the block size.
+#include <cooperative_groups.h>
+
 #include "evs_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace evs {
 namespace {
@@ -36,43 +40,59 @@ struct AddF { __device__ float operator()(float a, float b) const { return a + b
 struct MaxF { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
 struct AddU { __device__ unsigned long long operator()(unsigned long long a, unsigned long long b) const { return a + b; } };
 
-// RMSNorm of row t of X (already final in X) into xn
+// Residual update + RMSNorm of one token row, spread over the CTAs of a
+// thread-block cluster (grid (CL, n), cluster (CL, 1, 1)): CTA r owns
+// columns [r*d/CL, (r+1)*d/CL).  mode 0 sets X[t] = E[token_t] (and marks
+// the block pending), mode 1 adds the GEMM partials.  Each CTA's sum of
+// squares is summed over the cluster's shared memory in rank order, so the
+// result is the same whatever the number of rows.
 template <typename T>
-__device__ void norm_row(const float* x, int d, float eps, T* xo, float* scratch) {
+__global__ void __launch_bounds__(256) row_norm_kernel(int mode, const T* E, const int32_t* tokens, int V,
+                                                       Partials P, float* X, int d, float eps, T* xn,
+                                                       evs_book* book, int n_mark) {
+  __shared__ float scratch[32];
+  __shared__ float ss_cta;
+  cg::cluster_group cl = cg::this_cluster();
+  const int ncl = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const int t = blockIdx.y;
+  const int cols = d / ncl, c0 = rank * cols;
+  pdl_trigger();
+  pdl_wait();
+  float* x = X + (size_t)t * d;
   float ss = 0.f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(x[c], x[c], ss);
+  if (mode == 0) {
+    if (n_mark > 0 && t == 0 && rank == 0 && threadIdx.x == 0) book->pending_n = n_mark;
+    const int tok = tokens[t];
+    const bool ok = tok >= 0 && tok < V;
+    if (!ok && rank == 0 && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
+    for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) {
+      const float v = ok ? to_f(E[(size_t)tok * d + c]) : 0.f;
+      x[c] = v;
+      ss = fmaf(v, v, ss);
+    }
+  } else {
+    for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) {
+      const float v = x[c] + partial_sum(P, t, c);
+      x[c] = v;
+      ss = fmaf(v, v, ss);
+    }
+  }
   ss = block_reduce(ss, AddF(), scratch);
-  const float den = sqrtf(ss / (float)d + eps);
-  for (int c = threadIdx.x; c < d; c += blockDim.x) xo[c] = from_f<T>(x[c] / den);
+  if (threadIdx.x == 0) ss_cta = ss;
+  cl.sync();
+  float tot = 0.f;
+  for (int q = 0; q < ncl; ++q) tot += *cl.map_shared_rank(&ss_cta, q);
+  const float den = sqrtf(tot / (float)d + eps);
+  T* xo = xn + (size_t)t * d;
+  for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) xo[c] = from_f<T>(x[c] / den);
+  cl.sync();  // ss_cta stays alive until every CTA of the cluster has read it
 }
 
-template <typename T>
-__global__ void __launch_bounds__(512) embed_norm_kernel(const T* E, const int32_t* tokens, int n, int d,
-                                                         int V, float eps, float* X, T* xn, evs_book* book) {
-  __shared__ float scratch[32];
-  const int t = blockIdx.x;
-  pdl_trigger();
-  pdl_wait();
-  if (t == 0 && threadIdx.x == 0) book->pending_n = n;
-  const int tok = tokens[t];
-  const bool ok = tok >= 0 && tok < V;
-  if (!ok && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
-  float* x = X + (size_t)t * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) x[c] = ok ? to_f(E[(size_t)tok * d + c]) : 0.f;
-  __syncthreads();
-  norm_row<T>(x, d, eps, xn + (size_t)t * d, scratch);
-}
-
-template <typename T>
-__global__ void __launch_bounds__(512) residual_norm_kernel(Partials P, float* X, int d, float eps, T* xn) {
-  __shared__ float scratch[32];
-  const int t = blockIdx.x;
-  pdl_trigger();
-  pdl_wait();
-  float* x = X + (size_t)t * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) x[c] += partial_sum(P, t, c);
-  __syncthreads();
-  norm_row<T>(x, d, eps, xn + (size_t)t * d, scratch);
+// CTAs per token row: up to 8, each owning >= 256 columns (a multiple of 32)
+int row_cluster(int d) {
+  int cl = 8;
+  while (cl > 1 && (d % (cl * 32) != 0 || d / cl < 256)) cl >>= 1;
+  return cl;
 }
 
 template <typename T>
@@ -289,18 +309,23 @@ __global__ void book_set_kernel(evs_book* book, evs_book v) {
 
 cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, const int32_t* tokens, int n,
                               int d, int V, float eps, float* X, void* xn, evs_book* book) {
+  const int cl = row_cluster(d);
+  Partials none{};
   if (dtype == EVS_BF16)
-    return launch(L, embed_norm_kernel<bf16>, dim3(n), dim3(512), 0, (const bf16*)E, tokens, n, d, V, eps, X,
-                  (bf16*)xn, book);
-  return launch(L, embed_norm_kernel<float>, dim3(n), dim3(512), 0, (const float*)E, tokens, n, d, V, eps, X,
-                (float*)xn, book);
+    return launch_cl(L, cl, row_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, 0, (const bf16*)E, tokens, V, none,
+                     X, d, eps, (bf16*)xn, book, n);
+  return launch_cl(L, cl, row_norm_kernel<float>, dim3(cl, n), dim3(256), 0, 0, (const float*)E, tokens, V, none,
+                   X, d, eps, (float*)xn, book, n);
 }
 
 cudaError_t launch_residual_norm(const LaunchCtx& L, int dtype, const Partials& P, float* X, int n, int d,
                                  float eps, void* xn) {
+  const int cl = row_cluster(d);
   if (dtype == EVS_BF16)
-    return launch(L, residual_norm_kernel<bf16>, dim3(n), dim3(512), 0, P, X, d, eps, (bf16*)xn);
-  return launch(L, residual_norm_kernel<float>, dim3(n), dim3(512), 0, P, X, d, eps, (float*)xn);
+    return launch_cl(L, cl, row_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, 1, (const bf16*)nullptr,
+                     (const int32_t*)nullptr, 0, P, X, d, eps, (bf16*)xn, (evs_book*)nullptr, 0);
+  return launch_cl(L, cl, row_norm_kernel<float>, dim3(cl, n), dim3(256), 0, 1, (const float*)nullptr,
+                   (const int32_t*)nullptr, 0, P, X, d, eps, (float*)xn, (evs_book*)nullptr, 0);
 }
 
 cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const Partials& P, int n, int F, void* h) {
