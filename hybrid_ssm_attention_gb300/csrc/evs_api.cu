@@ -111,12 +111,18 @@ struct evs_state {
   int host_pending;
   float* X;
   void *xn, *g, *h;
+  float* fin;   // [NTOK][max(3d, 2F)] final GEMM sums (mixer / MLP inputs)
+  float* ss;    // [tiles of d][NTOK] per-tile sums of squares
+  int* cnt;     // [max tiles] GEMM arrival counters
+  int cnt_len;
   float* ws[2];
   void* attn_scratch;
   AttnBufs ab;
   std::vector<LayerS> S;
   CUtensorMap m_xn, m_g, m_h;
   bool use_graphs, pdl;
+  int pf_units;  // next-weight L2 prefetch per CTA (units of 128x64)
+  unsigned long long* trace;  // EVS_TRACE builds: GEMM timeline slots
   cudaStream_t cap;
   std::vector<GraphEntry> graphs;
   unsigned long long tick;
@@ -146,15 +152,52 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
   const float eps = c.norm_eps;
   int wsi = 0;
+  // Weight matrices in the order the step reads them; each GEMM prefetches
+  // the start of the next one into L2 (the head's successor is the next
+  // round's first in-projection).
+  const int nl = (int)m->L.size();
+  auto seq = [&](int k, const Partials** P, const CUtensorMap** map) {
+    k %= 4 * nl + 1;
+    if (k == 4 * nl) {
+      *P = &m->p_head;
+      *map = &m->m_head;
+      return;
+    }
+    const LayerW& w = m->L[k / 4];
+    const Partials* plans[4] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down};
+    const CUtensorMap* maps[4] = {&w.m_in, &w.m_out, &w.m_gu, &w.m_down};
+    *P = plans[k % 4];
+    *map = maps[k % 4];
+  };
+  int gk = 0;
+  // GEMM_FINAL writes fin[tok][col] (row stride ld); GEMM_RESID adds into X
+  // and leaves per-tile sums of squares for the next RMSNorm
   auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const void* W, const CUtensorMap& xm,
-                  const void* X, int K, Partials* out) -> int {
+                  const void* Xin, int K, int mode, float* fin, int ld) -> int {
     Partials P = plan;
     P.ws = s->ws[(wsi++) & 1];
+    P.cnt = s->cnt;
+    P.mode = mode;
+    P.n = n;
+    P.fin = fin;
+    P.fin_ld = ld;
+    P.X = s->X;
+    P.ss = s->ss;
+    const Partials* np;
+    const CUtensorMap* nmap;
+    seq(++gk, &np, &nmap);
+    P.pf_units = s->pf_units;
+    P.nG = np->G;
+    P.nKB = np->KB;
+    P.nU = np->U;
+#ifdef EVS_TRACE
+    P.trace = s->trace;
+    P.trace_slot = gk - 1;
+#endif
     if (m->tc)
-      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, &s->book->status));
+      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, *nmap, P, K, &s->book->status));
     else
-      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, n, P, K));
-    *out = P;
+      CUDA_TRY(launch_gemm_simt(Lc, dt, W, Xin, K, P, K));
     return EVS_OK;
   };
   const size_t xbytes = sizeof(float) * (size_t)n * d;
@@ -163,9 +206,8 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
     LayerS& st = s->S[i];
-    Partials P;
-    EVS_TRY(gemm(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, d, &P));
-    MixSrc src{&P, nullptr, 0};
+    EVS_TRY(gemm(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d));
+    MixSrc src{s->fin, 3 * d, 1};
     if (w.kind == EVS_LAYER_FIR) {
       CUDA_TRY(launch_fir(Lc, dt, src, d, n, w.param, w.taps, st.ext[0], st.ext[1], s->book, s->g));
     } else if (w.kind == EVS_LAYER_IIR) {
@@ -174,18 +216,16 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
       CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk,
                                 st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
     }
-    EVS_TRY(gemm(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, &P));
-    CUDA_TRY(launch_residual_norm(Lc, dt, P, s->X, n, d, eps, s->xn));
-    EVS_TRY(gemm(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, d, &P));
-    CUDA_TRY(launch_mlp_act(Lc, dt, P, n, F, s->h));
-    EVS_TRY(gemm(m->p_down, w.m_down, w.w_down, s->m_h, s->h, F, &P));
-    CUDA_TRY(launch_residual_norm(Lc, dt, P, s->X, n, d, eps, s->xn));
+    EVS_TRY(gemm(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
+    CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
+    EVS_TRY(gemm(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 2 * F));
+    CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, s->h));
+    EVS_TRY(gemm(m->p_down, w.m_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
+    CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
     if (trace)
       CUDA_TRY(cudaMemcpyAsync(trace + (i + 1) * (size_t)n * d, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   }
-  Partials P;
-  EVS_TRY(gemm(m->p_head, m->m_head, m->head, s->m_xn, s->xn, d, &P));
-  CUDA_TRY(launch_logits(Lc, P, n, V, logits));
+  EVS_TRY(gemm(m->p_head, m->m_head, m->head, s->m_xn, s->xn, d, GEMM_FINAL, logits, V));
   return EVS_OK;
 }
 
@@ -288,8 +328,8 @@ int check_cfg(const evs_config* c) {
       if (c->n_heads * c->head_dim != c->d_model) return fail(EVS_ERR_ARG, "n_heads * head_dim != d_model");
       if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
         return fail(EVS_ERR_UNSUPPORTED, "head_dim must be 32, 64 or 128");
-      if (c->attn_chunk < 32 || c->attn_chunk % 32 || c->attn_chunk > 1024)
-        return fail(EVS_ERR_UNSUPPORTED, "attn_chunk must be a multiple of 32 in [32, 1024]");
+      if (c->attn_chunk != 32 && c->attn_chunk != 64 && c->attn_chunk != 128 && c->attn_chunk != 256)
+        return fail(EVS_ERR_UNSUPPORTED, "attn_chunk must be 32, 64, 128 or 256");
       if (!(c->rope_base > 0.f)) return fail(EVS_ERR_ARG, "rope_base must be > 0");
     } else {
       return fail(EVS_ERR_ARG, "layer %d: unknown kind %d", i, k);
@@ -429,6 +469,8 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   s->use_graphs = true;
   const char* pdl_env = getenv("EVS_PDL");
   s->pdl = !(pdl_env && pdl_env[0] == '0');
+  const char* pf_env = getenv("EVS_PREFETCH_UNITS");
+  s->pf_units = pf_env ? std::max(0, atoi(pf_env)) : 12;
   const evs_config& c = m->cfg;
   const int d = c.d_model, F = c.d_ffn, nm = m->n_max;
   const size_t es = esize(c.dtype);
@@ -445,6 +487,13 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   ALLOC(s->xn, es * NTOK * d);
   ALLOC(s->g, es * NTOK * d);
   ALLOC(s->h, es * NTOK * F);
+  ALLOC(s->fin, sizeof(float) * NTOK * std::max(3 * d, std::max(2 * F, c.vocab)));
+  ALLOC(s->ss, sizeof(float) * NTOK * ((d + TILE_M - 1) / TILE_M));
+  s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
+  ALLOC(s->cnt, sizeof(int) * s->cnt_len);
+#ifdef EVS_TRACE
+  ALLOC(s->trace, sizeof(unsigned long long) * 3 * 1024);
+#endif
   size_t wsb = 0;
   wsb = m->ws_bytes;
   ALLOC(s->ws[0], wsb);
@@ -521,6 +570,7 @@ extern "C" int evs_state_reset(evs_state* s, cudaStream_t stream) {
         CUDA_TRY(cudaMemsetAsync(s->S[i].ext[b], 0, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * m->cfg.d_model, stream));
   }
   LaunchCtx Lc{stream, false};
+  CUDA_TRY(cudaMemsetAsync(s->cnt, 0, sizeof(int) * s->cnt_len, stream));
   CUDA_TRY(launch_book_set(Lc, s->book, initial_book()));
   s->host_pos = 0;
   s->host_pos_known = true;
@@ -731,7 +781,7 @@ extern "C" int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_
     return fail(EVS_ERR_ARG, "bad FIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{nullptr, abv, 3 * d}, d, n, L, taps, e0, e1, book, g));
+  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, n, L, taps, e0, e1, book, g));
   return EVS_OK;
 }
 
@@ -743,7 +793,7 @@ extern "C" int evs_op_iir(int32_t M, int32_t d, int32_t n, int32_t n_max, int32_
     return fail(EVS_ERR_ARG, "bad IIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_iir(Lc, dtype, MixSrc{nullptr, abv, 3 * d}, d, n, M, lam, res, s0, s1, book, g));
+  CUDA_TRY(launch_iir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, n, M, lam, res, s0, s1, book, g));
   return EVS_OK;
 }
 
@@ -758,7 +808,7 @@ extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max,
                                 void* g, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   if (!qkv || !kc || !vc || !book || !g || !scratch) return fail(EVS_ERR_ARG, "null argument");
   if (H < 1 || (Dh != 32 && Dh != 64 && Dh != 128) || n < 1 || n > NTOK || n > n_max || ctx_max < 1 ||
-      chunk < 32 || chunk % 32 || chunk > 1024)
+      (chunk != 32 && chunk != 64 && chunk != 128 && chunk != 256))
     return fail(EVS_ERR_ARG, "bad attention shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   if (scratch_bytes < attn_scratch_bytes(H, Dh, ctx_max, chunk)) return fail(EVS_ERR_ARG, "scratch too small");
@@ -768,7 +818,7 @@ extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max,
   attn_bufs_from_scratch(scratch, H, Dh, ctx_max, chunk, &B);
   LaunchCtx Lc{stream, false};
   CUDA_TRY(fill_rope_table(B, Dh, base, stream));
-  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{nullptr, qkv, 3 * H * Dh}, H, Dh, n, ctx_max, chunk, kc, vc, book,
+  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{qkv, 3 * H * Dh, dtype == EVS_F32}, H, Dh, n, ctx_max, chunk, kc, vc, book,
                             B, g, sms));
   return EVS_OK;
 }
@@ -781,13 +831,15 @@ extern "C" int evs_op_commit(evs_book* book, int32_t keep, int32_t n, cudaStream
   return EVS_OK;
 }
 
-// Operator GEMM scratch: [partial slots][slot table, 256-aligned][error flag, 256 bytes]
+// Operator GEMM scratch: [partial slots][slot table][arrival counters][error flag],
+// each part 256-byte aligned
 static int gemm_plan_op(int32_t N, int32_t K, GemmPlan* g, size_t* table_off, size_t* total) {
   int sms = 0;
   EVS_TRY(num_sms_current(&sms));
   if (!plan_gemm(N, K, sms, g)) return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d unsupported", N, K);
-  *table_off = (partials_bytes(*g) + 255) & ~(size_t)255;
-  *total = *table_off + ((table_bytes(*g) + 255) & ~(size_t)255) + 256;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  *table_off = al(partials_bytes(*g));
+  *total = *table_off + 2 * al(table_bytes(*g)) + 256;
   return EVS_OK;
 }
 
@@ -812,8 +864,15 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
   Partials P = g.P;
   P.ws = (float*)scratch;
   P.tab = (const int4*)((char*)scratch + toff);
+  const size_t tb = (table_bytes(g) + 255) & ~(size_t)255;
+  P.cnt = (int*)((char*)scratch + toff + tb);
+  P.mode = GEMM_FINAL;
+  P.n = n;
+  P.fin = Y;
+  P.fin_ld = N;
   int* err_flag = (int*)((char*)scratch + total - 256);
   CUDA_TRY(cudaMemcpyAsync((void*)P.tab, g.tab, table_bytes(g), cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemsetAsync(P.cnt, 0, tb, stream));
   CUDA_TRY(cudaStreamSynchronize(stream));  // g is reused by the next call
   LaunchCtx Lc{stream, false};
   if (dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X)) {
@@ -823,11 +882,10 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
         !encode_tmap_2d(&xm, X, K, n, TILE_K, NTOK, err, sizeof err))
       return fail(EVS_ERR_CUDA, "%s", err);
     CUDA_TRY(cudaMemsetAsync(err_flag, 0, sizeof(int), stream));
-    CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, err_flag));
+    CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, err_flag));  // P.pf_units = 0: no prefetch
   } else {
-    CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, n, P, K));
+    CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, P, K));
   }
-  CUDA_TRY(launch_logits(Lc, P, n, N, Y));
   return EVS_OK;
 }
 
@@ -854,11 +912,16 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
                  int N, int K) -> int {
     Partials P = plan;
     P.ws = s->ws[k & 1];
+    P.cnt = s->cnt;
+    P.mode = GEMM_FINAL;  // final sums to the scratch buffer: the state is untouched
+    P.n = n;
+    P.fin = s->fin;
+    P.fin_ld = N;
     CUDA_TRY(cudaEventRecord(ev[k], stream));
     if (m->tc)
-      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, P, K, &s->book->status));
+      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, &s->book->status));  // no prefetch: timed alone
     else
-      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, n, P, K));
+      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, P, K));
     bytes_host[k] = (int64_t)N * K * es + (int64_t)n * K * es + (int64_t)n * N * 4;
     ++k;
     return EVS_OK;
@@ -881,6 +944,25 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   *count = k;
   return r;
 }
+
+#ifdef EVS_TRACE
+// Timeline of the GEMM launches since the previous call: out[3k..3k+2] =
+// {entry, dependency release, exit} of the k-th GEMM; re-arms the slots.
+extern "C" int evs_trace_read(evs_state* s, unsigned long long* out, int32_t max_slots) {
+  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
+  const int k = std::min(max_slots, 1024);
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(out, s->trace, sizeof(unsigned long long) * 3 * k, cudaMemcpyDeviceToHost));
+  std::vector<unsigned long long> init(3 * 1024);
+  for (int i = 0; i < 1024; ++i) {
+    init[3 * i] = ~0ull;
+    init[3 * i + 1] = ~0ull;
+    init[3 * i + 2] = 0;
+  }
+  CUDA_TRY(cudaMemcpy(s->trace, init.data(), sizeof(unsigned long long) * 3 * 1024, cudaMemcpyHostToDevice));
+  return EVS_OK;
+}
+#endif
 
 // =================================================================== misc
 extern "C" const char* evs_last_error(void) { return g_err.c_str(); }

@@ -28,7 +28,9 @@ bool plan_gemm(int N, int K, int num_sms, GemmPlan* g) {
   if (T > 1024 || N < 1 || K < 1 || num_sms < 1) return false;
   P.KB = (K + TILE_K - 1) / TILE_K;
   P.U = (long long)T * P.KB;
-  P.G = (int)std::min<long long>(num_sms, P.U);
+  // at most MAX_CONTRIB CTAs per tile: the last one sums their slots
+  constexpr int MAX_CONTRIB = 8;
+  P.G = (int)std::min<long long>(std::min<long long>(num_sms, P.U), (long long)T * MAX_CONTRIB);
   int base = 0;
   for (int t = 0; t < T; ++t) {
     const int c0 = unit_owner(P.U, P.G, (long long)t * P.KB);
@@ -70,13 +72,16 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 namespace {
 
-constexpr int STAGES = 8;
+#ifndef EVS_GEMM_STAGES
+#define EVS_GEMM_STAGES 8
+#endif
+constexpr int STAGES = EVS_GEMM_STAGES;
 constexpr int A_BYTES = TILE_M * TILE_K * 2;  // 16 KB weight tile
 constexpr int B_BYTES = NTOK * TILE_K * 2;    // 2 KB activation tile
 constexpr int GEMM_THREADS = 192;             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint64_t WAIT_NS = 4000000000ull;   // upper bound on any pipeline wait
 constexpr int NBARS = 2 * STAGES + 5;         // full, empty, acc_full[2], acc_empty[2], drain
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + NBARS * 8 + 16;
+constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + NBARS * 8 + 16 + 4 * NTOK * 4;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -135,6 +140,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+// Bring one tensor tile into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -195,9 +207,94 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NTOK >> 3) << 17) |
                            ((uint32_t)(TILE_M >> 4) << 24);
 
+// Synchronisation of the 128 threads that drain a tile segment: the four
+// epilogue warps (named barrier 1) in the tensor-core kernel, the whole CTA
+// in the SIMT kernel.
+template <bool NAMED>
+__device__ __forceinline__ void group_sync() {
+  if (NAMED)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    __syncthreads();
+}
+
+// Called by the 128 group threads (thread `row` holds column tile*128+row)
+// after the CTA's partial slot for `tile` is written.  The contributor that
+// arrives last sums the tile's slots in contributor order and writes the
+// output of P.mode; it then re-arms the counter for the next launch.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+template <bool NAMED>
+__device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_flag, float* s_red) {
+  // The barrier orders the group's slot stores before thread 0's
+  // acquire-release increment (release publishes them to the GPU; acquire
+  // makes the other contributors' stores visible to whoever finishes last,
+  // and the next barrier extends that to the whole group).
+  group_sync<NAMED>();
+  if (row == 0) *s_flag = atom_add_acq_rel(P.cnt + tile, 1);
+  group_sync<NAMED>();
+  const int4 e = __ldg(P.tab + tile);
+  const int arrived = *s_flag;
+  group_sync<NAMED>();  // every thread has read the flag before it is reused
+  if (arrived != e.y - 1) return;
+  const int col = tile * TILE_M + row;
+  const bool ok = col < P.N;
+  const int n = P.n;
+  const float* p = P.ws + (size_t)e.x * NTOK * TILE_M + row;
+  float v[NTOK];
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) v[t] = 0.f;
+  // slots are loaded four at a time (independent loads in flight) and
+  // added strictly in contributor order
+  for (int j0 = 0; j0 < e.y; j0 += 4) {
+    float a[4][NTOK];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float* q = p + (size_t)(j0 + k) * NTOK * TILE_M;
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) a[k][t] = (j0 + k < e.y && t < n) ? __ldcg(q + t * TILE_M) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (j0 + k < e.y) {
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
+      }
+  }
+  if (P.mode == GEMM_FINAL) {
+    if (ok) {
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t)
+        if (t < n) P.fin[(size_t)t * P.fin_ld + col] = v[t];
+    }
+  } else {
+    const int lane = row & 31, w = row >> 5;
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      float sq = 0.f;
+      if (t < n && ok) {
+        const float x = P.X[(size_t)t * P.N + col] + v[t];
+        P.X[(size_t)t * P.N + col] = x;
+        sq = x * x;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (lane == 0) s_red[w * NTOK + t] = sq;
+    }
+    group_sync<NAMED>();
+    if (row < NTOK) P.ss[tile * NTOK + row] = ((s_red[row] + s_red[NTOK + row]) + s_red[2 * NTOK + row]) +
+                                              s_red[3 * NTOK + row];
+  }
+  if (row == 0) P.cnt[tile] = 0;
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
-                   Partials P, int* err_flag) {
+                   const __grid_constant__ CUtensorMap nmap, Partials P, int* err_flag) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -205,6 +302,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  float* s_red = reinterpret_cast<float*>(tmem_slot + 4);  // [4][NTOK]
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto acc_full = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
@@ -229,6 +329,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+#ifdef EVS_TRACE
+    if (P.trace) atomicMin(P.trace + 3 * P.trace_slot, gtimer());
+#endif
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
@@ -256,6 +359,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   (int)(u / P.KB) * TILE_M, pol_w);
     }
     pdl_wait();  // activations are written by the preceding kernel
+#ifdef EVS_TRACE
+    if (P.trace) atomicMin(P.trace + 3 * P.trace_slot + 1, gtimer());
+#endif
     for (int i = 0; i < pre; ++i) {
       const long long u = ub + i;
       tma_load_2d(smem_u32(sB + i * B_BYTES), &xmap, full(i), (int)(u % P.KB) * TILE_K, 0, pol_x);
@@ -270,6 +376,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tma_load_2d(smem_u32(sA + s * A_BYTES), &wmap, full(s), (int)(u % P.KB) * TILE_K,
                   (int)(u / P.KB) * TILE_M, pol_w);
       tma_load_2d(smem_u32(sB + s * B_BYTES), &xmap, full(s), (int)(u % P.KB) * TILE_K, 0, pol_x);
+    }
+    // All own tiles are requested: keep HBM busy through this kernel's tail
+    // and the consumers that follow by pulling the first units of the next
+    // weight matrix (the ones the CTA of the same index will read first)
+    // into L2.
+    if (i == nunits && P.pf_units > 0 && c < P.nG) {
+      const long long nb = unit_begin(P.nU, P.nG, c), ne = unit_begin(P.nU, P.nG, c + 1);
+      const long long stop = std::min<long long>(ne, nb + P.pf_units);
+      for (long long u = nb; u < stop; ++u)
+        tma_prefetch_l2(&nmap, (int)(u % P.nKB) * TILE_K, (int)(u / P.nKB) * TILE_M);
     }
     // make sure no copy into this CTA's shared memory is still in flight
     for (long long j = std::max<long long>(0, i - STAGES); j < i; ++j) {
@@ -313,22 +429,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     volatile int local_abort = 0;
     mbar_wait(drain, 0, &local_abort);
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> partial slots
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;
+    // ---------------- epilogue: TMEM -> partial slots -> tile fixup
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;  // column within the tile
+    const int g = threadIdx.x - 64; // index within the epilogue group
     for (int seg = 0; seg < nseg; ++seg) {
       const int b = seg & 1;
-      if (!warp_wait(acc_full(b), (uint32_t)(seg >> 1) & 1, abort_flag)) break;
+      // one thread waits; the decision is shared so the group stays in step
+      if (g == 0) *s_ok = mbar_wait(acc_full(b), (uint32_t)(seg >> 1) & 1, abort_flag) ? 1 : 0;
+      group_sync<true>();
+      const int go = *s_ok;
+      group_sync<true>();
+      if (!go) break;
       tc_fence_after();
       float v[NTOK];
       tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NTOK), v);
       tc_fence_before();
       mbar_arrive(acc_empty(b));
-      const int4 e = __ldg(P.tab + first_tile + seg);
+      const int tile = first_tile + seg;
+      const int4 e = __ldg(P.tab + tile);
       const long long slot = e.x + (c - e.z);
       float* dst = P.ws + slot * NTOK * TILE_M + row;
 #pragma unroll
-      for (int j = 0; j < NTOK; ++j) __stcg(dst + j * TILE_M, v[j]);
+      for (int j = 0; j < NTOK; ++j)
+        if (j < P.n) __stcg(dst + j * TILE_M, v[j]);
+      tile_done<true>(P, tile, row, s_flag, s_red);
     }
   }
 
@@ -339,14 +464,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
+#ifdef EVS_TRACE
+  if (threadIdx.x == 0 && P.trace) atomicMax(P.trace + 3 * P.trace_slot + 2, gtimer());
+#endif
 }
 
 // SIMT variant with the same unit schedule and partial layout (float32
 // storage, or shapes the tensor-core path does not take).
 template <typename T>
-__global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, int ldx, int n,
-                                                        Partials P, int K) {
+__global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, int ldx, Partials P, int K) {
   __shared__ float xs[NTOK][TILE_K];
+  __shared__ int s_flag;
+  __shared__ float s_red[4 * NTOK];
+  const int n = P.n;
   pdl_trigger();
   pdl_wait();
   const int c = blockIdx.x;
@@ -381,14 +511,16 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
     const long long slot = e.x + (c - e.z);
     float* dst = P.ws + slot * NTOK * TILE_M + threadIdx.x;
 #pragma unroll
-    for (int t = 0; t < NTOK; ++t) dst[t * TILE_M] = acc[t];
+    for (int t = 0; t < NTOK; ++t)
+      if (t < n) __stcg(dst + t * TILE_M, acc[t]);
+    tile_done<false>(P, tile, threadIdx.x, &s_flag, s_red);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                           const Partials& P, int K, int* err_flag) {
+                           const CUtensorMap& nmap, const Partials& P, int K, int* err_flag) {
   (void)K;
   static bool attr_set = false;
   if (!attr_set) {
@@ -397,16 +529,16 @@ cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CU
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(L, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), GEMM_SMEM, wmap, xmap, P, err_flag);
+  return launch(L, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), GEMM_SMEM, wmap, xmap, nmap, P, err_flag);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& L, int dtype, const void* W, const void* X, int ldx,
-                             int n, const Partials& P, int K) {
+                             const Partials& P, int K) {
   if (dtype == EVS_BF16)
     return launch(L, gemm_simt_kernel<bf16>, dim3(P.G), dim3(128), 0, (const bf16*)W, (const bf16*)X,
-                  ldx, n, P, K);
+                  ldx, P, K);
   return launch(L, gemm_simt_kernel<float>, dim3(P.G), dim3(128), 0, (const float*)W, (const float*)X,
-                ldx, n, P, K);
+                ldx, P, K);
 }
 
 }  // namespace evs

@@ -37,22 +37,29 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c0 = blockIdx.x * 32, c = c0 + lane;
 
-  for (int j = warp; j < Lf; j += NW) tap_s[j * 32 + lane] = taps[(size_t)j * d + c];
   pdl_trigger();
-  pdl_wait();
+  // Taps, the committed window and its copy into the spare bank do not
+  // depend on the in-projection: done while the preceding GEMM still runs
+  // (the bank / offset are fixed for the whole verify).
   const int bank = book->fir_bank, off = book->fir_off;
   const float* src_ext = bank ? ext1 : ext0;
   float* dst_ext = bank ? ext0 : ext1;
-  for (int r = warp; r < Lf - 1; r += NW) ext_s[r * 32 + lane] = src_ext[(size_t)(off + r) * d + c];
+  for (int j = warp; j < Lf; j += NW) tap_s[j * 32 + lane] = taps[(size_t)j * d + c];
+  for (int r = warp; r < Lf - 1; r += NW) {
+    const float w = src_ext[(size_t)(off + r) * d + c];
+    ext_s[r * 32 + lane] = w;
+    dst_ext[(size_t)r * d + c] = w;
+  }
+  pdl_wait();
   for (int t = warp; t < n; t += NW) {
     const float a = stored<T>(src.get(t, c));
     const float b = stored<T>(src.get(t, d + c));
     const float v = stored<T>(src.get(t, 2 * d + c));
     a_s[t * 32 + lane] = a;
     ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
+    dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
   }
   __syncthreads();
-  for (int r = warp; r < rows; r += NW) dst_ext[(size_t)r * d + c] = ext_s[r * 32 + lane];
   const int j0 = warp * J, j1 = min(Lf, j0 + J);
   for (int t = 0; t < n; ++t) {
     float acc = 0.f;
@@ -79,9 +86,16 @@ __global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const f
   __shared__ float a_s[NTOK][CPB];
   const int cl = threadIdx.x / M, m = threadIdx.x % M;
   const int c = blockIdx.x * CPB + cl;
+  pdl_trigger();
+  // poles, residues and the committed state do not depend on the
+  // in-projection: loaded while the preceding GEMM still runs
   const float2 L = lam[(size_t)c * M + m];
   const float2 R = res[(size_t)c * M + m];
-  pdl_trigger();
+  const int bank = book->iir_bank, slot = book->iir_slot;
+  const float2* cur = bank ? st1 : st0;
+  float2* dst = bank ? st0 : st1;
+  float2 s = make_float2(0.f, 0.f);
+  if (slot >= 0) s = cur[((size_t)slot * d + c) * M + m];
   pdl_wait();
   for (int e = threadIdx.x; e < n * CPB; e += 256) {
     const int t = e / CPB, cc = blockIdx.x * CPB + e % CPB;
@@ -92,11 +106,6 @@ __global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const f
     z_s[t][e % CPB] = b * v;
   }
   __syncthreads();
-  const int bank = book->iir_bank, slot = book->iir_slot;
-  const float2* cur = bank ? st1 : st0;
-  float2* dst = bank ? st0 : st1;
-  float2 s = make_float2(0.f, 0.f);
-  if (slot >= 0) s = cur[((size_t)slot * d + c) * M + m];
   for (int t = 0; t < n; ++t) {
     const float z = z_s[t][cl];
     const float sr = fmaf(L.x, s.x, fmaf(-L.y, s.y, z));
@@ -118,8 +127,18 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = Dh >> 1;
   const int d = H * Dh;
   pdl_trigger();
-  pdl_wait();
+  // the position is fixed for the whole verify: the rotation is computed
+  // while the in-projection still runs.  Angle pos * base^(-2i/Dh) in
+  // double (table built on the host in double), reduced to [-pi, pi] in
+  // double, then sin / cos in float.
   const long long pos = (long long)book->pos + t;
+  const double TWO_PI = 6.283185307179586476925287;
+  const double ang = (double)pos * inv_freq[i];
+  const double turns = rint(ang * (1.0 / TWO_PI));
+  const float red = (float)fma(-turns, TWO_PI, ang);
+  float sn, cs;
+  sincosf(red, &sn, &cs);
+  pdl_wait();
   if (pos >= ctx_max) {
     if (i == 0) set_status(book, EVS_DEV_KV_OVERFLOW);
     return;
@@ -128,14 +147,6 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   const float q1 = stored<T>(src.get(t, col)), q2 = stored<T>(src.get(t, col + half));
   const float k1 = stored<T>(src.get(t, d + col)), k2 = stored<T>(src.get(t, d + col + half));
   const float v1 = stored<T>(src.get(t, 2 * d + col)), v2 = stored<T>(src.get(t, 2 * d + col + half));
-  // angle pos * base^(-2i/Dh) in double (table built on the host in
-  // double), reduced to [-pi, pi] in double, then sin / cos in float
-  const double TWO_PI = 6.283185307179586476925287;
-  const double ang = (double)pos * inv_freq[i];
-  const double turns = rint(ang * (1.0 / TWO_PI));
-  const float red = (float)fma(-turns, TWO_PI, ang);
-  float sn, cs;
-  sincosf(red, &sn, &cs);
   const float rq1 = q1 * cs - q2 * sn, rq2 = q1 * sn + q2 * cs;
   const float rk1 = k1 * cs - k2 * sn, rk2 = k1 * sn + k2 * cs;
   const size_t row = ((size_t)h * ctx_max + pos) * Dh;
@@ -148,84 +159,125 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   qo[i + half] = stored<T>(rq2);
 }
 
-// (2) split-KV: CTA (x, h) handles chunks x, x+gridDim.x, ... of `chunk` keys
-// at absolute positions [cidx*chunk, (cidx+1)*chunk).  Query t (position
-// pos+t) sees keys <= pos+t.  Per chunk and query it stores the running max,
-// the sum of exp and the unnormalised output.  Every reduction runs over
-// fixed key slots, masked slots contributing exactly zero, so a query's
-// result does not depend on the other queries of the block.
-template <typename T, int DH>
+// (2) split-KV: CTA (x, h) handles chunks x, x+gridDim.x, ... of CH keys
+// at absolute positions [cidx*CH, (cidx+1)*CH).  Query t (position pos+t)
+// sees keys <= pos+t.  Each chunk's K and V rows are staged in shared
+// memory (K rows padded by 16 bytes so the per-key dot products of a warp
+// hit distinct banks); per chunk and query the kernel stores the max, the
+// sum of exp and the unnormalised output.  Every reduction runs over fixed
+// key slots, masked slots contributing exact zeros, so a query's result does
+// not depend on the other queries of the block.
+template <typename T, int DH, int CH>
 __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict__ qbuf, const T* __restrict__ kc,
                                                          const T* __restrict__ vc, int H, int n,
-                                                         long long ctx_max, int chunk,
-                                                         const evs_book* book, float* part_o,
+                                                         long long ctx_max, const evs_book* book, float* part_o,
                                                          float* part_ml, int nchunk_max) {
-  extern __shared__ float sm[];
-  float* q_s = sm;                    // [NTOK][DH]
-  float* p_s = q_s + NTOK * DH;       // [NTOK][chunk]
-  float* ml_s = p_s + NTOK * chunk;   // [NTOK][2]
+  constexpr int KP = DH * (int)sizeof(T) + 16;  // padded K row pitch in bytes
+  constexpr int VP = DH * (int)sizeof(T);
+  constexpr int QG = 256 / CH;                   // query groups in the score phase
+  constexpr int QS = NTOK / QG > 0 ? NTOK / QG : 1;
+  constexpr int DP = DH / 2;                     // output dim pairs
+  constexpr int OG = 256 / DP;                   // query groups in the PV phase
+  constexpr int OS = (NTOK + OG - 1) / OG;
+  extern __shared__ __align__(16) unsigned char smraw[];
+  float* q_s = reinterpret_cast<float*>(smraw);                    // [NTOK][DH]
+  float* p_s = q_s + NTOK * DH;                                    // [NTOK][CH]
+  float* ml_s = p_s + NTOK * CH;                                   // [NTOK][2]
+  unsigned char* k_s = reinterpret_cast<unsigned char*>(ml_s + NTOK * 2);  // [CH][KP]
+  unsigned char* v_s = k_s + CH * KP;                              // [CH][VP]
   const int h = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
-  pdl_wait();
+  // the committed length is fixed for the whole verify: pull this CTA's
+  // committed keys / values into L2 while the in-projection still runs
   const long long pos = book->pos;
-  const long long total = pos + n;
-  const int nchunks = (int)((total + chunk - 1) / chunk);
+  const long long total = min(pos + n, ctx_max);
+  const int nchunks = (int)((total + CH - 1) / CH);
+  if (tid == 0) {
+    for (int cidx = blockIdx.x; cidx < nchunks; cidx += gridDim.x) {
+      const long long k0 = (long long)cidx * CH;
+      const long long nk = min((long long)CH, min(pos, ctx_max) - k0);
+      if (nk > 0) {
+        const unsigned bytes = (unsigned)(nk * DH * sizeof(T));
+        const T* kr = kc + ((size_t)h * ctx_max + k0) * DH;
+        const T* vr = vc + ((size_t)h * ctx_max + k0) * DH;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kr), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vr), "r"(bytes) : "memory");
+      }
+    }
+  }
+  pdl_wait();
   const float scale = rsqrtf((float)DH);
   for (int e = tid; e < NTOK * DH; e += 256) {
     const int t = e / DH;
     q_s[e] = t < n ? qbuf[((size_t)t * H + h) * DH + e % DH] : 0.f;
   }
   for (int cidx = blockIdx.x; cidx < nchunks; cidx += gridDim.x) {
-    const long long k0 = (long long)cidx * chunk;
+    const long long k0 = (long long)cidx * CH;
+    const int kmax = (int)min((long long)CH, total - k0);
     __syncthreads();
-    // scores: one thread per key slot
-    for (int j = tid; j < chunk; j += 256) {
-      const long long kp = k0 + j;
-      float dots[NTOK];
+    // stage K and V rows [k0, k0+kmax) with 16-byte loads
+    constexpr int VEC = DH * (int)sizeof(T) / 16;  // 16-byte vectors per row
+    for (int e = tid; e < kmax * VEC; e += 256) {
+      const int j = e / VEC, w = e % VEC;
+      const uint4 kv = *reinterpret_cast<const uint4*>(kc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
+      const uint4 vv = *reinterpret_cast<const uint4*>(vc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
+      *reinterpret_cast<uint4*>(k_s + j * KP + w * 16) = kv;
+      *reinterpret_cast<uint4*>(v_s + j * VP + w * 16) = vv;
+    }
+    __syncthreads();
+    // scores: thread = (key slot j, query group tq)
+    {
+      const int j = tid % CH, tq = tid / CH;
+      float dots[QS];
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) dots[t] = 0.f;
-      if (kp < total) {
-        const T* kr = kc + ((size_t)h * ctx_max + kp) * DH;
+      for (int r = 0; r < QS; ++r) dots[r] = 0.f;
+      if (j < kmax) {
 #pragma unroll 4
-        for (int e = 0; e < DH; e += 8) {
-          float kv[8];
+        for (int w = 0; w < VEC; ++w) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(k_s + j * KP + w * 16);
+          float kv[16 / sizeof(T)];
           if constexpr (sizeof(T) == 2) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(kr + e);
             const bf16* b = reinterpret_cast<const bf16*>(&raw);
 #pragma unroll
             for (int z = 0; z < 8; ++z) kv[z] = __bfloat162float(b[z]);
           } else {
-            const float4 r0 = *reinterpret_cast<const float4*>(kr + e);
-            const float4 r1 = *reinterpret_cast<const float4*>(kr + e + 4);
-            kv[0] = r0.x; kv[1] = r0.y; kv[2] = r0.z; kv[3] = r0.w;
-            kv[4] = r1.x; kv[5] = r1.y; kv[6] = r1.z; kv[7] = r1.w;
-          }
+            const float* f = reinterpret_cast<const float*>(&raw);
 #pragma unroll
-          for (int t = 0; t < NTOK; ++t) {
+            for (int z = 0; z < 4; ++z) kv[z] = f[z];
+          }
+          constexpr int EPV = 16 / sizeof(T);
+#pragma unroll
+          for (int r = 0; r < QS; ++r) {
+            const int t = tq + r * QG;
             if (t < n) {
 #pragma unroll
-              for (int z = 0; z < 8; ++z) dots[t] = fmaf(q_s[t * DH + e + z], kv[z], dots[t]);
+              for (int z = 0; z < EPV; ++z) dots[r] = fmaf(q_s[t * DH + w * EPV + z], kv[z], dots[r]);
             }
           }
         }
       }
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t)
-        if (t < n) p_s[t * chunk + j] = (kp <= pos + t) ? dots[t] * scale : -INFINITY;
+      for (int r = 0; r < QS; ++r) {
+        const int t = tq + r * QG;
+        if (t < n) {
+          const long long kp = k0 + j;
+          p_s[t * CH + j] = (j < kmax && kp <= pos + t) ? dots[r] * scale : -INFINITY;
+        }
+      }
     }
     __syncthreads();
     // per query: max and sum of exp over the chunk's slots (warp per query)
     for (int t = warp; t < n; t += 8) {
       float mx = -INFINITY;
-      for (int j = lane; j < chunk; j += 32) mx = fmaxf(mx, p_s[t * chunk + j]);
+      for (int j = lane; j < CH; j += 32) mx = fmaxf(mx, p_s[t * CH + j]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       float sum = 0.f;
-      for (int j = lane; j < chunk; j += 32) {
-        const float s = p_s[t * chunk + j];
-        const float p = (mx == -INFINITY || s == -INFINITY) ? 0.f : expf(s - mx);
-        p_s[t * chunk + j] = p;
+      for (int j = lane; j < CH; j += 32) {
+        const float sc = p_s[t * CH + j];
+        const float p = (mx == -INFINITY || sc == -INFINITY) ? 0.f : expf(sc - mx);
+        p_s[t * CH + j] = p;
         sum += p;
       }
 #pragma unroll
@@ -236,43 +288,42 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
       }
     }
     __syncthreads();
-    // unnormalised output: thread owns 2 dims for queries t = tq, tq + QS, ...
-    constexpr int DP = DH / 2;          // dim pairs
-    constexpr int QS = 256 / DP;        // query stride
-    const int dp = tid % DP, tq = tid / DP;
-    float o0[NTOK / QS + 1], o1[NTOK / QS + 1];
+    // unnormalised output: thread = (dim pair dp, query group tq)
+    {
+      const int dp = tid % DP, tq = tid / DP;
+      float o0[OS], o1[OS];
 #pragma unroll
-    for (int r = 0; r <= NTOK / QS; ++r) o0[r] = o1[r] = 0.f;
-    const int kmax = (int)std::min<long long>(chunk, total - k0);
-    for (int j = 0; j < kmax; ++j) {
-      const T* vr = vc + ((size_t)h * ctx_max + k0 + j) * DH + 2 * dp;
-      float v0, v1;
-      if constexpr (sizeof(T) == 2) {
-        const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(vr);
-        v0 = __low2float(vv);
-        v1 = __high2float(vv);
-      } else {
-        const float2 vv = *reinterpret_cast<const float2*>(vr);
-        v0 = vv.x;
-        v1 = vv.y;
-      }
+      for (int r = 0; r < OS; ++r) o0[r] = o1[r] = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < kmax; ++j) {
+        float v0, v1;
+        if constexpr (sizeof(T) == 2) {
+          const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(v_s + j * VP + dp * 4);
+          v0 = __low2float(vv);
+          v1 = __high2float(vv);
+        } else {
+          const float2 vv = *reinterpret_cast<const float2*>(v_s + j * VP + dp * 8);
+          v0 = vv.x;
+          v1 = vv.y;
+        }
 #pragma unroll
-      for (int r = 0; r <= NTOK / QS; ++r) {
-        const int t = tq + r * QS;
-        if (t < n) {
-          const float p = p_s[t * chunk + j];
-          o0[r] = fmaf(p, v0, o0[r]);
-          o1[r] = fmaf(p, v1, o1[r]);
+        for (int r = 0; r < OS; ++r) {
+          const int t = tq + r * OG;
+          if (t < n) {
+            const float p = p_s[t * CH + j];
+            o0[r] = fmaf(p, v0, o0[r]);
+            o1[r] = fmaf(p, v1, o1[r]);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int r = 0; r <= NTOK / QS; ++r) {
-      const int t = tq + r * QS;
-      if (t < n) {
-        float* o = part_o + (((size_t)h * nchunk_max + cidx) * NTOK + t) * DH + 2 * dp;
-        o[0] = o0[r];
-        o[1] = o1[r];
+      for (int r = 0; r < OS; ++r) {
+        const int t = tq + r * OG;
+        if (t < n) {
+          float* o = part_o + (((size_t)h * nchunk_max + cidx) * NTOK + t) * DH + 2 * dp;
+          o[0] = o0[r];
+          o[1] = o1[r];
+        }
       }
     }
     if (tid < n) {
@@ -286,11 +337,11 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
 // (3) combine: grid (n, H), Dh threads; chunks in ascending order.
 template <typename T>
 __global__ void attn_combine_kernel(const float* part_o, const float* part_ml, int H, int Dh, int n,
-                                    int chunk, const evs_book* book, int nchunk_max, T* g) {
+                                    int chunk, long long ctx_max, const evs_book* book, int nchunk_max, T* g) {
   const int t = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
   pdl_trigger();
   pdl_wait();
-  const long long qpos = (long long)book->pos + t;
+  const long long qpos = min((long long)book->pos + t, ctx_max - 1);
   const int nc = (int)(qpos / chunk) + 1;  // chunks holding keys <= qpos
   const float* ml = part_ml + ((size_t)h * nchunk_max * NTOK + t) * 2;
   float M = -INFINITY;
@@ -342,18 +393,33 @@ cudaError_t iir_dispatch(const LaunchCtx& L, Src s, int d, int n, int M, const f
   }
 }
 
+template <typename T, int DH, int CH>
+cudaError_t attn_split_launch(const LaunchCtx& L, int H, int n, long long ctx_max, evs_book* book,
+                              const AttnBufs& B, void* kc, void* vc, int num_sms) {
+  const size_t smem = sizeof(float) * (NTOK * DH + NTOK * CH + NTOK * 2) +
+                      (size_t)CH * (DH * sizeof(T) + 16) + (size_t)CH * DH * sizeof(T);
+  auto k = attn_split_kernel<T, DH, CH>;
+  static bool attr_set = false;
+  if (!attr_set && smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int gx = std::max(1, std::min(B.nchunk_max, (4 * num_sms + H - 1) / H));
+  return launch(L, k, dim3(gx, H), dim3(256), smem, (const float*)B.qbuf, (const T*)kc, (const T*)vc, H, n,
+                ctx_max, (const evs_book*)book, B.part_o, B.part_ml, B.nchunk_max);
+}
+
 template <typename T, int DH>
 cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, int n, long long ctx_max, int chunk,
                                 evs_book* book, const AttnBufs& B, void* kc, void* vc, int num_sms) {
-  const size_t smem = sizeof(float) * (NTOK * DH + NTOK * chunk + NTOK * 2);
-  auto k = attn_split_kernel<T, DH>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  switch (chunk) {
+    case 32: return attn_split_launch<T, DH, 32>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
+    case 64: return attn_split_launch<T, DH, 64>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
+    case 128: return attn_split_launch<T, DH, 128>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
+    case 256: return attn_split_launch<T, DH, 256>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
+    default: return cudaErrorInvalidValue;
   }
-  const int gx = std::max(1, std::min(B.nchunk_max, (2 * num_sms + H - 1) / H));
-  return launch(L, k, dim3(gx, H), dim3(256), smem, (const float*)B.qbuf, (const T*)kc, (const T*)vc, H,
-                n, ctx_max, chunk, (const evs_book*)book, B.part_o, B.part_ml, B.nchunk_max);
 }
 
 template <typename T, typename Src>
@@ -370,37 +436,29 @@ cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, int n, long lo
   }
   if (e != cudaSuccess) return e;
   return launch(L, attn_combine_kernel<T>, dim3(n, H), dim3(Dh), 0, (const float*)B.part_o,
-                (const float*)B.part_ml, H, Dh, n, chunk, (const evs_book*)book, B.nchunk_max, (T*)g);
+                (const float*)B.part_ml, H, Dh, n, chunk, ctx_max, (const evs_book*)book, B.nchunk_max, (T*)g);
 }
 
 }  // namespace
 
 cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, int Lf, const float* taps,
                        float* ext0, float* ext1, const evs_book* book, void* g) {
-  if (src.part) {
-    SrcPartials s{*src.part};
-    return dtype == EVS_BF16 ? fir_dispatch<bf16>(L, s, d, n, Lf, taps, ext0, ext1, book, g)
-                             : fir_dispatch<float>(L, s, d, n, Lf, taps, ext0, ext1, book, g);
-  }
+  const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.plain, src.ld}, d, n, Lf, taps, ext0, ext1,
-                              book, g);
-  return fir_dispatch<float>(L, SrcPlain<float>{(const float*)src.plain, src.ld}, d, n, Lf, taps, ext0, ext1,
-                             book, g);
+    return src.f32 ? fir_dispatch<bf16>(L, sf, d, n, Lf, taps, ext0, ext1, book, g)
+                   : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, n, Lf, taps, ext0,
+                                        ext1, book, g);
+  return fir_dispatch<float>(L, sf, d, n, Lf, taps, ext0, ext1, book, g);
 }
 
 cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, int M, const float* lam,
                        const float* res, float* st0, float* st1, const evs_book* book, void* g) {
-  if (src.part) {
-    SrcPartials s{*src.part};
-    return dtype == EVS_BF16 ? iir_dispatch<bf16>(L, s, d, n, M, lam, res, st0, st1, book, g)
-                             : iir_dispatch<float>(L, s, d, n, M, lam, res, st0, st1, book, g);
-  }
+  const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return iir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.plain, src.ld}, d, n, M, lam, res, st0, st1,
-                              book, g);
-  return iir_dispatch<float>(L, SrcPlain<float>{(const float*)src.plain, src.ld}, d, n, M, lam, res, st0,
-                             st1, book, g);
+    return src.f32 ? iir_dispatch<bf16>(L, sf, d, n, M, lam, res, st0, st1, book, g)
+                   : iir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, n, M, lam, res, st0,
+                                        st1, book, g);
+  return iir_dispatch<float>(L, sf, d, n, M, lam, res, st0, st1, book, g);
 }
 
 size_t attn_scratch_bytes(int H, int Dh, long long ctx_max, int chunk) {
@@ -436,17 +494,12 @@ cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStre
 cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, int n,
                              long long ctx_max, int chunk, void* kc, void* vc,
                              evs_book* book, const AttnBufs& B, void* g, int num_sms) {
-  if (src.part) {
-    SrcPartials s{*src.part};
-    return dtype == EVS_BF16
-               ? attention_t<bf16>(L, s, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms)
-               : attention_t<float>(L, s, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms);
-  }
+  const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.plain, src.ld}, H, Dh, n, ctx_max, chunk,
-                             kc, vc, book, B, g, num_sms);
-  return attention_t<float>(L, SrcPlain<float>{(const float*)src.plain, src.ld}, H, Dh, n, ctx_max, chunk,
-                            kc, vc, book, B, g, num_sms);
+    return src.f32 ? attention_t<bf16>(L, sf, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms)
+                   : attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, H, Dh, n, ctx_max, chunk,
+                                       kc, vc, book, B, g, num_sms);
+  return attention_t<float>(L, sf, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms);
 }
 
 }  // namespace evs

@@ -40,16 +40,15 @@ struct AddF { __device__ float operator()(float a, float b) const { return a + b
 struct MaxF { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
 struct AddU { __device__ unsigned long long operator()(unsigned long long a, unsigned long long b) const { return a + b; } };
 
-// Residual update + RMSNorm of one token row, spread over the CTAs of a
+// Embedding + RMSNorm of one token row, spread over the CTAs of a
 // thread-block cluster (grid (CL, n), cluster (CL, 1, 1)): CTA r owns
-// columns [r*d/CL, (r+1)*d/CL).  mode 0 sets X[t] = E[token_t] (and marks
-// the block pending), mode 1 adds the GEMM partials.  Each CTA's sum of
-// squares is summed over the cluster's shared memory in rank order, so the
-// result is the same whatever the number of rows.
+// columns [r*d/CL, (r+1)*d/CL).  Sets X[t] = E[token_t], marks the block
+// pending, writes xn[t].  Each CTA's sum of squares is summed over the
+// cluster's shared memory in rank order, so the result does not depend on
+// the number of rows.
 template <typename T>
-__global__ void __launch_bounds__(256) row_norm_kernel(int mode, const T* E, const int32_t* tokens, int V,
-                                                       Partials P, float* X, int d, float eps, T* xn,
-                                                       evs_book* book, int n_mark) {
+__global__ void __launch_bounds__(256) embed_norm_kernel(const T* E, const int32_t* tokens, int V, float* X,
+                                                         int d, float eps, T* xn, evs_book* book, int n_mark) {
   __shared__ float scratch[32];
   __shared__ float ss_cta;
   cg::cluster_group cl = cg::this_cluster();
@@ -60,22 +59,14 @@ __global__ void __launch_bounds__(256) row_norm_kernel(int mode, const T* E, con
   pdl_wait();
   float* x = X + (size_t)t * d;
   float ss = 0.f;
-  if (mode == 0) {
-    if (n_mark > 0 && t == 0 && rank == 0 && threadIdx.x == 0) book->pending_n = n_mark;
-    const int tok = tokens[t];
-    const bool ok = tok >= 0 && tok < V;
-    if (!ok && rank == 0 && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
-    for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) {
-      const float v = ok ? to_f(E[(size_t)tok * d + c]) : 0.f;
-      x[c] = v;
-      ss = fmaf(v, v, ss);
-    }
-  } else {
-    for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) {
-      const float v = x[c] + partial_sum(P, t, c);
-      x[c] = v;
-      ss = fmaf(v, v, ss);
-    }
+  if (t == 0 && rank == 0 && threadIdx.x == 0) book->pending_n = n_mark;
+  const int tok = tokens[t];
+  const bool ok = tok >= 0 && tok < V;
+  if (!ok && rank == 0 && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
+  for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) {
+    const float v = ok ? to_f(E[(size_t)tok * d + c]) : 0.f;
+    x[c] = v;
+    ss = fmaf(v, v, ss);
   }
   ss = block_reduce(ss, AddF(), scratch);
   if (threadIdx.x == 0) ss_cta = ss;
@@ -95,22 +86,35 @@ int row_cluster(int d) {
   return cl;
 }
 
+// RMSNorm of rows whose residual update the out / down GEMM already applied:
+// the row's sum of squares is the GEMM's per-tile sums added in tile order.
 template <typename T>
-__global__ void mlp_act_kernel(Partials P, int F, T* h) {
+__global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const float* ss, int ntiles, int d,
+                                                         float eps, T* xn) {
+  __shared__ float s_den;
+  const int t = blockIdx.y;
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int k = 0; k < ntiles; ++k) tot += ss[k * NTOK + t];
+    s_den = sqrtf(tot / (float)d + eps);
+  }
+  __syncthreads();
+  const float den = s_den;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c < d) xn[(size_t)t * d + c] = from_f<T>(X[(size_t)t * d + c] / den);
+}
+
+template <typename T>
+__global__ void mlp_act_kernel(const float* gu, int F, T* h) {
   const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_trigger();
   pdl_wait();
   if (j >= F) return;
-  const float gt = partial_sum(P, t, j), up = partial_sum(P, t, F + j);
+  const float gt = gu[(size_t)t * 2 * F + j], up = gu[(size_t)t * 2 * F + F + j];
   const float s = gt / (1.f + expf(-gt));
   h[(size_t)t * F + j] = from_f<T>(s * up);
-}
-
-__global__ void logits_kernel(Partials P, int V, float* logits) {
-  const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
-  pdl_trigger();
-  pdl_wait();
-  if (j < V) logits[(size_t)t * V + j] = partial_sum(P, t, j);
 }
 
 // One CTA per row.  top-k by rank: entry j is kept iff fewer than k entries
@@ -310,32 +314,26 @@ __global__ void book_set_kernel(evs_book* book, evs_book v) {
 cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, const int32_t* tokens, int n,
                               int d, int V, float eps, float* X, void* xn, evs_book* book) {
   const int cl = row_cluster(d);
-  Partials none{};
   if (dtype == EVS_BF16)
-    return launch_cl(L, cl, row_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, 0, (const bf16*)E, tokens, V, none,
-                     X, d, eps, (bf16*)xn, book, n);
-  return launch_cl(L, cl, row_norm_kernel<float>, dim3(cl, n), dim3(256), 0, 0, (const float*)E, tokens, V, none,
-                   X, d, eps, (float*)xn, book, n);
+    return launch_cl(L, cl, embed_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, (const bf16*)E, tokens, V, X, d,
+                     eps, (bf16*)xn, book, n);
+  return launch_cl(L, cl, embed_norm_kernel<float>, dim3(cl, n), dim3(256), 0, (const float*)E, tokens, V, X, d,
+                   eps, (float*)xn, book, n);
 }
 
-cudaError_t launch_residual_norm(const LaunchCtx& L, int dtype, const Partials& P, float* X, int n, int d,
-                                 float eps, void* xn) {
-  const int cl = row_cluster(d);
+cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, const float* ss, int n, int d,
+                              float eps, void* xn) {
+  const int ntiles = (d + TILE_M - 1) / TILE_M;
+  const dim3 g((d + 255) / 256, n);
   if (dtype == EVS_BF16)
-    return launch_cl(L, cl, row_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, 1, (const bf16*)nullptr,
-                     (const int32_t*)nullptr, 0, P, X, d, eps, (bf16*)xn, (evs_book*)nullptr, 0);
-  return launch_cl(L, cl, row_norm_kernel<float>, dim3(cl, n), dim3(256), 0, 1, (const float*)nullptr,
-                   (const int32_t*)nullptr, 0, P, X, d, eps, (float*)xn, (evs_book*)nullptr, 0);
+    return launch(L, norm_apply_kernel<bf16>, g, dim3(256), 0, X, ss, ntiles, d, eps, (bf16*)xn);
+  return launch(L, norm_apply_kernel<float>, g, dim3(256), 0, X, ss, ntiles, d, eps, (float*)xn);
 }
 
-cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const Partials& P, int n, int F, void* h) {
+cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const float* gu, int n, int F, void* h) {
   const dim3 g((F + 255) / 256, n);
-  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, P, F, (bf16*)h);
-  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, P, F, (float*)h);
-}
-
-cudaError_t launch_logits(const LaunchCtx& L, const Partials& P, int n, int V, float* logits) {
-  return launch(L, logits_kernel, dim3((V + 255) / 256, n), dim3(256), 0, P, V, logits);
+  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, gu, F, (bf16*)h);
+  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, gu, F, (float*)h);
 }
 
 cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, float T, int top_k, float* p) {

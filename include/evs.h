@@ -93,7 +93,7 @@ typedef struct evs_config {
   int32_t d_ffn;
   int32_t gamma_max;      /* verify blocks hold n <= gamma_max + 1 <= 16 tokens */
   int32_t dtype;          /* EVS_BF16 or EVS_F32 */
-  int32_t attn_chunk;     /* keys per split-KV chunk, multiple of 32 (e.g. 256) */
+  int32_t attn_chunk;     /* keys per split-KV chunk: 32, 64, 128 or 256 */
   float rope_base;        /* e.g. 10000 */
   float norm_eps;         /* e.g. 1e-6 */
   const int32_t* layer_kind_host;   /* [n_layers] EVS_LAYER_* */

@@ -50,7 +50,7 @@ class ModelShape:
     residue_std: float = 0.25
     rope_base: float = 10000.0
     norm_eps: float = 1e-6
-    attn_chunk: int = 256                 # keys per split-KV chunk on the GPU (absolute, fixed)
+    attn_chunk: int = 64                  # keys per split-KV chunk on the GPU (absolute, fixed)
 
     @property
     def n_block(self) -> int:
