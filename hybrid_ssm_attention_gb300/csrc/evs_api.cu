@@ -190,6 +190,7 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     P.nG = np->G;
     P.nKB = np->KB;
     P.nU = np->U;
+    P.ncl = np->cl;
 #ifdef EVS_TRACE
     P.trace = s->trace;
     P.trace_slot = gk - 1;
@@ -320,7 +321,7 @@ int check_cfg(const evs_config* c) {
   for (int i = 0; i < c->n_layers; ++i) {
     const int k = c->layer_kind_host[i], p = c->layer_param_host[i];
     if (k == EVS_LAYER_FIR) {
-      if (p < 1 || p > 1024) return fail(EVS_ERR_UNSUPPORTED, "layer %d: FIR length must be in [1, 1024]", i);
+      if (p < 1 || p > 256) return fail(EVS_ERR_UNSUPPORTED, "layer %d: FIR length must be in [1, 256]", i);
     } else if (k == EVS_LAYER_IIR) {
       if (p < 1 || p > 32 || (p & (p - 1))) return fail(EVS_ERR_UNSUPPORTED, "layer %d: IIR poles must be a power of two <= 32", i);
       if (c->d_model % (256 / p)) return fail(EVS_ERR_UNSUPPORTED, "layer %d: d_model * poles must be a multiple of 256", i);
@@ -408,7 +409,12 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     size_t tb = 0;
     m->ws_bytes = 0;
     for (int k = 0; k < 5; ++k) {
-      if (!plan_gemm(shapes[k][0], shapes[k][1], m->num_sms, &plans[k])) {
+      const char* cl_env = getenv("EVS_GEMM_CLUSTER");
+      const bool allow_cl = m->tc && !(cl_env && cl_env[0] == '0');
+      const int cl = allow_cl ? gemm_cluster_choice(shapes[k][0], shapes[k][1], m->num_sms) : 0;
+      const bool planned = cl ? plan_gemm_cluster(shapes[k][0], shapes[k][1], cl, &plans[k])
+                              : plan_gemm(shapes[k][0], shapes[k][1], m->num_sms, &plans[k]);
+      if (!planned) {
         delete m;
         return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d has too many column tiles", shapes[k][0], shapes[k][1]);
       }
@@ -492,7 +498,7 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
   ALLOC(s->cnt, sizeof(int) * s->cnt_len);
 #ifdef EVS_TRACE
-  ALLOC(s->trace, sizeof(unsigned long long) * 3 * 1024);
+  ALLOC(s->trace, sizeof(unsigned long long) * 6 * 1024);
 #endif
   size_t wsb = 0;
   wsb = m->ws_bytes;
@@ -777,7 +783,7 @@ extern "C" int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_
                           const float* taps, float* e0, float* e1, const evs_book* book, void* g,
                           cudaStream_t stream) {
   if (!abv || !taps || !e0 || !e1 || !book || !g) return fail(EVS_ERR_ARG, "null argument");
-  if (L < 1 || L > 1024 || d < 32 || d % 32 || n < 1 || n > NTOK || n > n_max)
+  if (L < 1 || L > 256 || d < 32 || d % 32 || n < 1 || n > NTOK || n > n_max)
     return fail(EVS_ERR_ARG, "bad FIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
@@ -832,14 +838,17 @@ extern "C" int evs_op_commit(evs_book* book, int32_t keep, int32_t n, cudaStream
 }
 
 // Operator GEMM scratch: [partial slots][slot table][arrival counters][error flag],
-// each part 256-byte aligned
-static int gemm_plan_op(int32_t N, int32_t K, GemmPlan* g, size_t* table_off, size_t* total) {
+// each part 256-byte aligned.  The stream-K plan is sized; the tensor-core
+// path may use the (slot-free) cluster plan within the same scratch.
+static int gemm_plan_op(int32_t N, int32_t K, bool cluster_ok, GemmPlan* g, size_t* table_off, size_t* total) {
   int sms = 0;
   EVS_TRY(num_sms_current(&sms));
   if (!plan_gemm(N, K, sms, g)) return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d unsupported", N, K);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   *table_off = al(partials_bytes(*g));
   *total = *table_off + 2 * al(table_bytes(*g)) + 256;
+  const int cl = cluster_ok ? gemm_cluster_choice(N, K, sms) : 0;
+  if (cl && !plan_gemm_cluster(N, K, cl, g)) return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d unsupported", N, K);
   return EVS_OK;
 }
 
@@ -848,7 +857,7 @@ extern "C" size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype)
   if (N < 1 || K < 1) return 0;
   static thread_local GemmPlan g;
   size_t toff = 0, total = 0;
-  if (gemm_plan_op(N, K, &g, &toff, &total) != EVS_OK) return 0;
+  if (gemm_plan_op(N, K, false, &g, &toff, &total) != EVS_OK) return 0;
   return total;
 }
 
@@ -859,7 +868,8 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   static thread_local GemmPlan g;
   size_t toff = 0, total = 0;
-  EVS_TRY(gemm_plan_op(N, K, &g, &toff, &total));
+  const bool tc = dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X);
+  EVS_TRY(gemm_plan_op(N, K, tc, &g, &toff, &total));
   if (scratch_bytes < total) return fail(EVS_ERR_ARG, "scratch too small (%zu < %zu)", scratch_bytes, total);
   Partials P = g.P;
   P.ws = (float*)scratch;
@@ -875,7 +885,7 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
   CUDA_TRY(cudaMemsetAsync(P.cnt, 0, tb, stream));
   CUDA_TRY(cudaStreamSynchronize(stream));  // g is reused by the next call
   LaunchCtx Lc{stream, false};
-  if (dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X)) {
+  if (tc) {
     CUtensorMap wm, xm;
     char err[256] = {0};
     if (!encode_tmap_2d(&wm, W, K, N, TILE_K, TILE_M, err, sizeof err) ||
@@ -946,20 +956,20 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
 }
 
 #ifdef EVS_TRACE
-// Timeline of the GEMM launches since the previous call: out[3k..3k+2] =
-// {entry, dependency release, exit} of the k-th GEMM; re-arms the slots.
+// Timeline of the GEMM launches since the previous call: out[6k..6k+5] =
+// {first entry, first dependency release, last exit, first MMA, last
+// accumulator drain, last fixup end} of the k-th GEMM; re-arms the slots.
 extern "C" int evs_trace_read(evs_state* s, unsigned long long* out, int32_t max_slots) {
   if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
   const int k = std::min(max_slots, 1024);
   CUDA_TRY(cudaDeviceSynchronize());
-  CUDA_TRY(cudaMemcpy(out, s->trace, sizeof(unsigned long long) * 3 * k, cudaMemcpyDeviceToHost));
-  std::vector<unsigned long long> init(3 * 1024);
+  CUDA_TRY(cudaMemcpy(out, s->trace, sizeof(unsigned long long) * 6 * k, cudaMemcpyDeviceToHost));
+  std::vector<unsigned long long> init(6 * 1024);
   for (int i = 0; i < 1024; ++i) {
-    init[3 * i] = ~0ull;
-    init[3 * i + 1] = ~0ull;
-    init[3 * i + 2] = 0;
+    init[6 * i] = init[6 * i + 1] = init[6 * i + 3] = ~0ull;
+    init[6 * i + 2] = init[6 * i + 4] = init[6 * i + 5] = 0;
   }
-  CUDA_TRY(cudaMemcpy(s->trace, init.data(), sizeof(unsigned long long) * 3 * 1024, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(s->trace, init.data(), sizeof(unsigned long long) * 6 * 1024, cudaMemcpyHostToDevice));
   return EVS_OK;
 }
 #endif

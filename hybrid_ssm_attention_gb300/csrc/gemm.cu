@@ -31,6 +31,7 @@ bool plan_gemm(int N, int K, int num_sms, GemmPlan* g) {
   // at most MAX_CONTRIB CTAs per tile: the last one sums their slots
   constexpr int MAX_CONTRIB = 8;
   P.G = (int)std::min<long long>(std::min<long long>(num_sms, P.U), (long long)T * MAX_CONTRIB);
+  P.stages = 8;
   int base = 0;
   for (int t = 0; t < T; ++t) {
     const int c0 = unit_owner(P.U, P.G, (long long)t * P.KB);
@@ -40,6 +41,38 @@ bool plan_gemm(int N, int K, int num_sms, GemmPlan* g) {
   }
   g->slots = base;
   return true;
+}
+
+bool plan_gemm_cluster(int N, int K, int cl, GemmPlan* g) {
+  Partials& P = g->P;
+  P = Partials{};
+  P.N = N;
+  const int T = (N + TILE_M - 1) / TILE_M;
+  if (T > 1024 || N < 1 || K < 1 || cl < 1 || cl > 8) return false;
+  P.KB = (K + TILE_K - 1) / TILE_K;
+  if (P.KB < cl) return false;
+  P.U = (long long)T * P.KB;
+  P.G = T * cl;
+  P.cl = cl;
+  // a CTA that owns a whole tile has the shared memory to itself: deepest ring
+  P.stages = cl == 1 ? GEMM_MAX_STAGES : 8;
+  for (int t = 0; t < T; ++t) g->tab[t] = make_int4(0, 0, 0, 0);
+  g->slots = 0;
+  return true;
+}
+
+// Tiles that would each be shared by several stream-K CTAs (few tiles for
+// the SMs) reduce inside a cluster instead: the largest portable cluster
+// size cl <= 8 with T * cl <= num_sms and KB >= cl; a single K-block gives
+// tile mode (cl = 1).  Tile-rich shapes (more than num_sms / 2 tiles) keep
+// stream-K (0): one tile per CTA there leaves SMs idle and measured slower.
+int gemm_cluster_choice(int N, int K, int num_sms) {
+  const int T = (N + TILE_M - 1) / TILE_M;
+  const int KB = (K + TILE_K - 1) / TILE_K;
+  if (2 * T > num_sms) return 0;
+  int cl = 8;
+  while (cl > 1 && (T * cl > num_sms || KB < cl)) cl >>= 1;
+  return cl;
 }
 
 bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
@@ -72,16 +105,18 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 namespace {
 
-#ifndef EVS_GEMM_STAGES
-#define EVS_GEMM_STAGES 8
-#endif
-constexpr int STAGES = EVS_GEMM_STAGES;
 constexpr int A_BYTES = TILE_M * TILE_K * 2;  // 16 KB weight tile
 constexpr int B_BYTES = NTOK * TILE_K * 2;    // 2 KB activation tile
 constexpr int GEMM_THREADS = 192;             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint64_t WAIT_NS = 4000000000ull;   // upper bound on any pipeline wait
-constexpr int NBARS = 2 * STAGES + 5;         // full, empty, acc_full[2], acc_empty[2], drain
-constexpr size_t GEMM_SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + NBARS * 8 + 16 + 4 * NTOK * 4;
+constexpr size_t CL_SLOT = (size_t)NTOK * TILE_M * sizeof(float);  // one rank's accumulator
+// dynamic shared memory of a launch with S ring stages and cl cluster ranks:
+// alignment slack, ring, barriers (full, empty: S each; acc_full[2],
+// acc_empty[2], drain), TMEM slot + flags, reduction scratch, cluster slots
+__host__ __device__ constexpr size_t gemm_smem(int S, int cl) {
+  return 1024 + (size_t)S * (A_BYTES + B_BYTES) + (size_t)(2 * S + 5) * 8 + 16 + 4 * NTOK * 4 +
+         (size_t)(cl > 1 ? cl - 1 : 0) * CL_SLOT;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -228,6 +263,47 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// Writes the final sums v[] of column tile*128+row: GEMM_FINAL to P.fin,
+// GEMM_RESID into P.X plus the tile's per-token sums of squares (butterfly
+// within each warp, then the four warps in order).  Called by the 128
+// group threads.
+template <bool NAMED>
+__device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red) {
+  const int col = tile * TILE_M + row;
+  const bool ok = col < P.N;
+  const int n = P.n;
+  if (P.mode == GEMM_FINAL) {
+    if (ok) {
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t)
+        if (t < n) P.fin[(size_t)t * P.fin_ld + col] = v[t];
+    }
+  } else {
+    const int lane = row & 31, w = row >> 5;
+    // all residual loads first (independent, in flight together), then the
+    // updates and the per-token butterflies
+    float x[NTOK];
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) x[t] = (t < n && ok) ? P.X[(size_t)t * P.N + col] : 0.f;
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t)
+      if (t < n && ok) {
+        x[t] += v[t];
+        P.X[(size_t)t * P.N + col] = x[t];
+      }
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      float sq = x[t] * x[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (lane == 0) s_red[w * NTOK + t] = sq;
+    }
+    group_sync<NAMED>();
+    if (row < NTOK) P.ss[tile * NTOK + row] = ((s_red[row] + s_red[NTOK + row]) + s_red[2 * NTOK + row]) +
+                                              s_red[3 * NTOK + row];
+  }
+}
+
 template <bool NAMED>
 __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_flag, float* s_red) {
   // The barrier orders the group's slot stores before thread 0's
@@ -241,8 +317,6 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
   const int arrived = *s_flag;
   group_sync<NAMED>();  // every thread has read the flag before it is reused
   if (arrived != e.y - 1) return;
-  const int col = tile * TILE_M + row;
-  const bool ok = col < P.N;
   const int n = P.n;
   const float* p = P.ws + (size_t)e.x * NTOK * TILE_M + row;
   float v[NTOK];
@@ -265,30 +339,7 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
         for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
       }
   }
-  if (P.mode == GEMM_FINAL) {
-    if (ok) {
-#pragma unroll
-      for (int t = 0; t < NTOK; ++t)
-        if (t < n) P.fin[(size_t)t * P.fin_ld + col] = v[t];
-    }
-  } else {
-    const int lane = row & 31, w = row >> 5;
-#pragma unroll
-    for (int t = 0; t < NTOK; ++t) {
-      float sq = 0.f;
-      if (t < n && ok) {
-        const float x = P.X[(size_t)t * P.N + col] + v[t];
-        P.X[(size_t)t * P.N + col] = x;
-        sq = x * x;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      if (lane == 0) s_red[w * NTOK + t] = sq;
-    }
-    group_sync<NAMED>();
-    if (row < NTOK) P.ss[tile * NTOK + row] = ((s_red[row] + s_red[NTOK + row]) + s_red[2 * NTOK + row]) +
-                                              s_red[3 * NTOK + row];
-  }
+  tile_output<NAMED>(P, tile, row, v, s_red);
   if (row == 0) P.cnt[tile] = 0;
 }
 
@@ -296,15 +347,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const __grid_constant__ CUtensorMap nmap, Partials P, int* err_flag) {
   extern __shared__ uint8_t smem_raw[];
+  const int STAGES = P.stages;  // ring depth of this launch
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
   float* s_red = reinterpret_cast<float*>(tmem_slot + 4);  // [4][NTOK]
+  float* s_cl = s_red + 4 * NTOK;  // cluster mode, rank 0: [cl-1][NTOK][TILE_M] partials of ranks 1..cl-1
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto acc_full = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
@@ -313,10 +366,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const long long ub = unit_begin(P.U, P.G, c), ue = unit_begin(P.U, P.G, c + 1);
+  // cl >= 1: one tile per CTA group (cl == 1: a whole tile per CTA, no
+  // reduction; cl > 1: K split over the ranks of a cluster); cl == 0: stream-K
+  const bool clmode = P.cl >= 1;
+  int crank = 0;
+  long long ub, ue;
+  if (clmode) {
+    if (P.cl > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    const long long t0 = (long long)(c / P.cl) * P.KB;
+    ub = t0 + (long long)crank * P.KB / P.cl;
+    ue = t0 + (long long)(crank + 1) * P.KB / P.cl;
+  } else {
+    ub = unit_begin(P.U, P.G, c);
+    ue = unit_begin(P.U, P.G, c + 1);
+  }
   const long long nunits = ue - ub;
   const int first_tile = (int)(ub / P.KB);
   const int nseg = (int)((ue - 1) / P.KB) - first_tile + 1;
+  float vkeep[NTOK];  // cluster mode: this CTA's accumulator column, kept across the cluster barrier
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) vkeep[t] = 0.f;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -330,7 +399,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
 #ifdef EVS_TRACE
-    if (P.trace) atomicMin(P.trace + 3 * P.trace_slot, gtimer());
+    if (P.trace) atomicMin(P.trace + 6 * P.trace_slot, gtimer());
 #endif
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
@@ -360,7 +429,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     pdl_wait();  // activations are written by the preceding kernel
 #ifdef EVS_TRACE
-    if (P.trace) atomicMin(P.trace + 3 * P.trace_slot + 1, gtimer());
+    if (P.trace) atomicMin(P.trace + 6 * P.trace_slot + 1, gtimer());
 #endif
     for (int i = 0; i < pre; ++i) {
       const long long u = ub + i;
@@ -382,7 +451,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // weight matrix (the ones the CTA of the same index will read first)
     // into L2.
     if (i == nunits && P.pf_units > 0 && c < P.nG) {
-      const long long nb = unit_begin(P.nU, P.nG, c), ne = unit_begin(P.nU, P.nG, c + 1);
+      long long nb, ne;
+      if (P.ncl >= 1) {
+        const long long t0 = (long long)(c / P.ncl) * P.nKB;
+        nb = t0 + (long long)(c % P.ncl) * P.nKB / P.ncl;
+        ne = t0 + (long long)(c % P.ncl + 1) * P.nKB / P.ncl;
+      } else {
+        nb = unit_begin(P.nU, P.nG, c);
+        ne = unit_begin(P.nU, P.nG, c + 1);
+      }
       const long long stop = std::min<long long>(ne, nb + P.pf_units);
       for (long long u = nb; u < stop; ++u)
         tma_prefetch_l2(&nmap, (int)(u % P.nKB) * TILE_K, (int)(u / P.nKB) * TILE_M);
@@ -419,6 +496,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < TILE_K / 16; ++k)  // 16 bf16 = 32 bytes per MMA step along K
           mma_bf16(dt, ad + 2 * k, bd + 2 * k, IDESC, (first && k == 0) ? 0u : 1u);
+#ifdef EVS_TRACE
+        if (i == 0 && P.trace) atomicMin(P.trace + 6 * P.trace_slot + 3, gtimer());
+#endif
         first = false;
         mma_commit(empty(s));
       }
@@ -446,7 +526,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NTOK), v);
       tc_fence_before();
       mbar_arrive(acc_empty(b));
+#ifdef EVS_TRACE
+      if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 4, gtimer());
+#endif
       const int tile = first_tile + seg;
+      if (clmode) {
+        // ranks 1..cl-1 send their column to rank 0's shared memory
+        if (crank == 0) {
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j) vkeep[j] = v[j];
+        } else {
+          const uint32_t local = smem_u32(s_cl + ((size_t)(crank - 1) * NTOK) * TILE_M + row);
+          uint32_t remote;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(0));
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j)
+            if (j < P.n)
+              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote + (uint32_t)(j * TILE_M * 4)), "f"(v[j])
+                           : "memory");
+        }
+        continue;
+      }
       const int4 e = __ldg(P.tab + tile);
       const long long slot = e.x + (c - e.z);
       float* dst = P.ws + slot * NTOK * TILE_M + row;
@@ -454,18 +554,46 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int j = 0; j < NTOK; ++j)
         if (j < P.n) __stcg(dst + j * TILE_M, v[j]);
       tile_done<true>(P, tile, row, s_flag, s_red);
+#ifdef EVS_TRACE
+      if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 5, gtimer());
+#endif
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (clmode) {
+    if (P.cl > 1) {
+      // every thread of every rank: the partials sent to rank 0 are visible
+      // after this barrier (release / acquire at cluster scope)
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
+    if (crank == 0 && warp >= 2 && !*abort_flag) {
+      const int row = (warp & 3) * 32 + lane;
+      for (int r = 1; r < P.cl; ++r) {
+        const float* src = s_cl + ((size_t)(r - 1) * NTOK) * TILE_M + row;
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j)
+          if (j < P.n) vkeep[j] += src[j * TILE_M];
+      }
+      tile_output<true>(P, first_tile, row, vkeep, s_red);
+#ifdef EVS_TRACE
+      if (threadIdx.x == 64 && P.trace) {
+        const unsigned long long now = gtimer();
+        atomicMax(P.trace + 6 * P.trace_slot + 5, now);
+        atomicMax(P.trace + 6 * P.trace_slot + 2, now);  // the kernel's real end
+      }
+#endif
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
 #ifdef EVS_TRACE
-  if (threadIdx.x == 0 && P.trace) atomicMax(P.trace + 3 * P.trace_slot + 2, gtimer());
+  if (threadIdx.x == 0 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 2, gtimer());
 #endif
 }
 
@@ -522,14 +650,17 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
 cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CUtensorMap& xmap,
                            const CUtensorMap& nmap, const Partials& P, int K, int* err_flag) {
   (void)K;
+  const int cl = P.cl > 1 ? P.cl : 1;
+  const size_t smem = gemm_smem(P.stages, cl);
+  if (P.stages < 2 || P.stages > GEMM_MAX_STAGES || smem > 232448) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)GEMM_SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(L, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), GEMM_SMEM, wmap, xmap, nmap, P, err_flag);
+  return launch_cl(L, cl, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), smem, wmap, xmap, nmap, P, err_flag);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& L, int dtype, const void* W, const void* X, int ldx,

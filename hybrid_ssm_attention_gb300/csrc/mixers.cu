@@ -21,10 +21,21 @@
 namespace evs {
 namespace {
 
+// 16-byte global -> shared copy that does not block the issuing thread;
+// cp_async_wait_all() waits for all of the thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ FIR
-// Block = 32 channels x NW warps; warp w sums taps [w*J, (w+1)*J).
-template <typename T, typename Src>
-__global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf, int J,
+// Block = 32 channels x NW warps; warp w sums taps [w*J, (w+1)*J), J = JT.
+// Each lane keeps its J taps and the J + 15 window values they touch in
+// registers.
+template <typename T, typename Src, int JT>
+__global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
                                                   const float* __restrict__ taps, float* ext0,
                                                   float* ext1, const evs_book* book, T* g) {
   extern __shared__ float sm[];
@@ -44,11 +55,22 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
   const int bank = book->fir_bank, off = book->fir_off;
   const float* src_ext = bank ? ext1 : ext0;
   float* dst_ext = bank ? ext0 : ext1;
-  for (int j = warp; j < Lf; j += NW) tap_s[j * 32 + lane] = taps[(size_t)j * d + c];
-  for (int r = warp; r < Lf - 1; r += NW) {
-    const float w = src_ext[(size_t)(off + r) * d + c];
-    ext_s[r * 32 + lane] = w;
-    dst_ext[(size_t)r * d + c] = w;
+  // rows of 32 channels = 128 bytes = 8 x 16-byte pieces, all copies in flight at once
+  const int nthr = blockDim.x;
+  for (int e = threadIdx.x; e < Lf * 8; e += nthr) {
+    const int j = e >> 3, w = e & 7;
+    cp_async16(tap_s + j * 32 + w * 4, taps + (size_t)j * d + c0 + w * 4);
+  }
+  for (int e = threadIdx.x; e < (Lf - 1) * 8; e += nthr) {
+    const int r = e >> 3, w = e & 7;
+    cp_async16(ext_s + r * 32 + w * 4, src_ext + (size_t)(off + r) * d + c0 + w * 4);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int e = threadIdx.x; e < (Lf - 1) * 8; e += nthr) {
+    const int r = e >> 3, w = e & 7;
+    *reinterpret_cast<float4*>(dst_ext + (size_t)r * d + c0 + w * 4) =
+        *reinterpret_cast<const float4*>(ext_s + r * 32 + w * 4);
   }
   pdl_wait();
   for (int t = warp; t < n; t += NW) {
@@ -60,11 +82,28 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
     dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
   }
   __syncthreads();
-  const int j0 = warp * J, j1 = min(Lf, j0 + J);
-  for (int t = 0; t < n; ++t) {
-    float acc = 0.f;
-    for (int j = j0; j < j1; ++j) acc = fmaf(tap_s[j * 32 + lane], ext_s[(Lf - 1 + t - j) * 32 + lane], acc);
-    part_s[(warp * n + t) * 32 + lane] = acc;
+  // y_t partial = sum_{j in [j0, j0+JT), j < Lf} h[j] * ext[Lf-1+t-j]; the
+  // window rows used are base .. base+JT+NTOK-2 with base = Lf-1-j0-(JT-1)
+  const int j0 = warp * JT;
+  const int base = Lf - 1 - j0 - (JT - 1);
+  float hreg[JT];
+  float wreg[JT + NTOK - 1];
+#pragma unroll
+  for (int q = 0; q < JT; ++q) hreg[q] = (j0 + q < Lf) ? tap_s[(j0 + q) * 32 + lane] : 0.f;
+#pragma unroll
+  for (int q = 0; q < JT + NTOK - 1; ++q) {
+    const int p = base + q;
+    wreg[q] = (p >= 0 && p < rows) ? ext_s[p * 32 + lane] : 0.f;
+  }
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) {
+    if (t < n) {
+      float acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < JT; ++q)
+        if (j0 + q < Lf) acc = fmaf(hreg[q], wreg[t - q + JT - 1], acc);
+      part_s[(warp * n + t) * 32 + lane] = acc;
+    }
   }
   __syncthreads();
   for (int t = warp; t < n; t += NW) {
@@ -220,11 +259,10 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
     constexpr int VEC = DH * (int)sizeof(T) / 16;  // 16-byte vectors per row
     for (int e = tid; e < kmax * VEC; e += 256) {
       const int j = e / VEC, w = e % VEC;
-      const uint4 kv = *reinterpret_cast<const uint4*>(kc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
-      const uint4 vv = *reinterpret_cast<const uint4*>(vc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
-      *reinterpret_cast<uint4*>(k_s + j * KP + w * 16) = kv;
-      *reinterpret_cast<uint4*>(v_s + j * VP + w * 16) = vv;
+      cp_async16(k_s + j * KP + w * 16, kc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
+      cp_async16(v_s + j * VP + w * 16, vc + ((size_t)h * ctx_max + k0 + j) * DH + w * 16 / sizeof(T));
     }
+    cp_async_wait_all();
     __syncthreads();
     // scores: thread = (key slot j, query group tq)
     {
@@ -345,14 +383,19 @@ __global__ void attn_combine_kernel(const float* part_o, const float* part_ml, i
   const int nc = (int)(qpos / chunk) + 1;  // chunks holding keys <= qpos
   const float* ml = part_ml + ((size_t)h * nchunk_max * NTOK + t) * 2;
   float M = -INFINITY;
+#pragma unroll 8
   for (int c = 0; c < nc; ++c) M = fmaxf(M, ml[(size_t)c * NTOK * 2]);
   float l = 0.f, o = 0.f;
+  // loads are independent of the running sums: unrolled so they overlap
+#pragma unroll 8
   for (int c = 0; c < nc; ++c) {
     const float mc = ml[(size_t)c * NTOK * 2];
+    const float lc = ml[(size_t)c * NTOK * 2 + 1];
+    const float oc = part_o[(((size_t)h * nchunk_max + c) * NTOK + t) * Dh + e];
     if (mc == -INFINITY) continue;
     const float w = expf(mc - M);
-    l = fmaf(ml[(size_t)c * NTOK * 2 + 1], w, l);
-    o = fmaf(part_o[(((size_t)h * nchunk_max + c) * NTOK + t) * Dh + e], w, o);
+    l = fmaf(lc, w, l);
+    o = fmaf(oc, w, o);
   }
   g[(size_t)t * H * Dh + h * Dh + e] = from_f<T>(o / l);
 }
@@ -361,14 +404,24 @@ template <typename T, typename Src>
 cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, int n, int Lf, const float* taps,
                          float* e0, float* e1, const evs_book* book, void* g) {
   const int NW = std::min(8, Lf);
-  const int J = (Lf + NW - 1) / NW;
+  int J = 1;
+  while (J * NW < Lf) J <<= 1;  // taps per warp, a power of two <= 32 (Lf <= 256)
   const size_t smem = sizeof(float) * 32 * ((Lf - 1 + n) + n + Lf + NW * n);
-  auto k = fir_kernel<T, Src>;
+  void (*k)(Src, int, int, int, const float*, float*, float*, const evs_book*, T*);
+  switch (J) {
+    case 1: k = fir_kernel<T, Src, 1>; break;
+    case 2: k = fir_kernel<T, Src, 2>; break;
+    case 4: k = fir_kernel<T, Src, 4>; break;
+    case 8: k = fir_kernel<T, Src, 8>; break;
+    case 16: k = fir_kernel<T, Src, 16>; break;
+    case 32: k = fir_kernel<T, Src, 32>; break;
+    default: return cudaErrorInvalidValue;
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch(L, k, dim3(d / 32), dim3(32 * NW), smem, s, d, n, Lf, J, taps, e0, e1, book, (T*)g);
+  return launch(L, k, dim3(d / 32), dim3(32 * NW), smem, s, d, n, Lf, taps, e0, e1, book, (T*)g);
 }
 
 template <typename T, typename Src, int M>

@@ -6,7 +6,7 @@
         default shape) is larger than L2, so each launch streams it from HBM.
     python -m hybrid_ssm_attention_gb300.profile_case fir 128 4096 13
     python -m hybrid_ssm_attention_gb300.profile_case iir 16 4096 13
-    python -m hybrid_ssm_attention_gb300.profile_case attn 8192 13
+    python -m hybrid_ssm_attention_gb300.profile_case attn 8192 13   (split-KV chunks of 64 keys)
 """
 from __future__ import annotations
 
@@ -56,7 +56,7 @@ def main():
                 evs.evs_op_iir(P, d, n, n, evs.EVS_BF16, abv, lam, res, s0, s1, book, gout)
     else:
         P, n = (a.args + [8192, 13][len(a.args):])[:2]
-        H, Dh, chunk = 32, 128, 256
+        H, Dh, chunk = 32, 128, 64
         ctx = P + n
         kc = torch.randn(H, ctx, Dh, device=dev, generator=g).to(torch.bfloat16)
         vc = torch.randn(H, ctx, Dh, device=dev, generator=g).to(torch.bfloat16)

@@ -74,7 +74,7 @@ enum { EVS_GREEDY = 0, EVS_SAMPLE = 1 };
 /* ---------------------------------------------------------------- model */
 /* Shape of the hybrid stack.  Layer i is
  *   EVS_LAYER_FIR  : Hyena mixer with an explicit causal filter of length
- *                    layer_param[i] (short / medium FIR, [systems]);
+ *                    layer_param[i] in [1, 256] (short / medium FIR, [systems]);
  *   EVS_LAYER_IIR  : Hyena mixer with a modal IIR filter of layer_param[i]
  *                    diagonal complex poles (1..32) ([systems]);
  *   EVS_LAYER_ATTN : multi-head attention with rotary embedding over an
@@ -260,7 +260,8 @@ int evs_round(evs_state* s, const int32_t* tokens_dev, int32_t n, float* logits_
  * abv_dev [n][3d] storage dtype (a|b|v), taps [L][d], ext banks
  * [L-1+n_max][d] float32, book_dev: fir_bank / fir_off / pos are read,
  * nothing written.  Writes g_dev [n][d] storage dtype = a * (h (*) (b*v))
- * and ext rows [0, L-1+n) of bank 1-fir_bank.  Needs d % 32 == 0. */
+ * and ext rows [0, L-1+n) of bank 1-fir_bank.  Needs d % 32 == 0 and
+ * 1 <= L <= 256. */
 int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_t dtype,
                const void* abv_dev, const float* taps_dev, float* ext0_dev, float* ext1_dev,
                const evs_book* book_dev, void* g_dev, cudaStream_t stream);
