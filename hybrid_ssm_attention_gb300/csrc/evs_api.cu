@@ -61,6 +61,7 @@ struct LayerW {
   const void *w_in, *w_out, *w_gu, *w_down;
   const float *taps, *lam, *res;
   CUtensorMap m_in, m_out, m_gu, m_down;
+  const uint8_t *pk_in, *pk_out, *pk_gu, *pk_down;  // packed copies (bf16), in wpack
 };
 
 struct LayerS {
@@ -94,11 +95,20 @@ struct evs_model {
   const void* embed;
   const void* head;
   CUtensorMap m_head;
+  const uint8_t* pk_head;
+  uint8_t* wpack;  // library-owned packed projection weights (bf16), or null
   std::vector<LayerW> L;
   Partials p_in, p_out, p_gu, p_down, p_head;  // with device slot tables
   int4* tab_dev;                               // the five slot tables
   size_t ws_bytes;                             // largest partial workspace
   bool has_attn;
+  // bf16: projection weights repacked (library copy in wpack) with the
+  // gate/up rows interleaved for the SwiGLU column order
+  bool packed;
+  // packed tensor-core GEMMs normalise their own B tiles (RMSNorm) and the
+  // gate/up GEMM applies SiLU-and-multiply in its epilogue: no separate
+  // normalisation or activation kernels
+  bool fuse;
   int n_max;
 };
 
@@ -112,6 +122,7 @@ struct evs_state {
   float* X;
   void *xn, *g, *h;
   float* fin;   // [NTOK][max(3d, 2F)] final GEMM sums (mixer / MLP inputs)
+  float* pout;  // same size: GEMM outputs of evs_profile_gemms
   float* ss;    // [tiles of d][NTOK] per-tile sums of squares
   int* cnt;     // [max tiles] GEMM arrival counters
   int cnt_len;
@@ -120,9 +131,11 @@ struct evs_state {
   AttnBufs ab;
   std::vector<LayerS> S;
   CUtensorMap m_xn, m_g, m_h;
+  CUtensorMap m_xf;  // fp32 X [NTOK][d] (RMSNorm converter source)
   bool use_graphs, pdl;
   int pf_units;  // next-weight L2 prefetch per CTA (units of 128x64)
   unsigned long long* trace;  // EVS_TRACE builds: GEMM timeline slots
+  int cta_slot = -1;          // EVS_TRACE builds: GEMM launch with per-CTA timeline
   cudaStream_t cap;
   std::vector<GraphEntry> graphs;
   unsigned long long tick;
@@ -156,25 +169,38 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   // the start of the next one into L2 (the head's successor is the next
   // round's first in-projection).
   const int nl = (int)m->L.size();
-  auto seq = [&](int k, const Partials** P, const CUtensorMap** map) {
+  auto seq = [&](int k, const Partials** P, const CUtensorMap** map, const uint8_t** pk) {
     k %= 4 * nl + 1;
     if (k == 4 * nl) {
       *P = &m->p_head;
       *map = &m->m_head;
+      *pk = m->pk_head;
       return;
     }
     const LayerW& w = m->L[k / 4];
     const Partials* plans[4] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down};
     const CUtensorMap* maps[4] = {&w.m_in, &w.m_out, &w.m_gu, &w.m_down};
+    const uint8_t* pks[4] = {w.pk_in, w.pk_out, w.pk_gu, w.pk_down};
     *P = plans[k % 4];
     *map = maps[k % 4];
+    *pk = pks[k % 4];
   };
   int gk = 0;
   // GEMM_FINAL writes fin[tok][col] (row stride ld); GEMM_RESID adds into X
   // and leaves per-tile sums of squares for the next RMSNorm
-  auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const void* W, const CUtensorMap& xm,
-                  const void* Xin, int K, int mode, float* fin, int ld) -> int {
+  auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
+                  const CUtensorMap& xm, const void* Xin, int K, int mode, float* fin, int ld,
+                  int bsrc = GEMM_B_TMA) -> int {
     Partials P = plan;
+    P.wpk = pk;
+    P.bsrc = bsrc;
+    P.Kdim = K;
+    P.ss_in = s->ss;
+    P.ss_tiles = (d + TILE_M - 1) / TILE_M;
+    P.norm_d = d;
+    P.eps = eps;
+    P.hout = static_cast<bf16*>(s->h);
+    P.h_cols = F;
     P.ws = s->ws[(wsi++) & 1];
     P.cnt = s->cnt;
     P.mode = mode;
@@ -185,7 +211,9 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     P.ss = s->ss;
     const Partials* np;
     const CUtensorMap* nmap;
-    seq(++gk, &np, &nmap);
+    const uint8_t* npk;
+    seq(++gk, &np, &nmap, &npk);
+    P.nwpk = npk;
     P.pf_units = s->pf_units;
     P.nG = np->G;
     P.nKB = np->KB;
@@ -194,6 +222,7 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
 #ifdef EVS_TRACE
     P.trace = s->trace;
     P.trace_slot = gk - 1;
+    P.cta_slot = s->cta_slot;
 #endif
     if (m->tc)
       CUDA_TRY(launch_gemm_tc(Lc, wm, xm, *nmap, P, K, &s->book->status));
@@ -204,10 +233,16 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   const size_t xbytes = sizeof(float) * (size_t)n * d;
   CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, n, d, V, eps, s->X, s->xn, s->book));
   if (trace) CUDA_TRY(cudaMemcpyAsync(trace, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
+  const bool fz = m->fuse;
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
     LayerS& st = s->S[i];
-    EVS_TRY(gemm(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d));
+    // the first in-projection reads the embedding kernel's normalised rows;
+    // later ones normalise the residual stream themselves when fused
+    if (fz && i > 0)
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, d, GEMM_FINAL, s->fin, 3 * d, GEMM_B_NORM));
+    else
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d));
     MixSrc src{s->fin, 3 * d, 1};
     if (w.kind == EVS_LAYER_FIR) {
       CUDA_TRY(launch_fir(Lc, dt, src, d, n, w.param, w.taps, st.ext[0], st.ext[1], s->book, s->g));
@@ -217,16 +252,23 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
       CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk,
                                 st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
     }
-    EVS_TRY(gemm(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
-    CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
-    EVS_TRY(gemm(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 2 * F));
-    CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, s->h));
-    EVS_TRY(gemm(m->p_down, w.m_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
-    CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
+    EVS_TRY(gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
+    if (fz) {
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, GEMM_SWIGLU, nullptr, 0, GEMM_B_NORM));
+    } else {
+      CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 2 * F));
+      CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, m->packed, s->h));
+    }
+    EVS_TRY(gemm(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
+    if (!fz) CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
     if (trace)
       CUDA_TRY(cudaMemcpyAsync(trace + (i + 1) * (size_t)n * d, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   }
-  EVS_TRY(gemm(m->p_head, m->m_head, m->head, s->m_xn, s->xn, d, GEMM_FINAL, logits, V));
+  if (fz)
+    EVS_TRY(gemm(m->p_head, m->m_head, m->pk_head, m->head, s->m_xf, s->X, d, GEMM_FINAL, logits, V, GEMM_B_NORM));
+  else
+    EVS_TRY(gemm(m->p_head, m->m_head, m->pk_head, m->head, s->m_xn, s->xn, d, GEMM_FINAL, logits, V));
   return EVS_OK;
 }
 
@@ -363,6 +405,13 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
   m->head = w->lm_head;
   m->n_max = cfg->gamma_max + 1;
   m->has_attn = false;
+  {
+    const char* pk = getenv("EVS_WPACK");
+    const char* fz = getenv("EVS_FUSE");
+    m->packed = m->tc && !(pk && pk[0] == '0') && cfg->d_ffn % (TILE_M / 2) == 0;
+    // fp32 rows staged by TMA need 16-byte row strides
+    m->fuse = m->packed && cfg->d_model % 4 == 0 && !(fz && fz[0] == '0');
+  }
   const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;
   char err[256] = {0};
   auto enc = [&](CUtensorMap* map, const void* base, int N, int K) -> bool {
@@ -418,6 +467,13 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
         delete m;
         return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d has too many column tiles", shapes[k][0], shapes[k][1]);
       }
+      // ring depth that fits next to this GEMM's B-source staging
+      const int bs[5] = {GEMM_B_NORM, GEMM_B_TMA, GEMM_B_NORM, GEMM_B_TMA, GEMM_B_NORM};
+      if (m->tc)
+        plans[k].P.stages =
+            std::min(plans[k].P.stages, gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA));
+      const char* st_env = getenv("EVS_GEMM_STAGES");
+      if (st_env && m->tc) plans[k].P.stages = std::max(2, std::min(GEMM_MAX_STAGES, atoi(st_env)));
       tb += table_bytes(plans[k]);
       m->ws_bytes = std::max(m->ws_bytes, partials_bytes(plans[k]));
     }
@@ -440,12 +496,46 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
       off += T;
     }
   }
+  // bf16: repack every projection matrix into the unit-major swizzled layout
+  // the tensor-core GEMM streams with contiguous bulk copies
+  if (m->packed) {
+    const size_t per_layer = packed_bytes(m->p_in) + packed_bytes(m->p_out) + packed_bytes(m->p_gu) +
+                             packed_bytes(m->p_down);
+    const size_t total = per_layer * m->L.size() + packed_bytes(m->p_head);
+    cudaError_t e = cudaMalloc(&m->wpack, total);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      m->wpack = nullptr;
+      evs_model_destroy(m);
+      return fail(EVS_ERR_OOM, "cudaMalloc(%zu) for packed weights: %s", total, cudaGetErrorString(e));
+    }
+    size_t off = 0;
+    auto pack = [&](const void* W, int N, int K, const Partials& P, int swg_half = 0) -> const uint8_t* {
+      uint8_t* dst = m->wpack + off;
+      off += packed_bytes(P);
+      if (e == cudaSuccess) e = launch_pack_weights(0, static_cast<const bf16*>(W), N, K, P, swg_half, dst);
+      return dst;
+    };
+    for (LayerW& L : m->L) {
+      L.pk_in = pack(L.w_in, 3 * d, d, m->p_in);
+      L.pk_out = pack(L.w_out, d, d, m->p_out);
+      L.pk_gu = pack(L.w_gu, 2 * F, d, m->p_gu, F);  // gate/up interleaved by 64 rows
+      L.pk_down = pack(L.w_down, d, F, m->p_down);
+    }
+    m->pk_head = pack(m->head, V, d, m->p_head);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+    if (e != cudaSuccess) {
+      evs_model_destroy(m);
+      return fail(EVS_ERR_CUDA, "packing weights: %s", cudaGetErrorString(e));
+    }
+  }
   *out = m;
   return EVS_OK;
 }
 
 extern "C" int evs_model_destroy(evs_model* m) {
   if (m && m->tab_dev) cudaFree(m->tab_dev);
+  if (m && m->wpack) cudaFree(m->wpack);
   delete m;
   return EVS_OK;
 }
@@ -494,11 +584,12 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   ALLOC(s->g, es * NTOK * d);
   ALLOC(s->h, es * NTOK * F);
   ALLOC(s->fin, sizeof(float) * NTOK * std::max(3 * d, std::max(2 * F, c.vocab)));
+  ALLOC(s->pout, sizeof(float) * NTOK * std::max(3 * d, std::max(2 * F, c.vocab)));
   ALLOC(s->ss, sizeof(float) * NTOK * ((d + TILE_M - 1) / TILE_M));
   s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
   ALLOC(s->cnt, sizeof(int) * s->cnt_len);
 #ifdef EVS_TRACE
-  ALLOC(s->trace, sizeof(unsigned long long) * 6 * 1024);
+  ALLOC(s->trace, sizeof(unsigned long long) * (6 * 1024 + 4 * 1024 + 512));
 #endif
   size_t wsb = 0;
   wsb = m->ws_bytes;
@@ -533,7 +624,8 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
     char err[256] = {0};
     if (!encode_tmap_2d(&s->m_xn, s->xn, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
         !encode_tmap_2d(&s->m_g, s->g, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
-        !encode_tmap_2d(&s->m_h, s->h, F, NTOK, TILE_K, NTOK, err, sizeof err)) {
+        !encode_tmap_2d(&s->m_h, s->h, F, NTOK, TILE_K, NTOK, err, sizeof err) ||
+        (m->fuse && !encode_tmap_2d_f32(&s->m_xf, s->X, d, NTOK, TILE_K, NTOK, err, sizeof err))) {
       state_free(s);
       return fail(EVS_ERR_CUDA, "activation tensor map: %s", err);
     }
@@ -918,32 +1010,54 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   CUDA_TRY(launch_busy(Lc, 2000000));
   int k = 0;
   int r = EVS_OK;
-  auto one = [&](const Partials& plan, const CUtensorMap& wm, const void* W, const CUtensorMap& xm, const void* X,
-                 int N, int K) -> int {
+  // each GEMM with the B source the verify step gives it
+  // (outputs go to a scratch buffer: the state is untouched)
+  auto one = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
+                 const CUtensorMap& xm, const void* X, int N, int K, int bsrc = GEMM_B_TMA,
+                 int mode = GEMM_FINAL) -> int {
     Partials P = plan;
+    P.wpk = pk;
+    P.bsrc = bsrc;
+    P.Kdim = K;
+    P.ss_in = s->ss;
+    P.ss_tiles = (d + TILE_M - 1) / TILE_M;
+    P.norm_d = d;
+    P.eps = c.norm_eps;
+    P.hout = reinterpret_cast<bf16*>(s->pout);
+    P.h_cols = F;
     P.ws = s->ws[k & 1];
     P.cnt = s->cnt;
-    P.mode = GEMM_FINAL;  // final sums to the scratch buffer: the state is untouched
+    P.mode = mode;
     P.n = n;
-    P.fin = s->fin;
+    P.fin = s->pout;
     P.fin_ld = N;
     CUDA_TRY(cudaEventRecord(ev[k], stream));
     if (m->tc)
       CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, &s->book->status));  // no prefetch: timed alone
     else
       CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, P, K));
-    bytes_host[k] = (int64_t)N * K * es + (int64_t)n * K * es + (int64_t)n * N * 4;
+    const int64_t in_es = bsrc == GEMM_B_TMA ? (int64_t)es : 4;
+    const int64_t out_b = mode == GEMM_SWIGLU ? (int64_t)n * (N / 2) * 2 : (int64_t)n * N * 4;
+    bytes_host[k] = (int64_t)N * K * es + (int64_t)n * K * in_es + out_b;
     ++k;
     return EVS_OK;
   };
   for (int i = 0; i < nl && r == EVS_OK; ++i) {
     const LayerW& w = m->L[i];
-    r = one(m->p_in, w.m_in, w.w_in, s->m_xn, s->xn, 3 * d, d);
-    if (r == EVS_OK) r = one(m->p_out, w.m_out, w.w_out, s->m_g, s->g, d, d);
-    if (r == EVS_OK) r = one(m->p_gu, w.m_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d);
-    if (r == EVS_OK) r = one(m->p_down, w.m_down, w.w_down, s->m_h, s->h, d, F);
+    const bool fz = m->fuse;
+    if (fz && i > 0)
+      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, 3 * d, d, GEMM_B_NORM);
+    else
+      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, 3 * d, d);
+    if (r == EVS_OK) r = one(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, d);
+    if (r == EVS_OK)
+      r = fz ? one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, 2 * F, d, GEMM_B_NORM, GEMM_SWIGLU)
+             : one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d);
+    if (r == EVS_OK) r = one(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, d, F);
   }
-  if (r == EVS_OK) r = one(m->p_head, m->m_head, m->head, s->m_xn, s->xn, V, d);
+  if (r == EVS_OK)
+    r = m->fuse ? one(m->p_head, m->m_head, m->pk_head, m->head, s->m_xf, s->X, V, d, GEMM_B_NORM)
+                : one(m->p_head, m->m_head, m->pk_head, m->head, s->m_xn, s->xn, V, d);
   if (r == EVS_OK) {
     cudaError_t e = cudaEventRecord(ev[k], stream);
     if (e == cudaSuccess) e = cudaEventSynchronize(ev[k]);
@@ -972,6 +1086,20 @@ extern "C" int evs_trace_read(evs_state* s, unsigned long long* out, int32_t max
   CUDA_TRY(cudaMemcpy(s->trace, init.data(), sizeof(unsigned long long) * 6 * 1024, cudaMemcpyHostToDevice));
   return EVS_OK;
 }
+// Per-CTA timeline {first MMA, SM id, last accumulator read, end}
+// of GEMM launch `slot` of later verifies: out[4c..4c+3] for CTA c < 1024;
+// then out[4096 + 256 w + 64 k + i]: CTA (w ? 100 : 0), unit i < 64, event k
+// (0 issue, 1 converter saw its rows, 2 B tile ready, 3 MMA start).
+// Reads the previous recording, then arms slot for the next ones.
+extern "C" int evs_trace_cta(evs_state* s, int32_t slot, unsigned long long* out) {
+  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemcpy(out, s->trace + 6 * 1024, sizeof(unsigned long long) * (4 * 1024 + 512),
+                      cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(s->trace + 6 * 1024, 0, sizeof(unsigned long long) * (4 * 1024 + 512)));
+  s->cta_slot = slot;
+  return EVS_OK;
+}
 #endif
 
 // =================================================================== misc
@@ -982,6 +1110,9 @@ extern "C" int32_t evs_verify_kernel_count(const evs_state* s, int32_t n) {
   (void)n;
   if (!s) return -1;
   int k = 1 + 2;  // embed, head GEMM, logits
-  for (const auto& L : s->m->L) k += 7 + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
+  // per layer: 4 GEMMs + the mixer (3 kernels for attention), plus two
+  // RMSNorm kernels and the activation kernel when they are not fused into
+  // the GEMMs
+  for (const auto& L : s->m->L) k += (s->m->fuse ? 4 : 7) + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
   return k;
 }

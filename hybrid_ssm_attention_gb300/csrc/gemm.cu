@@ -75,8 +75,9 @@ int gemm_cluster_choice(int N, int K, int num_sms) {
   return cl;
 }
 
-bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                    uint32_t box_inner, uint32_t box_outer, char* err, size_t errlen) {
+static bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, size_t esize, CUtensorMapSwizzle swz,
+                       const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                       char* err, size_t errlen) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
@@ -89,12 +90,11 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(err, errlen, "cuTensorMapEncodeTiled failed (%d) for [%llu][%llu]", (int)r,
              (unsigned long long)outer, (unsigned long long)inner);
@@ -103,20 +103,40 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
   return true;
 }
 
+bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint32_t box_inner, uint32_t box_outer, char* err, size_t errlen) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_128B, base, inner, outer,
+                     box_inner, box_outer, err, errlen);
+}
+
+bool encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, char* err, size_t errlen) {
+  return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_NONE, base, inner, outer,
+                     box_inner, box_outer, err, errlen);
+}
+
 namespace {
 
 constexpr int A_BYTES = TILE_M * TILE_K * 2;  // 16 KB weight tile
 constexpr int B_BYTES = NTOK * TILE_K * 2;    // 2 KB activation tile
-constexpr int GEMM_THREADS = 192;             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 B-tile converters
+constexpr int GEMM_THREADS = 320;
+constexpr int N_CONV = 4;
 constexpr uint64_t WAIT_NS = 4000000000ull;   // upper bound on any pipeline wait
 constexpr size_t CL_SLOT = (size_t)NTOK * TILE_M * sizeof(float);  // one rank's accumulator
-// dynamic shared memory of a launch with S ring stages and cl cluster ranks:
-// alignment slack, ring, barriers (full, empty: S each; acc_full[2],
-// acc_empty[2], drain), TMEM slot + flags, reduction scratch, cluster slots
-__host__ __device__ constexpr size_t gemm_smem(int S, int cl) {
-  return 1024 + (size_t)S * (A_BYTES + B_BYTES) + (size_t)(2 * S + 5) * 8 + 16 + 4 * NTOK * 4 +
-         (size_t)(cl > 1 ? cl - 1 : 0) * CL_SLOT;
+// fp32 source rows staged per stage for a converted (RMSNorm) B tile
+__host__ __device__ constexpr int raw_bytes(int bsrc) { return bsrc == GEMM_B_NORM ? NTOK * TILE_K * 4 : 0; }
+constexpr int SWG_BYTES = NTOK * (TILE_M / 2) * 4;  // gate/up exchange of the SwiGLU epilogue
+// dynamic shared memory of a launch with S ring stages, cl cluster ranks and
+// B source bsrc: alignment slack, ring (weights, B tiles, raw rows),
+// barriers (full, empty, ready: S each; acc_full[2], acc_empty[2], drain),
+// TMEM slot + flags, reduction scratch, converter row scales, SwiGLU
+// exchange, cluster slots
+__host__ __device__ constexpr size_t gemm_smem(int S, int cl, int bsrc) {
+  return 1024 + (size_t)S * (A_BYTES + B_BYTES + raw_bytes(bsrc)) + (size_t)(3 * S + 5) * 8 + 16 +
+         4 * NTOK * 4 + 2 * NTOK * 4 + SWG_BYTES + (size_t)(cl > 1 ? cl - 1 : 0) * CL_SLOT;
 }
+constexpr size_t GEMM_SMEM_MAX = 232448;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -141,9 +161,9 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false once WAIT_NS elapsed (the abort flag is then raised)
-// or another role already aborted.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try(bar, parity)) return true;
+// or another role already aborted.  The first probe is inlined: the
+// single-thread producer and MMA loops are latency-critical.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = gtimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(bar, parity)) return true;
@@ -155,6 +175,9 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_fla
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort_flag);
 }
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   int ok = 0;
@@ -182,6 +205,19 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
                    reinterpret_cast<uint64_t>(map)),
                "r"(x), "r"(y)
                : "memory");
+}
+// Contiguous global -> shared copy completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -265,10 +301,11 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 
 // Writes the final sums v[] of column tile*128+row: GEMM_FINAL to P.fin,
 // GEMM_RESID into P.X plus the tile's per-token sums of squares (butterfly
-// within each warp, then the four warps in order).  Called by the 128
-// group threads.
+// within each warp, then the four warps in order), GEMM_SWIGLU the bf16
+// activation of the tile's 64 gate / 64 up columns (exchanged through
+// s_xch).  Called by the 128 group threads.
 template <bool NAMED>
-__device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red) {
+__device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red, float* s_xch) {
   const int col = tile * TILE_M + row;
   const bool ok = col < P.N;
   const int n = P.n;
@@ -278,6 +315,21 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
       for (int t = 0; t < NTOK; ++t)
         if (t < n) P.fin[(size_t)t * P.fin_ld + col] = v[t];
     }
+  } else if (P.mode == GEMM_SWIGLU) {
+    constexpr int HALF = TILE_M / 2;
+    if (row >= HALF) {
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t)
+        if (t < n) s_xch[t * HALF + row - HALF] = v[t];
+    }
+    group_sync<NAMED>();
+    const int hc = tile * HALF + row;
+    if (row < HALF && hc < P.h_cols) {
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t)
+        if (t < n) P.hout[(size_t)t * P.h_cols + hc] = __float2bfloat16_rn(silu_f(v[t]) * s_xch[t * HALF + row]);
+    }
+    group_sync<NAMED>();  // the exchange buffer is free again
   } else {
     const int lane = row & 31, w = row >> 5;
     // all residual loads first (independent, in flight together), then the
@@ -305,7 +357,7 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
 }
 
 template <bool NAMED>
-__device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_flag, float* s_red) {
+__device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_flag, float* s_red, float* s_xch) {
   // The barrier orders the group's slot stores before thread 0's
   // acquire-release increment (release publishes them to the GPU; acquire
   // makes the other contributors' stores visible to whoever finishes last,
@@ -339,9 +391,23 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
         for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
       }
   }
-  tile_output<NAMED>(P, tile, row, v, s_red);
+  tile_output<NAMED>(P, tile, row, v, s_red, s_xch);
   if (row == 0) P.cnt[tile] = 0;
 }
+
+#ifdef EVS_TRACE
+// unit-level timeline of CTAs 0 and 100 of the per-CTA traced launch:
+// [which][kind][unit < 64], kind 0 issue, 1 converter saw full, 2 ready, 3 MMA start
+#define UNIT_TRACE(kind, i)                                                                        \
+  do {                                                                                             \
+    if (P.trace && P.trace_slot == P.cta_slot && (c == 0 || c == 100) && (i) < 64)                 \
+      P.trace[6 * 1024 + 4 * 1024 + (c == 0 ? 0 : 256) + (kind) * 64 + (int)(i)] = gtimer();       \
+  } while (0)
+#else
+#define UNIT_TRACE(kind, i) \
+  do {                      \
+  } while (0)
+#endif
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
@@ -349,20 +415,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const int STAGES = P.stages;  // ring depth of this launch
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int RAW = raw_bytes(P.bsrc);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sR = sB + STAGES * B_BYTES;  // fp32 source rows of converted B tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sR + STAGES * RAW);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
   float* s_red = reinterpret_cast<float*>(tmem_slot + 4);  // [4][NTOK]
-  float* s_cl = s_red + 4 * NTOK;  // cluster mode, rank 0: [cl-1][NTOK][TILE_M] partials of ranks 1..cl-1
+  float* s_scale = s_red + 4 * NTOK;  // [2][NTOK] RMSNorm divisors and their reciprocals
+  float* s_xch = s_scale + 2 * NTOK;  // [NTOK][64] SwiGLU up sums
+  float* s_cl = s_xch + SWG_BYTES / 4;  // cluster mode, rank 0: [cl-1][NTOK][TILE_M] partials of ranks 1..cl-1
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
-  auto acc_full = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
-  auto acc_empty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
-  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+  auto ready = [&](int s) { return smem_u32(bars + 2 * STAGES + s); };  // converted B tile written
+  auto acc_full = [&](int b) { return smem_u32(bars + 3 * STAGES + b); };
+  auto acc_empty = [&](int b) { return smem_u32(bars + 3 * STAGES + 2 + b); };
+  const uint32_t drain = smem_u32(bars + 3 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -391,6 +462,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
+      mbar_init(ready(s), N_CONV);  // one arrival per converter warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -402,7 +474,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (P.trace) atomicMin(P.trace + 6 * P.trace_slot, gtimer());
 #endif
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+    if (!P.wpk) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   }
   if (warp == 1) {
@@ -421,30 +493,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     const int pre = (int)std::min<long long>(STAGES, nunits);
     // weight tiles do not depend on the preceding kernel: start streaming now
+    // Unit cursor (K-block kb of tile t; packed block wp) advanced
+    // incrementally: this thread's per-unit work is on the critical path.
+    const int KB = P.KB;
+    const int kb0 = (int)(ub % KB), t0 = (int)(ub / KB);
+    const uint8_t* wp0 = P.wpk ? P.wpk + (size_t)c * A_BYTES : nullptr;
+    const size_t wstep = (size_t)P.G * A_BYTES;
+    const uint32_t sA_u = smem_u32(sA), sB_u = smem_u32(sB), sR_u = smem_u32(sR), full0 = full(0);
+    auto load_w = [&](int s, int kb, int t, const uint8_t* wp) {
+      if (wp)
+        bulk_load(sA_u + s * A_BYTES, wp, A_BYTES, full0 + 8 * s, pol_w);
+      else
+        tma_load_2d(sA_u + s * A_BYTES, &wmap, full0 + 8 * s, kb * TILE_K, t * TILE_M, pol_w);
+    };
+    // activations: the bf16 B tile itself, or the fp32 rows it is built from
+    auto load_b = [&](int s, int kb) {
+      const int x = kb * TILE_K;
+      if (P.bsrc == GEMM_B_TMA) {
+        tma_load_2d(sB_u + s * B_BYTES, &xmap, full0 + 8 * s, x, 0, pol_x);
+      } else {
+        tma_load_2d(sR_u + s * RAW, &xmap, full0 + 8 * s, x, 0, pol_x);
+      }
+    };
+    const uint32_t stage_tx = A_BYTES + (P.bsrc == GEMM_B_TMA ? B_BYTES : RAW);
+    int kb = kb0, t = t0;
+    const uint8_t* wp = wp0;
     for (int i = 0; i < pre; ++i) {
-      const long long u = ub + i;
-      mbar_expect_tx(full(i), A_BYTES + B_BYTES);
-      tma_load_2d(smem_u32(sA + i * A_BYTES), &wmap, full(i), (int)(u % P.KB) * TILE_K,
-                  (int)(u / P.KB) * TILE_M, pol_w);
+      UNIT_TRACE(0, i);
+      mbar_expect_tx(full0 + 8 * i, stage_tx);
+      load_w(i, kb, t, wp);
+      if (++kb == KB) kb = 0, ++t;
+      if (wp) wp += wstep;
     }
     pdl_wait();  // activations are written by the preceding kernel
 #ifdef EVS_TRACE
     if (P.trace) atomicMin(P.trace + 6 * P.trace_slot + 1, gtimer());
 #endif
-    for (int i = 0; i < pre; ++i) {
-      const long long u = ub + i;
-      tma_load_2d(smem_u32(sB + i * B_BYTES), &xmap, full(i), (int)(u % P.KB) * TILE_K, 0, pol_x);
+    for (int i = 0, k2 = kb0; i < pre; ++i) {
+      load_b(i, k2);
+      if (++k2 == KB) k2 = 0;
     }
+    // refills: unit i >= STAGES reuses stage i % STAGES once the MMA of unit
+    // i - STAGES released it (empty phase (i / STAGES - 1) & 1)
+    const uint32_t empty0 = empty(0);
+    int s = 0;
+    uint32_t ph = 0;
     long long i = pre;
     for (; i < nunits; ++i) {
-      const int s = (int)(i % STAGES);
-      const uint32_t round = (uint32_t)(i / STAGES);
-      if (!mbar_wait(empty(s), (round - 1) & 1, abort_flag)) break;
-      const long long u = ub + i;
-      mbar_expect_tx(full(s), A_BYTES + B_BYTES);
-      tma_load_2d(smem_u32(sA + s * A_BYTES), &wmap, full(s), (int)(u % P.KB) * TILE_K,
-                  (int)(u / P.KB) * TILE_M, pol_w);
-      tma_load_2d(smem_u32(sB + s * B_BYTES), &xmap, full(s), (int)(u % P.KB) * TILE_K, 0, pol_x);
+      if (!mbar_wait(empty0 + 8 * s, ph, abort_flag)) break;
+      UNIT_TRACE(0, i);
+      mbar_expect_tx(full0 + 8 * s, stage_tx);
+      load_w(s, kb, t, wp);
+      load_b(s, kb);
+      if (++kb == KB) kb = 0, ++t;
+      if (wp) wp += wstep;
+      if (++s == STAGES) s = 0, ph ^= 1;
     }
     // All own tiles are requested: keep HBM busy through this kernel's tail
     // and the consumers that follow by pulling the first units of the next
@@ -461,8 +564,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         ne = unit_begin(P.nU, P.nG, c + 1);
       }
       const long long stop = std::min<long long>(ne, nb + P.pf_units);
-      for (long long u = nb; u < stop; ++u)
-        tma_prefetch_l2(&nmap, (int)(u % P.nKB) * TILE_K, (int)(u / P.nKB) * TILE_M);
+      if (P.nwpk) {
+        for (long long u = nb; u < stop; ++u) bulk_prefetch_l2(P.nwpk + ((u - nb) * P.nG + c) * A_BYTES, A_BYTES);
+      } else {
+        for (long long u = nb; u < stop; ++u)
+          tma_prefetch_l2(&nmap, (int)(u % P.nKB) * TILE_K, (int)(u / P.nKB) * TILE_M);
+      }
     }
     // make sure no copy into this CTA's shared memory is still in flight
     for (long long j = std::max<long long>(0, i - STAGES); j < i; ++j) {
@@ -473,6 +580,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ---------------- MMA issuer
     long long i = 0;
     bool ok = true;
+    // stage / phase cursor and descriptors advanced incrementally (the
+    // descriptors' 14-bit start-address field holds any shared address)
+    const uint32_t wait0 = P.bsrc == GEMM_B_TMA ? full(0) : ready(0), empty0 = empty(0);
+    const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+    int s = 0;
+    uint32_t ph = 0;
     for (int seg = 0; seg < nseg && ok; ++seg) {
       const int tile = first_tile + seg;
       const long long seg_end = std::min<long long>(ue, (long long)(tile + 1) * P.KB);
@@ -484,31 +597,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const uint32_t dt = tmem + (uint32_t)(b * NTOK);
       bool first = true;
-      for (; ub + i < seg_end; ++i) {
-        const int s = (int)(i % STAGES);
-        if (!mbar_wait(full(s), (uint32_t)(i / STAGES) & 1, abort_flag)) {
+      const int cnt = (int)(seg_end - (ub + i));
+      for (int j = 0; j < cnt; ++j, ++i) {
+        if (!mbar_wait(wait0 + 8 * s, ph, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_desc(smem_u32(sA + s * A_BYTES));
-        const uint64_t bd = sw128_desc(smem_u32(sB + s * B_BYTES));
+        UNIT_TRACE(3, i);
+        const uint64_t ad = ad0 + (uint64_t)(s * (A_BYTES >> 4));
+        const uint64_t bd = bd0 + (uint64_t)(s * (B_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < TILE_K / 16; ++k)  // 16 bf16 = 32 bytes per MMA step along K
           mma_bf16(dt, ad + 2 * k, bd + 2 * k, IDESC, (first && k == 0) ? 0u : 1u);
 #ifdef EVS_TRACE
         if (i == 0 && P.trace) atomicMin(P.trace + 6 * P.trace_slot + 3, gtimer());
+        if (i == 0 && P.trace && P.trace_slot == P.cta_slot && c < 1024) P.trace[6 * 1024 + 4 * c] = gtimer();
 #endif
         first = false;
-        mma_commit(empty(s));
+        mma_commit(empty0 + 8 * s);
+        if (++s == STAGES) s = 0, ph ^= 1;
       }
       if (ok) mma_commit(acc_full(b));
     }
+#ifdef EVS_TRACE
+    if (P.trace && P.trace_slot == P.cta_slot && c < 1024) {
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      P.trace[6 * 1024 + 4 * c + 1] = smid;
+    }
+#endif
     // wait for every issued MMA before TMEM is released
     mma_commit(drain);
     volatile int local_abort = 0;
     mbar_wait(drain, 0, &local_abort);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ---------------- epilogue: TMEM -> partial slots -> tile fixup
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;  // column within the tile
@@ -528,6 +651,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_arrive(acc_empty(b));
 #ifdef EVS_TRACE
       if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 4, gtimer());
+      if (g == 0 && seg == nseg - 1 && P.trace && P.trace_slot == P.cta_slot && c < 1024)
+        P.trace[6 * 1024 + 4 * c + 2] = gtimer();
 #endif
       const int tile = first_tile + seg;
       if (clmode) {
@@ -553,10 +678,77 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
       for (int j = 0; j < NTOK; ++j)
         if (j < P.n) __stcg(dst + j * TILE_M, v[j]);
-      tile_done<true>(P, tile, row, s_flag, s_red);
+      tile_done<true>(P, tile, row, s_flag, s_red, s_xch);
 #ifdef EVS_TRACE
       if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 5, gtimer());
 #endif
+    }
+  } else if (warp >= 6 && P.bsrc != GEMM_B_TMA) {
+    // ---------------- B-tile converters: fp32 residual rows (staged by TMA)
+    // -> bf16 RMSNorm rows in the 128-byte swizzled K-major layout the MMA
+    // reads.  Every unit is shared by the N_CONV warps (warp w: rows
+    // 4w .. 4w+3), so the first tile is ready after a quarter of the work.
+    const int w = warp - 6;
+    pdl_wait();  // ss_in and X are written by the preceding kernels
+    if (w == 0 && lane < NTOK) {
+      // row divisor sqrt(mean square + eps): per-tile sums added in tile
+      // order, loaded sixteen at a time
+      const float* p = P.ss_in + lane;
+      float tot = 0.f;
+      int k = 0;
+      for (; k + 16 <= P.ss_tiles; k += 16) {
+        float a[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = __ldcg(p + (k + e) * NTOK);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tot += a[e];
+      }
+      for (; k < P.ss_tiles; ++k) tot += __ldcg(p + k * NTOK);
+      const float den = sqrtf(tot / (float)P.norm_d + P.eps);
+      s_scale[lane] = den;
+      s_scale[NTOK + lane] = 1.f / den;
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(N_CONV * 32) : "memory");
+    // lane -> (row parity, float4 column group): one instruction covers two
+    // whole 256-byte source rows and two 128-byte B rows (no bank conflicts)
+    const int cq = lane & 15, rh = lane >> 4;
+    const int r0 = 4 * w + rh, r1 = r0 + 2;  // this lane's two rows
+    const float den0 = s_scale[r0], rd0 = s_scale[NTOK + r0];
+    const float den1 = s_scale[r1], rd1 = s_scale[NTOK + r1];
+    int s = 0, kb = (int)(ub % P.KB);
+    uint32_t ph = 0;
+    for (long long i = 0; i < nunits; ++i) {
+      if (!warp_wait(full(s), ph, abort_flag)) break;
+      if (w == 0 && lane == 0) UNIT_TRACE(1, i);
+      const int col = kb * TILE_K + 4 * cq;  // first of this lane's four columns
+      const float* raw = reinterpret_cast<const float*>(sR + s * RAW) + 4 * cq;
+      uint8_t* dstB = sB + s * B_BYTES + (cq & 1) * 8;
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int r = m ? r1 : r0;
+        const float den = m ? den1 : den0, rden = m ? rd1 : rd0;
+        const float4 x4 = *reinterpret_cast<const float4*>(raw + r * TILE_K);
+        const float v[4] = {div_row(x4.x, den, rden), div_row(x4.y, den, rden), div_row(x4.z, den, rden),
+                            div_row(x4.w, den, rden)};
+        uint32_t wd[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool lo_ok = r < P.n && col + 2 * e < P.Kdim;
+          const bool hi_ok = r < P.n && col + 2 * e + 1 < P.Kdim;
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(lo_ok ? v[2 * e] : 0.f));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(hi_ok ? v[2 * e + 1] : 0.f));
+          wd[e] = lo | (hi << 16);
+        }
+        // 16-byte chunk j = cq / 2 of row r sits at position j ^ (r & 7)
+        *reinterpret_cast<uint2*>(dstB + r * 128 + (((cq >> 1) ^ (r & 7)) << 4)) = make_uint2(wd[0], wd[1]);
+      }
+      // generic-proxy writes -> visible to the tensor core's async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready(s));
+      if (w == 0 && lane == 0) UNIT_TRACE(2, i);
+      if (++s == STAGES) s = 0, ph ^= 1;
+      if (++kb == P.KB) kb = 0;
     }
   }
 
@@ -569,7 +761,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
       asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
-    if (crank == 0 && warp >= 2 && !*abort_flag) {
+    if (crank == 0 && warp >= 2 && warp < 6 && !*abort_flag) {
       const int row = (warp & 3) * 32 + lane;
       for (int r = 1; r < P.cl; ++r) {
         const float* src = s_cl + ((size_t)(r - 1) * NTOK) * TILE_M + row;
@@ -577,7 +769,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int j = 0; j < NTOK; ++j)
           if (j < P.n) vkeep[j] += src[j * TILE_M];
       }
-      tile_output<true>(P, first_tile, row, vkeep, s_red);
+      tile_output<true>(P, first_tile, row, vkeep, s_red, s_xch);
 #ifdef EVS_TRACE
       if (threadIdx.x == 64 && P.trace) {
         const unsigned long long now = gtimer();
@@ -594,6 +786,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
 #ifdef EVS_TRACE
   if (threadIdx.x == 0 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 2, gtimer());
+  if (threadIdx.x == 0 && P.trace && P.trace_slot == P.cta_slot && c < 1024) P.trace[6 * 1024 + 4 * c + 3] = gtimer();
 #endif
 }
 
@@ -641,22 +834,78 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
 #pragma unroll
     for (int t = 0; t < NTOK; ++t)
       if (t < n) __stcg(dst + t * TILE_M, acc[t]);
-    tile_done<false>(P, tile, threadIdx.x, &s_flag, s_red);
+    tile_done<false>(P, tile, threadIdx.x, &s_flag, s_red, nullptr);
+  }
+}
+
+// One CTA per 16 KB unit u (tile-major): 128 rows x 8 chunks of 16 bytes,
+// chunk j of row r stored at position j ^ (r & 7); out-of-range rows /
+// columns are zero.  The block goes to i * G + c for the CTA c that owns u
+// (stream-K range or cluster rank) and u's index i within that CTA.
+__global__ void __launch_bounds__(256) pack_weights_kernel(const bf16* W, int N, int K, Partials P, int swg_half,
+                                                           uint8_t* dst) {
+  const long long u = blockIdx.x;
+  const int KB = P.KB;
+  const int t = (int)(u / KB), kb = (int)(u % KB);
+  long long pos;
+  if (P.cl >= 1) {
+    const int r = (int)unit_owner(KB, P.cl, kb);
+    pos = (long long)(kb - (int)unit_begin(KB, P.cl, r)) * P.G + (long long)t * P.cl + r;
+  } else {
+    const int c = unit_owner(P.U, P.G, u);
+    pos = (u - unit_begin(P.U, P.G, c)) * P.G + c;
+  }
+  uint8_t* blk = dst + pos * A_BYTES;
+  for (int e = threadIdx.x; e < TILE_M * 8; e += blockDim.x) {
+    const int r = e >> 3, jp = e & 7, j = jp ^ (r & 7);
+    constexpr int HALF = TILE_M / 2;
+    const long long row = swg_half > 0 ? (r < HALF ? (long long)t * HALF + r : swg_half + (long long)t * HALF + r - HALF)
+                                       : (long long)t * TILE_M + r;
+    const int col = kb * TILE_K + j * 8;
+    union {
+      uint4 v;
+      bf16 h[8];
+    } x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      x.h[i] = (row < N && col + i < K) ? W[row * K + col + i] : __float2bfloat16_rn(0.f);
+    *reinterpret_cast<uint4*>(blk + r * 128 + jp * 16) = x.v;
   }
 }
 
 }  // namespace
 
+int gemm_stages_for(int cl, int bsrc) {
+  int S = 8;
+  while (S > 2 && gemm_smem(S, cl, bsrc) > GEMM_SMEM_MAX) --S;
+  return S;
+}
+
+cudaError_t launch_pack_weights(cudaStream_t stream, const bf16* W, int N, int K, const Partials& P, int swg_half,
+                                uint8_t* dst) {
+  const long long U = (long long)((N + TILE_M - 1) / TILE_M) * ((K + TILE_K - 1) / TILE_K);
+  if (U < 1 || U > 0x7fffffffLL || U != P.U) return cudaErrorInvalidValue;
+  if (swg_half > 0 && (N != 2 * swg_half || swg_half % (TILE_M / 2) != 0)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(dst, 0, packed_bytes(P), stream);  // holes
+  if (e != cudaSuccess) return e;
+  count_launch();
+  pack_weights_kernel<<<(unsigned)U, 256, 0, stream>>>(W, N, K, P, swg_half, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CUtensorMap& xmap,
                            const CUtensorMap& nmap, const Partials& P, int K, int* err_flag) {
   (void)K;
   const int cl = P.cl > 1 ? P.cl : 1;
-  const size_t smem = gemm_smem(P.stages, cl);
-  if (P.stages < 2 || P.stages > GEMM_MAX_STAGES || smem > 232448) return cudaErrorInvalidValue;
+  const size_t smem = gemm_smem(P.stages, cl, P.bsrc);
+  if (P.stages < 2 || P.stages > GEMM_MAX_STAGES || smem > GEMM_SMEM_MAX) return cudaErrorInvalidValue;
+  if (P.bsrc != GEMM_B_TMA && P.n > NTOK) return cudaErrorInvalidValue;
+  if (P.mode == GEMM_SWIGLU && (P.N != 2 * P.h_cols || P.h_cols % (TILE_M / 2) != 0 || !P.hout))
+    return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM_MAX);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

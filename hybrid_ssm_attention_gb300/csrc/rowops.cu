@@ -73,9 +73,9 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const T* E, const int32
   cl.sync();
   float tot = 0.f;
   for (int q = 0; q < ncl; ++q) tot += *cl.map_shared_rank(&ss_cta, q);
-  const float den = sqrtf(tot / (float)d + eps);
+  const float den = sqrtf(tot / (float)d + eps), rden = 1.f / den;
   T* xo = xn + (size_t)t * d;
-  for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) xo[c] = from_f<T>(x[c] / den);
+  for (int c = c0 + threadIdx.x; c < c0 + cols; c += blockDim.x) xo[c] = from_f<T>(div_row(x[c], den, rden));
   cl.sync();  // ss_cta stays alive until every CTA of the cluster has read it
 }
 
@@ -91,7 +91,7 @@ int row_cluster(int d) {
 template <typename T>
 __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const float* ss, int ntiles, int d,
                                                          float eps, T* xn) {
-  __shared__ float s_den;
+  __shared__ float s_den, s_rcp;
   const int t = blockIdx.y;
   pdl_trigger();
   pdl_wait();
@@ -99,22 +99,24 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
     float tot = 0.f;
     for (int k = 0; k < ntiles; ++k) tot += ss[k * NTOK + t];
     s_den = sqrtf(tot / (float)d + eps);
+    s_rcp = 1.f / s_den;
   }
   __syncthreads();
   const float den = s_den;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c < d) xn[(size_t)t * d + c] = from_f<T>(X[(size_t)t * d + c] / den);
+  if (c < d) xn[(size_t)t * d + c] = from_f<T>(div_row(X[(size_t)t * d + c], den, s_rcp));
 }
 
 template <typename T>
-__global__ void mlp_act_kernel(const float* gu, int F, T* h) {
+__global__ void mlp_act_kernel(const float* gu, int F, int il, T* h) {
   const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_trigger();
   pdl_wait();
   if (j >= F) return;
-  const float gt = gu[(size_t)t * 2 * F + j], up = gu[(size_t)t * 2 * F + F + j];
-  const float s = gt / (1.f + expf(-gt));
-  h[(size_t)t * F + j] = from_f<T>(s * up);
+  const float* row = gu + (size_t)t * 2 * F;
+  const int gj = il ? (j / 64) * 128 + j % 64 : j, uj = il ? gj + 64 : F + j;
+  const float gt = row[gj], up = row[uj];
+  h[(size_t)t * F + j] = from_f<T>(silu_f(gt) * up);
 }
 
 // One CTA per row.  top-k by rank: entry j is kept iff fewer than k entries
@@ -330,10 +332,10 @@ cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, con
   return launch(L, norm_apply_kernel<float>, g, dim3(256), 0, X, ss, ntiles, d, eps, (float*)xn);
 }
 
-cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const float* gu, int n, int F, void* h) {
+cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const float* gu, int n, int F, bool il, void* h) {
   const dim3 g((F + 255) / 256, n);
-  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, gu, F, (bf16*)h);
-  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, gu, F, (float*)h);
+  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, gu, F, (int)il, (bf16*)h);
+  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, gu, F, (int)il, (float*)h);
 }
 
 cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, float T, int top_k, float* p) {

@@ -128,8 +128,14 @@ typedef struct evs_weights {
 typedef struct evs_model evs_model;
 typedef struct evs_state evs_state;
 
-/* Creates a model on the current device; builds TMA descriptors for the
- * bf16 weights.  Returns EVS_ERR_UNSUPPORTED for shapes the kernels lack. */
+/* Creates a model on the current device.  With bf16 storage it also copies
+ * every projection matrix (w_in, w_out, w_gu, w_down, lm_head) into a
+ * library-owned device buffer in the GEMM's streaming layout: 16 KB blocks
+ * of 128 rows x 64 columns in the order the GEMM reads them, each already in
+ * its shared-memory (128-byte swizzled) image, zero-padded at ragged edges.
+ * This costs one extra copy of those matrices in device memory and
+ * synchronizes the device once.  Returns EVS_ERR_UNSUPPORTED for shapes the
+ * kernels lack, EVS_ERR_OOM when the packed copy does not fit. */
 int evs_model_create(const evs_config* cfg, const evs_weights* w, evs_model** out);
 int evs_model_destroy(evs_model* m);
 

@@ -113,6 +113,44 @@ def test_small_bf16_spec_equals_native_bitwise(graphs):
     assert sp.check() == 0 and nat.check() == 0
 
 
+def wide_shape():
+    # 7B widths, two layers: in-projection and gate/up take the stream-K
+    # split, down and head the cluster split
+    return synth.ModelShape(name="wide-bf16", vocab=512, d_model=4096, layers=[("MR", 128), ("ATT", 0)],
+                            n_heads=32, head_dim=128, d_ffn=11008, gamma=12, dtype="bf16", attn_chunk=64)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("which", ["small", "wide"])
+def test_fused_norm_and_activation_equal_separate_kernels_bitwise(which, monkeypatch):
+    # RMSNorm and SiLU-and-multiply built inside the consuming GEMM (B-tile
+    # converters) against the standalone kernels: identical logits and book
+    import hybrid_ssm_attention_gb300 as evs
+    shape = small_shape() if which == "small" else wide_shape()
+    W = synth.make_weights(shape, 21)
+    m_f = evs.Model(shape, W)
+    monkeypatch.setenv("EVS_FUSE", "0")
+    m_s = evs.Model(shape, W)
+    monkeypatch.delenv("EVS_FUSE")
+    st_f, st_s = evs.State(m_f, 256), evs.State(m_s, 256)
+    nb = shape.n_block
+    L = len(shape.layers)
+    assert evs.evs_verify_kernel_count(st_s, nb) - evs.evs_verify_kernel_count(st_f, nb) == 3 * L
+    prompt = [int(x) for x in synth.prompt(shape, 21, 3 * nb + 5)]
+    for s0 in range(0, len(prompt), nb):
+        chunk = prompt[s0:s0 + nb]
+        lf, _ = _verify(evs, st_f, chunk, shape.vocab)
+        ls, _ = _verify(evs, st_s, chunk, shape.vocab)
+        a, b = to_np(lf), to_np(ls)
+        assert np.isfinite(a).all()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), s0
+        keep = len(chunk) - (s0 // nb) % 3
+        evs.evs_commit(st_f, keep)
+        evs.evs_commit(st_s, keep)
+    assert st_f.book() == st_s.book()
+    assert st_f.check() == 0 and st_s.check() == 0
+
+
 def _load_synth_state(evs, shape, st, S, P):
     t = torch()
     for li, (kind, param) in enumerate(shape.layers):
