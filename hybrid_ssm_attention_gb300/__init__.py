@@ -20,7 +20,7 @@ from ._abi import (EVS_BF16, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN, EVS_LAYER_FIR,
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
            "evs_commit", "evs_commit_dev", "evs_round", "evs_op_fir", "evs_op_iir",
-           "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_kernel_launches"]
+           "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_kernel_launches"]
 
 KIND_CODES = {"SE": EVS_LAYER_FIR, "MR": EVS_LAYER_FIR, "FIR": EVS_LAYER_FIR,
               "LI": EVS_LAYER_IIR, "IIR": EVS_LAYER_IIR, "ATT": EVS_LAYER_ATTN, "ATTN": EVS_LAYER_ATTN}
@@ -257,6 +257,11 @@ def evs_op_gemm_scratch_bytes(N, K, dtype) -> int:
 def evs_op_gemm(w, x, N, K, n, dtype, y, scratch, stream=None):
     _check(lib().evs_op_gemm(_ptr(w), _ptr(x), N, K, n, dtype, _ptr(y), _ptr(scratch),
                              scratch.numel() * scratch.element_size(), _stream(stream)), "evs_op_gemm")
+
+
+def evs_op_gemm_static(w, x, N, K, n, dtype, y, stream=None):
+    _check(lib().evs_op_gemm_static(_ptr(w), _ptr(x), N, K, n, dtype, _ptr(y), _stream(stream)),
+           "evs_op_gemm_static")
 
 
 def evs_kernel_launches() -> int:

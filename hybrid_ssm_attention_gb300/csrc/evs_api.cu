@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -985,6 +986,76 @@ extern "C" int evs_op_gemm(const void* W, const void* X, int32_t N, int32_t K, i
       return fail(EVS_ERR_CUDA, "%s", err);
     CUDA_TRY(cudaMemsetAsync(err_flag, 0, sizeof(int), stream));
     CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, err_flag));  // P.pf_units = 0: no prefetch
+  } else {
+    CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, P, K));
+  }
+  return EVS_OK;
+}
+
+// ------------------------------------------- operator GEMM, static scratch
+// evs_op_gemm for callers that must not allocate device memory on their
+// path: a serving loop that forbids allocation once it runs (an allocation
+// can synchronize the device and fail when memory is fragmented), or a
+// plug-in whose host framework owns all device memory and hands it no
+// scratch.  Its scratch ([partial slots][slot table][arrival counters][error
+// flag], as evs_op_gemm lays it out) is this file-scope device array, one per
+// device; calls that overlap in time share it and race.
+constexpr size_t STATIC_GEMM_SCRATCH = EVS_OP_GEMM_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_static_gemm_scratch[STATIC_GEMM_SCRATCH];
+
+// The array's device address, looked up once per device.  The first lookup
+// may load the module, so the first call on a device belongs outside
+// stream capture.
+static int static_gemm_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(EVS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) CUDA_TRY(cudaGetSymbolAddress(&addr[dev], g_static_gemm_scratch));
+  *out = addr[dev];
+  return EVS_OK;
+}
+
+extern "C" int evs_op_gemm_static(const void* W, const void* X, int32_t N, int32_t K, int32_t n, int32_t dtype,
+                                  float* Y, cudaStream_t stream) {
+  if (!W || !X || !Y) return fail(EVS_ERR_ARG, "null argument");
+  if (N < 1 || K < 1 || n < 1 || n > NTOK) return fail(EVS_ERR_ARG, "bad GEMM shape");
+  if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
+  static thread_local GemmPlan g;
+  size_t toff = 0, total = 0;
+  const bool tc = dtype == EVS_BF16 && N % TILE_M == 0 && K % TILE_K == 0 && aligned16(W) && aligned16(X);
+  EVS_TRY(gemm_plan_op(N, K, tc, &g, &toff, &total));
+  if (total > STATIC_GEMM_SCRATCH)
+    return fail(EVS_ERR_CAPACITY, "GEMM %d x %d needs %zu bytes of scratch; the static array holds %zu", N, K, total,
+                STATIC_GEMM_SCRATCH);
+  void* scratch = nullptr;
+  EVS_TRY(static_gemm_scratch(&scratch));
+  Partials P = g.P;
+  P.ws = (float*)scratch;
+  P.tab = (const int4*)((char*)scratch + toff);
+  const size_t tb = (table_bytes(g) + 255) & ~(size_t)255;
+  P.cnt = (int*)((char*)scratch + toff + tb);
+  P.mode = GEMM_FINAL;
+  P.n = n;
+  P.fin = Y;
+  P.fin_ld = N;
+  int* err_flag = (int*)((char*)scratch + total - 256);
+  // arrival counters and error flag start at zero (memsets, no allocation);
+  // the partial slots need no initial value
+  CUDA_TRY(cudaMemcpyAsync((void*)P.tab, g.tab, table_bytes(g), cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemsetAsync(P.cnt, 0, tb, stream));
+  CUDA_TRY(cudaMemsetAsync(err_flag, 0, sizeof(int), stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));  // g is reused by the next call
+  LaunchCtx Lc{stream, false};
+  if (tc) {
+    CUtensorMap wm, xm;
+    char err[256] = {0};
+    if (!encode_tmap_2d(&wm, W, K, N, TILE_K, TILE_M, err, sizeof err) ||
+        !encode_tmap_2d(&xm, X, K, n, TILE_K, NTOK, err, sizeof err))
+      return fail(EVS_ERR_CUDA, "%s", err);
+    CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, err_flag));
   } else {
     CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, P, K));
   }

@@ -300,6 +300,24 @@ size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype);
 int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
                 int32_t dtype, float* y_dev, void* scratch_dev, size_t scratch_bytes,
                 cudaStream_t stream);
+/* The same GEMM without caller scratch: an engineering entry point with no
+ * counterpart in the pages.  Same arguments (minus the scratch), layout,
+ * results and errors as evs_op_gemm, but it allocates no device memory: its
+ * partial slots, slot table, arrival counters and error flag live in one
+ * library-owned device array of EVS_OP_GEMM_STATIC_SCRATCH_BYTES per device.
+ * It serves callers that must not allocate on their path (a serving loop
+ * that forbids allocation once running; a plug-in whose host framework owns
+ * all device memory).  A shape whose scratch need (evs_op_gemm_scratch_bytes)
+ * exceeds the array returns EVS_ERR_CAPACITY before any device work.  The
+ * array's address is looked up on the first call on each device: make that
+ * call outside stream capture.  Each call clears the counters and the error
+ * flag with memsets and synchronizes `stream` after uploading the slot
+ * table, as evs_op_gemm does.  Calls share the array: calls that overlap in
+ * time on one device (other streams or host threads) race, so the caller
+ * serializes them. */
+#define EVS_OP_GEMM_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+int evs_op_gemm_static(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
+                       int32_t dtype, float* y_dev, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- profiling */
 /* Times every weight GEMM of one verify step of n tokens (per layer: in,
