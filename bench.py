@@ -150,6 +150,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM traffic per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum,
+# averaged over the 129 weight GEMMs of a step) from the ncu capture summarised
+# in profiles/gemm_tc_7b_packed_weight_stream.md; valid only for the kernel
+# source it was taken on (sha256 prefix of gemm.cu), else reported as null.
+GEMM_TRAFFIC = {"gemm_cu_sha256": "b5cec21b4402163e", "bytes_per_launch": 100.96e6}
+
+
+def gemm_traffic():
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "hybrid_ssm_attention_gb300", "csrc", "gemm.cu")
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return GEMM_TRAFFIC["bytes_per_launch"] if h == GEMM_TRAFFIC["gemm_cu_sha256"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -313,7 +328,7 @@ def run_evs(args, rank, world, local):
     g_bytes, g_ms = float(sum(by)), float(sum(ms))
     achieved = g_bytes / (g_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "gemm_tc_kernel", "launches": len(ms),
+                "traffic": gemm_traffic(), "kernel": "gemm_tc_kernel", "launches": len(ms),
                 "avg_launch_us": 1e3 * g_ms / len(ms), "bytes_per_launch": g_bytes / len(ms),
                 "peak_source": peak_src}
     sb = step_bytes(shape, P0 - 1 + n * (args.warmup + args.steps // 2), n)

@@ -106,9 +106,18 @@ struct evs_model {
   // bf16: projection weights repacked (library copy in wpack) with the
   // gate/up rows interleaved for the SwiGLU column order
   bool packed;
-  // packed tensor-core GEMMs normalise their own B tiles (RMSNorm) and the
-  // gate/up GEMM applies SiLU-and-multiply in its epilogue: no separate
-  // normalisation or activation kernels
+  // Opt-in fusions of the small elementwise kernels into the GEMMs (packed
+  // weights only), bit-identical to the separate kernels:
+  //  swiglu (EVS_SWIGLU=1): the gate/up GEMM applies SiLU-and-multiply in
+  //    its epilogue (no activation kernel);
+  //  fuse (EVS_FUSE=1): the GEMMs that read RMSNorm output build their B
+  //    tiles from the fp32 residual rows (no normalisation kernels).
+  // Both measured slower on the 7B-shaped stack: with a small kernel in
+  // between, the next GEMM's CTAs are resident and loading weights before
+  // their inputs are ready, which hides more than the kernel costs; the
+  // converter also adds start-up latency and its larger blocks keep the next
+  // mixer from starting early.
+  bool swiglu;
   bool fuse;
   int n_max;
 };
@@ -234,7 +243,7 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   const size_t xbytes = sizeof(float) * (size_t)n * d;
   CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, n, d, V, eps, s->X, s->xn, s->book));
   if (trace) CUDA_TRY(cudaMemcpyAsync(trace, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
-  const bool fz = m->fuse;
+  const bool fz = m->fuse, sg = m->swiglu;
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
     LayerS& st = s->S[i];
@@ -254,13 +263,14 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
                                 st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
     }
     EVS_TRY(gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
+    const int gu_mode = sg ? GEMM_SWIGLU : GEMM_FINAL;
     if (fz) {
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, GEMM_SWIGLU, nullptr, 0, GEMM_B_NORM));
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, gu_mode, s->fin, 2 * F, GEMM_B_NORM));
     } else {
       CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 2 * F));
-      CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, m->packed, s->h));
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, gu_mode, s->fin, 2 * F));
     }
+    if (!sg) CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, m->packed, s->h));
     EVS_TRY(gemm(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
     if (!fz) CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
     if (trace)
@@ -409,9 +419,11 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
   {
     const char* pk = getenv("EVS_WPACK");
     const char* fz = getenv("EVS_FUSE");
+    const char* sw = getenv("EVS_SWIGLU");
     m->packed = m->tc && !(pk && pk[0] == '0') && cfg->d_ffn % (TILE_M / 2) == 0;
+    m->swiglu = m->packed && sw && sw[0] == '1';
     // fp32 rows staged by TMA need 16-byte row strides
-    m->fuse = m->packed && cfg->d_model % 4 == 0 && !(fz && fz[0] == '0');
+    m->fuse = m->packed && cfg->d_model % 4 == 0 && fz && fz[0] == '1';
   }
   const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;
   char err[256] = {0};
@@ -1116,14 +1128,15 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   for (int i = 0; i < nl && r == EVS_OK; ++i) {
     const LayerW& w = m->L[i];
     const bool fz = m->fuse;
+    const int gu_mode = m->swiglu ? GEMM_SWIGLU : GEMM_FINAL;
     if (fz && i > 0)
       r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, 3 * d, d, GEMM_B_NORM);
     else
       r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, 3 * d, d);
     if (r == EVS_OK) r = one(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, d);
     if (r == EVS_OK)
-      r = fz ? one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, 2 * F, d, GEMM_B_NORM, GEMM_SWIGLU)
-             : one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d);
+      r = fz ? one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, 2 * F, d, GEMM_B_NORM, gu_mode)
+             : one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d, GEMM_B_TMA, gu_mode);
     if (r == EVS_OK) r = one(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, d, F);
   }
   if (r == EVS_OK)
@@ -1182,8 +1195,8 @@ extern "C" int32_t evs_verify_kernel_count(const evs_state* s, int32_t n) {
   if (!s) return -1;
   int k = 1 + 2;  // embed, head GEMM, logits
   // per layer: 4 GEMMs + the mixer (3 kernels for attention), plus two
-  // RMSNorm kernels and the activation kernel when they are not fused into
-  // the GEMMs
-  for (const auto& L : s->m->L) k += (s->m->fuse ? 4 : 7) + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
+  // RMSNorm kernels and the activation kernel unless the GEMMs do that work
+  for (const auto& L : s->m->L)
+    k += 4 + (s->m->fuse ? 0 : 2) + (s->m->swiglu ? 0 : 1) + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
   return k;
 }

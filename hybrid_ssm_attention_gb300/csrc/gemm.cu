@@ -305,7 +305,8 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 // activation of the tile's 64 gate / 64 up columns (exchanged through
 // s_xch).  Called by the 128 group threads.
 template <bool NAMED>
-__device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red, float* s_xch) {
+__device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red, float* s_xch,
+                            const float* xpre = nullptr) {
   const int col = tile * TILE_M + row;
   const bool ok = col < P.N;
   const int n = P.n;
@@ -336,7 +337,7 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
     // updates and the per-token butterflies
     float x[NTOK];
 #pragma unroll
-    for (int t = 0; t < NTOK; ++t) x[t] = (t < n && ok) ? P.X[(size_t)t * P.N + col] : 0.f;
+    for (int t = 0; t < NTOK; ++t) x[t] = (t < n && ok) ? (xpre ? xpre[t] : P.X[(size_t)t * P.N + col]) : 0.f;
 #pragma unroll
     for (int t = 0; t < NTOK; ++t)
       if (t < n && ok) {
@@ -371,12 +372,13 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
   if (arrived != e.y - 1) return;
   const int n = P.n;
   const float* p = P.ws + (size_t)e.x * NTOK * TILE_M + row;
-  float v[NTOK];
+  // Fixed order: the later contributors' slots 1..count-1 in order, then the
+  // first contributor's slot is added to that sum.  Slots are loaded four at
+  // a time.
+  float v[NTOK], v0[NTOK];
 #pragma unroll
-  for (int t = 0; t < NTOK; ++t) v[t] = 0.f;
-  // slots are loaded four at a time (independent loads in flight) and
-  // added strictly in contributor order
-  for (int j0 = 0; j0 < e.y; j0 += 4) {
+  for (int t = 0; t < NTOK; ++t) v[t] = 0.f, v0[t] = (t < n) ? __ldcg(p + t * TILE_M) : 0.f;
+  for (int j0 = 1; j0 < e.y; j0 += 4) {
     float a[4][NTOK];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -391,9 +393,12 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
         for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
       }
   }
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t) v[t] = v0[t] + v[t];
   tile_output<NAMED>(P, tile, row, v, s_red, s_xch);
   if (row == 0) P.cnt[tile] = 0;
 }
+
 
 #ifdef EVS_TRACE
 // unit-level timeline of CTAs 0 and 100 of the per-CTA traced launch:
@@ -409,7 +414,10 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
   } while (0)
 #endif
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// At most 144 registers a thread (no spills): a 320-thread block then leaves
+// a 256-thread, 72-register mixer CTA room on the SM to start its prologue
+// while the GEMM drains.
+__global__ void __maxnreg__(144)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const __grid_constant__ CUtensorMap nmap, Partials P, int* err_flag) {
   extern __shared__ uint8_t smem_raw[];
@@ -455,8 +463,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int first_tile = (int)(ub / P.KB);
   const int nseg = (int)((ue - 1) / P.KB) - first_tile + 1;
   float vkeep[NTOK];  // cluster mode: this CTA's accumulator column, kept across the cluster barrier
+  float xpre[NTOK];   // cluster rank 0, residual mode: the tile's residual rows, loaded early
+  bool have_x = false;
 #pragma unroll
-  for (int t = 0; t < NTOK; ++t) vkeep[t] = 0.f;
+  for (int t = 0; t < NTOK; ++t) vkeep[t] = 0.f, xpre[t] = 0.f;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -636,8 +646,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;  // column within the tile
     const int g = threadIdx.x - 64; // index within the epilogue group
+    // cluster rank 0 of a residual GEMM: the residual rows of its tile do not
+    // depend on this GEMM; fetch them while the weights stream
+    if (clmode && crank == 0 && P.mode == GEMM_RESID) {
+      pdl_wait();
+      const int col = first_tile * TILE_M + row;
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) xpre[t] = (t < P.n && col < P.N) ? __ldcg(P.X + (size_t)t * P.N + col) : 0.f;
+      have_x = true;
+    }
     for (int seg = 0; seg < nseg; ++seg) {
       const int b = seg & 1;
+      const int tile = first_tile + seg;
       // one thread waits; the decision is shared so the group stays in step
       if (g == 0) *s_ok = mbar_wait(acc_full(b), (uint32_t)(seg >> 1) & 1, abort_flag) ? 1 : 0;
       group_sync<true>();
@@ -654,7 +674,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (g == 0 && seg == nseg - 1 && P.trace && P.trace_slot == P.cta_slot && c < 1024)
         P.trace[6 * 1024 + 4 * c + 2] = gtimer();
 #endif
-      const int tile = first_tile + seg;
       if (clmode) {
         // ranks 1..cl-1 send their column to rank 0's shared memory
         if (crank == 0) {
@@ -769,7 +788,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int j = 0; j < NTOK; ++j)
           if (j < P.n) vkeep[j] += src[j * TILE_M];
       }
-      tile_output<true>(P, first_tile, row, vkeep, s_red, s_xch);
+      tile_output<true>(P, first_tile, row, vkeep, s_red, s_xch, have_x ? xpre : nullptr);
 #ifdef EVS_TRACE
       if (threadIdx.x == 64 && P.trace) {
         const unsigned long long now = gtimer();
@@ -876,7 +895,7 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const bf16* W, int N,
 }  // namespace
 
 int gemm_stages_for(int cl, int bsrc) {
-  int S = 8;
+  int S = GEMM_MAX_STAGES;
   while (S > 2 && gemm_smem(S, cl, bsrc) > GEMM_SMEM_MAX) --S;
   return S;
 }
@@ -909,7 +928,10 @@ cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CU
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_cl(L, cl, gemm_tc_kernel, dim3(P.G), dim3(GEMM_THREADS), smem, wmap, xmap, nmap, P, err_flag);
+  // converter warps only where the B tile is built in shared memory: the
+  // smaller block leaves registers for the next kernel's CTAs to start early
+  const int threads = P.bsrc == GEMM_B_TMA ? GEMM_THREADS - N_CONV * 32 : GEMM_THREADS;
+  return launch_cl(L, cl, gemm_tc_kernel, dim3(P.G), dim3(threads), smem, wmap, xmap, nmap, P, err_flag);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& L, int dtype, const void* W, const void* X, int ldx,

@@ -95,11 +95,18 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
   const int t = blockIdx.y;
   pdl_trigger();
   pdl_wait();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    // the per-tile sums, 32 loads in flight at a time, added in tile order
+    const int lane = threadIdx.x;
     float tot = 0.f;
-    for (int k = 0; k < ntiles; ++k) tot += ss[k * NTOK + t];
-    s_den = sqrtf(tot / (float)d + eps);
-    s_rcp = 1.f / s_den;
+    for (int k0 = 0; k0 < ntiles; k0 += 32) {
+      const float mine = k0 + lane < ntiles ? __ldcg(ss + (k0 + lane) * NTOK + t) : 0.f;
+      for (int j = 0; j < 32 && k0 + j < ntiles; ++j) tot += __shfl_sync(0xffffffffu, mine, j);
+    }
+    if (lane == 0) {
+      s_den = sqrtf(tot / (float)d + eps);
+      s_rcp = 1.f / s_den;
+    }
   }
   __syncthreads();
   const float den = s_den;

@@ -7,6 +7,12 @@
     python -m hybrid_ssm_attention_gb300.profile_case fir 128 4096 13
     python -m hybrid_ssm_attention_gb300.profile_case iir 16 4096 13
     python -m hybrid_ssm_attention_gb300.profile_case attn 8192 13   (split-KV chunks of 64 keys)
+    python -m hybrid_ssm_attention_gb300.profile_case stack 2 13
+        the first L layers (default 2) of the 7B-shaped stack with the
+        library's packed weights: one warm-up verify of n tokens (4L+1 GEMM
+        launches and the row / mixer kernels), then every weight GEMM of a
+        step once more, each launched alone (in, out, gate/up, down per
+        layer, then the head).
 """
 from __future__ import annotations
 
@@ -22,7 +28,7 @@ def main():
     from hybrid_ssm_attention_gb300 import build as b
     b.build()
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["gemm", "fir", "iir", "attn"])
+    ap.add_argument("kind", choices=["gemm", "fir", "iir", "attn", "stack"])
     ap.add_argument("args", type=int, nargs="*")
     ap.add_argument("--reps", type=int, default=4)
     a = ap.parse_args()
@@ -30,7 +36,21 @@ def main():
     g = torch.Generator(device=dev).manual_seed(0)
     book = torch.zeros(8, dtype=torch.int32, device=dev)
     book[4] = -1
-    if a.kind == "gemm":
+    if a.kind == "stack":
+        import synth
+        L, n = (a.args + [2, 13][len(a.args):])[:2]
+        full = synth.stack_7b()
+        shape = synth.ModelShape(name=f"7b-first-{L}", vocab=full.vocab, d_model=full.d_model,
+                                 layers=full.layers[:L], n_heads=full.n_heads, head_dim=full.head_dim,
+                                 d_ffn=full.d_ffn, gamma=full.gamma, dtype="bf16", pole_mag=full.pole_mag)
+        m = evs.Model(shape, synth.make_weights(shape, 3))
+        st = evs.State(m, 256)
+        toks = torch.tensor([65 + (i % 4) for i in range(n)], dtype=torch.int32, device=dev)
+        lg = torch.empty((n, shape.vocab), device=dev)
+        evs.evs_verify_block(st, toks, n, lg)
+        evs.evs_commit(st, n)
+        evs.evs_profile_gemms(st, n)
+    elif a.kind == "gemm":
         N, K, n = (a.args + [22016, 4096, 13][len(a.args):])[:3]
         W = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
         X = torch.randn(n, K, device=dev, generator=g).to(torch.bfloat16)

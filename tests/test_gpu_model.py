@@ -123,32 +123,41 @@ def wide_shape():
 @pytest.mark.gpu
 @pytest.mark.parametrize("which", ["small", "wide"])
 def test_fused_norm_and_activation_equal_separate_kernels_bitwise(which, monkeypatch):
-    # RMSNorm and SiLU-and-multiply built inside the consuming GEMM (B-tile
-    # converters) against the standalone kernels: identical logits and book
+    # The three ways of running RMSNorm and SiLU-and-multiply agree bit for
+    # bit: separate kernels (default), SwiGLU in the gate/up GEMM's epilogue
+    # (EVS_SWIGLU=1), and RMSNorm built inside the consuming GEMMs as well
+    # (EVS_FUSE=1)
     import hybrid_ssm_attention_gb300 as evs
     shape = small_shape() if which == "small" else wide_shape()
     W = synth.make_weights(shape, 21)
-    m_f = evs.Model(shape, W)
-    monkeypatch.setenv("EVS_FUSE", "0")
-    m_s = evs.Model(shape, W)
-    monkeypatch.delenv("EVS_FUSE")
-    st_f, st_s = evs.State(m_f, 256), evs.State(m_s, 256)
+
+    def model(**env):
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        m = evs.Model(shape, W)
+        for k in env:
+            monkeypatch.delenv(k)
+        return m
+
+    models = [model(), model(EVS_SWIGLU="1"), model(EVS_SWIGLU="1", EVS_FUSE="1")]
+    states = [evs.State(m, 256) for m in models]
     nb = shape.n_block
     L = len(shape.layers)
-    assert evs.evs_verify_kernel_count(st_s, nb) - evs.evs_verify_kernel_count(st_f, nb) == 3 * L
+    counts = [evs.evs_verify_kernel_count(st, nb) for st in states]
+    assert counts[0] - counts[1] == L and counts[1] - counts[2] == 2 * L
     prompt = [int(x) for x in synth.prompt(shape, 21, 3 * nb + 5)]
     for s0 in range(0, len(prompt), nb):
         chunk = prompt[s0:s0 + nb]
-        lf, _ = _verify(evs, st_f, chunk, shape.vocab)
-        ls, _ = _verify(evs, st_s, chunk, shape.vocab)
-        a, b = to_np(lf), to_np(ls)
-        assert np.isfinite(a).all()
-        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), s0
+        outs = [to_np(_verify(evs, st, chunk, shape.vocab)[0]) for st in states]
+        assert np.isfinite(outs[0]).all()
+        for o in outs[1:]:
+            assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)), s0
         keep = len(chunk) - (s0 // nb) % 3
-        evs.evs_commit(st_f, keep)
-        evs.evs_commit(st_s, keep)
-    assert st_f.book() == st_s.book()
-    assert st_f.check() == 0 and st_s.check() == 0
+        for st in states:
+            evs.evs_commit(st, keep)
+    books = [st.book() for st in states]
+    assert books[1] == books[0] and books[2] == books[0]
+    assert all(st.check() == 0 for st in states)
 
 
 def _load_synth_state(evs, shape, st, S, P):
