@@ -198,19 +198,20 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   qo[i + half] = stored<T>(rq2);
 }
 
-// (2) split-KV: CTA (x, h) handles chunks x, x+gridDim.x, ... of CH keys
-// at absolute positions [cidx*CH, (cidx+1)*CH).  Query t (position pos+t)
-// sees keys <= pos+t.  Each chunk's K and V rows are staged in shared
-// memory (K rows padded by 16 bytes so the per-key dot products of a warp
-// hit distinct banks); per chunk and query the kernel stores the max, the
-// sum of exp and the unnormalised output.  Every reduction runs over fixed
-// key slots, masked slots contributing exact zeros, so a query's result does
-// not depend on the other queries of the block.
+// (2) split-KV (SIMT, any storage type): CTA (s, h) owns the keys of split s,
+// [s*span, (s+1)*span), and walks them in chunks of CH keys at absolute
+// positions.  Query t (position pos+t) sees keys <= pos+t.  Each chunk's K
+// and V rows are staged in shared memory (K rows padded by 16 bytes so the
+// per-key dot products of a warp hit distinct banks); per chunk and query
+// the kernel forms the max, the sum of exp and the unnormalised output and
+// folds them into the split's running (max, sum, output).  Every reduction
+// runs over fixed key slots, masked slots contributing exact zeros, so a
+// query's result does not depend on the other queries of the block.
 template <typename T, int DH, int CH>
 __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict__ qbuf, const T* __restrict__ kc,
                                                          const T* __restrict__ vc, int H, int n,
-                                                         long long ctx_max, const evs_book* book, float* part_o,
-                                                         float* part_ml, int nchunk_max) {
+                                                         long long ctx_max, const evs_book* book, int span,
+                                                         float* part_o, float* part_ml, int nsplit_max) {
   constexpr int KP = DH * (int)sizeof(T) + 16;  // padded K row pitch in bytes
   constexpr int VP = DH * (int)sizeof(T);
   constexpr int QG = 256 / CH;                   // query groups in the score phase
@@ -221,39 +222,46 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
   extern __shared__ __align__(16) unsigned char smraw[];
   float* q_s = reinterpret_cast<float*>(smraw);                    // [NTOK][DH]
   float* p_s = q_s + NTOK * DH;                                    // [NTOK][CH]
-  float* ml_s = p_s + NTOK * CH;                                   // [NTOK][2]
-  unsigned char* k_s = reinterpret_cast<unsigned char*>(ml_s + NTOK * 2);  // [CH][KP]
+  float* ml_s = p_s + NTOK * CH;                                   // [NTOK][4]: running max, sum; chunk weights
+  unsigned char* k_s = reinterpret_cast<unsigned char*>(ml_s + NTOK * 4);  // [CH][KP]
   unsigned char* v_s = k_s + CH * KP;                              // [CH][VP]
-  const int h = blockIdx.y;
+  const int h = blockIdx.y, sp = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
-  // the committed length is fixed for the whole verify: pull this CTA's
+  // the committed length is fixed for the whole verify: pull this split's
   // committed keys / values into L2 while the in-projection still runs
   const long long pos = book->pos;
   const long long total = min(pos + n, ctx_max);
-  const int nchunks = (int)((total + CH - 1) / CH);
+  const long long kb0 = (long long)sp * span, kb1 = min(kb0 + span, total);
   if (tid == 0) {
-    for (int cidx = blockIdx.x; cidx < nchunks; cidx += gridDim.x) {
-      const long long k0 = (long long)cidx * CH;
-      const long long nk = min((long long)CH, min(pos, ctx_max) - k0);
-      if (nk > 0) {
-        const unsigned bytes = (unsigned)(nk * DH * sizeof(T));
-        const T* kr = kc + ((size_t)h * ctx_max + k0) * DH;
-        const T* vr = vc + ((size_t)h * ctx_max + k0) * DH;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kr), "r"(bytes) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vr), "r"(bytes) : "memory");
-      }
+    const long long pre_end = min(kb1, min(pos, ctx_max));
+    if (pre_end > kb0) {
+      const unsigned bytes = (unsigned)((pre_end - kb0) * DH * sizeof(T));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kc + ((size_t)h * ctx_max + kb0) * DH),
+                   "r"(bytes)
+                   : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vc + ((size_t)h * ctx_max + kb0) * DH),
+                   "r"(bytes)
+                   : "memory");
     }
   }
   pdl_wait();
+  if (kb0 >= total) return;  // this split holds no key of the block
   const float scale = rsqrtf((float)DH);
   for (int e = tid; e < NTOK * DH; e += 256) {
     const int t = e / DH;
     q_s[e] = t < n ? qbuf[((size_t)t * H + h) * DH + e % DH] : 0.f;
   }
-  for (int cidx = blockIdx.x; cidx < nchunks; cidx += gridDim.x) {
-    const long long k0 = (long long)cidx * CH;
-    const int kmax = (int)min((long long)CH, total - k0);
+  if (tid < NTOK) {
+    ml_s[tid * 4] = -INFINITY;
+    ml_s[tid * 4 + 1] = 0.f;
+  }
+  const int dp = tid % DP, tqo = tid / DP;
+  float r0[OS], r1[OS];  // running unnormalised output
+#pragma unroll
+  for (int r = 0; r < OS; ++r) r0[r] = r1[r] = 0.f;
+  for (long long k0 = kb0; k0 < kb1; k0 += CH) {
+    const int kmax = (int)min((long long)CH, kb1 - k0);
     __syncthreads();
     // stage K and V rows [k0, k0+kmax) with 16-byte loads
     constexpr int VEC = DH * (int)sizeof(T) / 16;  // 16-byte vectors per row
@@ -305,7 +313,8 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
       }
     }
     __syncthreads();
-    // per query: max and sum of exp over the chunk's slots (warp per query)
+    // per query: the chunk's max and sum of exp, folded into the running pair
+    // (warp per query; the weights of old and new go to ml_s[t][2..3])
     for (int t = warp; t < n; t += 8) {
       float mx = -INFINITY;
       for (int j = lane; j < CH; j += 32) mx = fmaxf(mx, p_s[t * CH + j]);
@@ -321,14 +330,18 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       if (lane == 0) {
-        ml_s[t * 2] = mx;
-        ml_s[t * 2 + 1] = sum;
+        const float M = ml_s[t * 4], Mn = fmaxf(M, mx);
+        const float wo = Mn == -INFINITY ? 1.f : expf(M - Mn);
+        const float wc = mx == -INFINITY ? 0.f : expf(mx - Mn);
+        ml_s[t * 4] = Mn;
+        ml_s[t * 4 + 1] = fmaf(ml_s[t * 4 + 1], wo, sum * wc);
+        ml_s[t * 4 + 2] = wo;
+        ml_s[t * 4 + 3] = wc;
       }
     }
     __syncthreads();
-    // unnormalised output: thread = (dim pair dp, query group tq)
+    // chunk output, folded into the running output: thread = (dim pair, query group)
     {
-      const int dp = tid % DP, tq = tid / DP;
       float o0[OS], o1[OS];
 #pragma unroll
       for (int r = 0; r < OS; ++r) o0[r] = o1[r] = 0.f;
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
         }
 #pragma unroll
         for (int r = 0; r < OS; ++r) {
-          const int t = tq + r * OG;
+          const int t = tqo + r * OG;
           if (t < n) {
             const float p = p_s[t * CH + j];
             o0[r] = fmaf(p, v0, o0[r]);
@@ -356,32 +369,298 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
       }
 #pragma unroll
       for (int r = 0; r < OS; ++r) {
-        const int t = tq + r * OG;
+        const int t = tqo + r * OG;
         if (t < n) {
-          float* o = part_o + (((size_t)h * nchunk_max + cidx) * NTOK + t) * DH + 2 * dp;
-          o[0] = o0[r];
-          o[1] = o1[r];
+          const float wo = ml_s[t * 4 + 2], wc = ml_s[t * 4 + 3];
+          r0[r] = fmaf(r0[r], wo, o0[r] * wc);
+          r1[r] = fmaf(r1[r], wo, o1[r] * wc);
         }
       }
     }
-    if (tid < n) {
-      float* ml = part_ml + (((size_t)h * nchunk_max + cidx) * NTOK + tid) * 2;
-      ml[0] = ml_s[tid * 2];
-      ml[1] = ml_s[tid * 2 + 1];
+  }
+#pragma unroll
+  for (int r = 0; r < OS; ++r) {
+    const int t = tqo + r * OG;
+    if (t < n) {
+      float* o = part_o + (((size_t)h * nsplit_max + sp) * NTOK + t) * DH + 2 * dp;
+      o[0] = r0[r];
+      o[1] = r1[r];
+    }
+  }
+  if (tid < n) {
+    float* ml = part_ml + (((size_t)h * nsplit_max + sp) * NTOK + tid) * 2;
+    ml[0] = ml_s[tid * 4];
+    ml[1] = ml_s[tid * 4 + 1];
+  }
+}
+
+// (2b) split-KV attention on tensor cores (bf16 caches): grid (splits, H),
+// 4 warps.  Split s owns keys [s*span, (s+1)*span) of head h (span fixed per
+// state, so a query's key partition never depends on the block size n).
+// Keys stream through a 3-stage cp.async ring of 64-key stages (K and V rows
+// of 2*DH bytes, 16-byte chunks XOR-swizzled by row so ldmatrix is
+// conflict-free); warp w takes keys 16w..16w+15 of each stage:
+//   S = Q K^T  (mma.sync m16n8k16, Q rows = the block's queries, bf16),
+//   online softmax per query row (running max / sum, fp32),
+//   O += P V   (P rounded to bf16 as the A operand, V by ldmatrix.trans).
+// The four warps' (m, l, O) merge in warp order into one partial per split.
+constexpr int AT_WARPS = 4, AT_STAGE = 64, AT_NST = 3;
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+__device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int DH>
+__host__ __device__ constexpr size_t attn_mma_smem() {
+  return (size_t)AT_NST * 2 * AT_STAGE * DH * 2;  // K and V stages (the warp merge reuses them)
+}
+
+template <int DH>
+__global__ void __launch_bounds__(AT_WARPS * 32) attn_mma_kernel(const float* __restrict__ qbuf,
+                                                                  const bf16* __restrict__ kc,
+                                                                  const bf16* __restrict__ vc, int H, int n,
+                                                                  long long ctx_max, const evs_book* book, int span,
+                                                                  int nsplit_max, float* part_o, float* part_ml) {
+  static_assert(DH % 16 == 0 && DH <= 256, "head dim");
+  constexpr int RB = DH * 2;                  // bytes per key row
+  constexpr int CPR = DH / 8;                 // 16-byte chunks per row
+  constexpr int SWZ = CPR < 8 ? CPR - 1 : 7;  // XOR mask of the chunk index
+  constexpr int STAGE_B = AT_STAGE * RB;      // one of K / V for a stage
+  constexpr int KS = DH / 16;                 // k-steps of Q K^T
+  constexpr int NT = DH / 8;                  // 8-dim output tiles
+  extern __shared__ __align__(128) unsigned char at_sm[];
+  const int h = blockIdx.y, sp = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
+  pdl_trigger();
+  const long long pos = book->pos;
+  const long long total = min(pos + n, ctx_max);
+  const long long k_begin = (long long)sp * span;
+  const long long k_end = min(k_begin + span, total);
+  const int nstage = k_end > k_begin ? (int)((k_end - k_begin + AT_STAGE - 1) / AT_STAGE) : 0;
+  const bf16* kh = kc + (size_t)h * ctx_max * DH;
+  const bf16* vh = vc + (size_t)h * ctx_max * DH;
+  // committed keys do not change in this verify: warm L2 with the first
+  // stages while the preceding kernels finish
+  if (tid == 0 && nstage > 0) {
+    const long long pre_end = min(k_begin + (long long)AT_NST * AT_STAGE, min(pos, k_end));
+    if (pre_end > k_begin) {
+      const unsigned bytes = (unsigned)((pre_end - k_begin) * RB);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kh + k_begin * DH), "r"(bytes) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vh + k_begin * DH), "r"(bytes) : "memory");
+    }
+  }
+  pdl_wait();
+  if (sp * (long long)span >= total) return;  // this split holds no key of the block
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(at_sm);
+  auto stage_k = [&](int st) { return sbase + (uint32_t)(st % AT_NST) * 2 * STAGE_B; };
+  auto stage_v = [&](int st) { return stage_k(st) + STAGE_B; };
+  // stage st: keys k_begin + 64 st ..; rows past k_end: K left as is (masked),
+  // V zeroed (P = 0 must not meet a non-finite value)
+  auto issue = [&](int st) {
+    if (st < nstage) {
+      const long long key0 = k_begin + (long long)st * AT_STAGE;
+      unsigned char* kd = at_sm + (st % AT_NST) * 2 * STAGE_B;
+      unsigned char* vd = kd + STAGE_B;
+      for (int e = tid; e < AT_STAGE * CPR; e += AT_WARPS * 32) {
+        const int r = e / CPR, c = e % CPR;
+        const int off = r * RB + ((c ^ (r & SWZ)) << 4);
+        const long long key = key0 + r;
+        if (key < k_end) {
+          cp_async16(kd + off, kh + key * DH + c * 8);
+          cp_async16(vd + off, vh + key * DH + c * 8);
+        } else {
+          *reinterpret_cast<uint4*>(vd + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int st = 0; st < AT_NST - 1; ++st) issue(st);
+
+  // Q as the A operand: rows g and g+8 (queries), k-step kk
+  uint32_t qa[KS][4];
+  {
+    const float* q0 = qbuf + ((size_t)g * H + h) * DH;
+    const float* q1 = qbuf + ((size_t)(g + 8) * H + h) * DH;
+    const bool ok0 = g < n, ok1 = g + 8 < n;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int c0 = kk * 16 + 2 * t4;
+      qa[kk][0] = ok0 ? pack_bf16(q0[c0], q0[c0 + 1]) : 0u;
+      qa[kk][1] = ok1 ? pack_bf16(q1[c0], q1[c0 + 1]) : 0u;
+      qa[kk][2] = ok0 ? pack_bf16(q0[c0 + 8], q0[c0 + 9]) : 0u;
+      qa[kk][3] = ok1 ? pack_bf16(q1[c0 + 8], q1[c0 + 9]) : 0u;
+    }
+  }
+  const float scale = rsqrtf((float)DH);
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g, g+8 (l: this thread's share)
+  const long long lim0 = pos + g, lim1 = pos + g + 8;         // last key each row may see
+
+  for (int st = 0; st < nstage; ++st) {
+    issue(st + AT_NST - 1);
+    cp_async_wait_group<AT_NST - 1>();
+    __syncthreads();
+    const long long kw = k_begin + (long long)st * AT_STAGE + 16 * w;  // this warp's first key
+    if (kw < k_end) {
+      // S = Q K^T for 16 keys: two 8-key tiles
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t kb = stage_k(st);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int mi = lane >> 3;
+        const int r = 16 * w + ((mi >> 1) << 3) + (lane & 7);
+        const int c = 2 * kk + (mi & 1);
+        uint32_t b[4];
+        ldsm_x4(kb + r * RB + ((c ^ (r & SWZ)) << 4), b);
+        mma_16816(sc[0], qa[kk], b[0], b[1]);
+        mma_16816(sc[1], qa[kk], b[2], b[3]);
+      }
+      // mask, running max, probabilities
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const long long key = kw + 8 * j + 2 * t4 + (e & 1);
+          const bool ok = key < k_end && key <= ((e >> 1) ? lim1 : lim0);
+          sc[j][e] = ok ? sc[j][e] * scale : -INFINITY;
+          if (e >> 1) mx1 = fmaxf(mx1, sc[j][e]); else mx0 = fmaxf(mx0, sc[j][e]);
+        }
+#pragma unroll
+      for (int x = 1; x < 4; x <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+      }
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float a0 = n0 == -INFINITY ? 1.f : expf(m0 - n0);
+      const float a1 = n1 == -INFINITY ? 1.f : expf(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      float p[2][4];
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mm = (e >> 1) ? n1 : n0;
+          p[j][e] = sc[j][e] == -INFINITY ? 0.f : expf(sc[j][e] - mm);
+          if (e >> 1) ps1 += p[j][e]; else ps0 += p[j][e];
+        }
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= a0;
+        o[j][1] *= a0;
+        o[j][2] *= a1;
+        o[j][3] *= a1;
+      }
+      // O += P V: P (16 queries x 16 keys) as the A operand
+      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
+                              pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
+      const uint32_t vb = stage_v(st);
+#pragma unroll
+      for (int jd = 0; jd < NT; jd += 2) {
+        const int mi = lane >> 3;
+        const int r = 16 * w + ((mi & 1) << 3) + (lane & 7);
+        const int c = jd + (mi >> 1);
+        uint32_t b[4];
+        ldsm_x4_t(vb + r * RB + ((c ^ (r & SWZ)) << 4), b);
+        mma_16816(o[jd], pa, b[0], b[1]);
+        mma_16816(o[jd + 1], pa, b[2], b[3]);
+      }
+    }
+    __syncthreads();  // the stage buffer is refilled by the next iteration's issue
+  }
+  cp_async_wait_group<0>();
+  __syncthreads();
+  // row sums over the quad, then merge the four warps in order
+#pragma unroll
+  for (int x = 1; x < 4; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+  }
+  float* mw = reinterpret_cast<float*>(at_sm);  // [4][16] max, [4][16] sum, [4][16][DH] O
+  float* lw = mw + AT_WARPS * 16;
+  float* ow = lw + AT_WARPS * 16;
+  if (t4 == 0) {
+    mw[w * 16 + g] = m0;
+    mw[w * 16 + g + 8] = m1;
+    lw[w * 16 + g] = l0;
+    lw[w * 16 + g + 8] = l1;
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    float* r0 = ow + ((size_t)w * 16 + g) * DH + 8 * j + 2 * t4;
+    float* r1 = r0 + 8 * DH;
+    r0[0] = o[j][0];
+    r0[1] = o[j][1];
+    r1[0] = o[j][2];
+    r1[1] = o[j][3];
+  }
+  __syncthreads();
+  for (int e = tid; e < n * DH; e += AT_WARPS * 32) {
+    const int t = e / DH, dd = e % DH;
+    float M = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < AT_WARPS; ++v) M = fmaxf(M, mw[v * 16 + t]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int v = 0; v < AT_WARPS; ++v) {
+      const float mv = mw[v * 16 + t];
+      if (mv == -INFINITY) continue;
+      const float f = expf(mv - M);
+      L = fmaf(lw[v * 16 + t], f, L);
+      O = fmaf(ow[((size_t)v * 16 + t) * DH + dd], f, O);
+    }
+    part_o[(((size_t)h * nsplit_max + sp) * NTOK + t) * DH + dd] = O;
+    if (dd == 0) {
+      float* ml = part_ml + (((size_t)h * nsplit_max + sp) * NTOK + t) * 2;
+      ml[0] = M;
+      ml[1] = L;
     }
   }
 }
 
-// (3) combine: grid (n, H), Dh threads; chunks in ascending order.
+// (3) combine: grid (n, H), Dh threads; splits in ascending order.
 template <typename T>
 __global__ void attn_combine_kernel(const float* part_o, const float* part_ml, int H, int Dh, int n,
-                                    int chunk, long long ctx_max, const evs_book* book, int nchunk_max, T* g) {
+                                    int span, long long ctx_max, const evs_book* book, int nsplit_max, T* g) {
   const int t = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
   pdl_trigger();
   pdl_wait();
   const long long qpos = min((long long)book->pos + t, ctx_max - 1);
-  const int nc = (int)(qpos / chunk) + 1;  // chunks holding keys <= qpos
-  const float* ml = part_ml + ((size_t)h * nchunk_max * NTOK + t) * 2;
+  const int nc = (int)(qpos / span) + 1;  // splits holding keys <= qpos
+  const float* ml = part_ml + ((size_t)h * nsplit_max * NTOK + t) * 2;
   float M = -INFINITY;
 #pragma unroll 8
   for (int c = 0; c < nc; ++c) M = fmaxf(M, ml[(size_t)c * NTOK * 2]);
@@ -391,7 +670,7 @@ __global__ void attn_combine_kernel(const float* part_o, const float* part_ml, i
   for (int c = 0; c < nc; ++c) {
     const float mc = ml[(size_t)c * NTOK * 2];
     const float lc = ml[(size_t)c * NTOK * 2 + 1];
-    const float oc = part_o[(((size_t)h * nchunk_max + c) * NTOK + t) * Dh + e];
+    const float oc = part_o[(((size_t)h * nsplit_max + c) * NTOK + t) * Dh + e];
     if (mc == -INFINITY) continue;
     const float w = expf(mc - M);
     l = fmaf(lc, w, l);
@@ -448,8 +727,8 @@ cudaError_t iir_dispatch(const LaunchCtx& L, Src s, int d, int n, int M, const f
 
 template <typename T, int DH, int CH>
 cudaError_t attn_split_launch(const LaunchCtx& L, int H, int n, long long ctx_max, evs_book* book,
-                              const AttnBufs& B, void* kc, void* vc, int num_sms) {
-  const size_t smem = sizeof(float) * (NTOK * DH + NTOK * CH + NTOK * 2) +
+                              const AttnBufs& B, void* kc, void* vc) {
+  const size_t smem = sizeof(float) * (NTOK * DH + NTOK * CH + NTOK * 4) +
                       (size_t)CH * (DH * sizeof(T) + 16) + (size_t)CH * DH * sizeof(T);
   auto k = attn_split_kernel<T, DH, CH>;
   static bool attr_set = false;
@@ -458,19 +737,33 @@ cudaError_t attn_split_launch(const LaunchCtx& L, int H, int n, long long ctx_ma
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int gx = std::max(1, std::min(B.nchunk_max, (4 * num_sms + H - 1) / H));
-  return launch(L, k, dim3(gx, H), dim3(256), smem, (const float*)B.qbuf, (const T*)kc, (const T*)vc, H, n,
-                ctx_max, (const evs_book*)book, B.part_o, B.part_ml, B.nchunk_max);
+  return launch(L, k, dim3(B.nsplit_max, H), dim3(256), smem, (const float*)B.qbuf, (const T*)kc, (const T*)vc, H,
+                n, ctx_max, (const evs_book*)book, B.span, B.part_o, B.part_ml, B.nsplit_max);
 }
 
 template <typename T, int DH>
 cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, int n, long long ctx_max, int chunk,
-                                evs_book* book, const AttnBufs& B, void* kc, void* vc, int num_sms) {
+                                evs_book* book, const AttnBufs& B, void* kc, void* vc) {
+  if constexpr (sizeof(T) == 2) {
+    // bf16 caches: tensor-core kernel (the chunk only shapes the span)
+    constexpr size_t smem = attn_mma_smem<DH>();
+    auto k = attn_mma_kernel<DH>;
+    static bool attr_set = false;
+    if (!attr_set && smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    if (B.span % AT_STAGE) return cudaErrorInvalidValue;
+    return launch(L, k, dim3(B.nsplit_max, H), dim3(AT_WARPS * 32), smem, (const float*)B.qbuf, (const bf16*)kc,
+                  (const bf16*)vc, H, n, ctx_max, (const evs_book*)book, B.span, B.nsplit_max, B.part_o,
+                  B.part_ml);
+  }
   switch (chunk) {
-    case 32: return attn_split_launch<T, DH, 32>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
-    case 64: return attn_split_launch<T, DH, 64>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
-    case 128: return attn_split_launch<T, DH, 128>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
-    case 256: return attn_split_launch<T, DH, 256>(L, H, n, ctx_max, book, B, kc, vc, num_sms);
+    case 32: return attn_split_launch<T, DH, 32>(L, H, n, ctx_max, book, B, kc, vc);
+    case 64: return attn_split_launch<T, DH, 64>(L, H, n, ctx_max, book, B, kc, vc);
+    case 128: return attn_split_launch<T, DH, 128>(L, H, n, ctx_max, book, B, kc, vc);
+    case 256: return attn_split_launch<T, DH, 256>(L, H, n, ctx_max, book, B, kc, vc);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -482,14 +775,14 @@ cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, int n, long lo
                          (const double*)B.inv_freq, (T*)kc, (T*)vc, B.qbuf, book);
   if (e != cudaSuccess) return e;
   switch (Dh) {
-    case 32: e = attn_split_dispatch<T, 32>(L, H, n, ctx_max, chunk, book, B, kc, vc, num_sms); break;
-    case 64: e = attn_split_dispatch<T, 64>(L, H, n, ctx_max, chunk, book, B, kc, vc, num_sms); break;
-    case 128: e = attn_split_dispatch<T, 128>(L, H, n, ctx_max, chunk, book, B, kc, vc, num_sms); break;
+    case 32: e = attn_split_dispatch<T, 32>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
+    case 64: e = attn_split_dispatch<T, 64>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
+    case 128: e = attn_split_dispatch<T, 128>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   return launch(L, attn_combine_kernel<T>, dim3(n, H), dim3(Dh), 0, (const float*)B.part_o,
-                (const float*)B.part_ml, H, Dh, n, chunk, ctx_max, (const evs_book*)book, B.nchunk_max, (T*)g);
+                (const float*)B.part_ml, H, Dh, n, B.span, ctx_max, (const evs_book*)book, B.nsplit_max, (T*)g);
 }
 
 }  // namespace
@@ -514,15 +807,25 @@ cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, 
   return iir_dispatch<float>(L, sf, d, n, M, lam, res, st0, st1, book, g);
 }
 
+// Key span of a split: max(chunk, 64) * 2^j, the smallest with at most
+// ATTN_SPLITS_MAX splits over ctx_max.  Fixed per cache, so the partition
+// of a query's keys never depends on the block size.
+long long attn_span(long long ctx_max, int chunk) {
+  long long span = std::max(chunk, 64);
+  while ((ctx_max + span - 1) / span > ATTN_SPLITS_MAX) span *= 2;
+  return span;
+}
+
 size_t attn_scratch_bytes(int H, int Dh, long long ctx_max, int chunk) {
-  const long long nchunk = (ctx_max + chunk - 1) / chunk;
+  const long long nsplit = (ctx_max + attn_span(ctx_max, chunk) - 1) / attn_span(ctx_max, chunk);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return al(sizeof(double) * (Dh / 2)) + al(sizeof(float) * NTOK * H * Dh) +
-         al(sizeof(float) * H * nchunk * NTOK * Dh) + al(sizeof(float) * H * nchunk * NTOK * 2);
+         al(sizeof(float) * H * nsplit * NTOK * Dh) + al(sizeof(float) * H * nsplit * NTOK * 2);
 }
 
 void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int chunk, AttnBufs* out) {
-  const long long nchunk = (ctx_max + chunk - 1) / chunk;
+  const long long span = attn_span(ctx_max, chunk);
+  const long long nsplit = (ctx_max + span - 1) / span;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* p = (char*)scratch;
   out->inv_freq = (double*)p;
@@ -530,9 +833,10 @@ void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int
   out->qbuf = (float*)p;
   p += al(sizeof(float) * NTOK * H * Dh);
   out->part_o = (float*)p;
-  p += al(sizeof(float) * H * nchunk * NTOK * Dh);
+  p += al(sizeof(float) * H * nsplit * NTOK * Dh);
   out->part_ml = (float*)p;
-  out->nchunk_max = (int)nchunk;
+  out->nsplit_max = (int)nsplit;
+  out->span = (int)span;
 }
 
 cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStream_t stream) {

@@ -162,11 +162,12 @@ __global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, 
   for (int j = threadIdx.x; j < V; j += blockDim.x) p[(size_t)t * V + j] = w_s[j] / sum;
 }
 
-// argmax over a row, ties to the lowest index
-__device__ int block_argmax(const float* row, int V, float* fs, int* is) {
+// argmax over a row by one warp, same ties rule (lowest index); all-NaN -> 0
+__device__ int warp_argmax(const float* row, int V) {
+  const int lane = threadIdx.x & 31;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
-  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+  for (int j = lane; j < V; j += 32) {
     const float v = row[j];
     if (v > bv || (v == bv && j < bi)) { bv = v; bi = j; }
   }
@@ -176,15 +177,6 @@ __device__ int block_argmax(const float* row, int V, float* fs, int* is) {
     const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
     if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();
-  if (lane == 0) { fs[warp] = bv; is[warp] = bi; }
-  __syncthreads();
-  bv = fs[0];
-  bi = is[0];
-  for (int w = 1; w < nw; ++w)
-    if (fs[w] > bv || (fs[w] == bv && is[w] < bi)) { bv = fs[w]; bi = is[w]; }
-  __syncthreads();
   return bi == 0x7fffffff ? 0 : bi;
 }
 
@@ -228,28 +220,36 @@ __device__ int ladder_find(const unsigned int* W, int V, unsigned long long thr,
 __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float* q, const int32_t* drafts,
                                                      const float* u, int n, int V, int mode, int32_t* out_a,
                                                      int32_t* out_tok) {
-  extern __shared__ unsigned int Wsm[];  // [V]
-  __shared__ float fs[32];
-  __shared__ int is[32];
+  extern __shared__ unsigned int Wsm[];  // [V], then s_arg[n], s_ok[n]
   __shared__ unsigned long long us[256];
   __shared__ int found;
+  int* s_arg = reinterpret_cast<int*>(Wsm + V);  // greedy: argmax of every row
+  int* s_ok = s_arg + n;                          // [i]: draft i passes its own test (1..gamma)
   pdl_trigger();
   pdl_wait();
   const int gamma = n - 1;
-  int a = gamma;
-  for (int i = 1; i <= gamma; ++i) {
-    const int d = drafts[i - 1];
-    bool ok;
-    if (mode == EVS_GREEDY) {
-      ok = d == block_argmax(p + (size_t)(i - 1) * V, V, fs, is);
-    } else {
-      ok = d >= 0 && d < V && __fmul_rn(u[i - 1], q[(size_t)(i - 1) * V + d]) < p[(size_t)(i - 1) * V + d];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // every row's test at once (one warp per row), then the first rejection
+  if (mode == EVS_GREEDY) {
+    for (int r = warp; r < n; r += nw) {
+      const int am = warp_argmax(p + (size_t)r * V, V);
+      if (lane == 0) s_arg[r] = am;
     }
-    if (!ok) { a = i - 1; break; }
+    __syncthreads();
+    for (int i = 1 + threadIdx.x; i <= gamma; i += blockDim.x) s_ok[i] = drafts[i - 1] == s_arg[i - 1];
+  } else {
+    for (int i = 1 + threadIdx.x; i <= gamma; i += blockDim.x) {
+      const int d = drafts[i - 1];
+      s_ok[i] = d >= 0 && d < V && __fmul_rn(u[i - 1], q[(size_t)(i - 1) * V + d]) < p[(size_t)(i - 1) * V + d];
+    }
   }
+  __syncthreads();
+  int a = gamma;
+  for (int i = 1; i <= gamma; ++i)
+    if (!s_ok[i]) { a = i - 1; break; }
   int token;
   if (mode == EVS_GREEDY) {
-    token = block_argmax(p + (size_t)a * V, V, fs, is);
+    token = s_arg[a];
   } else {
     const float* pa = p + (size_t)a * V;
     unsigned long long S = 0;
@@ -356,8 +356,9 @@ cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, 
 
 cudaError_t launch_accept(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
                           const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok) {
-  const size_t smem = sizeof(unsigned int) * V;
+  const size_t smem = sizeof(unsigned int) * V + 2 * sizeof(int) * n;
   if (smem > 48 * 1024) {
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }

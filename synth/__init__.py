@@ -302,6 +302,15 @@ def layer_state(seed: int, kind: str, param: int, d: int, P: int = 0, n_heads: i
     return synth_state(shape, seed, P)["layers"][0]
 
 
+def kv_head(seed: int, head: int, P: int, head_dim: int) -> tuple:
+    """Long-context cache rows of one attention head: K and V [P][head_dim]
+    ~ N(0, 1), bf16 bit patterns (one head at a time, so a 262k-position
+    cache can be synthesised for the heads a test samples)."""
+    k = _dense(np.random.SeedSequence([seed, 11, head]), (P, head_dim), 1.0, "bf16")
+    v = _dense(np.random.SeedSequence([seed, 12, head]), (P, head_dim), 1.0, "bf16")
+    return k, v
+
+
 def abv_block(seed: int, n: int, d: int, dtype: str = "bf16") -> np.ndarray:
     """Mixer inputs for an operator-level test: [n][3d] ~ N(0, 1) (a | b | v)."""
     ss = np.random.SeedSequence([seed, 7])
