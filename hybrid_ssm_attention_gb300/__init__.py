@@ -187,6 +187,10 @@ class State:
     def clone_into(self, dst: "State", stream=None):
         _check(lib().evs_state_clone(self.handle, dst.handle, _stream(stream)), "evs_state_clone")
 
+    def snapshot_into(self, dst: "State", stream=None):
+        """Recurrent state + bookkeeping only (KV caches are append-only)."""
+        _check(lib().evs_state_snapshot(self.handle, dst.handle, _stream(stream)), "evs_state_snapshot")
+
 
 # ------------------------------------------------------------------ C-named calls
 def evs_verify_block(state: State, tokens, n: int, logits, stream=None):

@@ -61,6 +61,7 @@ PROTOTYPES = {
     "evs_state_destroy": (i32, [vp]),
     "evs_state_reset": (i32, [vp, vp]),
     "evs_state_clone": (i32, [vp, vp, vp]),
+    "evs_state_snapshot": (i32, [vp, vp, vp]),
     "evs_state_layer_view": (i32, [vp, i32, C.POINTER(evs_layer_view)]),
     "evs_state_book_dev": (i32, [vp, PP]),
     "evs_state_book_read": (i32, [vp, C.POINTER(evs_book), vp]),

@@ -748,6 +748,34 @@ extern "C" int evs_state_use_graphs(evs_state* s, int32_t enable) {
   return EVS_OK;
 }
 
+extern "C" int evs_state_snapshot(const evs_state* src, evs_state* dst, cudaStream_t stream) {
+  if (!src || !dst) return fail(EVS_ERR_ARG, "null state");
+  if (src->m != dst->m || src->ctx_max != dst->ctx_max)
+    return fail(EVS_ERR_ARG, "snapshot needs the same model and ctx_max");
+  evs_book b;
+  EVS_TRY(evs_state_book_read(src, &b, stream));
+  const evs_model* m = src->m;
+  const evs_config& c = m->cfg;
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    const LayerW& L = m->L[i];
+    const LayerS &a = src->S[i], &z = dst->S[i];
+    if (L.kind == EVS_LAYER_FIR) {
+      for (int k = 0; k < 2; ++k)
+        CUDA_TRY(cudaMemcpyAsync(z.ext[k], a.ext[k], sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
+                                 cudaMemcpyDeviceToDevice, stream));
+    } else if (L.kind == EVS_LAYER_IIR) {
+      for (int k = 0; k < 2; ++k)
+        CUDA_TRY(cudaMemcpyAsync(z.st[k], a.st[k], sizeof(float) * 2 * (size_t)m->n_max * c.d_model * L.param,
+                                 cudaMemcpyDeviceToDevice, stream));
+    }
+  }
+  CUDA_TRY(cudaMemcpyAsync(dst->book, src->book, sizeof(evs_book), cudaMemcpyDeviceToDevice, stream));
+  dst->host_pos = b.pos;
+  dst->host_pos_known = true;
+  dst->host_pending = b.pending_n;
+  return EVS_OK;
+}
+
 extern "C" int evs_state_clone(const evs_state* src, evs_state* dst, cudaStream_t stream) {
   if (!src || !dst) return fail(EVS_ERR_ARG, "null state");
   if (src->m != dst->m || src->ctx_max != dst->ctx_max) return fail(EVS_ERR_ARG, "clone needs the same model and ctx_max");

@@ -180,6 +180,15 @@ int evs_state_reset(evs_state* s, cudaStream_t stream);
 /* Copies every buffer and the bookkeeping of src into dst (same model and
  * ctx_max): the snapshot of snapshot-and-replay rollback ([abstract]). */
 int evs_state_clone(const evs_state* src, evs_state* dst, cudaStream_t stream);
+/* Copies the recurrent state only (FIR windows, IIR modal states) and the
+ * bookkeeping of src into dst (same model and ctx_max); the KV caches are
+ * not copied: they are append-only, rows below pos never change and rows
+ * from pos on are rewritten by the next verify.  This is the snapshot (and,
+ * copied back, the restore) of the snapshot-and-replay baseline that
+ * per-position state slicing replaces ([abstract], [systems]): snapshot,
+ * verify, restore, verify the kept tokens again, commit.  Synchronous read
+ * of src's bookkeeping; the copies are enqueued on stream. */
+int evs_state_snapshot(const evs_state* src, evs_state* dst, cudaStream_t stream);
 int evs_state_layer_view(const evs_state* s, int32_t layer, evs_layer_view* out);
 /* Device address of the bookkeeping (for graph-captured callers). */
 int evs_state_book_dev(const evs_state* s, evs_book** out);

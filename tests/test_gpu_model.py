@@ -113,6 +113,47 @@ def test_small_bf16_spec_equals_native_bitwise(graphs):
     assert sp.check() == 0 and nat.check() == 0
 
 
+@pytest.mark.gpu
+def test_snapshot_replay_equals_sliced_commit_bitwise():
+    # The baseline that per-position slicing replaces: snapshot the recurrent
+    # state, verify the block, restore, verify only the kept tokens again,
+    # commit.  Its state must equal the sliced commit's: the next block's
+    # logits agree bit for bit, for every keep tried.
+    import hybrid_ssm_attention_gb300 as evs
+    shape = small_shape()
+    W = synth.make_weights(shape, 23)
+    m = evs.Model(shape, W)
+    nb = shape.n_block
+    prompt = [int(x) for x in synth.prompt(shape, 23, 6 * nb)]
+    a, b, snap = evs.State(m, 512), evs.State(m, 512), evs.State(m, 512)
+    for st in (a, b):
+        _verify(evs, st, prompt[:nb], shape.vocab)
+        evs.evs_commit(st, nb)
+    s0 = nb
+    for keep in (0, 5, nb, 1):
+        blk = prompt[s0:s0 + nb]
+        la, _ = _verify(evs, a, blk, shape.vocab)          # sliced: verify once, commit keep
+        evs.evs_commit(a, keep)
+        b.snapshot_into(snap)                               # replay baseline
+        lb, _ = _verify(evs, b, blk, shape.vocab)
+        assert np.array_equal(to_np(la).view(np.uint32), to_np(lb).view(np.uint32))
+        snap.snapshot_into(b)
+        if keep:
+            _verify(evs, b, blk[:keep], shape.vocab)
+            evs.evs_commit(b, keep)
+        assert a.book()["pos"] == b.book()["pos"]
+        nxt = prompt[s0 + nb:s0 + 2 * nb]
+        ta = evs.State(m, 512)
+        a.clone_into(ta)
+        l1, _ = _verify(evs, ta, nxt, shape.vocab)
+        tb = evs.State(m, 512)
+        b.clone_into(tb)
+        l2, _ = _verify(evs, tb, nxt, shape.vocab)
+        assert np.array_equal(to_np(l1).view(np.uint32), to_np(l2).view(np.uint32)), keep
+        s0 += nb
+    assert a.check() == 0 and b.check() == 0
+
+
 def wide_shape():
     # 7B widths, two layers: in-projection and gate/up take the stream-K
     # split, down and head the cluster split
