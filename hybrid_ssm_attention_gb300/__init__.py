@@ -268,6 +268,10 @@ def evs_op_gemm_static(w, x, N, K, n, dtype, y, stream=None):
            "evs_op_gemm_static")
 
 
+def evs_selftest_wait_timeout(status, limit_ns, stream=None):
+    _check(lib().evs_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)), "evs_selftest_wait_timeout")
+
+
 def evs_kernel_launches() -> int:
     return int(lib().evs_kernel_launches())
 

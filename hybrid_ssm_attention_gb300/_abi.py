@@ -83,6 +83,7 @@ PROTOTYPES = {
     "evs_op_gemm_scratch_bytes": (sz, [i32, i32, i32]),
     "evs_op_gemm": (i32, [vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]),
     "evs_op_gemm_static": (i32, [vp, vp, i32, i32, i32, i32, vp, vp]),
+    "evs_selftest_wait_timeout": (i32, [vp, i64, vp]),
     "evs_profile_gemms": (i32, [vp, i32, C.POINTER(C.c_float), C.POINTER(i64), i32, C.POINTER(i32), vp]),
     "evs_last_error": (C.c_char_p, []),
     "evs_version": (C.c_char_p, []),

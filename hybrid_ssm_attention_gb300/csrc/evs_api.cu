@@ -150,20 +150,33 @@ struct evs_state {
   std::vector<GraphEntry> graphs;
   unsigned long long tick;
   std::vector<void*> allocs;
+  size_t alloc_bytes = 0;
 };
 
 namespace {
 
 size_t esize(int dtype) { return dtype == EVS_BF16 ? 2 : 4; }
 
+// Fault injection for tests: EVS_ALLOC_LIMIT=<bytes> caps one state's
+// device allocations; beyond it dmalloc reports EVS_ERR_OOM without
+// allocating (the same path a real cudaMalloc failure takes).
+size_t alloc_limit() {
+  const char* v = getenv("EVS_ALLOC_LIMIT");
+  return v ? (size_t)strtoull(v, nullptr, 10) : 0;
+}
+
 int dmalloc(evs_state* s, void** p, size_t bytes) {
   if (bytes == 0) bytes = 16;
+  const size_t lim = alloc_limit();
+  if (lim && s->alloc_bytes + bytes > lim)
+    return fail(EVS_ERR_OOM, "allocation of %zu bytes exceeds EVS_ALLOC_LIMIT (%zu in use)", bytes, s->alloc_bytes);
   cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(EVS_ERR_OOM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
   }
   s->allocs.push_back(*p);
+  s->alloc_bytes += bytes;
   return EVS_OK;
 }
 
@@ -1213,6 +1226,13 @@ extern "C" int evs_trace_cta(evs_state* s, int32_t slot, unsigned long long* out
   return EVS_OK;
 }
 #endif
+
+extern "C" int evs_selftest_wait_timeout(int32_t* status_dev, int64_t limit_ns, cudaStream_t stream) {
+  if (!status_dev) return fail(EVS_ERR_ARG, "null status");
+  if (limit_ns < 1000 || limit_ns > 1000000000) return fail(EVS_ERR_ARG, "limit_ns outside [1e3, 1e9]");
+  CUDA_TRY(launch_wait_selftest(stream, status_dev, (unsigned long long)limit_ns));
+  return EVS_OK;
+}
 
 // =================================================================== misc
 extern "C" const char* evs_last_error(void) { return g_err.c_str(); }

@@ -163,13 +163,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait: false once WAIT_NS elapsed (the abort flag is then raised)
 // or another role already aborted.  The first probe is inlined: the
 // single-thread producer and MMA loops are latency-critical.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           uint64_t limit_ns = WAIT_NS) {
   const uint64_t t0 = gtimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(bar, parity)) return true;
     if ((i & 31) == 0) {
       if (*abort_flag) return false;
-      if (gtimer() - t0 > WAIT_NS) {
+      if (gtimer() - t0 > limit_ns) {
         *abort_flag = 1;
         return false;
       }
@@ -857,6 +858,21 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const T* W, const T* X, 
   }
 }
 
+// Exercises the pipeline's bounded wait: an mbarrier that nothing ever
+// arrives on, waited on with a short limit; the expiry must come back as
+// EVS_DEV_TIMEOUT in *status, with the kernel returning normally.
+__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  volatile int* ab = &abort_flag;
+  if (!mbar_try(smem_u32(&bar), 0) && !mbar_wait_slow(smem_u32(&bar), 0, ab, limit_ns))
+    atomicOr(status, EVS_DEV_TIMEOUT);
+}
+
 // One CTA per 16 KB unit u (tile-major): 128 rows x 8 chunks of 16 bytes,
 // chunk j of row r stored at position j ^ (r & 7); out-of-range rows /
 // columns are zero.  The block goes to i * G + c for the CTA c that owns u
@@ -893,6 +909,12 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const bf16* W, int N,
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, unsigned long long limit_ns) {
+  count_launch();
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 int gemm_stages_for(int cl, int bsrc) {
   int S = GEMM_MAX_STAGES;

@@ -328,6 +328,14 @@ int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int3
 int evs_op_gemm_static(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
                        int32_t dtype, float* y_dev, cudaStream_t stream);
 
+/* Self-test of the device-side bounded wait that guards every pipeline wait
+ * of the GEMM (no counterpart in the pages): one thread waits on an
+ * mbarrier nothing arrives on, for limit_ns in [1e3, 1e9]; the expiry ORs
+ * EVS_DEV_TIMEOUT into *status_dev (device int, caller-owned) and the
+ * kernel returns normally, leaving the context usable.  Asynchronous on
+ * stream. */
+int evs_selftest_wait_timeout(int32_t* status_dev, int64_t limit_ns, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- profiling */
 /* Times every weight GEMM of one verify step of n tokens (per layer: in,
  * out, gate/up, down; then the head) with CUDA events around each launch,

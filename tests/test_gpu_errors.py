@@ -7,7 +7,11 @@ hangs):
   (EVS_ERR_ARG); committed length + n > ctx_max (EVS_ERR_CAPACITY);
 * device: a token outside the vocabulary (EVS_DEV_BAD_TOKEN), a device-side
   keep outside [0, n] (EVS_DEV_BAD_KEEP, state left as before the verify),
-  an append past ctx_max after device-side commits (EVS_DEV_KV_OVERFLOW).
+  an append past ctx_max after device-side commits (EVS_DEV_KV_OVERFLOW);
+* injected faults: a device allocation limit (EVS_ALLOC_LIMIT) makes state
+  creation fail with EVS_ERR_OOM and the library stays usable; a bounded
+  pipeline wait on an mbarrier nothing arrives on expires after 2 ms and
+  reports EVS_DEV_TIMEOUT in a status word, the kernel returning normally.
 """
 import numpy as np
 import pytest
@@ -15,8 +19,8 @@ import pytest
 import synth
 from gpu_util import to_np, torch
 
-ERR_ARG, ERR_STATE, ERR_CAPACITY = 1, 2, 3
-BAD_TOKEN, KV_OVERFLOW, BAD_KEEP = 1, 2, 4
+ERR_ARG, ERR_STATE, ERR_CAPACITY, ERR_OOM = 1, 2, 3, 4
+BAD_TOKEN, KV_OVERFLOW, BAD_KEEP, DEV_TIMEOUT = 1, 2, 4, 8
 
 
 def _tiny(ctx):
@@ -123,3 +127,37 @@ def test_kv_overflow_after_device_commits():
     _v(evs, st, [1, 2, 3, 4, 5], shape.vocab)   # host no longer knows pos: device check
     status = st.check()
     assert status & KV_OVERFLOW
+
+
+@pytest.mark.gpu
+def test_allocation_limit_reports_oom_and_recovers(monkeypatch):
+    import hybrid_ssm_attention_gb300 as evs
+    shape = synth.tiny()
+    m = evs.Model(shape, synth.make_weights(shape, 0))
+    monkeypatch.setenv("EVS_ALLOC_LIMIT", "4096")
+    with pytest.raises(evs.EvsError) as e:
+        evs.State(m, 64)
+    assert e.value.code == ERR_OOM
+    monkeypatch.delenv("EVS_ALLOC_LIMIT")
+    st = evs.State(m, 64)
+    lg = _v(evs, st, [1, 2, 3], shape.vocab)
+    assert np.isfinite(to_np(lg)).all() and st.check() == 0
+
+
+@pytest.mark.gpu
+def test_bounded_wait_expires_with_status():
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    status = t.zeros(1, dtype=t.int32, device="cuda")
+    evs.evs_selftest_wait_timeout(status, 2_000_000)
+    t.cuda.synchronize()
+    assert int(status.item()) == DEV_TIMEOUT
+    # the context is still usable: a GEMM right after
+    W = t.ones((128, 64), dtype=t.float32, device="cuda")
+    X = t.ones((2, 64), dtype=t.float32, device="cuda")
+    y = t.empty((2, 128), dtype=t.float32, device="cuda")
+    scratch = t.empty(evs.evs_op_gemm_scratch_bytes(128, 64, evs.EVS_F32), dtype=t.uint8, device="cuda")
+    evs.evs_op_gemm(W, X, 128, 64, 2, evs.EVS_F32, y, scratch)
+    assert float(y.min().item()) == 64.0 and float(y.max().item()) == 64.0
+    with pytest.raises(evs.EvsError):
+        evs.evs_selftest_wait_timeout(status, 10_000_000_000)   # limit above 1 s is refused
