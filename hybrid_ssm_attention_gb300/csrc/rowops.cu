@@ -93,8 +93,11 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
                                                          float eps, T* xn) {
   __shared__ float s_den, s_rcp;
   const int t = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_trigger();
   pdl_wait();
+  // this thread's residual value is loaded alongside the per-tile sums
+  const float x = c < d ? __ldcg(X + (size_t)t * d + c) : 0.f;
   if (threadIdx.x < 32) {
     // the per-tile sums, 32 loads in flight at a time, added in tile order
     const int lane = threadIdx.x;
@@ -109,9 +112,7 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
     }
   }
   __syncthreads();
-  const float den = s_den;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c < d) xn[(size_t)t * d + c] = from_f<T>(div_row(X[(size_t)t * d + c], den, s_rcp));
+  if (c < d) xn[(size_t)t * d + c] = from_f<T>(div_row(x, s_den, s_rcp));
 }
 
 template <typename T>
