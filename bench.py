@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-replay", action="store_true")
+    ap.add_argument("--long-gen", type=int, default=0,
+                    help="also generate this many tokens natively and speculatively (drafts with random "
+                         "corrupted tails) and report whether the two sequences are identical")
     return ap.parse_args()
 
 
@@ -240,6 +243,83 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ GPU arm
+def long_generation(evs, torch, model, shape, prompt, ntok, seed, dev):
+    """Greedy generation of ntok tokens twice from the same prompt: native
+    (one token per round) and speculative (gamma=12 drafts = the native
+    continuation with the tail after a random cut replaced by random tokens,
+    so every round has an accepted prefix, a rejection or a bonus).  Also
+    times the prompt's chunked prefill (block verify with keep = n)."""
+    n = shape.n_block
+    P0 = len(prompt)
+    ctx = P0 + ntok + 2 * n
+    st = evs.State(model, ctx)
+    lg = torch.empty((n, shape.vocab), dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for s0 in range(0, P0 - 1, n):
+        blk = torch.tensor(prompt[s0:min(s0 + n, P0 - 1)], dtype=torch.int32, device=dev)
+        evs.evs_verify_block(st, blk, blk.numel(), lg[:blk.numel()])
+        evs.evs_commit(st, blk.numel())
+    e1.record()
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    snap = evs.State(model, ctx)
+    st.clone_into(snap)
+    # native
+    y = torch.empty(ntok + 1, dtype=torch.int32, device=dev)
+    y[0] = prompt[-1]
+    tok1 = y[:1].clone()
+    lg1 = torch.empty((1, shape.vocab), dtype=torch.float32, device=dev)
+    acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    otok = torch.zeros(1, dtype=torch.int32, device=dev)
+    e0.record()
+    for i in range(ntok):
+        evs.evs_round(st, tok1, 1, lg1, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
+        tok1.copy_(otok)
+        y[i + 1:i + 2].copy_(otok)
+    e1.record()
+    torch.cuda.synchronize()
+    native_ms = e0.elapsed_time(e1)
+    native = y.cpu().numpy()
+    # speculative, drafts built on the host from the native sequence
+    snap.clone_into(st)
+    g = np.random.default_rng(seed)
+    out = []
+    pend = int(native[0])
+    toks = torch.empty(n, dtype=torch.int32, device=dev)
+    rounds = 0
+    accepted = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    while len(out) < ntok:
+        k = len(out)
+        nxt = [int(v) for v in native[k + 1:k + n]]
+        drafts = (nxt + [0] * (n - 1))[:n - 1]
+        cut = int(g.integers(0, n))
+        drafts = drafts[:cut] + [int(v) for v in g.integers(0, shape.vocab, n - 1 - cut)]
+        toks.copy_(torch.tensor([pend] + drafts, dtype=torch.int32))
+        evs.evs_round(st, toks, n, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
+        a, x = int(acc.item()), int(otok.item())
+        out += drafts[:a] + [x]
+        pend = x
+        rounds += 1
+        accepted += a
+    spec_s = time.perf_counter() - t0
+    out = np.asarray(out[:ntok], np.int64)
+    ref = native[1:ntok + 1].astype(np.int64)
+    mism = np.nonzero(out != ref)[0]
+    st.close()
+    snap.close()
+    return {"tokens": ntok, "identical": bool(mism.size == 0),
+            "first_mismatch": int(mism[0]) if mism.size else None,
+            "native_ms_per_token": native_ms / ntok, "spec_rounds": rounds,
+            "mean_accepted_per_round": accepted / rounds,
+            "spec_tok_s_host_driven": ntok / spec_s,
+            "prefill": {"tokens": P0 - 1, "ms": prefill_ms, "tok_s": (P0 - 1) / (prefill_ms / 1e3)},
+            "context_end": P0 + ntok}
+
+
 def run_evs(args, rank, world, local):
     import torch
 
@@ -388,6 +468,10 @@ def run_evs(args, rank, world, local):
         e2e = {"value": reduce_sum(emitted_e2e, world) / reduce_max(dt, world), "unit": UNIT,
                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 8}
 
+    longgen = None
+    if args.long_gen > 0:
+        longgen = long_generation(evs, torch, model, shape, prompt, args.long_gen, args.seed + 100, dev)
+
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
         st.close()
@@ -416,6 +500,7 @@ def run_evs(args, rank, world, local):
             "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms_per_step / 1e3) / 1e9,
                          "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "snapshot_replay": replay,
+            "long_generation": longgen,
             "gpu_launches": int(launches),
             "clocks": clk}
     print(json.dumps(line), flush=True)

@@ -154,6 +154,60 @@ def test_snapshot_replay_equals_sliced_commit_bitwise():
     assert a.check() == 0 and b.check() == 0
 
 
+@pytest.mark.gpu
+def test_small_long_generation_spec_equals_native():
+    # Chunked prefill of a 256-token prompt, then 1,200 tokens generated
+    # natively and speculatively (gamma = 12, drafts = the native
+    # continuation with a random corrupted tail, so rounds end in a
+    # rejection or a bonus): the two sequences are identical.
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    shape = small_shape()
+    W = synth.make_weights(shape, 31)
+    m = evs.Model(shape, W)
+    nb = shape.n_block
+    prompt = [int(x) for x in synth.prompt(shape, 31, 256)]
+    N = 1200
+    ctx = len(prompt) + N + 2 * nb
+
+    def prefilled():
+        st = evs.State(m, ctx)
+        for s0 in range(0, len(prompt) - 1, nb):
+            chunk = prompt[s0:min(s0 + nb, len(prompt) - 1)]
+            _verify(evs, st, chunk, shape.vocab)
+            evs.evs_commit(st, len(chunk))
+        return st
+
+    nat = prefilled()
+    acc = t.zeros(1, dtype=t.int32, device="cuda")
+    tok = t.zeros(1, dtype=t.int32, device="cuda")
+    lg1 = t.empty((1, shape.vocab), dtype=t.float32, device="cuda")
+    tk = t.tensor([prompt[-1]], dtype=t.int32, device="cuda")
+    native = []
+    for _ in range(N):
+        evs.evs_round(nat, tk, 1, lg1, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, tok)
+        tk.copy_(tok)
+        native.append(int(tok.item()))
+    sp = prefilled()
+    g = np.random.default_rng(8)
+    lg = t.empty((nb, shape.vocab), dtype=t.float32, device="cuda")
+    out, pend, rejected = [], prompt[-1], 0
+    while len(out) < N:
+        k = len(out)
+        drafts = (native[k:k + nb - 1] + [0] * nb)[:nb - 1]
+        cut = int(g.integers(0, nb))
+        drafts = drafts[:cut] + [int(x) for x in g.integers(0, shape.vocab, nb - 1 - cut)]
+        tt = t.tensor([pend] + drafts, dtype=t.int32, device="cuda")
+        evs.evs_round(sp, tt, nb, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, tok)
+        a, x = int(acc.item()), int(tok.item())
+        rejected += a < nb - 1
+        out += drafts[:a] + [x]
+        pend = x
+    assert out[:N] == native
+    assert rejected > 0
+    assert sp.check() == 0 and nat.check() == 0
+
+
 def wide_shape():
     # 7B widths, two layers: in-projection and gate/up take the stream-K
     # split, down and head the cluster split
