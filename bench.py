@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-replay", action="store_true")
+    ap.add_argument("--no-batch", action="store_true")
     ap.add_argument("--long-gen", type=int, default=0,
                     help="also generate this many tokens natively and speculatively (drafts with random "
                          "corrupted tails) and report whether the two sequences are identical")
@@ -320,6 +321,37 @@ def long_generation(evs, torch, model, shape, prompt, ntok, seed, dev):
             "context_end": P0 + ntok}
 
 
+def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, rounds=24, warm=4):
+    """Batched verify (one pass over B sequences' blocks, B * n = 16 rows or
+    13 for B = 1): round time and verified rows per second for each (B, n),
+    every sequence committing its whole block (host keep) after each pass.
+    The sequences start from the same post-prompt state."""
+    out = []
+    V = shape.vocab
+    g = np.random.default_rng(7)
+    for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1)):
+        states = [evs.State(model, ctx) for _ in range(B)]
+        for st in states:
+            post_prompt.clone_into(st)
+        lg = torch.empty((B * n, V), dtype=torch.float32, device=dev)
+        toks = torch.tensor(g.integers(65, 85, (rounds + warm, B * n)).astype(np.int32), device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for r in range(rounds + warm):
+            if r == warm:
+                torch.cuda.synchronize()
+                e0.record()
+            evs.evs_verify_batch(states, toks[r], [n] * B, lg)
+            for st in states:
+                evs.evs_commit(st, n)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / rounds
+        out.append({"B": B, "n": n, "rows": B * n, "ms_per_round": ms, "rows_per_s": B * n / (ms / 1e3)})
+        for st in states:
+            st.close()
+    return out
+
+
 def run_evs(args, rank, world, local):
     import torch
 
@@ -468,6 +500,10 @@ def run_evs(args, rank, world, local):
         e2e = {"value": reduce_sum(emitted_e2e, world) / reduce_max(dt, world), "unit": UNIT,
                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 8}
 
+    batched = None
+    if not args.no_batch:
+        batched = batched_sweep(evs, torch, model, shape, snap, ctx, dev)
+
     longgen = None
     if args.long_gen > 0:
         longgen = long_generation(evs, torch, model, shape, prompt, args.long_gen, args.seed + 100, dev)
@@ -500,7 +536,7 @@ def run_evs(args, rank, world, local):
             "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms_per_step / 1e3) / 1e9,
                          "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "snapshot_replay": replay,
-            "long_generation": longgen,
+            "long_generation": longgen, "batched_verify": batched,
             "gpu_launches": int(launches),
             "clocks": clk}
     print(json.dumps(line), flush=True)

@@ -20,7 +20,8 @@ from ._abi import (EVS_BF16, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN, EVS_LAYER_FIR,
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
            "evs_commit", "evs_commit_dev", "evs_round", "evs_op_fir", "evs_op_iir",
-           "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_kernel_launches"]
+           "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_verify_batch",
+           "evs_kernel_launches"]
 
 KIND_CODES = {"SE": EVS_LAYER_FIR, "MR": EVS_LAYER_FIR, "FIR": EVS_LAYER_FIR,
               "LI": EVS_LAYER_IIR, "IIR": EVS_LAYER_IIR, "ATT": EVS_LAYER_ATTN, "ATTN": EVS_LAYER_ATTN}
@@ -270,6 +271,14 @@ def evs_op_gemm_static(w, x, N, K, n, dtype, y, stream=None):
 
 def evs_selftest_wait_timeout(status, limit_ns, stream=None):
     _check(lib().evs_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)), "evs_selftest_wait_timeout")
+
+
+def evs_verify_batch(states, tokens, ns, logits, stream=None):
+    """One verify pass over several sequences' blocks (rows back to back)."""
+    arr = (C.c_void_p * len(states))(*[st.handle for st in states])
+    nh = (C.c_int32 * len(ns))(*[int(x) for x in ns])
+    _check(lib().evs_verify_batch(arr, len(states), _ptr(tokens), nh, _ptr(logits), _stream(stream)),
+           "evs_verify_batch")
 
 
 def evs_kernel_launches() -> int:

@@ -70,6 +70,7 @@ PROTOTYPES = {
     "evs_state_use_graphs": (i32, [vp, i32]),
     "evs_verify_block": (i32, [vp, vp, i32, vp, vp]),
     "evs_verify_block_trace": (i32, [vp, vp, i32, vp, vp, vp]),
+    "evs_verify_batch": (i32, [vp, i32, vp, vp, vp, vp]),
     "evs_probs": (i32, [vp, i32, i32, f32, i32, vp, vp]),
     "evs_accept": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]),
     "evs_commit": (i32, [vp, i32, vp]),

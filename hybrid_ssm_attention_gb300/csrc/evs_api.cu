@@ -181,8 +181,14 @@ int dmalloc(evs_state* s, void** p, size_t bytes) {
 }
 
 // ------------------------------------------------------------------ verify sequence
-int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc,
-                   float* trace = nullptr) {
+// One verify pass over the block rows of nseq sequences: rows [row0[b],
+// row0[b+1]) belong to states[b].  The weight GEMMs run once over all rows;
+// the work buffers (residual, activations, partials) are states[0]'s, the
+// recurrent state, caches and bookkeeping each sequence's own.
+int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* tokens, float* logits,
+                   const LaunchCtx& Lc, float* trace = nullptr) {
+  evs_state* s = states[0];
+  const int n = sr.row0[sr.nseq];
   evs_model* m = s->m;
   const evs_config& c = m->cfg;
   const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
@@ -254,7 +260,14 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     return EVS_OK;
   };
   const size_t xbytes = sizeof(float) * (size_t)n * d;
-  CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, n, d, V, eps, s->X, s->xn, s->book));
+  const int nseq = sr.nseq;
+  SeqPtrs<evs_book*> books{};
+  SeqPtrs<const evs_book*> cbooks{};
+  for (int b = 0; b < nseq; ++b) {
+    books.p[b] = states[b]->book;
+    cbooks.p[b] = states[b]->book;
+  }
+  CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, sr, d, V, eps, s->X, s->xn, books));
   if (trace) CUDA_TRY(cudaMemcpyAsync(trace, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   const bool fz = m->fuse, sg = m->swiglu;
   for (size_t i = 0; i < m->L.size(); ++i) {
@@ -267,13 +280,25 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
     else
       EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d));
     MixSrc src{s->fin, 3 * d, 1};
+    (void)st;
     if (w.kind == EVS_LAYER_FIR) {
-      CUDA_TRY(launch_fir(Lc, dt, src, d, n, w.param, w.taps, st.ext[0], st.ext[1], s->book, s->g));
+      SeqPtrs<float*> e0{}, e1{};
+      for (int b = 0; b < nseq; ++b) e0.p[b] = states[b]->S[i].ext[0], e1.p[b] = states[b]->S[i].ext[1];
+      CUDA_TRY(launch_fir(Lc, dt, src, d, sr, w.param, w.taps, e0, e1, cbooks, s->g));
     } else if (w.kind == EVS_LAYER_IIR) {
-      CUDA_TRY(launch_iir(Lc, dt, src, d, n, w.param, w.lam, w.res, st.st[0], st.st[1], s->book, s->g));
+      SeqPtrs<float*> s0{}, s1{};
+      for (int b = 0; b < nseq; ++b) s0.p[b] = states[b]->S[i].st[0], s1.p[b] = states[b]->S[i].st[1];
+      CUDA_TRY(launch_iir(Lc, dt, src, d, sr, w.param, w.lam, w.res, s0, s1, cbooks, s->g));
     } else {
-      CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, n, s->ctx_max, c.attn_chunk,
-                                st.kc, st.vc, s->book, s->ab, s->g, m->num_sms));
+      AttnSeq as{};
+      for (int b = 0; b < nseq; ++b) {
+        as.kc.p[b] = states[b]->S[i].kc;
+        as.vc.p[b] = states[b]->S[i].vc;
+        as.book.p[b] = states[b]->book;
+        as.part_o.p[b] = states[b]->ab.part_o;
+        as.part_ml.p[b] = states[b]->ab.part_ml;
+      }
+      CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, sr, s->ctx_max, c.attn_chunk, as, s->ab, s->g));
     }
     EVS_TRY(gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
     const int gu_mode = sg ? GEMM_SWIGLU : GEMM_FINAL;
@@ -294,6 +319,11 @@ int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, co
   else
     EVS_TRY(gemm(m->p_head, m->m_head, m->pk_head, m->head, s->m_xn, s->xn, d, GEMM_FINAL, logits, V));
   return EVS_OK;
+}
+
+int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc,
+                   float* trace = nullptr) {
+  return enqueue_verify(&s, one_seq(n), tokens, logits, Lc, trace);
 }
 
 struct RoundArgs {
@@ -843,6 +873,29 @@ extern "C" int evs_verify_block(evs_state* s, const int32_t* tokens, int32_t n, 
   return EVS_OK;
 }
 
+extern "C" int evs_verify_batch(evs_state* const* states, int32_t nseq, const int32_t* tokens, const int32_t* n_host,
+                                float* logits, cudaStream_t stream) {
+  if (!states || !tokens || !n_host || !logits) return fail(EVS_ERR_ARG, "null argument");
+  if (nseq < 1 || nseq > MAX_SEQ) return fail(EVS_ERR_ARG, "nseq=%d outside [1, %d]", nseq, MAX_SEQ);
+  SeqRows sr{};
+  sr.nseq = nseq;
+  for (int b = 0; b < nseq; ++b) {
+    evs_state* s = states[b];
+    if (!s) return fail(EVS_ERR_ARG, "null state %d", b);
+    if (s->m != states[0]->m || s->ctx_max != states[0]->ctx_max)
+      return fail(EVS_ERR_ARG, "batched states need the same model and ctx_max");
+    for (int q = 0; q < b; ++q)
+      if (states[q] == s) return fail(EVS_ERR_ARG, "state %d appears twice", b);
+    EVS_TRY(check_block(s, n_host[b]));
+    sr.row0[b + 1] = sr.row0[b] + n_host[b];
+  }
+  if (sr.row0[nseq] > NTOK) return fail(EVS_ERR_ARG, "%d block rows in total, at most %d", sr.row0[nseq], NTOK);
+  LaunchCtx Lc{stream, states[0]->pdl};
+  EVS_TRY(enqueue_verify(states, sr, tokens, logits, Lc));
+  for (int b = 0; b < nseq; ++b) states[b]->host_pending = n_host[b];
+  return EVS_OK;
+}
+
 extern "C" int evs_verify_block_trace(evs_state* s, const int32_t* tokens, int32_t n, float* logits,
                                       float* x_trace, cudaStream_t stream) {
   if (!s || !tokens || !logits || !x_trace) return fail(EVS_ERR_ARG, "null argument");
@@ -933,7 +986,8 @@ extern "C" int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_
     return fail(EVS_ERR_ARG, "bad FIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, n, L, taps, e0, e1, book, g));
+  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, one_seq(n), L, taps, one_ptr(e0),
+                      one_ptr(e1), one_ptr(book), g));
   return EVS_OK;
 }
 
@@ -945,7 +999,8 @@ extern "C" int evs_op_iir(int32_t M, int32_t d, int32_t n, int32_t n_max, int32_
     return fail(EVS_ERR_ARG, "bad IIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_iir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, n, M, lam, res, s0, s1, book, g));
+  CUDA_TRY(launch_iir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, one_seq(n), M, lam, res, one_ptr(s0),
+                      one_ptr(s1), one_ptr(book), g));
   return EVS_OK;
 }
 
@@ -970,8 +1025,15 @@ extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max,
   attn_bufs_from_scratch(scratch, H, Dh, ctx_max, chunk, &B);
   LaunchCtx Lc{stream, false};
   CUDA_TRY(fill_rope_table(B, Dh, base, stream));
-  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{qkv, 3 * H * Dh, dtype == EVS_F32}, H, Dh, n, ctx_max, chunk, kc, vc, book,
-                            B, g, sms));
+  AttnSeq as{};
+  as.kc.p[0] = kc;
+  as.vc.p[0] = vc;
+  as.book.p[0] = book;
+  as.part_o.p[0] = B.part_o;
+  as.part_ml.p[0] = B.part_ml;
+  (void)sms;
+  CUDA_TRY(launch_attention(Lc, dtype, MixSrc{qkv, 3 * H * Dh, dtype == EVS_F32}, H, Dh, one_seq(n), ctx_max, chunk,
+                            as, B, g));
   return EVS_OK;
 }
 

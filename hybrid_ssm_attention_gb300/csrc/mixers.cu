@@ -35,11 +35,17 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Each lane keeps its J taps and the J + 15 window values they touch in
 // registers.
 template <typename T, typename Src, int JT>
-__global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
-                                                  const float* __restrict__ taps, float* ext0,
-                                                  float* ext1, const evs_book* book, T* g) {
+__global__ void __launch_bounds__(256)
+    fir_kernel(Src src, int d, int Lf, const float* __restrict__ taps, const __grid_constant__ SeqRows sr,
+               const __grid_constant__ SeqPtrs<float*> ext0s, const __grid_constant__ SeqPtrs<float*> ext1s,
+               const __grid_constant__ SeqPtrs<const evs_book*> books, T* g) {
   extern __shared__ float sm[];
   const int NW = blockDim.x >> 5;
+  // this CTA's sequence: block rows [r0, r0 + n), its own banks and bookkeeping
+  const int sq = blockIdx.y, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
+  float* ext0 = ext0s.p[sq];
+  float* ext1 = ext1s.p[sq];
+  const evs_book* book = books.p[sq];
   const int rows = Lf - 1 + n;
   float* ext_s = sm;                       // [rows][32]
   float* a_s = ext_s + rows * 32;          // [n][32]
@@ -74,9 +80,9 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
   }
   pdl_wait();
   for (int t = warp; t < n; t += NW) {
-    const float a = stored<T>(src.get(t, c));
-    const float b = stored<T>(src.get(t, d + c));
-    const float v = stored<T>(src.get(t, 2 * d + c));
+    const float a = stored<T>(src.get(r0 + t, c));
+    const float b = stored<T>(src.get(r0 + t, d + c));
+    const float v = stored<T>(src.get(r0 + t, 2 * d + c));
     a_s[t * 32 + lane] = a;
     ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
     dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
   for (int t = warp; t < n; t += NW) {
     float y = 0.f;
     for (int w = 0; w < NW; ++w) y += part_s[(w * n + t) * 32 + lane];
-    g[(size_t)t * d + c] = from_f<T>(a_s[t * 32 + lane] * y);
+    g[(size_t)(r0 + t) * d + c] = from_f<T>(a_s[t * 32 + lane] * y);
   }
 }
 
@@ -117,10 +123,17 @@ __global__ void __launch_bounds__(256) fir_kernel(Src src, int d, int n, int Lf,
 // Block = 256 threads = (256/M) channels x M poles, poles of a channel in
 // adjacent lanes.  Per-position states land in the spare bank [n][d][M].
 template <typename T, typename Src, int M>
-__global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const float2* __restrict__ lam,
-                                                  const float2* __restrict__ res, float2* st0,
-                                                  float2* st1, const evs_book* book, T* g) {
+__global__ void __launch_bounds__(256)
+    iir_kernel(Src src, int d, const float2* __restrict__ lam, const float2* __restrict__ res,
+               const __grid_constant__ SeqRows sr, const __grid_constant__ SeqPtrs<float2*> st0s,
+               const __grid_constant__ SeqPtrs<float2*> st1s, const __grid_constant__ SeqPtrs<const evs_book*> books,
+               T* g) {
   constexpr int CPB = 256 / M;
+  // this CTA's sequence: block rows [r0, r0 + n), its own banks and bookkeeping
+  const int sq = blockIdx.y, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
+  float2* st0 = st0s.p[sq];
+  float2* st1 = st1s.p[sq];
+  const evs_book* book = books.p[sq];
   __shared__ float z_s[NTOK][CPB];
   __shared__ float a_s[NTOK][CPB];
   const int cl = threadIdx.x / M, m = threadIdx.x % M;
@@ -138,9 +151,9 @@ __global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const f
   pdl_wait();
   for (int e = threadIdx.x; e < n * CPB; e += 256) {
     const int t = e / CPB, cc = blockIdx.x * CPB + e % CPB;
-    const float a = stored<T>(src.get(t, cc));
-    const float b = stored<T>(src.get(t, d + cc));
-    const float v = stored<T>(src.get(t, 2 * d + cc));
+    const float a = stored<T>(src.get(r0 + t, cc));
+    const float b = stored<T>(src.get(r0 + t, d + cc));
+    const float v = stored<T>(src.get(r0 + t, 2 * d + cc));
     a_s[t][e % CPB] = a;
     z_s[t][e % CPB] = b * v;
   }
@@ -154,16 +167,23 @@ __global__ void __launch_bounds__(256) iir_kernel(Src src, int d, int n, const f
     float y = fmaf(R.x, s.x, -R.y * s.y);
 #pragma unroll
     for (int o = M / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-    if (m == 0) g[(size_t)t * d + c] = from_f<T>(a_s[t][cl] * y);
+    if (m == 0) g[(size_t)(r0 + t) * d + c] = from_f<T>(a_s[t][cl] * y);
   }
 }
 
 // ------------------------------------------------------------------ attention
 // (1) rotary embedding + append: grid (n, H), Dh/2 threads, one rotation pair each.
 template <typename T, typename Src>
-__global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max, const double* inv_freq, T* kc,
-                                T* vc, float* qbuf, evs_book* book) {
-  const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = Dh >> 1;
+__global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const double* inv_freq,
+                                const __grid_constant__ SeqRows sr, const __grid_constant__ SeqPtrs<T*> kcs,
+                                const __grid_constant__ SeqPtrs<T*> vcs, float* qbuf,
+                                const __grid_constant__ SeqPtrs<evs_book*> books) {
+  // block row r: position t of sequence sq
+  const int r = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = Dh >> 1;
+  const int sq = seq_of_row(sr, r), t = r - sr.row0[sq];
+  T* kc = kcs.p[sq];
+  T* vc = vcs.p[sq];
+  evs_book* book = books.p[sq];
   const int d = H * Dh;
   pdl_trigger();
   // the position is fixed for the whole verify: the rotation is computed
@@ -183,9 +203,9 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
     return;
   }
   const int col = h * Dh + i;
-  const float q1 = stored<T>(src.get(t, col)), q2 = stored<T>(src.get(t, col + half));
-  const float k1 = stored<T>(src.get(t, d + col)), k2 = stored<T>(src.get(t, d + col + half));
-  const float v1 = stored<T>(src.get(t, 2 * d + col)), v2 = stored<T>(src.get(t, 2 * d + col + half));
+  const float q1 = stored<T>(src.get(r, col)), q2 = stored<T>(src.get(r, col + half));
+  const float k1 = stored<T>(src.get(r, d + col)), k2 = stored<T>(src.get(r, d + col + half));
+  const float v1 = stored<T>(src.get(r, 2 * d + col)), v2 = stored<T>(src.get(r, 2 * d + col + half));
   const float rq1 = q1 * cs - q2 * sn, rq2 = q1 * sn + q2 * cs;
   const float rk1 = k1 * cs - k2 * sn, rk2 = k1 * sn + k2 * cs;
   const size_t row = ((size_t)h * ctx_max + pos) * Dh;
@@ -193,7 +213,7 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
   kc[row + i + half] = from_f<T>(rk2);
   vc[row + i] = from_f<T>(v1);
   vc[row + i + half] = from_f<T>(v2);
-  float* qo = qbuf + ((size_t)t * H + h) * Dh;
+  float* qo = qbuf + ((size_t)r * H + h) * Dh;
   qo[i] = stored<T>(rq1);
   qo[i + half] = stored<T>(rq2);
 }
@@ -208,10 +228,12 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, int n, long long ctx_max
 // runs over fixed key slots, masked slots contributing exact zeros, so a
 // query's result does not depend on the other queries of the block.
 template <typename T, int DH, int CH>
-__global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict__ qbuf, const T* __restrict__ kc,
-                                                         const T* __restrict__ vc, int H, int n,
-                                                         long long ctx_max, const evs_book* book, int span,
-                                                         float* part_o, float* part_ml, int nsplit_max) {
+__global__ void __launch_bounds__(256)
+    attn_split_kernel(const float* __restrict__ qbuf, const __grid_constant__ SeqPtrs<const T*> kcs,
+                      const __grid_constant__ SeqPtrs<const T*> vcs, int H, const __grid_constant__ SeqRows sr,
+                      long long ctx_max, const __grid_constant__ SeqPtrs<const evs_book*> books, int span,
+                      const __grid_constant__ SeqPtrs<float*> part_os, const __grid_constant__ SeqPtrs<float*> part_mls,
+                      int nsplit_max) {
   constexpr int KP = DH * (int)sizeof(T) + 16;  // padded K row pitch in bytes
   constexpr int VP = DH * (int)sizeof(T);
   constexpr int QG = 256 / CH;                   // query groups in the score phase
@@ -227,6 +249,13 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
   unsigned char* v_s = k_s + CH * KP;                              // [CH][VP]
   const int h = blockIdx.y, sp = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // this CTA's sequence (blockIdx.z): its queries are block rows [r0, r0 + n)
+  const int sq = blockIdx.z, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
+  const T* kc = kcs.p[sq];
+  const T* vc = vcs.p[sq];
+  const evs_book* book = books.p[sq];
+  float* part_o = part_os.p[sq];
+  float* part_ml = part_mls.p[sq];
   pdl_trigger();
   // the committed length is fixed for the whole verify: pull this split's
   // committed keys / values into L2 while the in-projection still runs
@@ -250,16 +279,16 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
   const float scale = rsqrtf((float)DH);
   for (int e = tid; e < NTOK * DH; e += 256) {
     const int t = e / DH;
-    q_s[e] = t < n ? qbuf[((size_t)t * H + h) * DH + e % DH] : 0.f;
+    q_s[e] = t < n ? qbuf[((size_t)(r0 + t) * H + h) * DH + e % DH] : 0.f;
   }
   if (tid < NTOK) {
     ml_s[tid * 4] = -INFINITY;
     ml_s[tid * 4 + 1] = 0.f;
   }
   const int dp = tid % DP, tqo = tid / DP;
-  float r0[OS], r1[OS];  // running unnormalised output
+  float ra[OS], rb[OS];  // running unnormalised output
 #pragma unroll
-  for (int r = 0; r < OS; ++r) r0[r] = r1[r] = 0.f;
+  for (int r = 0; r < OS; ++r) ra[r] = rb[r] = 0.f;
   for (long long k0 = kb0; k0 < kb1; k0 += CH) {
     const int kmax = (int)min((long long)CH, kb1 - k0);
     __syncthreads();
@@ -372,8 +401,8 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
         const int t = tqo + r * OG;
         if (t < n) {
           const float wo = ml_s[t * 4 + 2], wc = ml_s[t * 4 + 3];
-          r0[r] = fmaf(r0[r], wo, o0[r] * wc);
-          r1[r] = fmaf(r1[r], wo, o1[r] * wc);
+          ra[r] = fmaf(ra[r], wo, o0[r] * wc);
+          rb[r] = fmaf(rb[r], wo, o1[r] * wc);
         }
       }
     }
@@ -383,8 +412,8 @@ __global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict
     const int t = tqo + r * OG;
     if (t < n) {
       float* o = part_o + (((size_t)h * nsplit_max + sp) * NTOK + t) * DH + 2 * dp;
-      o[0] = r0[r];
-      o[1] = r1[r];
+      o[0] = ra[r];
+      o[1] = rb[r];
     }
   }
   if (tid < n) {
@@ -440,11 +469,11 @@ __host__ __device__ constexpr size_t attn_mma_smem() {
 }
 
 template <int DH>
-__global__ void __launch_bounds__(AT_WARPS * 32) attn_mma_kernel(const float* __restrict__ qbuf,
-                                                                  const bf16* __restrict__ kc,
-                                                                  const bf16* __restrict__ vc, int H, int n,
-                                                                  long long ctx_max, const evs_book* book, int span,
-                                                                  int nsplit_max, float* part_o, float* part_ml) {
+__global__ void __launch_bounds__(AT_WARPS * 32)
+    attn_mma_kernel(const float* __restrict__ qbuf, const __grid_constant__ SeqPtrs<const bf16*> kcs,
+                    const __grid_constant__ SeqPtrs<const bf16*> vcs, int H, const __grid_constant__ SeqRows sr,
+                    long long ctx_max, const __grid_constant__ SeqPtrs<const evs_book*> books, int span, int nsplit_max,
+                    const __grid_constant__ SeqPtrs<float*> part_os, const __grid_constant__ SeqPtrs<float*> part_mls) {
   static_assert(DH % 16 == 0 && DH <= 256, "head dim");
   constexpr int RB = DH * 2;                  // bytes per key row
   constexpr int CPR = DH / 8;                 // 16-byte chunks per row
@@ -456,6 +485,13 @@ __global__ void __launch_bounds__(AT_WARPS * 32) attn_mma_kernel(const float* __
   const int h = blockIdx.y, sp = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
+  // this CTA's sequence (blockIdx.z): its queries are block rows [r0, r0 + n)
+  const int sq = blockIdx.z, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
+  const bf16* kc = kcs.p[sq];
+  const bf16* vc = vcs.p[sq];
+  const evs_book* book = books.p[sq];
+  float* part_o = part_os.p[sq];
+  float* part_ml = part_mls.p[sq];
   pdl_trigger();
   const long long pos = book->pos;
   const long long total = min(pos + n, ctx_max);
@@ -506,8 +542,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32) attn_mma_kernel(const float* __
   // Q as the A operand: rows g and g+8 (queries), k-step kk
   uint32_t qa[KS][4];
   {
-    const float* q0 = qbuf + ((size_t)g * H + h) * DH;
-    const float* q1 = qbuf + ((size_t)(g + 8) * H + h) * DH;
+    const float* q0 = qbuf + ((size_t)(r0 + g) * H + h) * DH;
+    const float* q1 = qbuf + ((size_t)(r0 + g + 8) * H + h) * DH;
     const bool ok0 = g < n, ok1 = g + 8 < n;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
@@ -653,9 +689,17 @@ __global__ void __launch_bounds__(AT_WARPS * 32) attn_mma_kernel(const float* __
 
 // (3) combine: grid (n, H), Dh threads; splits in ascending order.
 template <typename T>
-__global__ void attn_combine_kernel(const float* part_o, const float* part_ml, int H, int Dh, int n,
-                                    int span, long long ctx_max, const evs_book* book, int nsplit_max, T* g) {
-  const int t = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
+__global__ void attn_combine_kernel(const __grid_constant__ SeqPtrs<const float*> part_os,
+                                    const __grid_constant__ SeqPtrs<const float*> part_mls, int H, int Dh,
+                                    const __grid_constant__ SeqRows sr, int span, long long ctx_max,
+                                    const __grid_constant__ SeqPtrs<const evs_book*> books,
+                                    int nsplit_max, T* g) {
+  // block row r: query t of sequence sq
+  const int r = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
+  const int sq = seq_of_row(sr, r), t = r - sr.row0[sq];
+  const float* part_o = part_os.p[sq];
+  const float* part_ml = part_mls.p[sq];
+  const evs_book* book = books.p[sq];
   pdl_trigger();
   pdl_wait();
   const long long qpos = min((long long)book->pos + t, ctx_max - 1);
@@ -676,17 +720,25 @@ __global__ void attn_combine_kernel(const float* part_o, const float* part_ml, i
     l = fmaf(lc, w, l);
     o = fmaf(oc, w, o);
   }
-  g[(size_t)t * H * Dh + h * Dh + e] = from_f<T>(o / l);
+  g[(size_t)r * H * Dh + h * Dh + e] = from_f<T>(o / l);
+}
+
+static int max_rows(const SeqRows& sr) {
+  int m = 0;
+  for (int b = 0; b < sr.nseq; ++b) m = std::max(m, sr.row0[b + 1] - sr.row0[b]);
+  return m;
 }
 
 template <typename T, typename Src>
-cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, int n, int Lf, const float* taps,
-                         float* e0, float* e1, const evs_book* book, void* g) {
+cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, const SeqRows& sr, int Lf, const float* taps,
+                         const SeqPtrs<float*>& e0, const SeqPtrs<float*>& e1, const SeqPtrs<const evs_book*>& book,
+                         void* g) {
   const int NW = std::min(8, Lf);
   int J = 1;
   while (J * NW < Lf) J <<= 1;  // taps per warp, a power of two <= 32 (Lf <= 256)
+  const int n = max_rows(sr);
   const size_t smem = sizeof(float) * 32 * ((Lf - 1 + n) + n + Lf + NW * n);
-  void (*k)(Src, int, int, int, const float*, float*, float*, const evs_book*, T*);
+  void (*k)(Src, int, int, const float*, SeqRows, SeqPtrs<float*>, SeqPtrs<float*>, SeqPtrs<const evs_book*>, T*);
   switch (J) {
     case 1: k = fir_kernel<T, Src, 1>; break;
     case 2: k = fir_kernel<T, Src, 2>; break;
@@ -700,34 +752,48 @@ cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, int n, int Lf, const 
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch(L, k, dim3(d / 32), dim3(32 * NW), smem, s, d, n, Lf, taps, e0, e1, book, (T*)g);
+  return launch(L, k, dim3(d / 32, sr.nseq), dim3(32 * NW), smem, s, d, Lf, taps, sr, e0, e1, book, (T*)g);
 }
 
 template <typename T, typename Src, int M>
-cudaError_t iir_dispatch_m(const LaunchCtx& L, Src s, int d, int n, const float* lam, const float* res,
-                           float* s0, float* s1, const evs_book* book, void* g) {
+cudaError_t iir_dispatch_m(const LaunchCtx& L, Src s, int d, const SeqRows& sr, const float* lam, const float* res,
+                           const SeqPtrs<float*>& s0, const SeqPtrs<float*>& s1,
+                           const SeqPtrs<const evs_book*>& book, void* g) {
   constexpr int CPB = 256 / M;
-  return launch(L, iir_kernel<T, Src, M>, dim3(d / CPB), dim3(256), 0, s, d, n,
-                (const float2*)lam, (const float2*)res, (float2*)s0, (float2*)s1, book, (T*)g);
+  SeqPtrs<float2*> a{}, b{};
+  for (int q = 0; q < sr.nseq; ++q) {
+    a.p[q] = (float2*)s0.p[q];
+    b.p[q] = (float2*)s1.p[q];
+  }
+  return launch(L, iir_kernel<T, Src, M>, dim3(d / CPB, sr.nseq), dim3(256), 0, s, d, (const float2*)lam,
+                (const float2*)res, sr, a, b, book, (T*)g);
 }
 
 template <typename T, typename Src>
-cudaError_t iir_dispatch(const LaunchCtx& L, Src s, int d, int n, int M, const float* lam,
-                         const float* res, float* s0, float* s1, const evs_book* book, void* g) {
+cudaError_t iir_dispatch(const LaunchCtx& L, Src s, int d, const SeqRows& sr, int M, const float* lam,
+                         const float* res, const SeqPtrs<float*>& s0, const SeqPtrs<float*>& s1,
+                         const SeqPtrs<const evs_book*>& book, void* g) {
   switch (M) {
-    case 1: return iir_dispatch_m<T, Src, 1>(L, s, d, n, lam, res, s0, s1, book, g);
-    case 2: return iir_dispatch_m<T, Src, 2>(L, s, d, n, lam, res, s0, s1, book, g);
-    case 4: return iir_dispatch_m<T, Src, 4>(L, s, d, n, lam, res, s0, s1, book, g);
-    case 8: return iir_dispatch_m<T, Src, 8>(L, s, d, n, lam, res, s0, s1, book, g);
-    case 16: return iir_dispatch_m<T, Src, 16>(L, s, d, n, lam, res, s0, s1, book, g);
-    case 32: return iir_dispatch_m<T, Src, 32>(L, s, d, n, lam, res, s0, s1, book, g);
+    case 1: return iir_dispatch_m<T, Src, 1>(L, s, d, sr, lam, res, s0, s1, book, g);
+    case 2: return iir_dispatch_m<T, Src, 2>(L, s, d, sr, lam, res, s0, s1, book, g);
+    case 4: return iir_dispatch_m<T, Src, 4>(L, s, d, sr, lam, res, s0, s1, book, g);
+    case 8: return iir_dispatch_m<T, Src, 8>(L, s, d, sr, lam, res, s0, s1, book, g);
+    case 16: return iir_dispatch_m<T, Src, 16>(L, s, d, sr, lam, res, s0, s1, book, g);
+    case 32: return iir_dispatch_m<T, Src, 32>(L, s, d, sr, lam, res, s0, s1, book, g);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <typename P, typename Q>
+SeqPtrs<P> cast_ptrs(const SeqPtrs<Q>& in, int nseq) {
+  SeqPtrs<P> out{};
+  for (int b = 0; b < nseq; ++b) out.p[b] = (P)in.p[b];
+  return out;
+}
+
 template <typename T, int DH, int CH>
-cudaError_t attn_split_launch(const LaunchCtx& L, int H, int n, long long ctx_max, evs_book* book,
-                              const AttnBufs& B, void* kc, void* vc) {
+cudaError_t attn_split_launch(const LaunchCtx& L, int H, const SeqRows& sr, long long ctx_max, const AttnSeq& as,
+                              const AttnBufs& B) {
   const size_t smem = sizeof(float) * (NTOK * DH + NTOK * CH + NTOK * 4) +
                       (size_t)CH * (DH * sizeof(T) + 16) + (size_t)CH * DH * sizeof(T);
   auto k = attn_split_kernel<T, DH, CH>;
@@ -737,13 +803,14 @@ cudaError_t attn_split_launch(const LaunchCtx& L, int H, int n, long long ctx_ma
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch(L, k, dim3(B.nsplit_max, H), dim3(256), smem, (const float*)B.qbuf, (const T*)kc, (const T*)vc, H,
-                n, ctx_max, (const evs_book*)book, B.span, B.part_o, B.part_ml, B.nsplit_max);
+  return launch(L, k, dim3(B.nsplit_max, H, sr.nseq), dim3(256), smem, (const float*)B.qbuf,
+                cast_ptrs<const T*>(as.kc, sr.nseq), cast_ptrs<const T*>(as.vc, sr.nseq), H, sr, ctx_max,
+                cast_ptrs<const evs_book*>(as.book, sr.nseq), B.span, as.part_o, as.part_ml, B.nsplit_max);
 }
 
 template <typename T, int DH>
-cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, int n, long long ctx_max, int chunk,
-                                evs_book* book, const AttnBufs& B, void* kc, void* vc) {
+cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, const SeqRows& sr, long long ctx_max, int chunk,
+                                const AttnSeq& as, const AttnBufs& B) {
   if constexpr (sizeof(T) == 2) {
     // bf16 caches: tensor-core kernel (the chunk only shapes the span)
     constexpr size_t smem = attn_mma_smem<DH>();
@@ -755,56 +822,61 @@ cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, int n, long long ctx_
       attr_set = true;
     }
     if (B.span % AT_STAGE) return cudaErrorInvalidValue;
-    return launch(L, k, dim3(B.nsplit_max, H), dim3(AT_WARPS * 32), smem, (const float*)B.qbuf, (const bf16*)kc,
-                  (const bf16*)vc, H, n, ctx_max, (const evs_book*)book, B.span, B.nsplit_max, B.part_o,
-                  B.part_ml);
+    return launch(L, k, dim3(B.nsplit_max, H, sr.nseq), dim3(AT_WARPS * 32), smem, (const float*)B.qbuf,
+                  cast_ptrs<const bf16*>(as.kc, sr.nseq), cast_ptrs<const bf16*>(as.vc, sr.nseq), H, sr, ctx_max,
+                  cast_ptrs<const evs_book*>(as.book, sr.nseq), B.span, B.nsplit_max, as.part_o, as.part_ml);
   }
   switch (chunk) {
-    case 32: return attn_split_launch<T, DH, 32>(L, H, n, ctx_max, book, B, kc, vc);
-    case 64: return attn_split_launch<T, DH, 64>(L, H, n, ctx_max, book, B, kc, vc);
-    case 128: return attn_split_launch<T, DH, 128>(L, H, n, ctx_max, book, B, kc, vc);
-    case 256: return attn_split_launch<T, DH, 256>(L, H, n, ctx_max, book, B, kc, vc);
+    case 32: return attn_split_launch<T, DH, 32>(L, H, sr, ctx_max, as, B);
+    case 64: return attn_split_launch<T, DH, 64>(L, H, sr, ctx_max, as, B);
+    case 128: return attn_split_launch<T, DH, 128>(L, H, sr, ctx_max, as, B);
+    case 256: return attn_split_launch<T, DH, 256>(L, H, sr, ctx_max, as, B);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, typename Src>
-cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, int n, long long ctx_max, int chunk,
-                        void* kc, void* vc, evs_book* book, const AttnBufs& B, void* g, int num_sms) {
-  cudaError_t e = launch(L, qkv_rope_kernel<T, Src>, dim3(n, H), dim3(Dh / 2), 0, s, H, Dh, n, ctx_max,
-                         (const double*)B.inv_freq, (T*)kc, (T*)vc, B.qbuf, book);
+cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, const SeqRows& sr, long long ctx_max, int chunk,
+                        const AttnSeq& as, const AttnBufs& B, void* g) {
+  const int rows = sr.row0[sr.nseq];
+  cudaError_t e = launch(L, qkv_rope_kernel<T, Src>, dim3(rows, H), dim3(Dh / 2), 0, s, H, Dh, ctx_max,
+                         (const double*)B.inv_freq, sr, cast_ptrs<T*>(as.kc, sr.nseq), cast_ptrs<T*>(as.vc, sr.nseq),
+                         B.qbuf, as.book);
   if (e != cudaSuccess) return e;
   switch (Dh) {
-    case 32: e = attn_split_dispatch<T, 32>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
-    case 64: e = attn_split_dispatch<T, 64>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
-    case 128: e = attn_split_dispatch<T, 128>(L, H, n, ctx_max, chunk, book, B, kc, vc); break;
+    case 32: e = attn_split_dispatch<T, 32>(L, H, sr, ctx_max, chunk, as, B); break;
+    case 64: e = attn_split_dispatch<T, 64>(L, H, sr, ctx_max, chunk, as, B); break;
+    case 128: e = attn_split_dispatch<T, 128>(L, H, sr, ctx_max, chunk, as, B); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch(L, attn_combine_kernel<T>, dim3(n, H), dim3(Dh), 0, (const float*)B.part_o,
-                (const float*)B.part_ml, H, Dh, n, B.span, ctx_max, (const evs_book*)book, B.nsplit_max, (T*)g);
+  return launch(L, attn_combine_kernel<T>, dim3(rows, H), dim3(Dh), 0, cast_ptrs<const float*>(as.part_o, sr.nseq),
+                cast_ptrs<const float*>(as.part_ml, sr.nseq), H, Dh, sr, B.span, ctx_max,
+                cast_ptrs<const evs_book*>(as.book, sr.nseq), B.nsplit_max, (T*)g);
 }
 
 }  // namespace
 
-cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, int Lf, const float* taps,
-                       float* ext0, float* ext1, const evs_book* book, void* g) {
+cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, const SeqRows& sr, int Lf,
+                       const float* taps, const SeqPtrs<float*>& ext0, const SeqPtrs<float*>& ext1,
+                       const SeqPtrs<const evs_book*>& book, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return src.f32 ? fir_dispatch<bf16>(L, sf, d, n, Lf, taps, ext0, ext1, book, g)
-                   : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, n, Lf, taps, ext0,
+    return src.f32 ? fir_dispatch<bf16>(L, sf, d, sr, Lf, taps, ext0, ext1, book, g)
+                   : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, Lf, taps, ext0,
                                         ext1, book, g);
-  return fir_dispatch<float>(L, sf, d, n, Lf, taps, ext0, ext1, book, g);
+  return fir_dispatch<float>(L, sf, d, sr, Lf, taps, ext0, ext1, book, g);
 }
 
-cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, int n, int M, const float* lam,
-                       const float* res, float* st0, float* st1, const evs_book* book, void* g) {
+cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, const SeqRows& sr, int M,
+                       const float* lam, const float* res, const SeqPtrs<float*>& st0, const SeqPtrs<float*>& st1,
+                       const SeqPtrs<const evs_book*>& book, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return src.f32 ? iir_dispatch<bf16>(L, sf, d, n, M, lam, res, st0, st1, book, g)
-                   : iir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, n, M, lam, res, st0,
+    return src.f32 ? iir_dispatch<bf16>(L, sf, d, sr, M, lam, res, st0, st1, book, g)
+                   : iir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, M, lam, res, st0,
                                         st1, book, g);
-  return iir_dispatch<float>(L, sf, d, n, M, lam, res, st0, st1, book, g);
+  return iir_dispatch<float>(L, sf, d, sr, M, lam, res, st0, st1, book, g);
 }
 
 // Key span of a split: max(chunk, 64) * 2^j, the smallest with at most
@@ -848,15 +920,14 @@ cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStre
   return cudaStreamSynchronize(stream);  // tab lives on this stack frame
 }
 
-cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, int n,
-                             long long ctx_max, int chunk, void* kc, void* vc,
-                             evs_book* book, const AttnBufs& B, void* g, int num_sms) {
+cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, const SeqRows& sr,
+                             long long ctx_max, int chunk, const AttnSeq& as, const AttnBufs& B, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (dtype == EVS_BF16)
-    return src.f32 ? attention_t<bf16>(L, sf, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms)
-                   : attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, H, Dh, n, ctx_max, chunk,
-                                       kc, vc, book, B, g, num_sms);
-  return attention_t<float>(L, sf, H, Dh, n, ctx_max, chunk, kc, vc, book, B, g, num_sms);
+    return src.f32 ? attention_t<bf16>(L, sf, H, Dh, sr, ctx_max, chunk, as, B, g)
+                   : attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, H, Dh, sr, ctx_max, chunk, as,
+                                       B, g);
+  return attention_t<float>(L, sf, H, Dh, sr, ctx_max, chunk, as, B, g);
 }
 
 }  // namespace evs

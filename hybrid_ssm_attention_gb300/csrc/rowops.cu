@@ -48,7 +48,8 @@ struct AddU { __device__ unsigned long long operator()(unsigned long long a, uns
 // the number of rows.
 template <typename T>
 __global__ void __launch_bounds__(256) embed_norm_kernel(const T* E, const int32_t* tokens, int V, float* X,
-                                                         int d, float eps, T* xn, evs_book* book, int n_mark) {
+                                                         int d, float eps, T* xn, const __grid_constant__ SeqRows sr,
+                                                         const __grid_constant__ SeqPtrs<evs_book*> books) {
   __shared__ float scratch[32];
   __shared__ float ss_cta;
   cg::cluster_group cl = cg::this_cluster();
@@ -59,7 +60,10 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const T* E, const int32
   pdl_wait();
   float* x = X + (size_t)t * d;
   float ss = 0.f;
-  if (t == 0 && rank == 0 && threadIdx.x == 0) book->pending_n = n_mark;
+  // row t belongs to sequence sq; its first row records the block length
+  const int sq = seq_of_row(sr, t);
+  evs_book* book = books.p[sq];
+  if (t == sr.row0[sq] && rank == 0 && threadIdx.x == 0) book->pending_n = sr.row0[sq + 1] - sr.row0[sq];
   const int tok = tokens[t];
   const bool ok = tok >= 0 && tok < V;
   if (!ok && rank == 0 && threadIdx.x == 0) set_status(book, EVS_DEV_BAD_TOKEN);
@@ -321,14 +325,16 @@ __global__ void book_set_kernel(evs_book* book, evs_book v) {
 
 }  // namespace
 
-cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, const int32_t* tokens, int n,
-                              int d, int V, float eps, float* X, void* xn, evs_book* book) {
+cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, const int32_t* tokens,
+                              const SeqRows& sr, int d, int V, float eps, float* X, void* xn,
+                              const SeqPtrs<evs_book*>& book) {
   const int cl = row_cluster(d);
+  const int n = sr.row0[sr.nseq];
   if (dtype == EVS_BF16)
     return launch_cl(L, cl, embed_norm_kernel<bf16>, dim3(cl, n), dim3(256), 0, (const bf16*)E, tokens, V, X, d,
-                     eps, (bf16*)xn, book, n);
+                     eps, (bf16*)xn, sr, book);
   return launch_cl(L, cl, embed_norm_kernel<float>, dim3(cl, n), dim3(256), 0, (const float*)E, tokens, V, X, d,
-                   eps, (float*)xn, book, n);
+                   eps, (float*)xn, sr, book);
 }
 
 cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, const float* ss, int n, int d,

@@ -214,6 +214,21 @@ int evs_state_use_graphs(evs_state* s, int32_t enable);
 int evs_verify_block(evs_state* s, const int32_t* tokens_dev, int32_t n,
                      float* logits_dev, cudaStream_t stream);
 
+/* Batched block verify: one forward pass over the blocks of nseq sequences
+ * (the weights are read once for all of them), each sequence keeping its
+ * own per-position state for its own later commit (ragged rollback:
+ * evs_commit / evs_commit_dev per state) — the batched verify the pages
+ * name as the next step for serving ([systems], [regime]).
+ * states_host [nseq] (1 <= nseq <= 16): distinct states of one model and one
+ * ctx_max, none with a pending verify; n_host [nseq]: block lengths, each in
+ * [1, gamma_max+1], summing to at most 16; tokens_dev: the blocks back to
+ * back (sequence 0's n_host[0] tokens first); logits_dev [sum n][V] in the
+ * same row order.  The activations and workspaces of states_host[0] are
+ * used.  Each sequence's logits and retained state equal those of its own
+ * evs_verify_block bit for bit.  Launched directly on stream (not captured
+ * in a graph).  Errors as evs_verify_block, per state. */
+int evs_verify_batch(evs_state* const* states_host, int32_t nseq, const int32_t* tokens_dev,
+                     const int32_t* n_host, float* logits_dev, cudaStream_t stream);
 /* Block verify that also copies the residual stream after the embedding
  * and after every layer to x_trace_dev float32 [n_layers+1][n][d_model]
  * (layer-by-layer validation and tracing; runs without graph capture).

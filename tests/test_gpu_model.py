@@ -208,6 +208,54 @@ def test_small_long_generation_spec_equals_native():
     assert sp.check() == 0 and nat.check() == 0
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("which", ["small", "tiny"])
+def test_batched_verify_equals_separate_bitwise(which):
+    # Ragged batches of 3 sequences verified in one pass (evs_verify_batch)
+    # against each sequence's own evs_verify_block, then committed with
+    # different keeps per sequence: logits and the states' next results
+    # agree bit for bit (bf16 tensor-core path and the fp32 SIMT path).
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    shape = small_shape() if which == "small" else synth.tiny()
+    W = synth.make_weights(shape, 41)
+    m = evs.Model(shape, W)
+    V, nmax = shape.vocab, shape.n_block
+    g = np.random.default_rng(3)
+    B = 3
+    ref = [evs.State(m, 256) for _ in range(B)]
+    bat = [evs.State(m, 256) for _ in range(B)]
+    for b in range(B):
+        pr = [int(x) for x in synth.prompt(shape, 40 + b, 9 + 5 * b)]
+        for st in (ref[b], bat[b]):
+            for s0 in range(0, len(pr), nmax):
+                _verify(evs, st, pr[s0:s0 + nmax], V)
+                evs.evs_commit(st, len(pr[s0:s0 + nmax]))
+    plans = [(min(5, nmax), 1, min(7, nmax)), (3, 3, 3), (1, 1, 1), (nmax, 2, 1)]
+    for ns in plans:
+        toks = [[int(x) for x in g.integers(0, V, n)] for n in ns]
+        refl = [to_np(_verify(evs, ref[b], toks[b], V)[0]) for b in range(B)]
+        allt = t.tensor(np.concatenate([np.asarray(x, np.int32) for x in toks]), device="cuda")
+        lg = t.empty((sum(ns), V), dtype=t.float32, device="cuda")
+        evs.evs_verify_batch(bat, allt, ns, lg)
+        got = to_np(lg)
+        r0 = 0
+        for b in range(B):
+            assert np.array_equal(got[r0:r0 + ns[b]].view(np.uint32), refl[b].view(np.uint32)), (ns, b)
+            r0 += ns[b]
+        for b in range(B):
+            keep = int(g.integers(0, ns[b] + 1))
+            evs.evs_commit(ref[b], keep)
+            evs.evs_commit(bat[b], keep)
+    for b in range(B):
+        assert ref[b].book() == bat[b].book()
+        nxt = [int(x) for x in g.integers(0, V, 2)]
+        l1 = to_np(_verify(evs, ref[b], nxt, V)[0])
+        l2 = to_np(_verify(evs, bat[b], nxt, V)[0])
+        assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32))
+        assert ref[b].check() == 0 and bat[b].check() == 0
+
+
 def wide_shape():
     # 7B widths, two layers: in-projection and gate/up take the stream-K
     # split, down and head the cluster split
