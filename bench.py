@@ -322,14 +322,15 @@ def long_generation(evs, torch, model, shape, prompt, ntok, seed, dev):
 
 
 def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, rounds=24, warm=4):
-    """Batched verify (one pass over B sequences' blocks, B * n = 16 rows or
-    13 for B = 1): round time and verified rows per second for each (B, n),
-    every sequence committing its whole block (host keep) after each pass.
-    The sequences start from the same post-prompt state."""
+    """Batched verify (one pass over B sequences' blocks of n rows: one
+    16-row chunk up to B * n = 16, then 2..8 chunks side by side up to 128
+    rows): round time and verified rows per second for each (B, n), every
+    sequence committing its whole block (host keep) after each pass.  The
+    sequences start from the same post-prompt state."""
     out = []
     V = shape.vocab
     g = np.random.default_rng(7)
-    for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1)):
+    for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1), (2, 13), (4, 13), (8, 13), (16, 8)):
         states = [evs.State(model, ctx) for _ in range(B)]
         for st in states:
             post_prompt.clone_into(st)

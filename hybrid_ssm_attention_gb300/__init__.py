@@ -15,8 +15,9 @@ from typing import Optional, Sequence
 import numpy as np
 
 from . import _abi
-from ._abi import (EVS_BF16, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN, EVS_LAYER_FIR,  # noqa: F401
-                   EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
+from ._abi import (EVS_BF16, EVS_ERR_ARG, EVS_ERR_CAPACITY, EVS_ERR_CUDA, EVS_ERR_DEVICE,  # noqa: F401
+                   EVS_ERR_OOM, EVS_ERR_STATE, EVS_ERR_UNSUPPORTED, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN,
+                   EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
            "evs_commit", "evs_commit_dev", "evs_round", "evs_op_fir", "evs_op_iir",

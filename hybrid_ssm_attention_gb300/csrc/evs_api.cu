@@ -100,7 +100,11 @@ struct evs_model {
   uint8_t* wpack;  // library-owned packed projection weights (bf16), or null
   std::vector<LayerW> L;
   Partials p_in, p_out, p_gu, p_down, p_head;  // with device slot tables
-  int4* tab_dev;                               // the five slot tables
+  // the same five as stream-K plans over the same unit ranges (a cluster
+  // plan of cl ranks per tile becomes cl stream-K contributors per tile, so
+  // the packed weight order is unchanged): passes of more than 16 rows
+  Partials q_in, q_out, q_gu, q_down, q_head;
+  int4* tab_dev;                               // the ten slot tables
   size_t ws_bytes;                             // largest partial workspace
   bool has_attn;
   // bf16: projection weights repacked (library copy in wpack) with the
@@ -131,9 +135,11 @@ struct evs_state {
   int host_pending;
   float* X;
   void *xn, *g, *h;
-  float* fin;   // [NTOK][max(3d, 2F)] final GEMM sums (mixer / MLP inputs)
-  float* pout;  // same size: GEMM outputs of evs_profile_gemms
-  float* ss;    // [tiles of d][NTOK] per-tile sums of squares
+  // work buffers hold ROWS_MAX token rows (a batched pass over several
+  // sequences' blocks uses the first state's)
+  float* fin;   // [ROWS_MAX][max(3d, 2F, V)] final GEMM sums (mixer / MLP inputs)
+  float* pout;  // [NTOK][max(3d, 2F, V)]: GEMM outputs of evs_profile_gemms
+  float* ss;    // [tiles of d][ROWS_MAX] per-tile sums of squares
   int* cnt;     // [max tiles] GEMM arrival counters
   int cnt_len;
   float* ws[2];
@@ -141,7 +147,7 @@ struct evs_state {
   AttnBufs ab;
   std::vector<LayerS> S;
   CUtensorMap m_xn, m_g, m_h;
-  CUtensorMap m_xf;  // fp32 X [NTOK][d] (RMSNorm converter source)
+  CUtensorMap m_xf;  // fp32 X [ROWS_MAX][d] (RMSNorm converter source, 16-row boxes)
   bool use_graphs, pdl;
   int pf_units;  // next-weight L2 prefetch per CTA (units of 128x64)
   unsigned long long* trace;  // EVS_TRACE builds: GEMM timeline slots
@@ -217,10 +223,23 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
   int gk = 0;
   // GEMM_FINAL writes fin[tok][col] (row stride ld); GEMM_RESID adds into X
   // and leaves per-tile sums of squares for the next RMSNorm
+  const int nt = (n + NTOK - 1) / NTOK;
   auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
                   const CUtensorMap& xm, const void* Xin, int K, int mode, float* fin, int ld,
                   int bsrc = GEMM_B_TMA) -> int {
     Partials P = plan;
+    if (nt > 1) {
+      // more than 16 rows: the stream-K twin, with a ring that fits nt
+      // activation tiles per stage
+      const Partials* one[5] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head};
+      const Partials* many[5] = {&m->q_in, &m->q_out, &m->q_gu, &m->q_down, &m->q_head};
+      for (int k = 0; k < 5; ++k)
+        if (&plan == one[k]) P = *many[k];
+      if (P.cl != 0 || bsrc != GEMM_B_TMA || !m->tc)
+        return fail(EVS_ERR_UNSUPPORTED, "passes of more than %d rows need the bf16 path without EVS_FUSE", NTOK);
+      P.stages = std::min(P.stages, gemm_stages_for(0, GEMM_B_TMA, nt));
+    }
+    P.nt = nt;
     P.wpk = pk;
     P.bsrc = bsrc;
     P.Kdim = K;
@@ -508,9 +527,10 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     return fail(EVS_ERR_CUDA, "head: %s", err);
   }
   {
-    std::vector<GemmPlan> plans(5);
+    std::vector<GemmPlan> plans(10);
     const int shapes[5][2] = {{3 * d, d}, {d, d}, {2 * F, d}, {d, F}, {V, d}};
-    Partials* dst[5] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head};
+    Partials* dst[10] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head,
+                         &m->q_in, &m->q_out, &m->q_gu, &m->q_down, &m->q_head};
     size_t tb = 0;
     m->ws_bytes = 0;
     for (int k = 0; k < 5; ++k) {
@@ -530,8 +550,17 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
             std::min(plans[k].P.stages, gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA));
       const char* st_env = getenv("EVS_GEMM_STAGES");
       if (st_env && m->tc) plans[k].P.stages = std::max(2, std::min(GEMM_MAX_STAGES, atoi(st_env)));
-      tb += table_bytes(plans[k]);
+      // stream-K twin over the same CTA unit ranges (G = T * cl for a
+      // cluster plan), for passes of more than NTOK rows
+      GemmPlan& q = plans[5 + k];
+      if (!plan_gemm_grid(shapes[k][0], shapes[k][1], plans[k].P.G, &q)) {
+        delete m;
+        return fail(EVS_ERR_UNSUPPORTED, "GEMM shape %d x %d: no stream-K plan", shapes[k][0], shapes[k][1]);
+      }
+      q.P.stages = plans[k].P.stages;
+      tb += table_bytes(plans[k]) + table_bytes(q);
       m->ws_bytes = std::max(m->ws_bytes, partials_bytes(plans[k]));
+      if (m->tc) m->ws_bytes = std::max(m->ws_bytes, partials_bytes(q, ROWS_MAX));
     }
     cudaError_t e = cudaMalloc(&m->tab_dev, tb);
     if (e != cudaSuccess) {
@@ -539,7 +568,7 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
       return fail(EVS_ERR_OOM, "cudaMalloc(slot tables): %s", cudaGetErrorString(e));
     }
     size_t off = 0;
-    for (int k = 0; k < 5; ++k) {
+    for (int k = 0; k < 10; ++k) {
       const int T = (int)(table_bytes(plans[k]) / sizeof(int4));
       e = cudaMemcpy(m->tab_dev + off, plans[k].tab, table_bytes(plans[k]), cudaMemcpyHostToDevice);
       if (e != cudaSuccess) {
@@ -635,13 +664,14 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
     ptr = reinterpret_cast<decltype(ptr)>(p_);                         \
   } while (0)
   ALLOC(s->book, sizeof(evs_book));
-  ALLOC(s->X, sizeof(float) * NTOK * d);
-  ALLOC(s->xn, es * NTOK * d);
-  ALLOC(s->g, es * NTOK * d);
-  ALLOC(s->h, es * NTOK * F);
-  ALLOC(s->fin, sizeof(float) * NTOK * std::max(3 * d, std::max(2 * F, c.vocab)));
+  const size_t R = ROWS_MAX;
+  ALLOC(s->X, sizeof(float) * R * d);
+  ALLOC(s->xn, es * R * d);
+  ALLOC(s->g, es * R * d);
+  ALLOC(s->h, es * R * F);
+  ALLOC(s->fin, sizeof(float) * R * std::max(3 * d, std::max(2 * F, c.vocab)));
   ALLOC(s->pout, sizeof(float) * NTOK * std::max(3 * d, std::max(2 * F, c.vocab)));
-  ALLOC(s->ss, sizeof(float) * NTOK * ((d + TILE_M - 1) / TILE_M));
+  ALLOC(s->ss, sizeof(float) * R * ((d + TILE_M - 1) / TILE_M));
   s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
   ALLOC(s->cnt, sizeof(int) * s->cnt_len);
 #ifdef EVS_TRACE
@@ -678,10 +708,10 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
 #undef ALLOC
   if (m->tc) {
     char err[256] = {0};
-    if (!encode_tmap_2d(&s->m_xn, s->xn, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
-        !encode_tmap_2d(&s->m_g, s->g, d, NTOK, TILE_K, NTOK, err, sizeof err) ||
-        !encode_tmap_2d(&s->m_h, s->h, F, NTOK, TILE_K, NTOK, err, sizeof err) ||
-        (m->fuse && !encode_tmap_2d_f32(&s->m_xf, s->X, d, NTOK, TILE_K, NTOK, err, sizeof err))) {
+    if (!encode_tmap_2d(&s->m_xn, s->xn, d, ROWS_MAX, TILE_K, NTOK, err, sizeof err) ||
+        !encode_tmap_2d(&s->m_g, s->g, d, ROWS_MAX, TILE_K, NTOK, err, sizeof err) ||
+        !encode_tmap_2d(&s->m_h, s->h, F, ROWS_MAX, TILE_K, NTOK, err, sizeof err) ||
+        (m->fuse && !encode_tmap_2d_f32(&s->m_xf, s->X, d, ROWS_MAX, TILE_K, NTOK, err, sizeof err))) {
       state_free(s);
       return fail(EVS_ERR_CUDA, "activation tensor map: %s", err);
     }
@@ -692,9 +722,9 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
     return fail(EVS_ERR_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
   }
   // zero activations once (rows beyond a block's n are read but never used)
-  cudaMemset(s->xn, 0, es * NTOK * d);
-  cudaMemset(s->g, 0, es * NTOK * d);
-  cudaMemset(s->h, 0, es * NTOK * F);
+  cudaMemset(s->xn, 0, es * R * d);
+  cudaMemset(s->g, 0, es * R * d);
+  cudaMemset(s->h, 0, es * R * F);
   r = evs_state_reset(s, 0);
   if (r == EVS_OK) {
     e = cudaDeviceSynchronize();
@@ -889,7 +919,11 @@ extern "C" int evs_verify_batch(evs_state* const* states, int32_t nseq, const in
     EVS_TRY(check_block(s, n_host[b]));
     sr.row0[b + 1] = sr.row0[b] + n_host[b];
   }
-  if (sr.row0[nseq] > NTOK) return fail(EVS_ERR_ARG, "%d block rows in total, at most %d", sr.row0[nseq], NTOK);
+  const evs_model* m = states[0]->m;
+  const int rows_max = m->tc && !m->fuse ? ROWS_MAX : NTOK;
+  if (sr.row0[nseq] > rows_max)
+    return fail(sr.row0[nseq] > ROWS_MAX ? EVS_ERR_ARG : EVS_ERR_UNSUPPORTED,
+                "%d block rows in total, at most %d for this model", sr.row0[nseq], rows_max);
   LaunchCtx Lc{stream, states[0]->pdl};
   EVS_TRY(enqueue_verify(states, sr, tokens, logits, Lc));
   for (int b = 0; b < nseq; ++b) states[b]->host_pending = n_host[b];

@@ -20,17 +20,28 @@
 
 namespace evs {
 
+// at most MAX_CONTRIB CTAs per tile: the last one sums their slots
+constexpr int MAX_CONTRIB = 8;
+
 bool plan_gemm(int N, int K, int num_sms, GemmPlan* g) {
+  const int T = (N + TILE_M - 1) / TILE_M;
+  const long long U = (long long)T * ((K + TILE_K - 1) / TILE_K);
+  if (T > 1024 || N < 1 || K < 1 || num_sms < 1) return false;
+  return plan_gemm_grid(N, K, (int)std::min<long long>(std::min<long long>(num_sms, U), (long long)T * MAX_CONTRIB),
+                        g);
+}
+
+bool plan_gemm_grid(int N, int K, int G, GemmPlan* g) {
   Partials& P = g->P;
   P = Partials{};
   P.N = N;
   const int T = (N + TILE_M - 1) / TILE_M;
-  if (T > 1024 || N < 1 || K < 1 || num_sms < 1) return false;
+  if (T > 1024 || N < 1 || K < 1 || G < 1) return false;
+  P.nt = 1;
   P.KB = (K + TILE_K - 1) / TILE_K;
   P.U = (long long)T * P.KB;
-  // at most MAX_CONTRIB CTAs per tile: the last one sums their slots
-  constexpr int MAX_CONTRIB = 8;
-  P.G = (int)std::min<long long>(std::min<long long>(num_sms, P.U), (long long)T * MAX_CONTRIB);
+  if (G > P.U || G > T * MAX_CONTRIB) return false;
+  P.G = G;
   P.stages = 8;
   int base = 0;
   for (int t = 0; t < T; ++t) {
@@ -54,6 +65,7 @@ bool plan_gemm_cluster(int N, int K, int cl, GemmPlan* g) {
   P.U = (long long)T * P.KB;
   P.G = T * cl;
   P.cl = cl;
+  P.nt = 1;
   // a CTA that owns a whole tile has the shared memory to itself: deepest ring
   P.stages = cl == 1 ? GEMM_MAX_STAGES : 8;
   for (int t = 0; t < T; ++t) g->tab[t] = make_int4(0, 0, 0, 0);
@@ -132,8 +144,8 @@ constexpr int SWG_BYTES = NTOK * (TILE_M / 2) * 4;  // gate/up exchange of the S
 // barriers (full, empty, ready: S each; acc_full[2], acc_empty[2], drain),
 // TMEM slot + flags, reduction scratch, converter row scales, SwiGLU
 // exchange, cluster slots
-__host__ __device__ constexpr size_t gemm_smem(int S, int cl, int bsrc) {
-  return 1024 + (size_t)S * (A_BYTES + B_BYTES + raw_bytes(bsrc)) + (size_t)(3 * S + 5) * 8 + 16 +
+__host__ __device__ constexpr size_t gemm_smem(int S, int cl, int bsrc, int nt = 1) {
+  return 1024 + (size_t)S * (A_BYTES + nt * B_BYTES + raw_bytes(bsrc)) + (size_t)(3 * S + 5) * 8 + 16 +
          4 * NTOK * 4 + 2 * NTOK * 4 + SWG_BYTES + (size_t)(cl > 1 ? cl - 1 : 0) * CL_SLOT;
 }
 constexpr size_t GEMM_SMEM_MAX = 232448;
@@ -275,9 +287,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 }
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
-// N = 16 (bits 17-22 hold N/8), M = 128 (bits 24-28 hold M/16).
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NTOK >> 3) << 17) |
-                           ((uint32_t)(TILE_M >> 4) << 24);
+// N (bits 17-22 hold N/8, N = 16..256), M = 128 (bits 24-28 hold M/16).
+__host__ __device__ constexpr uint32_t idesc_n(int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TILE_M >> 4) << 24);
+}
 
 // Synchronisation of the 128 threads that drain a tile segment: the four
 // epilogue warps (named barrier 1) in the tensor-core kernel, the whole CTA
@@ -307,15 +320,16 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 // s_xch).  Called by the 128 group threads.
 template <bool NAMED>
 __device__ void tile_output(const Partials& P, int tile, int row, const float* v, float* s_red, float* s_xch,
-                            const float* xpre = nullptr) {
+                            const float* xpre = nullptr, int chunk = 0) {
   const int col = tile * TILE_M + row;
   const bool ok = col < P.N;
-  const int n = P.n;
+  const int r0 = chunk * NTOK;  // this chunk's first token row
+  const int n = min(NTOK, P.n - r0);
   if (P.mode == GEMM_FINAL) {
     if (ok) {
 #pragma unroll
       for (int t = 0; t < NTOK; ++t)
-        if (t < n) P.fin[(size_t)t * P.fin_ld + col] = v[t];
+        if (t < n) P.fin[(size_t)(r0 + t) * P.fin_ld + col] = v[t];
     }
   } else if (P.mode == GEMM_SWIGLU) {
     constexpr int HALF = TILE_M / 2;
@@ -329,7 +343,8 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
     if (row < HALF && hc < P.h_cols) {
 #pragma unroll
       for (int t = 0; t < NTOK; ++t)
-        if (t < n) P.hout[(size_t)t * P.h_cols + hc] = __float2bfloat16_rn(silu_f(v[t]) * s_xch[t * HALF + row]);
+        if (t < n)
+          P.hout[(size_t)(r0 + t) * P.h_cols + hc] = __float2bfloat16_rn(silu_f(v[t]) * s_xch[t * HALF + row]);
     }
     group_sync<NAMED>();  // the exchange buffer is free again
   } else {
@@ -338,12 +353,13 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
     // updates and the per-token butterflies
     float x[NTOK];
 #pragma unroll
-    for (int t = 0; t < NTOK; ++t) x[t] = (t < n && ok) ? (xpre ? xpre[t] : P.X[(size_t)t * P.N + col]) : 0.f;
+    for (int t = 0; t < NTOK; ++t)
+      x[t] = (t < n && ok) ? (xpre ? xpre[t] : P.X[(size_t)(r0 + t) * P.N + col]) : 0.f;
 #pragma unroll
     for (int t = 0; t < NTOK; ++t)
       if (t < n && ok) {
         x[t] += v[t];
-        P.X[(size_t)t * P.N + col] = x[t];
+        P.X[(size_t)(r0 + t) * P.N + col] = x[t];
       }
 #pragma unroll
     for (int t = 0; t < NTOK; ++t) {
@@ -353,12 +369,15 @@ __device__ void tile_output(const Partials& P, int tile, int row, const float* v
       if (lane == 0) s_red[w * NTOK + t] = sq;
     }
     group_sync<NAMED>();
-    if (row < NTOK) P.ss[tile * NTOK + row] = ((s_red[row] + s_red[NTOK + row]) + s_red[2 * NTOK + row]) +
-                                              s_red[3 * NTOK + row];
+    if (row < NTOK)
+      P.ss[tile * ROWS_MAX + r0 + row] =
+          ((s_red[row] + s_red[NTOK + row]) + s_red[2 * NTOK + row]) + s_red[3 * NTOK + row];
+    group_sync<NAMED>();  // s_red is free again (the next chunk reuses it)
   }
 }
 
-template <bool NAMED>
+// MC: the launch may carry several row chunks (P.nt); otherwise exactly one
+template <bool NAMED, bool MC = false>
 __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_flag, float* s_red, float* s_xch) {
   // The barrier orders the group's slot stores before thread 0's
   // acquire-release increment (release publishes them to the GPU; acquire
@@ -371,32 +390,36 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
   const int arrived = *s_flag;
   group_sync<NAMED>();  // every thread has read the flag before it is reused
   if (arrived != e.y - 1) return;
-  const int n = P.n;
-  const float* p = P.ws + (size_t)e.x * NTOK * TILE_M + row;
-  // Fixed order: the later contributors' slots 1..count-1 in order, then the
-  // first contributor's slot is added to that sum.  Slots are loaded four at
-  // a time.
-  float v[NTOK], v0[NTOK];
+  const int nt = MC ? P.nt : 1;
+  const size_t slot_f = (size_t)nt * NTOK * TILE_M;  // floats per slot
+  for (int c = 0; c < nt; ++c) {
+    const int n = min(NTOK, P.n - c * NTOK);
+    const float* p = P.ws + (size_t)e.x * slot_f + (size_t)c * NTOK * TILE_M + row;
+    // Fixed order: the later contributors' slots 1..count-1 in order, then
+    // the first contributor's slot is added to that sum.  Slots are loaded
+    // four at a time.
+    float v[NTOK], v0[NTOK];
 #pragma unroll
-  for (int t = 0; t < NTOK; ++t) v[t] = 0.f, v0[t] = (t < n) ? __ldcg(p + t * TILE_M) : 0.f;
-  for (int j0 = 1; j0 < e.y; j0 += 4) {
-    float a[4][NTOK];
+    for (int t = 0; t < NTOK; ++t) v[t] = 0.f, v0[t] = (t < n) ? __ldcg(p + t * TILE_M) : 0.f;
+    for (int j0 = 1; j0 < e.y; j0 += 4) {
+      float a[4][NTOK];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float* q = p + (size_t)(j0 + k) * NTOK * TILE_M;
+      for (int k = 0; k < 4; ++k) {
+        const float* q = p + (size_t)(j0 + k) * slot_f;
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) a[k][t] = (j0 + k < e.y && t < n) ? __ldcg(q + t * TILE_M) : 0.f;
+        for (int t = 0; t < NTOK; ++t) a[k][t] = (j0 + k < e.y && t < n) ? __ldcg(q + t * TILE_M) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (j0 + k < e.y) {
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
+        }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (j0 + k < e.y) {
-#pragma unroll
-        for (int t = 0; t < NTOK; ++t) v[t] += a[k][t];
-      }
+    for (int t = 0; t < NTOK; ++t) v[t] = v0[t] + v[t];
+    tile_output<NAMED>(P, tile, row, v, s_red, s_xch, nullptr, c);
   }
-#pragma unroll
-  for (int t = 0; t < NTOK; ++t) v[t] = v0[t] + v[t];
-  tile_output<NAMED>(P, tile, row, v, s_red, s_xch);
   if (row == 0) P.cnt[tile] = 0;
 }
 
@@ -418,6 +441,9 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
 // At most 144 registers a thread (no spills): a 320-thread block then leaves
 // a 256-thread, 72-register mixer CTA room on the SM to start its prologue
 // while the GEMM drains.
+// MC: several 16-row chunks (P.nt > 1); a separate instance so that the
+// one-chunk kernel keeps its register allocation.
+template <bool MC>
 __global__ void __maxnreg__(144)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const __grid_constant__ CUtensorMap nmap, Partials P, int* err_flag) {
@@ -425,9 +451,16 @@ __global__ void __maxnreg__(144)
   const int STAGES = P.stages;  // ring depth of this launch
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int RAW = raw_bytes(P.bsrc);
+  // token rows in NT chunks of 16: MMA N = 16 NT, B stage = NT 2 KB tiles
+  // (consecutive 8-row core-matrix groups, so one descriptor spans them all)
+  const int NT = MC ? P.nt : 1;
+  const int NN = NTOK * NT;
+  const int BST = NT * B_BYTES;
+  // TMEM columns: two accumulators of NN columns, a power of two >= 32
+  const uint32_t tmem_cols = NN <= 16 ? 32u : NN <= 32 ? 64u : NN <= 64 ? 128u : 256u;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint8_t* sR = sB + STAGES * B_BYTES;  // fp32 source rows of converted B tiles
+  uint8_t* sR = sB + STAGES * BST;  // fp32 source rows of converted B tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(sR + STAGES * RAW);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -489,7 +522,8 @@ __global__ void __maxnreg__(144)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(smem_u32(tmem_slot))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -521,12 +555,13 @@ __global__ void __maxnreg__(144)
     auto load_b = [&](int s, int kb) {
       const int x = kb * TILE_K;
       if (P.bsrc == GEMM_B_TMA) {
-        tma_load_2d(sB_u + s * B_BYTES, &xmap, full0 + 8 * s, x, 0, pol_x);
+        for (int ch = 0; ch < NT; ++ch)
+          tma_load_2d(sB_u + s * BST + ch * B_BYTES, &xmap, full0 + 8 * s, x, ch * NTOK, pol_x);
       } else {
         tma_load_2d(sR_u + s * RAW, &xmap, full0 + 8 * s, x, 0, pol_x);
       }
     };
-    const uint32_t stage_tx = A_BYTES + (P.bsrc == GEMM_B_TMA ? B_BYTES : RAW);
+    const uint32_t stage_tx = A_BYTES + (P.bsrc == GEMM_B_TMA ? BST : RAW);
     int kb = kb0, t = t0;
     const uint8_t* wp = wp0;
     for (int i = 0; i < pre; ++i) {
@@ -595,6 +630,7 @@ __global__ void __maxnreg__(144)
     // descriptors' 14-bit start-address field holds any shared address)
     const uint32_t wait0 = P.bsrc == GEMM_B_TMA ? full(0) : ready(0), empty0 = empty(0);
     const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
+    const uint32_t idesc = idesc_n(NN);
     int s = 0;
     uint32_t ph = 0;
     for (int seg = 0; seg < nseg && ok; ++seg) {
@@ -606,7 +642,7 @@ __global__ void __maxnreg__(144)
         break;
       }
       tc_fence_after();
-      const uint32_t dt = tmem + (uint32_t)(b * NTOK);
+      const uint32_t dt = tmem + (uint32_t)(b * NN);
       bool first = true;
       const int cnt = (int)(seg_end - (ub + i));
       for (int j = 0; j < cnt; ++j, ++i) {
@@ -617,10 +653,10 @@ __global__ void __maxnreg__(144)
         tc_fence_after();
         UNIT_TRACE(3, i);
         const uint64_t ad = ad0 + (uint64_t)(s * (A_BYTES >> 4));
-        const uint64_t bd = bd0 + (uint64_t)(s * (B_BYTES >> 4));
+        const uint64_t bd = bd0 + (uint64_t)(s * (BST >> 4));
 #pragma unroll
         for (int k = 0; k < TILE_K / 16; ++k)  // 16 bf16 = 32 bytes per MMA step along K
-          mma_bf16(dt, ad + 2 * k, bd + 2 * k, IDESC, (first && k == 0) ? 0u : 1u);
+          mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
 #ifdef EVS_TRACE
         if (i == 0 && P.trace) atomicMin(P.trace + 6 * P.trace_slot + 3, gtimer());
         if (i == 0 && P.trace && P.trace_slot == P.cta_slot && c < 1024) P.trace[6 * 1024 + 4 * c] = gtimer();
@@ -666,10 +702,13 @@ __global__ void __maxnreg__(144)
       group_sync<true>();
       if (!go) break;
       tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NN);
       float v[NTOK];
-      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * NTOK), v);
-      tc_fence_before();
-      mbar_arrive(acc_empty(b));
+      tmem_ld16(tacc, v);
+      if (NT == 1) {
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+      }
 #ifdef EVS_TRACE
       if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 4, gtimer());
       if (g == 0 && seg == nseg - 1 && P.trace && P.trace_slot == P.cta_slot && c < 1024)
@@ -694,11 +733,23 @@ __global__ void __maxnreg__(144)
       }
       const int4 e = __ldg(P.tab + tile);
       const long long slot = e.x + (c - e.z);
-      float* dst = P.ws + slot * NTOK * TILE_M + row;
+      float* dst = P.ws + slot * NN * TILE_M + row;
+      // row chunk by row chunk into the slot ([NT][16][128]); with several
+      // chunks the accumulator is released after the last one leaves TMEM
+      for (int ch = 0;;) {
+        const int nc = P.n - ch * NTOK;
 #pragma unroll
-      for (int j = 0; j < NTOK; ++j)
-        if (j < P.n) __stcg(dst + j * TILE_M, v[j]);
-      tile_done<true>(P, tile, row, s_flag, s_red, s_xch);
+        for (int j = 0; j < NTOK; ++j)
+          if (j < nc) __stcg(dst + j * TILE_M, v[j]);
+        if (++ch == NT) break;
+        tmem_ld16(tacc + (uint32_t)(ch * NTOK), v);
+        dst += NTOK * TILE_M;
+      }
+      if (NT > 1) {
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+      }
+      tile_done<true, MC>(P, tile, row, s_flag, s_red, s_xch);
 #ifdef EVS_TRACE
       if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 5, gtimer());
 #endif
@@ -719,11 +770,11 @@ __global__ void __maxnreg__(144)
       for (; k + 16 <= P.ss_tiles; k += 16) {
         float a[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = __ldcg(p + (k + e) * NTOK);
+        for (int e = 0; e < 16; ++e) a[e] = __ldcg(p + (k + e) * ROWS_MAX);
 #pragma unroll
         for (int e = 0; e < 16; ++e) tot += a[e];
       }
-      for (; k < P.ss_tiles; ++k) tot += __ldcg(p + k * NTOK);
+      for (; k < P.ss_tiles; ++k) tot += __ldcg(p + k * ROWS_MAX);
       const float den = sqrtf(tot / (float)P.norm_d + P.eps);
       s_scale[lane] = den;
       s_scale[NTOK + lane] = 1.f / den;
@@ -783,11 +834,20 @@ __global__ void __maxnreg__(144)
     }
     if (crank == 0 && warp >= 2 && warp < 6 && !*abort_flag) {
       const int row = (warp & 3) * 32 + lane;
-      for (int r = 1; r < P.cl; ++r) {
-        const float* src = s_cl + ((size_t)(r - 1) * NTOK) * TILE_M + row;
+      // the stream-K fixup's order: ranks 1..cl-1 summed in rank order, then
+      // rank 0's column added (a pass planned either way rounds alike)
+      if (P.cl > 1) {
+        float acc[NTOK];
 #pragma unroll
-        for (int j = 0; j < NTOK; ++j)
-          if (j < P.n) vkeep[j] += src[j * TILE_M];
+        for (int j = 0; j < NTOK; ++j) acc[j] = 0.f;
+        for (int r = 1; r < P.cl; ++r) {
+          const float* src = s_cl + ((size_t)(r - 1) * NTOK) * TILE_M + row;
+#pragma unroll
+          for (int j = 0; j < NTOK; ++j)
+            if (j < P.n) acc[j] += src[j * TILE_M];
+        }
+#pragma unroll
+        for (int j = 0; j < NTOK; ++j) vkeep[j] = vkeep[j] + acc[j];
       }
       tile_output<true>(P, first_tile, row, vkeep, s_red, s_xch, have_x ? xpre : nullptr);
 #ifdef EVS_TRACE
@@ -801,7 +861,7 @@ __global__ void __maxnreg__(144)
   }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
 #ifdef EVS_TRACE
@@ -916,9 +976,9 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, unsigned long
   return cudaGetLastError();
 }
 
-int gemm_stages_for(int cl, int bsrc) {
+int gemm_stages_for(int cl, int bsrc, int nt) {
   int S = GEMM_MAX_STAGES;
-  while (S > 2 && gemm_smem(S, cl, bsrc) > GEMM_SMEM_MAX) --S;
+  while (S > 2 && gemm_smem(S, cl, bsrc, nt) > GEMM_SMEM_MAX) --S;
   return S;
 }
 
@@ -938,26 +998,34 @@ cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CU
                            const CUtensorMap& nmap, const Partials& P, int K, int* err_flag) {
   (void)K;
   const int cl = P.cl > 1 ? P.cl : 1;
-  const size_t smem = gemm_smem(P.stages, cl, P.bsrc);
+  if (P.nt < 1 || P.nt > NT_MAX || P.n < 1 || P.n > NTOK * P.nt) return cudaErrorInvalidValue;
+  // several row chunks: stream-K with TMA activations only
+  if (P.nt > 1 && (P.cl != 0 || P.bsrc != GEMM_B_TMA)) return cudaErrorInvalidValue;
+  const size_t smem = gemm_smem(P.stages, cl, P.bsrc, P.nt);
   if (P.stages < 2 || P.stages > GEMM_MAX_STAGES || smem > GEMM_SMEM_MAX) return cudaErrorInvalidValue;
-  if (P.bsrc != GEMM_B_TMA && P.n > NTOK) return cudaErrorInvalidValue;
   if (P.mode == GEMM_SWIGLU && (P.N != 2 * P.h_cols || P.h_cols % (TILE_M / 2) != 0 || !P.hout))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM_MAX);
+        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM_MAX);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)GEMM_SMEM_MAX);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   // converter warps only where the B tile is built in shared memory: the
   // smaller block leaves registers for the next kernel's CTAs to start early
   const int threads = P.bsrc == GEMM_B_TMA ? GEMM_THREADS - N_CONV * 32 : GEMM_THREADS;
-  return launch_cl(L, cl, gemm_tc_kernel, dim3(P.G), dim3(threads), smem, wmap, xmap, nmap, P, err_flag);
+  if (P.nt > 1)
+    return launch_cl(L, cl, gemm_tc_kernel<true>, dim3(P.G), dim3(threads), smem, wmap, xmap, nmap, P, err_flag);
+  return launch_cl(L, cl, gemm_tc_kernel<false>, dim3(P.G), dim3(threads), smem, wmap, xmap, nmap, P, err_flag);
 }
 
 cudaError_t launch_gemm_simt(const LaunchCtx& L, int dtype, const void* W, const void* X, int ldx,
                              const Partials& P, int K) {
+  if (P.nt != 1 || P.n < 1 || P.n > NTOK) return cudaErrorInvalidValue;
   if (dtype == EVS_BF16)
     return launch(L, gemm_simt_kernel<bf16>, dim3(P.G), dim3(128), 0, (const bf16*)W, (const bf16*)X,
                   ldx, P, K);

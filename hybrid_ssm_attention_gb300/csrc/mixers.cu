@@ -891,7 +891,7 @@ long long attn_span(long long ctx_max, int chunk) {
 size_t attn_scratch_bytes(int H, int Dh, long long ctx_max, int chunk) {
   const long long nsplit = (ctx_max + attn_span(ctx_max, chunk) - 1) / attn_span(ctx_max, chunk);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al(sizeof(double) * (Dh / 2)) + al(sizeof(float) * NTOK * H * Dh) +
+  return al(sizeof(double) * (Dh / 2)) + al(sizeof(float) * ROWS_MAX * H * Dh) +
          al(sizeof(float) * H * nsplit * NTOK * Dh) + al(sizeof(float) * H * nsplit * NTOK * 2);
 }
 
@@ -903,7 +903,7 @@ void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int
   out->inv_freq = (double*)p;
   p += al(sizeof(double) * (Dh / 2));
   out->qbuf = (float*)p;
-  p += al(sizeof(float) * NTOK * H * Dh);
+  p += al(sizeof(float) * ROWS_MAX * H * Dh);
   out->part_o = (float*)p;
   p += al(sizeof(float) * H * nsplit * NTOK * Dh);
   out->part_ml = (float*)p;

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
     const int lane = threadIdx.x;
     float tot = 0.f;
     for (int k0 = 0; k0 < ntiles; k0 += 32) {
-      const float mine = k0 + lane < ntiles ? __ldcg(ss + (k0 + lane) * NTOK + t) : 0.f;
+      const float mine = k0 + lane < ntiles ? __ldcg(ss + (k0 + lane) * ROWS_MAX + t) : 0.f;
       for (int j = 0; j < 32 && k0 + j < ntiles; ++j) tot += __shfl_sync(0xffffffffu, mine, j);
     }
     if (lane == 0) {

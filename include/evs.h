@@ -221,12 +221,17 @@ int evs_verify_block(evs_state* s, const int32_t* tokens_dev, int32_t n,
  * name as the next step for serving ([systems], [regime]).
  * states_host [nseq] (1 <= nseq <= 16): distinct states of one model and one
  * ctx_max, none with a pending verify; n_host [nseq]: block lengths, each in
- * [1, gamma_max+1], summing to at most 16; tokens_dev: the blocks back to
+ * [1, gamma_max+1], summing to at most 128 (EVS_BATCH_ROWS_MAX) on the bf16
+ * path, at most 16 for float32 models and with EVS_FUSE=1
+ * (EVS_ERR_UNSUPPORTED between 17 and 128); tokens_dev: the blocks back to
  * back (sequence 0's n_host[0] tokens first); logits_dev [sum n][V] in the
- * same row order.  The activations and workspaces of states_host[0] are
- * used.  Each sequence's logits and retained state equal those of its own
- * evs_verify_block bit for bit.  Launched directly on stream (not captured
- * in a graph).  Errors as evs_verify_block, per state. */
+ * same row order.  The weight GEMMs take all rows in one pass (16-row
+ * chunks side by side in the tensor-core N dimension).  The activations and
+ * workspaces of states_host[0] are used.  Each sequence's logits and
+ * retained state equal those of its own evs_verify_block bit for bit.
+ * Launched directly on stream (not captured in a graph).  Errors as
+ * evs_verify_block, per state. */
+#define EVS_BATCH_ROWS_MAX 128
 int evs_verify_batch(evs_state* const* states_host, int32_t nseq, const int32_t* tokens_dev,
                      const int32_t* n_host, float* logits_dev, cudaStream_t stream);
 /* Block verify that also copies the residual stream after the embedding

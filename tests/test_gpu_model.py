@@ -415,3 +415,86 @@ def test_7b_block_verify_full_size():
         srt = np.sort(ref[i])
         if srt[-1] - srt[-2] > gap_tol:
             assert int(np.argmax(got[i])) == int(np.argmax(ref[i])), i
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("which", ["small", "wide"])
+def test_batches_beyond_16_rows_equal_separate_bitwise(which):
+    # Passes of 17..128 rows (up to 16 sequences): every weight GEMM takes the
+    # rows as 16-row chunks side by side in one tensor-core pass (the cluster
+    # split-K GEMMs switch to their stream-K twins over the same unit ranges).
+    # Each sequence's logits and next results still equal its own
+    # evs_verify_block bit for bit, including ragged chunks (26, 63 rows) and
+    # the 128-row maximum.
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    shape = small_shape() if which == "small" else wide_shape()
+    W = synth.make_weights(shape, 43)
+    m = evs.Model(shape, W)
+    V, nmax = shape.vocab, shape.n_block
+    g = np.random.default_rng(5)
+    B = 16
+    ref = [evs.State(m, 256) for _ in range(B)]
+    bat = [evs.State(m, 256) for _ in range(B)]
+    for b in range(B):
+        pr = [int(x) for x in synth.prompt(shape, 60 + b, 3 + 2 * b)]
+        for st in (ref[b], bat[b]):
+            for s0 in range(0, len(pr), nmax):
+                _verify(evs, st, pr[s0:s0 + nmax], V)
+                evs.evs_commit(st, len(pr[s0:s0 + nmax]))
+    plans = [(nmax, nmax), (nmax, 1, 7, nmax, nmax, 5, 2, 9, nmax), (nmax,) * 8, (8,) * 16, (3,) * 7]
+    for ns in plans:
+        k = len(ns)
+        toks = [[int(x) for x in g.integers(0, V, n)] for n in ns]
+        refl = [to_np(_verify(evs, ref[b], toks[b], V)[0]) for b in range(k)]
+        allt = t.tensor(np.concatenate([np.asarray(x, np.int32) for x in toks]), device="cuda")
+        lg = t.empty((sum(ns), V), dtype=t.float32, device="cuda")
+        evs.evs_verify_batch(bat[:k], allt, ns, lg)
+        got = to_np(lg)
+        assert np.isfinite(got).all()
+        r0 = 0
+        for b in range(k):
+            assert np.array_equal(got[r0:r0 + ns[b]].view(np.uint32), refl[b].view(np.uint32)), (ns, b)
+            r0 += ns[b]
+        for b in range(k):
+            keep = int(g.integers(0, ns[b] + 1))
+            evs.evs_commit(ref[b], keep)
+            evs.evs_commit(bat[b], keep)
+    for b in range(B):
+        assert ref[b].book() == bat[b].book()
+        nxt = [int(x) for x in g.integers(0, V, 2)]
+        l1 = to_np(_verify(evs, ref[b], nxt, V)[0])
+        l2 = to_np(_verify(evs, bat[b], nxt, V)[0])
+        assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32)), b
+        assert ref[b].check() == 0 and bat[b].check() == 0
+
+
+@pytest.mark.gpu
+def test_batch_row_limits(monkeypatch):
+    # More than 128 rows is an argument error; 17..128 rows need the bf16
+    # path without the fused RMSNorm converter (EVS_ERR_UNSUPPORTED otherwise,
+    # and nothing is left pending on the states).
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+
+    def attempt(m, ns, code):
+        sts = [evs.State(m, 64) for _ in ns]
+        toks = t.zeros(sum(ns), dtype=t.int32, device="cuda")
+        lg = t.empty((sum(ns), m.shape.vocab), dtype=t.float32, device="cuda")
+        with pytest.raises(evs.EvsError) as e:
+            evs.evs_verify_batch(sts, toks, ns, lg)
+        assert e.value.code == code, str(e.value)
+        for st in sts:  # usable afterwards
+            _verify(evs, st, [1], m.shape.vocab)
+            evs.evs_commit(st, 1)
+            assert st.check() == 0
+
+    small = small_shape()
+    W = synth.make_weights(small, 7)
+    attempt(evs.Model(small, W), (small.n_block,) * 10, evs.EVS_ERR_ARG)  # 130 rows
+    tiny = synth.tiny()
+    attempt(evs.Model(tiny, synth.make_weights(tiny, 7)), (tiny.n_block,) * 4, evs.EVS_ERR_UNSUPPORTED)
+    monkeypatch.setenv("EVS_FUSE", "1")
+    fused = evs.Model(small, W)
+    monkeypatch.delenv("EVS_FUSE")
+    attempt(fused, (small.n_block, small.n_block), evs.EVS_ERR_UNSUPPORTED)
