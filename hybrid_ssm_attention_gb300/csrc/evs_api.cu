@@ -123,6 +123,10 @@ struct evs_model {
   // mixer from starting early.
   bool swiglu;
   bool fuse;
+  // stream-K in-projection and gate/up GEMMs leave their partial slots to
+  // the consuming mixer / activation kernel (GEMM_SLOTS): no fixup tail
+  // (bf16; EVS_SLOTS=0 keeps the GEMM-side fixup)
+  bool slots;
   int n_max;
 };
 
@@ -224,9 +228,11 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
   // GEMM_FINAL writes fin[tok][col] (row stride ld); GEMM_RESID adds into X
   // and leaves per-tile sums of squares for the next RMSNorm
   const int nt = (n + NTOK - 1) / NTOK;
+  // mode GEMM_SLOTS falls back to GEMM_FINAL for a cluster plan; *out then
+  // describes where the consumer reads the result (slots or fin)
   auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
                   const CUtensorMap& xm, const void* Xin, int K, int mode, float* fin, int ld,
-                  int bsrc = GEMM_B_TMA) -> int {
+                  int bsrc = GEMM_B_TMA, MixSrc* out = nullptr) -> int {
     Partials P = plan;
     if (nt > 1) {
       // more than 16 rows: the stream-K twin, with a ring that fits nt
@@ -240,6 +246,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       P.stages = std::min(P.stages, gemm_stages_for(0, GEMM_B_TMA, nt));
     }
     P.nt = nt;
+    if (mode == GEMM_SLOTS && (P.cl != 0 || !m->slots)) mode = GEMM_FINAL;
     P.wpk = pk;
     P.bsrc = bsrc;
     P.Kdim = K;
@@ -272,6 +279,14 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
     P.trace_slot = gk - 1;
     P.cta_slot = s->cta_slot;
 #endif
+    if (out) {
+      *out = MixSrc{fin, ld, 1};
+      if (mode == GEMM_SLOTS) {
+        out->ws = P.ws;
+        out->tab = P.tab;
+        out->slot_rows = NTOK * nt;
+      }
+    }
     if (m->tc)
       CUDA_TRY(launch_gemm_tc(Lc, wm, xm, *nmap, P, K, &s->book->status));
     else
@@ -294,11 +309,11 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
     LayerS& st = s->S[i];
     // the first in-projection reads the embedding kernel's normalised rows;
     // later ones normalise the residual stream themselves when fused
+    MixSrc src{};
     if (fz && i > 0)
-      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, d, GEMM_FINAL, s->fin, 3 * d, GEMM_B_NORM));
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, d, GEMM_SLOTS, s->fin, 3 * d, GEMM_B_NORM, &src));
     else
-      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d));
-    MixSrc src{s->fin, 3 * d, 1};
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_SLOTS, s->fin, 3 * d, GEMM_B_TMA, &src));
     (void)st;
     if (w.kind == EVS_LAYER_FIR) {
       SeqPtrs<float*> e0{}, e1{};
@@ -320,14 +335,15 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, sr, s->ctx_max, c.attn_chunk, as, s->ab, s->g));
     }
     EVS_TRY(gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
-    const int gu_mode = sg ? GEMM_SWIGLU : GEMM_FINAL;
+    const int gu_mode = sg ? GEMM_SWIGLU : GEMM_SLOTS;
+    MixSrc gsrc{};
     if (fz) {
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, gu_mode, s->fin, 2 * F, GEMM_B_NORM));
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, gu_mode, s->fin, 2 * F, GEMM_B_NORM, &gsrc));
     } else {
       CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, gu_mode, s->fin, 2 * F));
+      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, gu_mode, s->fin, 2 * F, GEMM_B_TMA, &gsrc));
     }
-    if (!sg) CUDA_TRY(launch_mlp_act(Lc, dt, s->fin, n, F, m->packed, s->h));
+    if (!sg) CUDA_TRY(launch_mlp_act(Lc, dt, gsrc, n, F, m->packed, s->h));
     EVS_TRY(gemm(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
     if (!fz) CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
     if (trace)
@@ -486,6 +502,8 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     m->swiglu = m->packed && sw && sw[0] == '1';
     // fp32 rows staged by TMA need 16-byte row strides
     m->fuse = m->packed && cfg->d_model % 4 == 0 && fz && fz[0] == '1';
+    const char* sl = getenv("EVS_SLOTS");
+    m->slots = m->tc && !(sl && sl[0] == '0');
   }
   const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;
   char err[256] = {0};

@@ -749,7 +749,7 @@ __global__ void __maxnreg__(144)
         tc_fence_before();
         mbar_arrive(acc_empty(b));
       }
-      tile_done<true, MC>(P, tile, row, s_flag, s_red, s_xch);
+      if (P.mode != GEMM_SLOTS) tile_done<true, MC>(P, tile, row, s_flag, s_red, s_xch);
 #ifdef EVS_TRACE
       if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 5, gtimer());
 #endif
@@ -1005,6 +1005,7 @@ cudaError_t launch_gemm_tc(const LaunchCtx& L, const CUtensorMap& wmap, const CU
   if (P.stages < 2 || P.stages > GEMM_MAX_STAGES || smem > GEMM_SMEM_MAX) return cudaErrorInvalidValue;
   if (P.mode == GEMM_SWIGLU && (P.N != 2 * P.h_cols || P.h_cols % (TILE_M / 2) != 0 || !P.hout))
     return cudaErrorInvalidValue;
+  if (P.mode == GEMM_SLOTS && P.cl != 0) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =

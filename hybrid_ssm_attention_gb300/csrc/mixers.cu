@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(256)
     const int r = e >> 3, w = e & 7;
     cp_async16(ext_s + r * 32 + w * 4, src_ext + (size_t)(off + r) * d + c0 + w * 4);
   }
+  const auto ca = src.at(c), cb = src.at(d + c), cv = src.at(2 * d + c);
   cp_async_wait_all();
   __syncthreads();
   for (int e = threadIdx.x; e < (Lf - 1) * 8; e += nthr) {
@@ -80,9 +81,9 @@ __global__ void __launch_bounds__(256)
   }
   pdl_wait();
   for (int t = warp; t < n; t += NW) {
-    const float a = stored<T>(src.get(r0 + t, c));
-    const float b = stored<T>(src.get(r0 + t, d + c));
-    const float v = stored<T>(src.get(r0 + t, 2 * d + c));
+    const float a = stored<T>(src.get(ca, r0 + t, c));
+    const float b = stored<T>(src.get(cb, r0 + t, d + c));
+    const float v = stored<T>(src.get(cv, r0 + t, 2 * d + c));
     a_s[t * 32 + lane] = a;
     ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
     dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
@@ -148,12 +149,15 @@ __global__ void __launch_bounds__(256)
   float2* dst = bank ? st0 : st1;
   float2 s = make_float2(0.f, 0.f);
   if (slot >= 0) s = cur[((size_t)slot * d + c) * M + m];
+  // 256 is a multiple of CPB: this thread's staging column is fixed
+  const int cc = blockIdx.x * CPB + threadIdx.x % CPB;
+  const auto ca = src.at(cc), cb = src.at(d + cc), cv = src.at(2 * d + cc);
   pdl_wait();
   for (int e = threadIdx.x; e < n * CPB; e += 256) {
-    const int t = e / CPB, cc = blockIdx.x * CPB + e % CPB;
-    const float a = stored<T>(src.get(r0 + t, cc));
-    const float b = stored<T>(src.get(r0 + t, d + cc));
-    const float v = stored<T>(src.get(r0 + t, 2 * d + cc));
+    const int t = e / CPB;
+    const float a = stored<T>(src.get(ca, r0 + t, cc));
+    const float b = stored<T>(src.get(cb, r0 + t, d + cc));
+    const float v = stored<T>(src.get(cv, r0 + t, 2 * d + cc));
     a_s[t][e % CPB] = a;
     z_s[t][e % CPB] = b * v;
   }
@@ -197,15 +201,17 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const
   const float red = (float)fma(-turns, TWO_PI, ang);
   float sn, cs;
   sincosf(red, &sn, &cs);
+  const int col = h * Dh + i;
+  const auto cq1 = src.at(col), cq2 = src.at(col + half), ck1 = src.at(d + col), ck2 = src.at(d + col + half);
+  const auto cv1 = src.at(2 * d + col), cv2 = src.at(2 * d + col + half);
   pdl_wait();
   if (pos >= ctx_max) {
     if (i == 0) set_status(book, EVS_DEV_KV_OVERFLOW);
     return;
   }
-  const int col = h * Dh + i;
-  const float q1 = stored<T>(src.get(r, col)), q2 = stored<T>(src.get(r, col + half));
-  const float k1 = stored<T>(src.get(r, d + col)), k2 = stored<T>(src.get(r, d + col + half));
-  const float v1 = stored<T>(src.get(r, 2 * d + col)), v2 = stored<T>(src.get(r, 2 * d + col + half));
+  const float q1 = stored<T>(src.get(cq1, r, col)), q2 = stored<T>(src.get(cq2, r, col + half));
+  const float k1 = stored<T>(src.get(ck1, r, d + col)), k2 = stored<T>(src.get(ck2, r, d + col + half));
+  const float v1 = stored<T>(src.get(cv1, r, 2 * d + col)), v2 = stored<T>(src.get(cv2, r, 2 * d + col + half));
   const float rq1 = q1 * cs - q2 * sn, rq2 = q1 * sn + q2 * cs;
   const float rk1 = k1 * cs - k2 * sn, rk2 = k1 * sn + k2 * cs;
   const size_t row = ((size_t)h * ctx_max + pos) * Dh;
@@ -861,6 +867,10 @@ cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, const S
                        const float* taps, const SeqPtrs<float*>& ext0, const SeqPtrs<float*>& ext1,
                        const SeqPtrs<const evs_book*>& book, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
+  if (src.ws)
+    return dtype == EVS_BF16 ? fir_dispatch<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, d, sr, Lf, taps, ext0,
+                                                  ext1, book, g)
+                             : cudaErrorInvalidValue;
   if (dtype == EVS_BF16)
     return src.f32 ? fir_dispatch<bf16>(L, sf, d, sr, Lf, taps, ext0, ext1, book, g)
                    : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, Lf, taps, ext0,
@@ -872,6 +882,10 @@ cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, const S
                        const float* lam, const float* res, const SeqPtrs<float*>& st0, const SeqPtrs<float*>& st1,
                        const SeqPtrs<const evs_book*>& book, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
+  if (src.ws)
+    return dtype == EVS_BF16 ? iir_dispatch<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, d, sr, M, lam, res,
+                                                  st0, st1, book, g)
+                             : cudaErrorInvalidValue;
   if (dtype == EVS_BF16)
     return src.f32 ? iir_dispatch<bf16>(L, sf, d, sr, M, lam, res, st0, st1, book, g)
                    : iir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, M, lam, res, st0,
@@ -923,6 +937,10 @@ cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStre
 cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, const SeqRows& sr,
                              long long ctx_max, int chunk, const AttnSeq& as, const AttnBufs& B, void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
+  if (src.ws)
+    return dtype == EVS_BF16 ? attention_t<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, H, Dh, sr, ctx_max,
+                                                 chunk, as, B, g)
+                             : cudaErrorInvalidValue;
   if (dtype == EVS_BF16)
     return src.f32 ? attention_t<bf16>(L, sf, H, Dh, sr, ctx_max, chunk, as, B, g)
                    : attention_t<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, H, Dh, sr, ctx_max, chunk, as,

@@ -119,15 +119,16 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
   if (c < d) xn[(size_t)t * d + c] = from_f<T>(div_row(x, s_den, s_rcp));
 }
 
-template <typename T>
-__global__ void mlp_act_kernel(const float* gu, int F, int il, T* h) {
+template <typename T, typename Src>
+__global__ void mlp_act_kernel(const __grid_constant__ Src gu, int F, int il, T* h) {
   const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_trigger();
+  const int gj = il ? (j / 64) * 128 + j % 64 : j, uj = il ? gj + 64 : F + j;
+  typename Src::Col cg{}, cu{};
+  if (j < F) cg = gu.at(gj), cu = gu.at(uj);
   pdl_wait();
   if (j >= F) return;
-  const float* row = gu + (size_t)t * 2 * F;
-  const int gj = il ? (j / 64) * 128 + j % 64 : j, uj = il ? gj + 64 : F + j;
-  const float gt = row[gj], up = row[uj];
+  const float gt = gu.get(cg, t, gj), up = gu.get(cu, t, uj);
   h[(size_t)t * F + j] = from_f<T>(silu_f(gt) * up);
 }
 
@@ -346,10 +347,16 @@ cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, con
   return launch(L, norm_apply_kernel<float>, g, dim3(256), 0, X, ss, ntiles, d, eps, (float*)xn);
 }
 
-cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const float* gu, int n, int F, bool il, void* h) {
+cudaError_t launch_mlp_act(const LaunchCtx& L, int dtype, const MixSrc& gu, int n, int F, bool il, void* h) {
   const dim3 g((F + 255) / 256, n);
-  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16>, g, dim3(256), 0, gu, F, (int)il, (bf16*)h);
-  return launch(L, mlp_act_kernel<float>, g, dim3(256), 0, gu, F, (int)il, (float*)h);
+  if (gu.ws) {
+    if (dtype != EVS_BF16) return cudaErrorInvalidValue;
+    return launch(L, mlp_act_kernel<bf16, SrcSlots>, g, dim3(256), 0, SrcSlots{gu.ws, gu.tab, gu.slot_rows}, F,
+                  (int)il, (bf16*)h);
+  }
+  const SrcPlain<float> sf{(const float*)gu.p, 2 * F};
+  if (dtype == EVS_BF16) return launch(L, mlp_act_kernel<bf16, SrcPlain<float>>, g, dim3(256), 0, sf, F, (int)il, (bf16*)h);
+  return launch(L, mlp_act_kernel<float, SrcPlain<float>>, g, dim3(256), 0, sf, F, (int)il, (float*)h);
 }
 
 cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, float T, int top_k, float* p) {

@@ -13,6 +13,11 @@
         launches and the row / mixer kernels), then every weight GEMM of a
         step once more, each launched alone (in, out, gate/up, down per
         layer, then the head).
+    python -m hybrid_ssm_attention_gb300.profile_case batch 2 8 13
+        the first L layers of the 7B-shaped stack, B sequences of n rows each
+        verified in one batched pass (B * n rows: 16-row chunks side by side
+        in the GEMMs' N dimension), each sequence committing its block;
+        repeated `--reps` times.
 """
 from __future__ import annotations
 
@@ -28,7 +33,7 @@ def main():
     from hybrid_ssm_attention_gb300 import build as b
     b.build()
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["gemm", "fir", "iir", "attn", "stack"])
+    ap.add_argument("kind", choices=["gemm", "fir", "iir", "attn", "stack", "batch"])
     ap.add_argument("args", type=int, nargs="*")
     ap.add_argument("--reps", type=int, default=4)
     a = ap.parse_args()
@@ -36,7 +41,22 @@ def main():
     g = torch.Generator(device=dev).manual_seed(0)
     book = torch.zeros(8, dtype=torch.int32, device=dev)
     book[4] = -1
-    if a.kind == "stack":
+    if a.kind == "batch":
+        import synth
+        L, B, n = (a.args + [2, 8, 13][len(a.args):])[:3]
+        full = synth.stack_7b()
+        shape = synth.ModelShape(name=f"7b-first-{L}", vocab=full.vocab, d_model=full.d_model,
+                                 layers=full.layers[:L], n_heads=full.n_heads, head_dim=full.head_dim,
+                                 d_ffn=full.d_ffn, gamma=full.gamma, dtype="bf16", pole_mag=full.pole_mag)
+        m = evs.Model(shape, synth.make_weights(shape, 3))
+        sts = [evs.State(m, 256) for _ in range(B)]
+        toks = torch.tensor([65 + (i % 4) for i in range(B * n)], dtype=torch.int32, device=dev)
+        lg = torch.empty((B * n, shape.vocab), device=dev)
+        for _ in range(a.reps):
+            evs.evs_verify_batch(sts, toks, [n] * B, lg)
+            for st in sts:
+                evs.evs_commit(st, n)
+    elif a.kind == "stack":
         import synth
         L, n = (a.args + [2, 13][len(a.args):])[:2]
         full = synth.stack_7b()
