@@ -127,6 +127,10 @@ struct evs_model {
   // the consuming mixer / activation kernel (GEMM_SLOTS): no fixup tail
   // (bf16; EVS_SLOTS=0 keeps the GEMM-side fixup)
   bool slots;
+  // out / down GEMMs too (stream-K on every SM instead of cluster split-K),
+  // the residual add and its sums of squares done by resid_norm (fused
+  // converters: the GEMM's own residual epilogue, on the same split)
+  bool slots_resid;
   int n_max;
 };
 
@@ -228,8 +232,9 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
   // GEMM_FINAL writes fin[tok][col] (row stride ld); GEMM_RESID adds into X
   // and leaves per-tile sums of squares for the next RMSNorm
   const int nt = (n + NTOK - 1) / NTOK;
-  // mode GEMM_SLOTS falls back to GEMM_FINAL for a cluster plan; *out then
-  // describes where the consumer reads the result (slots or fin)
+  // with out set, a stream-K launch leaves its slots (GEMM_SLOTS) instead of
+  // running `mode`; *out then says where the consumer reads the result
+  // (the slots, or fin for GEMM_FINAL)
   auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
                   const CUtensorMap& xm, const void* Xin, int K, int mode, float* fin, int ld,
                   int bsrc = GEMM_B_TMA, MixSrc* out = nullptr) -> int {
@@ -246,7 +251,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       P.stages = std::min(P.stages, gemm_stages_for(0, GEMM_B_TMA, nt));
     }
     P.nt = nt;
-    if (mode == GEMM_SLOTS && (P.cl != 0 || !m->slots)) mode = GEMM_FINAL;
+    if (out && P.cl == 0 && m->slots) mode = GEMM_SLOTS;
     P.wpk = pk;
     P.bsrc = bsrc;
     P.Kdim = K;
@@ -311,9 +316,9 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
     // later ones normalise the residual stream themselves when fused
     MixSrc src{};
     if (fz && i > 0)
-      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, d, GEMM_SLOTS, s->fin, 3 * d, GEMM_B_NORM, &src));
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, d, GEMM_FINAL, s->fin, 3 * d, GEMM_B_NORM, &src));
     else
-      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_SLOTS, s->fin, 3 * d, GEMM_B_TMA, &src));
+      EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d, GEMM_B_TMA, &src));
     (void)st;
     if (w.kind == EVS_LAYER_FIR) {
       SeqPtrs<float*> e0{}, e1{};
@@ -334,18 +339,28 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       }
       CUDA_TRY(launch_attention(Lc, dt, src, c.n_heads, c.head_dim, sr, s->ctx_max, c.attn_chunk, as, s->ab, s->g));
     }
-    EVS_TRY(gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, GEMM_RESID, nullptr, 0));
-    const int gu_mode = sg ? GEMM_SWIGLU : GEMM_SLOTS;
+    // residual GEMM, then (unfused) the RMSNorm of the updated rows: by
+    // resid_norm from the GEMM's slots, or by norm_apply after the GEMM's
+    // own residual epilogue
+    auto resid_gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
+                          const CUtensorMap& xm, const void* Xin, int K) -> int {
+      MixSrc rs{};
+      EVS_TRY(gemm(plan, wm, pk, W, xm, Xin, K, GEMM_RESID, nullptr, 0, GEMM_B_TMA,
+                   fz || !m->slots_resid ? nullptr : &rs));
+      if (fz) return EVS_OK;
+      if (rs.ws)
+        CUDA_TRY(launch_resid_norm(Lc, dt, s->X, rs, n, d, eps, s->xn));
+      else
+        CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
+      return EVS_OK;
+    };
+    EVS_TRY(resid_gemm(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d));
+    const int gu_mode = sg ? GEMM_SWIGLU : GEMM_FINAL;
     MixSrc gsrc{};
-    if (fz) {
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, d, gu_mode, s->fin, 2 * F, GEMM_B_NORM, &gsrc));
-    } else {
-      CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
-      EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, d, gu_mode, s->fin, 2 * F, GEMM_B_TMA, &gsrc));
-    }
+    EVS_TRY(gemm(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, fz ? s->m_xf : s->m_xn, fz ? (const void*)s->X : s->xn, d, gu_mode,
+                 s->fin, 2 * F, fz ? GEMM_B_NORM : GEMM_B_TMA, sg ? nullptr : &gsrc));
     if (!sg) CUDA_TRY(launch_mlp_act(Lc, dt, gsrc, n, F, m->packed, s->h));
-    EVS_TRY(gemm(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, F, GEMM_RESID, nullptr, 0));
-    if (!fz) CUDA_TRY(launch_norm_apply(Lc, dt, s->X, s->ss, n, d, eps, s->xn));
+    EVS_TRY(resid_gemm(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, F));
     if (trace)
       CUDA_TRY(cudaMemcpyAsync(trace + (i + 1) * (size_t)n * d, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   }
@@ -504,6 +519,7 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     m->fuse = m->packed && cfg->d_model % 4 == 0 && fz && fz[0] == '1';
     const char* sl = getenv("EVS_SLOTS");
     m->slots = m->tc && !(sl && sl[0] == '0');
+    m->slots_resid = m->slots && resid_norm_ok(cfg->d_model);
   }
   const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;
   char err[256] = {0};
@@ -554,7 +570,9 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     for (int k = 0; k < 5; ++k) {
       const char* cl_env = getenv("EVS_GEMM_CLUSTER");
       const bool allow_cl = m->tc && !(cl_env && cl_env[0] == '0');
-      const int cl = allow_cl ? gemm_cluster_choice(shapes[k][0], shapes[k][1], m->num_sms) : 0;
+      const bool resid = k == 1 || k == 3;
+      const int cl = allow_cl && !(resid && m->slots_resid) ? gemm_cluster_choice(shapes[k][0], shapes[k][1], m->num_sms)
+                                                            : 0;
       const bool planned = cl ? plan_gemm_cluster(shapes[k][0], shapes[k][1], cl, &plans[k])
                               : plan_gemm(shapes[k][0], shapes[k][1], m->num_sms, &plans[k]);
       if (!planned) {

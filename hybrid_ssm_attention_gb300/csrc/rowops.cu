@@ -119,6 +119,94 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
   if (c < d) xn[(size_t)t * d + c] = from_f<T>(div_row(x, s_den, s_rcp));
 }
 
+// Residual add and RMSNorm of rows whose out / down GEMM left partial slots.
+// A cluster of CL CTAs per row, CTA = G groups of 128 threads; thread j of
+// group g owns column j of each of the group's TPC consecutive 128-column
+// tiles, so the sums of squares follow the GEMM_RESID epilogue exactly: per
+// tile, x^2 of each warp's 32 columns by xor butterfly (16, 8, 4, 2, 1),
+// then the four warps in order; the row's sum is the tile sums in tile
+// order.  Each CTA pushes its tile sums into every CTA's shared memory
+// before the one cluster barrier, after which only local memory is read.
+template <typename T, int TPC>
+__global__ void __launch_bounds__(256) resid_norm_kernel(float* X, const __grid_constant__ SrcSlots src, int d,
+                                                         float eps, T* xn) {
+  __shared__ float s_red[2][4][TPC];
+  __shared__ float s_all[RESID_TILES_ROW];  // the row's tile sums, tile order
+  __shared__ float s_den, s_rcp;
+  cg::cluster_group cl = cg::this_cluster();
+  const int ncl = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const int G = blockDim.x / TILE_M;
+  const int t = blockIdx.y, g = threadIdx.x / TILE_M, j = threadIdx.x % TILE_M;
+  const int ntiles = d / TILE_M, kc = rank * G * TPC, k0 = kc + g * TPC;
+  const int lane = j & 31, w = j >> 5;
+  pdl_trigger();
+  SrcSlots::Col cs[TPC];
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) cs[i] = src.at((k0 + i) * TILE_M + j);
+  pdl_wait();
+  float* xr = X + (size_t)t * d + j;
+  // every load before the first store (X may alias the slots for all the
+  // compiler knows); a tile has up to six stream-K contributors here
+  float x[TPC], sv[TPC];
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) {
+    x[i] = __ldcg(xr + (k0 + i) * TILE_M);
+    sv[i] = src.get<6>(cs[i], t, (k0 + i) * TILE_M + j);
+  }
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) {
+    x[i] += sv[i];
+    xr[(k0 + i) * TILE_M] = x[i];
+    float sq = x[i] * x[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) s_red[g][w][i] = sq;
+  }
+  __syncthreads();
+  // tile sum (g, i) -> position kc + g*TPC + i of every CTA's s_all
+  if (threadIdx.x < ncl * G * TPC) {
+    const int q = threadIdx.x / (G * TPC), e = threadIdx.x % (G * TPC), gg = e / TPC, i = e % TPC;
+    const float v = ((s_red[gg][0][i] + s_red[gg][1][i]) + s_red[gg][2][i]) + s_red[gg][3][i];
+    *cl.map_shared_rank(&s_all[kc + e], q) = v;
+  }
+  cl.sync();
+  if (threadIdx.x < 32) {
+    // the tile sums, 32 at a time, added in tile order
+    float tot = 0.f;
+    for (int q0 = 0; q0 < ntiles; q0 += 32) {
+      const float mine = q0 + lane < ntiles ? s_all[q0 + lane] : 0.f;
+      for (int q = 0; q < 32 && q0 + q < ntiles; ++q) tot += __shfl_sync(0xffffffffu, mine, q);
+    }
+    if (lane == 0) {
+      s_den = sqrtf(tot / (float)d + eps);
+      s_rcp = 1.f / s_den;
+    }
+  }
+  __syncthreads();
+  T* xo = xn + (size_t)t * d + j;
+#pragma unroll
+  for (int i = 0; i < TPC; ++i) xo[(k0 + i) * TILE_M] = from_f<T>(div_row(x[i], s_den, s_rcp));
+}
+
+// Shape of the row split: G groups of 128 threads (2 if the tile count is
+// even), CL CTAs (the largest of 4, 2, 1 that leaves a power-of-two TPC <=
+// RESID_TILES_MAX tiles per group).  False if none fits.
+bool resid_shape(int d, int* G, int* TPC, int* CL) {
+  if (d % TILE_M || d / TILE_M > RESID_TILES_ROW) return false;
+  const int nt = d / TILE_M;
+  *G = nt % 2 == 0 ? 2 : 1;
+  const int rest = nt / *G;
+  for (int cl = 4; cl >= 1; cl >>= 1) {
+    const int tpc = rest / cl;
+    if (rest % cl == 0 && tpc <= RESID_TILES_MAX && (tpc & (tpc - 1)) == 0) {
+      *TPC = tpc;
+      *CL = cl;
+      return true;
+    }
+  }
+  return false;
+}
+
 template <typename T, typename Src>
 __global__ void mlp_act_kernel(const __grid_constant__ Src gu, int F, int il, T* h) {
   const int t = blockIdx.y, j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -336,6 +424,28 @@ cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, cons
                      eps, (bf16*)xn, sr, book);
   return launch_cl(L, cl, embed_norm_kernel<float>, dim3(cl, n), dim3(256), 0, (const float*)E, tokens, V, X, d,
                    eps, (float*)xn, sr, book);
+}
+
+bool resid_norm_ok(int d) {
+  int G, TPC, CL;
+  return resid_shape(d, &G, &TPC, &CL);
+}
+
+cudaError_t launch_resid_norm(const LaunchCtx& L, int dtype, float* X, const MixSrc& slots, int n, int d, float eps,
+                              void* xn) {
+  int G, TPC, CL;
+  if (dtype != EVS_BF16 || !slots.ws || !resid_shape(d, &G, &TPC, &CL)) return cudaErrorInvalidValue;
+  const SrcSlots src{slots.ws, slots.tab, slots.slot_rows};
+  void (*k)(float*, SrcSlots, int, float, bf16*);
+  switch (TPC) {
+    case 1: k = resid_norm_kernel<bf16, 1>; break;
+    case 2: k = resid_norm_kernel<bf16, 2>; break;
+    case 4: k = resid_norm_kernel<bf16, 4>; break;
+    case 8: k = resid_norm_kernel<bf16, 8>; break;
+    case 16: k = resid_norm_kernel<bf16, 16>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  return launch_cl(L, CL, k, dim3(CL, n), dim3(G * TILE_M), 0, X, src, d, eps, (bf16*)xn);
 }
 
 cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, const float* ss, int n, int d,
