@@ -159,7 +159,7 @@ class ClockSampler:
 # averaged over the 129 weight GEMMs of a step) from the ncu capture summarised
 # in profiles/gemm_tc_7b_packed_weight_stream.md; valid only for the kernel
 # source it was taken on (sha256 prefix of gemm.cu), else reported as null.
-GEMM_TRAFFIC = {"gemm_cu_sha256": "271fb6b8ae99c6b4", "bytes_per_launch": 100.87e6}
+GEMM_TRAFFIC = {"gemm_cu_sha256": "36e304d05cd03395", "bytes_per_launch": 100.87e6}
 
 
 def gemm_traffic():
@@ -451,10 +451,10 @@ def run_evs(args, rank, world, local):
     # accept, restore, verify the kept tokens again, commit (the second
     # forward pass that per-position slicing removes)
     replay = None
-    if not args.no_replay:
+    R, Wr = min(args.steps, 16, rounds - 2), 2  # replayed blocks come from the same `rounds` blocks
+    if not args.no_replay and R >= 1:
         snap.clone_into(st)
         rsnap = evs.State(model, ctx)
-        R, Wr = min(args.steps, 16), 2
         emitted_r = 0
         for r in range(Wr + R):
             if r == Wr:

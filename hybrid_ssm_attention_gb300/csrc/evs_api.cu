@@ -687,7 +687,9 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   const char* pdl_env = getenv("EVS_PDL");
   s->pdl = !(pdl_env && pdl_env[0] == '0');
   const char* pf_env = getenv("EVS_PREFETCH_UNITS");
-  s->pf_units = pf_env ? std::max(0, atoi(pf_env)) : 12;
+  // 4 units (64 KB) per CTA, 9.7 MB in all: measured best on the 7B-shaped
+  // step (deeper prefetches compete with the running GEMM's own stream)
+  s->pf_units = pf_env ? std::max(0, atoi(pf_env)) : 4;
   const evs_config& c = m->cfg;
   const int d = c.d_model, F = c.d_ffn, nm = m->n_max;
   const size_t es = esize(c.dtype);
@@ -1266,8 +1268,9 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   CUDA_TRY(launch_busy(Lc, 2000000));
   int k = 0;
   int r = EVS_OK;
-  // each GEMM with the B source the verify step gives it
-  // (outputs go to a scratch buffer: the state is untouched)
+  // each GEMM with the B source and output mode the verify step gives it
+  // (outputs go to a scratch buffer and residual GEMMs write plain sums, so
+  // the state is untouched)
   auto one = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
                  const CUtensorMap& xm, const void* X, int N, int K, int bsrc = GEMM_B_TMA,
                  int mode = GEMM_FINAL) -> int {
@@ -1298,19 +1301,29 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
     ++k;
     return EVS_OK;
   };
+  const bool fz = m->fuse;
+  // the verify step's output modes: slots for stream-K GEMMs with slot
+  // consumers (residual GEMMs only when unfused), else the plain sums
+  auto slots_or = [&](const Partials& P, bool resid, int mode) {
+    return m->slots && P.cl == 0 && !(resid && (fz || !m->slots_resid)) ? GEMM_SLOTS : mode;
+  };
   for (int i = 0; i < nl && r == EVS_OK; ++i) {
     const LayerW& w = m->L[i];
-    const bool fz = m->fuse;
-    const int gu_mode = m->swiglu ? GEMM_SWIGLU : GEMM_FINAL;
+    const int gu_mode = m->swiglu ? GEMM_SWIGLU : slots_or(m->p_gu, false, GEMM_FINAL);
+    const int in_mode = slots_or(m->p_in, false, GEMM_FINAL);
     if (fz && i > 0)
-      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, 3 * d, d, GEMM_B_NORM);
+      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, 3 * d, d, GEMM_B_NORM, in_mode);
     else
-      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, 3 * d, d);
-    if (r == EVS_OK) r = one(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, d);
+      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, 3 * d, d, GEMM_B_TMA, in_mode);
+    if (r == EVS_OK)
+      r = one(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, d, GEMM_B_TMA,
+              slots_or(m->p_out, true, GEMM_FINAL));
     if (r == EVS_OK)
       r = fz ? one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, 2 * F, d, GEMM_B_NORM, gu_mode)
              : one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d, GEMM_B_TMA, gu_mode);
-    if (r == EVS_OK) r = one(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, d, F);
+    if (r == EVS_OK)
+      r = one(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, d, F, GEMM_B_TMA,
+              slots_or(m->p_down, true, GEMM_FINAL));
   }
   if (r == EVS_OK)
     r = m->fuse ? one(m->p_head, m->m_head, m->pk_head, m->head, s->m_xf, s->X, V, d, GEMM_B_NORM)

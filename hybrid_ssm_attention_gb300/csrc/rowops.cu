@@ -120,62 +120,71 @@ __global__ void __launch_bounds__(256) norm_apply_kernel(const float* X, const f
 }
 
 // Residual add and RMSNorm of rows whose out / down GEMM left partial slots.
-// A cluster of CL CTAs per row, CTA = G groups of 128 threads; thread j of
-// group g owns column j of each of the group's TPC consecutive 128-column
-// tiles, so the sums of squares follow the GEMM_RESID epilogue exactly: per
-// tile, x^2 of each warp's 32 columns by xor butterfly (16, 8, 4, 2, 1),
-// then the four warps in order; the row's sum is the tile sums in tile
-// order.  Each CTA pushes its tile sums into every CTA's shared memory
+// A cluster of ncl CTAs per row; warp w of CTA r owns 128-column tile
+// r * warps + w, lane l its four columns 4l .. 4l+3 (float4 loads of the
+// residual row and of every slot).  The tile's sum of squares follows the
+// GEMM_RESID epilogue exactly: there, column c sits in lane c % 32 of warp
+// c / 32 and each warp's squares meet by xor butterfly over 16, 8, 4, 2, 1,
+// then the four warps are added in order.  Here the xor partners c ^ 16,
+// c ^ 8, c ^ 4 are lanes l ^ 4, l ^ 2, l ^ 1 and c ^ 2, c ^ 1 are within
+// the lane; with commuted operands every partial sum is the same value,
+// so the tile sum is bit-identical.  The row's sum adds the tile sums in
+// tile order; each CTA pushes its tile sums into every CTA's shared memory
 // before the one cluster barrier, after which only local memory is read.
-template <typename T, int TPC>
+template <typename T>
 __global__ void __launch_bounds__(256) resid_norm_kernel(float* X, const __grid_constant__ SrcSlots src, int d,
                                                          float eps, T* xn) {
-  __shared__ float s_red[2][4][TPC];
   __shared__ float s_all[RESID_TILES_ROW];  // the row's tile sums, tile order
   __shared__ float s_den, s_rcp;
   cg::cluster_group cl = cg::this_cluster();
   const int ncl = (int)cl.num_blocks(), rank = (int)cl.block_rank();
-  const int G = blockDim.x / TILE_M;
-  const int t = blockIdx.y, g = threadIdx.x / TILE_M, j = threadIdx.x % TILE_M;
-  const int ntiles = d / TILE_M, kc = rank * G * TPC, k0 = kc + g * TPC;
-  const int lane = j & 31, w = j >> 5;
+  const int t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = rank * (blockDim.x >> 5) + warp, ntiles = d / TILE_M;
+  const int col = tile * TILE_M + 4 * lane;
   pdl_trigger();
-  SrcSlots::Col cs[TPC];
-#pragma unroll
-  for (int i = 0; i < TPC; ++i) cs[i] = src.at((k0 + i) * TILE_M + j);
+  const SrcSlots::Col c = src.at(col);
   pdl_wait();
-  float* xr = X + (size_t)t * d + j;
-  // every load before the first store (X may alias the slots for all the
-  // compiler knows); a tile has up to six stream-K contributors here
-  float x[TPC], sv[TPC];
+  float* xr = X + (size_t)t * d + col;
+  const size_t stride = (size_t)src.rows * TILE_M;
+  const float* p = c.p + (size_t)t * TILE_M;
+  // every load first (X may alias the slots for all the compiler knows):
+  // the row, the first slot, then up to five more without a branch
+  float4 x = __ldcg(reinterpret_cast<const float4*>(xr));
+  const float4 v0 = __ldcg(reinterpret_cast<const float4*>(p));
+  float4 a[6];
 #pragma unroll
-  for (int i = 0; i < TPC; ++i) {
-    x[i] = __ldcg(xr + (k0 + i) * TILE_M);
-    sv[i] = src.get<6>(cs[i], t, (k0 + i) * TILE_M + j);
-  }
+  for (int j = 1; j < 6; ++j)
+    a[j] = c.cnt > j ? __ldcg(reinterpret_cast<const float4*>(p + j * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < TPC; ++i) {
-    x[i] += sv[i];
-    xr[(k0 + i) * TILE_M] = x[i];
-    float sq = x[i] * x[i];
+  for (int j = 1; j < 6; ++j) v.x += a[j].x, v.y += a[j].y, v.z += a[j].z, v.w += a[j].w;
+  for (int j = 6; j < c.cnt; ++j) {
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p + j * stride));
+    v.x += b.x, v.y += b.y, v.z += b.z, v.w += b.w;
+  }
+  x.x += v0.x + v.x;
+  x.y += v0.y + v.y;
+  x.z += v0.z + v.z;
+  x.w += v0.w + v.w;
+  *reinterpret_cast<float4*>(xr) = x;
+  float q[4] = {x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) s_red[g][w][i] = sq;
-  }
-  __syncthreads();
-  // tile sum (g, i) -> position kc + g*TPC + i of every CTA's s_all
-  if (threadIdx.x < ncl * G * TPC) {
-    const int q = threadIdx.x / (G * TPC), e = threadIdx.x % (G * TPC), gg = e / TPC, i = e % TPC;
-    const float v = ((s_red[gg][0][i] + s_red[gg][1][i]) + s_red[gg][2][i]) + s_red[gg][3][i];
-    *cl.map_shared_rank(&s_all[kc + e], q) = v;
-  }
+  for (int o = 4; o > 0; o >>= 1)  // column xor 16, 8, 4
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] += __shfl_xor_sync(0xffffffffu, q[k], o);
+  const float wsum = (q[0] + q[2]) + (q[1] + q[3]);  // column xor 2, then 1
+  // tile sum: the four 32-column warps of the epilogue (lanes 0, 8, 16, 24)
+  const float w1 = __shfl_sync(0xffffffffu, wsum, 8), w2 = __shfl_sync(0xffffffffu, wsum, 16);
+  const float w3 = __shfl_sync(0xffffffffu, wsum, 24);
+  const float ts = ((wsum + w1) + w2) + w3;
+  if (lane < ncl) *cl.map_shared_rank(&s_all[tile], lane) = ts;
   cl.sync();
-  if (threadIdx.x < 32) {
+  if (warp == 0) {
     // the tile sums, 32 at a time, added in tile order
     float tot = 0.f;
     for (int q0 = 0; q0 < ntiles; q0 += 32) {
       const float mine = q0 + lane < ntiles ? s_all[q0 + lane] : 0.f;
-      for (int q = 0; q < 32 && q0 + q < ntiles; ++q) tot += __shfl_sync(0xffffffffu, mine, q);
+      for (int k = 0; k < 32 && q0 + k < ntiles; ++k) tot += __shfl_sync(0xffffffffu, mine, k);
     }
     if (lane == 0) {
       s_den = sqrtf(tot / (float)d + eps);
@@ -183,28 +192,22 @@ __global__ void __launch_bounds__(256) resid_norm_kernel(float* X, const __grid_
     }
   }
   __syncthreads();
-  T* xo = xn + (size_t)t * d + j;
-#pragma unroll
-  for (int i = 0; i < TPC; ++i) xo[(k0 + i) * TILE_M] = from_f<T>(div_row(x[i], s_den, s_rcp));
+  const float den = s_den, rden = s_rcp;
+  T* xo = xn + (size_t)t * d + col;
+  xo[0] = from_f<T>(div_row(x.x, den, rden));
+  xo[1] = from_f<T>(div_row(x.y, den, rden));
+  xo[2] = from_f<T>(div_row(x.z, den, rden));
+  xo[3] = from_f<T>(div_row(x.w, den, rden));
 }
 
-// Shape of the row split: G groups of 128 threads (2 if the tile count is
-// even), CL CTAs (the largest of 4, 2, 1 that leaves a power-of-two TPC <=
-// RESID_TILES_MAX tiles per group).  False if none fits.
-bool resid_shape(int d, int* G, int* TPC, int* CL) {
-  if (d % TILE_M || d / TILE_M > RESID_TILES_ROW) return false;
+// CTAs per row: the fewest of 1, 2, 4, 8 that leave <= 8 whole tiles (one
+// per warp) to each; 0 if none fits
+int resid_cluster(int d) {
+  if (d % TILE_M) return 0;
   const int nt = d / TILE_M;
-  *G = nt % 2 == 0 ? 2 : 1;
-  const int rest = nt / *G;
-  for (int cl = 4; cl >= 1; cl >>= 1) {
-    const int tpc = rest / cl;
-    if (rest % cl == 0 && tpc <= RESID_TILES_MAX && (tpc & (tpc - 1)) == 0) {
-      *TPC = tpc;
-      *CL = cl;
-      return true;
-    }
-  }
-  return false;
+  for (int cl = 1; cl <= 8; cl <<= 1)
+    if (nt % cl == 0 && nt / cl <= 8) return cl;
+  return 0;
 }
 
 template <typename T, typename Src>
@@ -426,26 +429,15 @@ cudaError_t launch_embed_norm(const LaunchCtx& L, int dtype, const void* E, cons
                    eps, (float*)xn, sr, book);
 }
 
-bool resid_norm_ok(int d) {
-  int G, TPC, CL;
-  return resid_shape(d, &G, &TPC, &CL);
-}
+bool resid_norm_ok(int d) { return resid_cluster(d) > 0; }
 
 cudaError_t launch_resid_norm(const LaunchCtx& L, int dtype, float* X, const MixSrc& slots, int n, int d, float eps,
                               void* xn) {
-  int G, TPC, CL;
-  if (dtype != EVS_BF16 || !slots.ws || !resid_shape(d, &G, &TPC, &CL)) return cudaErrorInvalidValue;
-  const SrcSlots src{slots.ws, slots.tab, slots.slot_rows};
-  void (*k)(float*, SrcSlots, int, float, bf16*);
-  switch (TPC) {
-    case 1: k = resid_norm_kernel<bf16, 1>; break;
-    case 2: k = resid_norm_kernel<bf16, 2>; break;
-    case 4: k = resid_norm_kernel<bf16, 4>; break;
-    case 8: k = resid_norm_kernel<bf16, 8>; break;
-    case 16: k = resid_norm_kernel<bf16, 16>; break;
-    default: return cudaErrorInvalidValue;
-  }
-  return launch_cl(L, CL, k, dim3(CL, n), dim3(G * TILE_M), 0, X, src, d, eps, (bf16*)xn);
+  const int cl = resid_cluster(d);
+  if (dtype != EVS_BF16 || !slots.ws || cl < 1) return cudaErrorInvalidValue;
+  const int warps = d / TILE_M / cl;
+  return launch_cl(L, cl, resid_norm_kernel<bf16>, dim3(cl, n), dim3(32 * warps), 0, X,
+                   SrcSlots{slots.ws, slots.tab, slots.slot_rows}, d, eps, (bf16*)xn);
 }
 
 cudaError_t launch_norm_apply(const LaunchCtx& L, int dtype, const float* X, const float* ss, int n, int d,

@@ -363,7 +363,10 @@ int evs_selftest_wait_timeout(int32_t* status_dev, int64_t limit_ns, cudaStream_
  * the events see only GPU time.  ms_host[i] = launch i's duration,
  * bytes_host[i] = its algorithmic bytes (weights + activations in +
  * outputs); *count = number of launches (4 * n_layers + 1 <= max_launches).
- * Uses the state's workspaces; leaves the decoding state unchanged. */
+ * Each launch ends as in a verify step (partial slots left for the consumer
+ * where the step does that, else the summed output; residual GEMMs write
+ * their sums to scratch instead of the residual stream).  Uses the state's
+ * workspaces; leaves the decoding state unchanged. */
 int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host,
                       int32_t max_launches, int32_t* count, cudaStream_t stream);
 
