@@ -237,7 +237,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
   // (the slots, or fin for GEMM_FINAL)
   auto gemm = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
                   const CUtensorMap& xm, const void* Xin, int K, int mode, float* fin, int ld,
-                  int bsrc = GEMM_B_TMA, MixSrc* out = nullptr) -> int {
+                  int bsrc = GEMM_B_TMA, MixSrc* out = nullptr, int cnt_max = SLOTS_MIX_MAX) -> int {
     Partials P = plan;
     if (nt > 1) {
       // more than 16 rows: the stream-K twin, with a ring that fits nt
@@ -251,7 +251,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       P.stages = std::min(P.stages, gemm_stages_for(0, GEMM_B_TMA, nt));
     }
     P.nt = nt;
-    if (out && P.cl == 0 && m->slots) mode = GEMM_SLOTS;
+    if (out && P.cl == 0 && m->slots && P.max_cnt <= cnt_max) mode = GEMM_SLOTS;
     P.wpk = pk;
     P.bsrc = bsrc;
     P.Kdim = K;
@@ -346,7 +346,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
                           const CUtensorMap& xm, const void* Xin, int K) -> int {
       MixSrc rs{};
       EVS_TRY(gemm(plan, wm, pk, W, xm, Xin, K, GEMM_RESID, nullptr, 0, GEMM_B_TMA,
-                   fz || !m->slots_resid ? nullptr : &rs));
+                   fz || !m->slots_resid ? nullptr : &rs, SLOTS_RESID_MAX));
       if (fz) return EVS_OK;
       if (rs.ws)
         CUDA_TRY(launch_resid_norm(Lc, dt, s->X, rs, n, d, eps, s->xn));
@@ -1305,7 +1305,10 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   // the verify step's output modes: slots for stream-K GEMMs with slot
   // consumers (residual GEMMs only when unfused), else the plain sums
   auto slots_or = [&](const Partials& P, bool resid, int mode) {
-    return m->slots && P.cl == 0 && !(resid && (fz || !m->slots_resid)) ? GEMM_SLOTS : mode;
+    return m->slots && P.cl == 0 && P.max_cnt <= (resid ? SLOTS_RESID_MAX : SLOTS_MIX_MAX) &&
+                   !(resid && (fz || !m->slots_resid))
+               ? GEMM_SLOTS
+               : mode;
   };
   for (int i = 0; i < nl && r == EVS_OK; ++i) {
     const LayerW& w = m->L[i];

@@ -51,6 +51,8 @@ bool plan_gemm_grid(int N, int K, int G, GemmPlan* g) {
     base += c1 - c0 + 1;
   }
   g->slots = base;
+  P.max_cnt = 0;
+  for (int t = 0; t < T; ++t) P.max_cnt = std::max(P.max_cnt, g->tab[t].y);
   return true;
 }
 

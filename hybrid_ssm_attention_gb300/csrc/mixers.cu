@@ -80,13 +80,27 @@ __global__ void __launch_bounds__(256)
         *reinterpret_cast<const float4*>(ext_s + r * 32 + w * 4);
   }
   pdl_wait();
-  for (int t = warp; t < n; t += NW) {
-    const float a = stored<T>(src.get(ca, r0 + t, c));
-    const float b = stored<T>(src.get(cb, r0 + t, d + c));
-    const float v = stored<T>(src.get(cv, r0 + t, 2 * d + c));
-    a_s[t * 32 + lane] = a;
-    ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
-    dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
+  // three of this warp's rows at a time, all reads issued before any use
+  // (rows past the block re-read its last row and are dropped)
+  for (int t0 = warp; t0 < n; t0 += 3 * NW) {
+    float av[3], bv[3], vv[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int t = min(t0 + k * NW, n - 1);
+      av[k] = src.get(ca, r0 + t, c);
+      bv[k] = src.get(cb, r0 + t, d + c);
+      vv[k] = src.get(cv, r0 + t, 2 * d + c);
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int t = t0 + k * NW;
+      if (t < n) {
+        const float a = stored<T>(av[k]), b = stored<T>(bv[k]), v = stored<T>(vv[k]);
+        a_s[t * 32 + lane] = a;
+        ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
+        dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
+      }
+    }
   }
   __syncthreads();
   // y_t partial = sum_{j in [j0, j0+JT), j < Lf} h[j] * ext[Lf-1+t-j]; the

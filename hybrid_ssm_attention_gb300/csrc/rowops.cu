@@ -148,20 +148,17 @@ __global__ void __launch_bounds__(256) resid_norm_kernel(float* X, const __grid_
   const size_t stride = (size_t)src.rows * TILE_M;
   const float* p = c.p + (size_t)t * TILE_M;
   // every load first (X may alias the slots for all the compiler knows):
-  // the row, the first slot, then up to five more without a branch
+  // the row, then all of the tile's slots (at most SLOTS_RESID_MAX, checked
+  // on the host) without a branch
   float4 x = __ldcg(reinterpret_cast<const float4*>(xr));
   const float4 v0 = __ldcg(reinterpret_cast<const float4*>(p));
-  float4 a[6];
+  float4 a[SLOTS_RESID_MAX];
 #pragma unroll
-  for (int j = 1; j < 6; ++j)
+  for (int j = 1; j < SLOTS_RESID_MAX; ++j)
     a[j] = c.cnt > j ? __ldcg(reinterpret_cast<const float4*>(p + j * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int j = 1; j < 6; ++j) v.x += a[j].x, v.y += a[j].y, v.z += a[j].z, v.w += a[j].w;
-  for (int j = 6; j < c.cnt; ++j) {
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(p + j * stride));
-    v.x += b.x, v.y += b.y, v.z += b.z, v.w += b.w;
-  }
+  for (int j = 1; j < SLOTS_RESID_MAX; ++j) v.x += a[j].x, v.y += a[j].y, v.z += a[j].z, v.w += a[j].w;
   x.x += v0.x + v.x;
   x.y += v0.y + v.y;
   x.z += v0.z + v.z;
