@@ -159,7 +159,7 @@ class ClockSampler:
 # averaged over the 129 weight GEMMs of a step) from the ncu capture summarised
 # in profiles/gemm_tc_7b_packed_weight_stream.md; valid only for the kernel
 # source it was taken on (sha256 prefix of gemm.cu), else reported as null.
-GEMM_TRAFFIC = {"gemm_cu_sha256": "36e304d05cd03395", "bytes_per_launch": 100.87e6}
+GEMM_TRAFFIC = {"gemm_cu_sha256": "f6ea79a125047c1a", "bytes_per_launch": 100.85e6}
 
 
 def gemm_traffic():

@@ -33,13 +33,18 @@ def _verify(evs, st, toks, V):
 
 
 @pytest.mark.gpu
-def test_small_bf16_stack_matches_oracle():
+@pytest.mark.parametrize("slots", ["1", "0"])
+def test_small_bf16_stack_matches_oracle(slots, monkeypatch):
+    # slots "1": GEMMs leave partial slots to the consuming kernels (default);
+    # "0": every GEMM sums its own slots (cluster split-K out / down)
     import hybrid_ssm_attention_gb300 as evs
     from oracle.model import Model as OModel
     from oracle.numerics import Arith
     shape = small_shape()
     W = synth.make_weights(shape, 11)
+    monkeypatch.setenv("EVS_SLOTS", slots)
     m = evs.Model(shape, W)
+    monkeypatch.delenv("EVS_SLOTS")
     st = evs.State(m, 512)
     om = OModel(shape, synth.weights_f32(W), Arith(np.float32, bf16_points=True))
     ost = om.new_state(512)
