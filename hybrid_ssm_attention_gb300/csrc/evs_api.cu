@@ -584,8 +584,11 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
       if (m->tc)
         plans[k].P.stages =
             std::min(plans[k].P.stages, gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA));
+      // EVS_GEMM_STAGES overrides the ring depth, clamped to what fits
       const char* st_env = getenv("EVS_GEMM_STAGES");
-      if (st_env && m->tc) plans[k].P.stages = std::max(2, std::min(GEMM_MAX_STAGES, atoi(st_env)));
+      if (st_env && m->tc)
+        plans[k].P.stages = std::max(2, std::min(gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA),
+                                                 atoi(st_env)));
       // stream-K twin over the same CTA unit ranges (G = T * cl for a
       // cluster plan), for passes of more than NTOK rows
       GemmPlan& q = plans[5 + k];
