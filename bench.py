@@ -321,33 +321,41 @@ def long_generation(evs, torch, model, shape, prompt, ntok, seed, dev):
             "context_end": P0 + ntok}
 
 
-def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, rounds=24, warm=4):
-    """Batched verify (one pass over B sequences' blocks of n rows: one
-    16-row chunk up to B * n = 16, then 2..8 chunks side by side up to 128
-    rows): round time and verified rows per second for each (B, n), every
-    sequence committing its whole block (host keep) after each pass.  The
-    sequences start from the same post-prompt state."""
+def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, y, rounds=24, warm=4):
+    """Batched rounds (evs_round_batch: one graph per round doing one verify
+    pass over B sequences' blocks of n rows, then every sequence's accept and
+    commit on the device).  Up to B * n = 16 rows the GEMMs take one 16-row
+    chunk, beyond that 2..8 chunks side by side (up to 128 rows).  Every
+    sequence starts from the post-prompt state and is fed the identity
+    drafter's blocks (y: the target's own greedy continuation), so every
+    draft is accepted (asserted).  Reports round time and verified rows per
+    second for each (B, n)."""
     out = []
     V = shape.vocab
-    g = np.random.default_rng(7)
     for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1), (2, 13), (4, 13), (8, 13), (16, 8)):
         states = [evs.State(model, ctx) for _ in range(B)]
         for st in states:
             post_prompt.clone_into(st)
         lg = torch.empty((B * n, V), dtype=torch.float32, device=dev)
-        toks = torch.tensor(g.integers(65, 85, (rounds + warm, B * n)).astype(np.int32), device=dev)
+        rounds = min(rounds, y.numel() // n - warm)  # the identity blocks available
+        toks = y[: n * (rounds + warm)].view(rounds + warm, 1, n).expand(rounds + warm, B, n).reshape(
+            rounds + warm, B * n).contiguous()
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        tok = torch.zeros(B, dtype=torch.int32, device=dev)
+        acc_log = torch.zeros((rounds + warm, B), dtype=torch.int32, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for r in range(rounds + warm):
             if r == warm:
                 torch.cuda.synchronize()
                 e0.record()
-            evs.evs_verify_batch(states, toks[r], [n] * B, lg)
-            for st in states:
-                evs.evs_commit(st, n)
+            evs.evs_round_batch(states, toks[r], [n] * B, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, tok)
+            acc_log[r].copy_(acc)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / rounds
-        out.append({"B": B, "n": n, "rows": B * n, "ms_per_round": ms, "rows_per_s": B * n / (ms / 1e3)})
+        all_acc = bool((acc_log == n - 1).all().item())
+        out.append({"B": B, "n": n, "rows": B * n, "ms_per_round": ms, "rows_per_s": B * n / (ms / 1e3),
+                    "all_accepted": all_acc})
         for st in states:
             st.close()
     return out
@@ -503,7 +511,7 @@ def run_evs(args, rank, world, local):
 
     batched = None
     if not args.no_batch:
-        batched = batched_sweep(evs, torch, model, shape, snap, ctx, dev)
+        batched = batched_sweep(evs, torch, model, shape, snap, ctx, dev, y)
 
     longgen = None
     if args.long_gen > 0:

@@ -20,7 +20,7 @@ from ._abi import (EVS_BF16, EVS_ERR_ARG, EVS_ERR_CAPACITY, EVS_ERR_CUDA, EVS_ER
                    EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
-           "evs_commit", "evs_commit_dev", "evs_round", "evs_op_fir", "evs_op_iir",
+           "evs_commit", "evs_commit_dev", "evs_round", "evs_round_batch", "evs_op_fir", "evs_op_iir",
            "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_verify_batch",
            "evs_kernel_launches"]
 
@@ -228,6 +228,16 @@ def evs_round(state: State, tokens, n: int, logits, p, q, u, T: float, top_k: in
     _check(lib().evs_round(state.handle, _ptr(tokens), int(n), _ptr(logits), _ptr(p), _ptr(q), _ptr(u),
                            float(T), int(top_k), int(mode), _ptr(out_accepted), _ptr(out_token),
                            _stream(stream)), "evs_round")
+
+
+def evs_round_batch(states, tokens, ns, logits, p, q, u, T: float, top_k: int, mode: int, out_accepted, out_token,
+                    stream=None):
+    """One graph launch: batched verify, then every sequence's accept and commit on the device."""
+    arr = (C.c_void_p * len(states))(*[st.handle for st in states])
+    nh = (C.c_int32 * len(ns))(*[int(x) for x in ns])
+    _check(lib().evs_round_batch(arr, len(states), _ptr(tokens), nh, _ptr(logits), _ptr(p), _ptr(q), _ptr(u),
+                                 float(T), int(top_k), int(mode), _ptr(out_accepted), _ptr(out_token),
+                                 _stream(stream)), "evs_round_batch")
 
 
 def evs_op_fir(L, d, n, n_max, dtype, abv, taps, ext0, ext1, book_dev, g, stream=None):

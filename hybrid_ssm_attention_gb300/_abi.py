@@ -76,6 +76,7 @@ PROTOTYPES = {
     "evs_commit": (i32, [vp, i32, vp]),
     "evs_commit_dev": (i32, [vp, vp, vp]),
     "evs_round": (i32, [vp, vp, i32, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
+    "evs_round_batch": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
     "evs_op_fir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
     "evs_op_iir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
     "evs_op_attention_scratch_bytes": (sz, [i32, i32, i64, i32, i32]),

@@ -24,6 +24,7 @@ namespace {
 
 thread_local std::string g_err;
 std::atomic<long long> g_launches{0};
+std::atomic<unsigned long long> g_state_uid{0};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -78,6 +79,11 @@ struct GraphEntry {
   float T;
   const void *tok, *logits, *p, *q, *u, *acc, *otok;
   bool round;
+  // batched rounds: the sequences' states (by creation id, never reused)
+  // and block lengths
+  int nseq;
+  unsigned long long uid[MAX_SEQ];
+  int ns[MAX_SEQ];
   // value
   cudaGraphExec_t exec;
   int kernels;
@@ -136,6 +142,7 @@ struct evs_model {
 
 struct evs_state {
   evs_model* m;
+  unsigned long long uid;  // creation id (graph keys of batched rounds)
   long long ctx_max;
   evs_book* book;
   int host_pos;
@@ -400,11 +407,31 @@ int enqueue_round(evs_state* s, const int32_t* tokens, int n, float* logits, con
   return EVS_OK;
 }
 
+// Batched round: one verify pass over every sequence's block, then (sample
+// mode) the target distributions of all rows, the accept rule per sequence
+// (one CTA each) and every sequence's commit with keep = accepted + 1.
+int enqueue_round_batch(evs_state* const* states, const SeqRows& sr, const int32_t* tokens, float* logits,
+                        const RoundArgs& r, const LaunchCtx& Lc) {
+  EVS_TRY(enqueue_verify(states, sr, tokens, logits, Lc));
+  const int V = states[0]->m->cfg.vocab;
+  const float* P = logits;
+  if (r.mode == EVS_SAMPLE) {
+    CUDA_TRY(launch_probs(Lc, logits, sr.row0[sr.nseq], V, r.T, r.top_k, r.p));
+    P = r.p;
+  }
+  CUDA_TRY(launch_accept_batch(Lc, P, r.q, r.drafts, r.u, sr, V, r.mode, r.acc, r.otok));
+  SeqPtrs<evs_book*> books{};
+  for (int b = 0; b < sr.nseq; ++b) books.p[b] = states[b]->book;
+  CUDA_TRY(launch_commit_batch(Lc, books, sr.nseq, r.acc));
+  return EVS_OK;
+}
+
 GraphEntry* find_graph(evs_state* s, const GraphEntry& key) {
   for (auto& g : s->graphs)
     if (g.round == key.round && g.n == key.n && g.tok == key.tok && g.logits == key.logits &&
         g.mode == key.mode && g.top_k == key.top_k && g.T == key.T && g.p == key.p && g.q == key.q &&
-        g.u == key.u && g.acc == key.acc && g.otok == key.otok)
+        g.u == key.u && g.acc == key.acc && g.otok == key.otok && g.nseq == key.nseq &&
+        std::equal(g.uid, g.uid + g.nseq, key.uid) && std::equal(g.ns, g.ns + g.nseq, key.ns))
       return &g;
   return nullptr;
 }
@@ -685,6 +712,7 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   *out = nullptr;
   evs_state* s = new evs_state();
   s->m = m;
+  s->uid = ++g_state_uid;
   s->ctx_max = ctx_max;
   s->use_graphs = true;
   const char* pdl_env = getenv("EVS_PDL");
@@ -944,12 +972,12 @@ extern "C" int evs_verify_block(evs_state* s, const int32_t* tokens, int32_t n, 
   return EVS_OK;
 }
 
-extern "C" int evs_verify_batch(evs_state* const* states, int32_t nseq, const int32_t* tokens, const int32_t* n_host,
-                                float* logits, cudaStream_t stream) {
-  if (!states || !tokens || !n_host || !logits) return fail(EVS_ERR_ARG, "null argument");
+// Checks a batch (states distinct, one model and ctx_max, each block valid,
+// rows within the model's pass limit) and fills its row ranges.
+static int check_batch(evs_state* const* states, int32_t nseq, const int32_t* n_host, SeqRows* sr) {
   if (nseq < 1 || nseq > MAX_SEQ) return fail(EVS_ERR_ARG, "nseq=%d outside [1, %d]", nseq, MAX_SEQ);
-  SeqRows sr{};
-  sr.nseq = nseq;
+  *sr = SeqRows{};
+  sr->nseq = nseq;
   for (int b = 0; b < nseq; ++b) {
     evs_state* s = states[b];
     if (!s) return fail(EVS_ERR_ARG, "null state %d", b);
@@ -958,13 +986,21 @@ extern "C" int evs_verify_batch(evs_state* const* states, int32_t nseq, const in
     for (int q = 0; q < b; ++q)
       if (states[q] == s) return fail(EVS_ERR_ARG, "state %d appears twice", b);
     EVS_TRY(check_block(s, n_host[b]));
-    sr.row0[b + 1] = sr.row0[b] + n_host[b];
+    sr->row0[b + 1] = sr->row0[b] + n_host[b];
   }
   const evs_model* m = states[0]->m;
   const int rows_max = m->tc && !m->fuse ? ROWS_MAX : NTOK;
-  if (sr.row0[nseq] > rows_max)
-    return fail(sr.row0[nseq] > ROWS_MAX ? EVS_ERR_ARG : EVS_ERR_UNSUPPORTED,
-                "%d block rows in total, at most %d for this model", sr.row0[nseq], rows_max);
+  if (sr->row0[nseq] > rows_max)
+    return fail(sr->row0[nseq] > ROWS_MAX ? EVS_ERR_ARG : EVS_ERR_UNSUPPORTED,
+                "%d block rows in total, at most %d for this model", sr->row0[nseq], rows_max);
+  return EVS_OK;
+}
+
+extern "C" int evs_verify_batch(evs_state* const* states, int32_t nseq, const int32_t* tokens, const int32_t* n_host,
+                                float* logits, cudaStream_t stream) {
+  if (!states || !tokens || !n_host || !logits) return fail(EVS_ERR_ARG, "null argument");
+  SeqRows sr{};
+  EVS_TRY(check_batch(states, nseq, n_host, &sr));
   LaunchCtx Lc{stream, states[0]->pdl};
   EVS_TRY(enqueue_verify(states, sr, tokens, logits, Lc));
   for (int b = 0; b < nseq; ++b) states[b]->host_pending = n_host[b];
@@ -1049,6 +1085,45 @@ extern "C" int evs_round(evs_state* s, const int32_t* tokens, int32_t n, float* 
   EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) { return enqueue_round(s, tokens, n, logits, r, Lc); }));
   s->host_pos_known = false;
   s->host_pending = 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_round_batch(evs_state* const* states, int32_t nseq, const int32_t* tokens, const int32_t* n_host,
+                               float* logits, float* p, const float* q, const float* u, float T, int32_t top_k,
+                               int32_t mode, int32_t* acc, int32_t* otok, cudaStream_t stream) {
+  if (!states || !tokens || !n_host || !logits || !acc || !otok) return fail(EVS_ERR_ARG, "null argument");
+  if (mode != EVS_GREEDY && mode != EVS_SAMPLE) return fail(EVS_ERR_ARG, "bad mode");
+  if (mode == EVS_SAMPLE && (!p || !u || !q || !(T > 0.f))) return fail(EVS_ERR_ARG, "sample mode needs p, q, u and T > 0");
+  SeqRows sr{};
+  EVS_TRY(check_batch(states, nseq, n_host, &sr));
+  const evs_model* m = states[0]->m;
+  const int V = m->cfg.vocab;
+  if (V > 8192) return fail(EVS_ERR_UNSUPPORTED, "accept needs V <= 8192");
+  RoundArgs r{p, q, tokens + 1, u, T, top_k, mode, acc, otok};
+  GraphEntry key{};
+  key.round = true;
+  key.n = sr.row0[nseq];
+  key.tok = tokens;
+  key.logits = logits;
+  key.p = p;
+  key.q = q;
+  key.u = u;
+  key.T = T;
+  key.top_k = top_k;
+  key.mode = mode;
+  key.acc = acc;
+  key.otok = otok;
+  key.nseq = nseq;
+  for (int b = 0; b < nseq; ++b) {
+    key.uid[b] = states[b]->uid;
+    key.ns[b] = n_host[b];
+  }
+  EVS_TRY(run_captured(states[0], key, stream,
+                       [&](const LaunchCtx& Lc) { return enqueue_round_batch(states, sr, tokens, logits, r, Lc); }));
+  for (int b = 0; b < nseq; ++b) {
+    states[b]->host_pos_known = false;
+    states[b]->host_pending = 0;
+  }
   return EVS_OK;
 }
 

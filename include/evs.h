@@ -285,6 +285,24 @@ int evs_round(evs_state* s, const int32_t* tokens_dev, int32_t n, float* logits_
               float* p_dev, const float* q_dev, const float* u_dev, float T, int32_t top_k,
               int32_t mode, int32_t* out_accepted_dev, int32_t* out_token_dev,
               cudaStream_t stream);
+/* Batched round ([systems] batched verification with ragged per-sequence
+ * rollback, with the bookkeeping on the device): one graph launch doing
+ * evs_verify_batch over the nseq sequences' blocks, then (EVS_SAMPLE) the
+ * target distributions of all rows, the accept rule of every sequence and
+ * every sequence's commit with its own keep = accepted + 1.  Row layout as
+ * evs_verify_batch: sequence b owns rows r0 = sum of n_host[0..b-1] ..
+ * r0 + n_host[b] - 1 of tokens_dev (pending token, then its drafts),
+ * logits_dev and p_dev [sum n][V]; q_dev [sum n][V] (row r0 + i: the
+ * drafter distribution of draft i + 1; the sequence's last row unused) and
+ * u_dev [sum n] (rows r0 .. r0 + n_host[b] - 1: that sequence's uniforms)
+ * in sample mode (p, q, u may be null in greedy mode).  Outputs
+ * out_accepted_dev[b], out_token_dev[b].  Each sequence's results and state
+ * equal those of its own evs_round bit for bit.  Limits and errors as
+ * evs_verify_batch; V <= 8192. */
+int evs_round_batch(evs_state* const* states_host, int32_t nseq, const int32_t* tokens_dev,
+                    const int32_t* n_host, float* logits_dev, float* p_dev, const float* q_dev,
+                    const float* u_dev, float T, int32_t top_k, int32_t mode,
+                    int32_t* out_accepted_dev, int32_t* out_token_dev, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- operators
  * Single-operator entry points over caller-owned buffers: the same kernels

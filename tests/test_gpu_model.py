@@ -503,3 +503,93 @@ def test_batch_row_limits(monkeypatch):
     fused = evs.Model(small, W)
     monkeypatch.delenv("EVS_FUSE")
     attempt(fused, (small.n_block, small.n_block), evs.EVS_ERR_UNSUPPORTED)
+
+
+def _greedy_continuation(evs, st, tmp, first, k, V):
+    # k greedy tokens after `first` from a copy of st (native steps)
+    t = torch()
+    st.clone_into(tmp)
+    out, tok = [], first
+    lg = t.empty((1, V), dtype=t.float32, device="cuda")
+    for _ in range(k):
+        evs.evs_verify_block(tmp, t.tensor([tok], dtype=t.int32, device="cuda"), 1, lg)
+        evs.evs_commit(tmp, 1)
+        tok = int(lg[0].argmax().item())
+        out.append(tok)
+    return out
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["greedy", "sample"])
+def test_round_batch_equals_separate_rounds_bitwise(mode):
+    # evs_round_batch (one graph: batched verify, per-sequence probs / accept /
+    # commit on the device) against each sequence's own evs_round, over
+    # ragged blocks whose drafts follow the greedy continuation up to a
+    # random cut: accepted counts, output tokens, logits, probabilities and
+    # the states' next results agree bit for bit.
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    shape = small_shape()
+    W = synth.make_weights(shape, 47)
+    m = evs.Model(shape, W)
+    V, nmax = shape.vocab, shape.n_block
+    g = np.random.default_rng(9)
+    B = 4
+    ref = [evs.State(m, 256) for _ in range(B)]
+    bat = [evs.State(m, 256) for _ in range(B)]
+    tmp = evs.State(m, 256)
+    pending = []
+    for b in range(B):
+        pr = [int(x) for x in synth.prompt(shape, 80 + b, 6 + 4 * b)]
+        for st in (ref[b], bat[b]):
+            body = pr[:-1]
+            for s0 in range(0, len(body), nmax):
+                _verify(evs, st, body[s0:s0 + nmax], V)
+                evs.evs_commit(st, len(body[s0:s0 + nmax]))
+        pending.append(pr[-1])
+    sample = mode == "sample"
+    md = evs.EVS_SAMPLE if sample else evs.EVS_GREEDY
+    accepted = []
+    for rnd in range(4):
+        ns = [int(x) for x in g.integers(1, nmax + 1, B)]
+        blocks = []
+        for b in range(B):
+            cont = _greedy_continuation(evs, ref[b], tmp, pending[b], ns[b] - 1, V)
+            cut = int(g.integers(0, ns[b]))
+            drafts = cont[:cut] + [int(x) for x in g.integers(0, V, ns[b] - 1 - cut)]
+            blocks.append([pending[b]] + drafts)
+        R = sum(ns)
+        r0 = np.concatenate([[0], np.cumsum(ns)]).astype(int)
+        allt = t.tensor(np.concatenate([np.asarray(x, np.int32) for x in blocks]), device="cuda")
+        q = t.softmax(t.tensor(g.standard_normal((R, V)), dtype=t.float32, device="cuda") * 2.0, dim=1)
+        u = t.tensor(g.random(R), dtype=t.float32, device="cuda")
+        lg = t.empty((R, V), dtype=t.float32, device="cuda")
+        p = t.empty((R, V), dtype=t.float32, device="cuda")
+        acc = t.zeros(B, dtype=t.int32, device="cuda")
+        tok = t.zeros(B, dtype=t.int32, device="cuda")
+        evs.evs_round_batch(bat, allt, ns, lg, p if sample else None, q if sample else None,
+                            u if sample else None, 1.0, 4, md, acc, tok)
+        for b in range(B):
+            n = ns[b]
+            tb = t.tensor(blocks[b], dtype=t.int32, device="cuda")
+            lb = t.empty((n, V), dtype=t.float32, device="cuda")
+            pb = t.empty((n, V), dtype=t.float32, device="cuda")
+            qb = q[r0[b]:r0[b] + max(n - 1, 1)].contiguous()
+            ub = u[r0[b]:r0[b] + n].contiguous()
+            ab = t.zeros(1, dtype=t.int32, device="cuda")
+            kb = t.zeros(1, dtype=t.int32, device="cuda")
+            evs.evs_round(ref[b], tb, n, lb, pb if sample else None, qb if sample else None,
+                          ub if sample else None, 1.0, 4, md, ab, kb)
+            assert int(ab.item()) == int(acc[b].item()) and int(kb.item()) == int(tok[b].item()), (rnd, b, ns)
+            assert np.array_equal(to_np(lg[r0[b]:r0[b + 1]]).view(np.uint32), to_np(lb).view(np.uint32)), (rnd, b)
+            if sample:
+                assert np.array_equal(to_np(p[r0[b]:r0[b + 1]]).view(np.uint32), to_np(pb).view(np.uint32))
+            accepted.append(int(ab.item()))
+            pending[b] = int(kb.item())
+    assert max(accepted) > 0  # some drafts were accepted
+    for b in range(B):
+        assert ref[b].book() == bat[b].book()
+        l1 = to_np(_verify(evs, ref[b], [pending[b]], V)[0])
+        l2 = to_np(_verify(evs, bat[b], [pending[b]], V)[0])
+        assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32)), b
+        assert ref[b].check() == 0 and bat[b].check() == 0
