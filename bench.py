@@ -444,15 +444,22 @@ def run_evs(args, rank, world, local):
     value = total_tokens / (t_max_ms / 1e3)
     ms_per_step = t_ms / args.steps
 
-    # dominant kernel: the weight-streaming GEMM, every launch of one step timed alone
+    # dominant kernel: the weight-streaming GEMM.  achieved = its algorithmic
+    # bytes / its launch time as it runs in the step (the step's 129 GEMMs
+    # back to back in one graph, PDL between them, next-weight prefetch),
+    # CUDA events around 10 chains; each launch timed alone is reported beside
     ms, by = evs.evs_profile_gemms(st, n)
     peak, peak_src = load_peaks()
-    g_bytes, g_ms = float(sum(by)), float(sum(ms))
-    achieved = g_bytes / (g_ms / 1e3) / 1e9
+    a_bytes, a_ms = float(sum(by)), float(sum(ms))
+    c_ms, c_bytes, c_launches = evs.evs_profile_gemm_chain(st, n, 10)
+    achieved = c_bytes / (c_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": gemm_traffic(), "kernel": "gemm_tc_kernel", "launches": len(ms),
-                "avg_launch_us": 1e3 * g_ms / len(ms), "bytes_per_launch": g_bytes / len(ms),
-                "peak_source": peak_src}
+                "traffic": gemm_traffic(), "kernel": "gemm_tc_kernel", "launches": c_launches,
+                "avg_launch_us": 1e3 * c_ms / c_launches, "bytes_per_launch": c_bytes / c_launches,
+                "peak_source": peak_src,
+                "timing": "the step's GEMM launches back to back (one graph, PDL, next-weight prefetch), CUDA events",
+                "alone": {"avg_launch_us": 1e3 * a_ms / len(ms), "achieved": a_bytes / (a_ms / 1e3) / 1e9,
+                          "frac": a_bytes / (a_ms / 1e3) / 1e9 / peak}}
     sb = step_bytes(shape, P0 - 1 + n * (args.warmup + args.steps // 2), n)
 
     # snapshot-and-replay baseline: snapshot the recurrent state, verify,

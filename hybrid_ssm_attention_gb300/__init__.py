@@ -300,6 +300,16 @@ def evs_verify_kernel_count(state: State, n: int) -> int:
     return int(lib().evs_verify_kernel_count(state.handle, int(n)))
 
 
+def evs_profile_gemm_chain(state: State, n: int, reps: int = 10, stream=None):
+    """(ms per chain, algorithmic bytes per chain, launches per chain) of the step's GEMMs back to back."""
+    ms = C.c_float()
+    by = C.c_int64()
+    cnt = C.c_int32()
+    _check(lib().evs_profile_gemm_chain(state.handle, int(n), int(reps), C.byref(ms), C.byref(by), C.byref(cnt),
+                                        _stream(stream)), "evs_profile_gemm_chain")
+    return float(ms.value), int(by.value), int(cnt.value)
+
+
 def evs_profile_gemms(state: State, n: int, stream=None):
     """Per-launch (ms, algorithmic bytes) of one verify step's weight GEMMs."""
     cap = 4 * len(state.model.shape.layers) + 1

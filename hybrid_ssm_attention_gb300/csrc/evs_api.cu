@@ -1328,87 +1328,118 @@ extern "C" int evs_op_gemm_static(const void* W, const void* X, int32_t N, int32
 }
 
 // =================================================================== profiling
-extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host, int32_t max_launches,
-                                 int32_t* count, cudaStream_t stream) {
-  if (!s || !ms_host || !bytes_host || !count) return fail(EVS_ERR_ARG, "null argument");
-  if (n < 1 || n > s->m->n_max) return fail(EVS_ERR_ARG, "n out of range");
+namespace {
+
+// One weight GEMM of a verify step as the step launches it (B source and
+// output mode), for the profiling entry points.
+struct GemmCall {
+  const Partials* plan;
+  const CUtensorMap *wm, *xm;
+  const uint8_t* pk;
+  const void *W, *X;
+  int N, K, bsrc, mode;
+};
+
+// The step's GEMMs in order: per layer in, out, gate/up, down; then the head.
+// Outputs go to scratch and residual GEMMs write plain sums (or slots), so
+// the decoding state is untouched.
+std::vector<GemmCall> step_gemms(evs_state* s) {
   const evs_model* m = s->m;
-  const int nl = (int)m->L.size();
-  const int total = 4 * nl + 1;
-  if (max_launches < total) return fail(EVS_ERR_ARG, "need room for %d launches", total);
   const evs_config& c = m->cfg;
-  const int d = c.d_model, F = c.d_ffn, V = c.vocab, dt = c.dtype;
-  const size_t es = esize(dt);
-  std::vector<cudaEvent_t> ev(total + 1);
-  for (auto& e : ev) CUDA_TRY(cudaEventCreate(&e));
-  LaunchCtx Lc{stream, false};
-  // keep the GPU busy while the host enqueues, so events time only the GEMMs
-  CUDA_TRY(launch_busy(Lc, 2000000));
-  int k = 0;
-  int r = EVS_OK;
-  // each GEMM with the B source and output mode the verify step gives it
-  // (outputs go to a scratch buffer and residual GEMMs write plain sums, so
-  // the state is untouched)
-  auto one = [&](const Partials& plan, const CUtensorMap& wm, const uint8_t* pk, const void* W,
-                 const CUtensorMap& xm, const void* X, int N, int K, int bsrc = GEMM_B_TMA,
-                 int mode = GEMM_FINAL) -> int {
-    Partials P = plan;
-    P.wpk = pk;
-    P.bsrc = bsrc;
-    P.Kdim = K;
-    P.ss_in = s->ss;
-    P.ss_tiles = (d + TILE_M - 1) / TILE_M;
-    P.norm_d = d;
-    P.eps = c.norm_eps;
-    P.hout = reinterpret_cast<bf16*>(s->pout);
-    P.h_cols = F;
-    P.ws = s->ws[k & 1];
-    P.cnt = s->cnt;
-    P.mode = mode;
-    P.n = n;
-    P.fin = s->pout;
-    P.fin_ld = N;
-    CUDA_TRY(cudaEventRecord(ev[k], stream));
-    if (m->tc)
-      CUDA_TRY(launch_gemm_tc(Lc, wm, xm, wm, P, K, &s->book->status));  // no prefetch: timed alone
-    else
-      CUDA_TRY(launch_gemm_simt(Lc, dt, W, X, K, P, K));
-    const int64_t in_es = bsrc == GEMM_B_TMA ? (int64_t)es : 4;
-    const int64_t out_b = mode == GEMM_SWIGLU ? (int64_t)n * (N / 2) * 2 : (int64_t)n * N * 4;
-    bytes_host[k] = (int64_t)N * K * es + (int64_t)n * K * in_es + out_b;
-    ++k;
-    return EVS_OK;
-  };
+  const int d = c.d_model, F = c.d_ffn, V = c.vocab;
   const bool fz = m->fuse;
-  // the verify step's output modes: slots for stream-K GEMMs with slot
-  // consumers (residual GEMMs only when unfused), else the plain sums
   auto slots_or = [&](const Partials& P, bool resid, int mode) {
     return m->slots && P.cl == 0 && P.max_cnt <= (resid ? SLOTS_RESID_MAX : SLOTS_MIX_MAX) &&
                    !(resid && (fz || !m->slots_resid))
                ? GEMM_SLOTS
                : mode;
   };
-  for (int i = 0; i < nl && r == EVS_OK; ++i) {
+  std::vector<GemmCall> v;
+  for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
-    const int gu_mode = m->swiglu ? GEMM_SWIGLU : slots_or(m->p_gu, false, GEMM_FINAL);
-    const int in_mode = slots_or(m->p_in, false, GEMM_FINAL);
-    if (fz && i > 0)
-      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xf, s->X, 3 * d, d, GEMM_B_NORM, in_mode);
-    else
-      r = one(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, 3 * d, d, GEMM_B_TMA, in_mode);
-    if (r == EVS_OK)
-      r = one(m->p_out, w.m_out, w.pk_out, w.w_out, s->m_g, s->g, d, d, GEMM_B_TMA,
-              slots_or(m->p_out, true, GEMM_FINAL));
-    if (r == EVS_OK)
-      r = fz ? one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xf, s->X, 2 * F, d, GEMM_B_NORM, gu_mode)
-             : one(m->p_gu, w.m_gu, w.pk_gu, w.w_gu, s->m_xn, s->xn, 2 * F, d, GEMM_B_TMA, gu_mode);
-    if (r == EVS_OK)
-      r = one(m->p_down, w.m_down, w.pk_down, w.w_down, s->m_h, s->h, d, F, GEMM_B_TMA,
-              slots_or(m->p_down, true, GEMM_FINAL));
+    const bool nin = fz && i > 0;
+    v.push_back({&m->p_in, &w.m_in, nin ? &s->m_xf : &s->m_xn, w.pk_in, w.w_in, nin ? (const void*)s->X : s->xn,
+                 3 * d, d, nin ? GEMM_B_NORM : GEMM_B_TMA, slots_or(m->p_in, false, GEMM_FINAL)});
+    v.push_back({&m->p_out, &w.m_out, &s->m_g, w.pk_out, w.w_out, s->g, d, d, GEMM_B_TMA,
+                 slots_or(m->p_out, true, GEMM_FINAL)});
+    v.push_back({&m->p_gu, &w.m_gu, fz ? &s->m_xf : &s->m_xn, w.pk_gu, w.w_gu, fz ? (const void*)s->X : s->xn,
+                 2 * F, d, fz ? GEMM_B_NORM : GEMM_B_TMA,
+                 m->swiglu ? GEMM_SWIGLU : slots_or(m->p_gu, false, GEMM_FINAL)});
+    v.push_back({&m->p_down, &w.m_down, &s->m_h, w.pk_down, w.w_down, s->h, d, F, GEMM_B_TMA,
+                 slots_or(m->p_down, true, GEMM_FINAL)});
   }
-  if (r == EVS_OK)
-    r = m->fuse ? one(m->p_head, m->m_head, m->pk_head, m->head, s->m_xf, s->X, V, d, GEMM_B_NORM)
-                : one(m->p_head, m->m_head, m->pk_head, m->head, s->m_xn, s->xn, V, d);
+  v.push_back({&m->p_head, &m->m_head, fz ? &s->m_xf : &s->m_xn, m->pk_head, m->head,
+               fz ? (const void*)s->X : s->xn, V, d, fz ? GEMM_B_NORM : GEMM_B_TMA, GEMM_FINAL});
+  return v;
+}
+
+// Launches call k of calls; with chain, it warms L2 with the first units of
+// call k + 1 (the next weight matrix) as the verify step does.
+int launch_profiled(evs_state* s, const std::vector<GemmCall>& calls, size_t k, int n, bool chain,
+                    const LaunchCtx& Lc, int64_t* bytes) {
+  const evs_model* m = s->m;
+  const evs_config& c = m->cfg;
+  const GemmCall& g = calls[k];
+  const size_t es = esize(c.dtype);
+  Partials P = *g.plan;
+  P.nt = 1;
+  P.wpk = g.pk;
+  P.bsrc = g.bsrc;
+  P.Kdim = g.K;
+  P.ss_in = s->ss;
+  P.ss_tiles = (c.d_model + TILE_M - 1) / TILE_M;
+  P.norm_d = c.d_model;
+  P.eps = c.norm_eps;
+  P.hout = reinterpret_cast<bf16*>(s->pout);
+  P.h_cols = c.d_ffn;
+  P.ws = s->ws[k & 1];
+  P.cnt = s->cnt;
+  P.mode = g.mode;
+  P.n = n;
+  P.fin = s->pout;
+  P.fin_ld = g.N;
+  const CUtensorMap* nmap = g.wm;
+  if (chain) {
+    const GemmCall& nx = calls[(k + 1) % calls.size()];
+    nmap = nx.wm;
+    P.nwpk = nx.pk;
+    P.pf_units = s->pf_units;
+    P.nG = nx.plan->G;
+    P.nKB = nx.plan->KB;
+    P.nU = nx.plan->U;
+    P.ncl = nx.plan->cl;
+  }
+  if (m->tc)
+    CUDA_TRY(launch_gemm_tc(Lc, *g.wm, *g.xm, *nmap, P, g.K, &s->book->status));
+  else
+    CUDA_TRY(launch_gemm_simt(Lc, c.dtype, g.W, g.X, g.K, P, g.K));
+  const int64_t in_es = g.bsrc == GEMM_B_TMA ? (int64_t)es : 4;
+  const int64_t out_b = g.mode == GEMM_SWIGLU ? (int64_t)n * (g.N / 2) * 2 : (int64_t)n * g.N * 4;
+  *bytes = (int64_t)g.N * g.K * es + (int64_t)n * g.K * in_es + out_b;
+  return EVS_OK;
+}
+
+}  // namespace
+
+extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host, int32_t max_launches,
+                                 int32_t* count, cudaStream_t stream) {
+  if (!s || !ms_host || !bytes_host || !count) return fail(EVS_ERR_ARG, "null argument");
+  if (n < 1 || n > s->m->n_max) return fail(EVS_ERR_ARG, "n out of range");
+  const std::vector<GemmCall> calls = step_gemms(s);
+  const int total = (int)calls.size();
+  if (max_launches < total) return fail(EVS_ERR_ARG, "need room for %d launches", total);
+  std::vector<cudaEvent_t> ev(total + 1);
+  for (auto& e : ev) CUDA_TRY(cudaEventCreate(&e));
+  LaunchCtx Lc{stream, false};
+  // keep the GPU busy while the host enqueues, so events time only the GEMMs
+  CUDA_TRY(launch_busy(Lc, 2000000));
+  int r = EVS_OK;
+  int k = 0;
+  for (; k < total && r == EVS_OK; ++k) {
+    cudaError_t e = cudaEventRecord(ev[k], stream);
+    if (e != cudaSuccess) r = fail(EVS_ERR_CUDA, "profiling events: %s", cudaGetErrorString(e));
+    if (r == EVS_OK) r = launch_profiled(s, calls, k, n, false, Lc, &bytes_host[k]);
+  }
   if (r == EVS_OK) {
     cudaError_t e = cudaEventRecord(ev[k], stream);
     if (e == cudaSuccess) e = cudaEventSynchronize(ev[k]);
@@ -1418,6 +1449,55 @@ extern "C" int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_
   for (auto& e : ev) cudaEventDestroy(e);
   *count = k;
   return r;
+}
+
+extern "C" int evs_profile_gemm_chain(evs_state* s, int32_t n, int32_t reps, float* ms_per_chain,
+                                      int64_t* bytes_per_chain, int32_t* launches, cudaStream_t stream) {
+  if (!s || !ms_per_chain || !bytes_per_chain || !launches) return fail(EVS_ERR_ARG, "null argument");
+  if (n < 1 || n > s->m->n_max || reps < 1 || reps > 1000) return fail(EVS_ERR_ARG, "n or reps out of range");
+  const std::vector<GemmCall> calls = step_gemms(s);
+  // the chain as one graph with programmatic dependent launch between GEMMs
+  int64_t bytes = 0;
+  const long long before = g_launches.load();
+  CUDA_TRY(cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeRelaxed));
+  LaunchCtx Lc{s->cap, s->pdl};
+  int r = EVS_OK;
+  for (size_t k = 0; k < calls.size() && r == EVS_OK; ++k) {
+    int64_t b = 0;
+    r = launch_profiled(s, calls, k, n, true, Lc, &b);
+    bytes += b;
+  }
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(s->cap, &graph);
+  g_launches -= g_launches.load() - before;  // captured, not launched: counted per graph launch below
+  if (r != EVS_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return r;
+  }
+  if (e != cudaSuccess) return fail(EVS_ERR_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(EVS_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaGraphLaunch(exec, stream);  // warm-up
+  if (e == cudaSuccess) e = cudaEventRecord(e0, stream);
+  for (int i = 0; i < reps && e == cudaSuccess; ++i) e = cudaGraphLaunch(exec, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaGraphExecDestroy(exec);
+  if (e != cudaSuccess) return fail(EVS_ERR_CUDA, "chain timing: %s", cudaGetErrorString(e));
+  count_launch((long long)(reps + 3) * (long long)calls.size());
+  *ms_per_chain = ms / reps;
+  *bytes_per_chain = bytes;
+  *launches = (int32_t)calls.size();
+  return EVS_OK;
 }
 
 #ifdef EVS_TRACE

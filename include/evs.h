@@ -387,6 +387,16 @@ int evs_selftest_wait_timeout(int32_t* status_dev, int64_t limit_ns, cudaStream_
  * workspaces; leaves the decoding state unchanged. */
 int evs_profile_gemms(evs_state* s, int32_t n, float* ms_host, int64_t* bytes_host,
                       int32_t max_launches, int32_t* count, cudaStream_t stream);
+/* The same GEMMs as they run in a verify step, back to back: one CUDA
+ * graph of all 4 * n_layers + 1 launches with programmatic dependent launch
+ * between them and each GEMM warming L2 with the next weight matrix's first
+ * units (the step without its small kernels in between).  Three warm-up
+ * launches of the graph, then reps (1..1000) timed with CUDA events on
+ * stream; synchronous.  *ms_per_chain = average time of one chain,
+ * *bytes_per_chain = its algorithmic bytes, *launches = GEMMs per chain.
+ * Uses the state's workspaces; leaves the decoding state unchanged. */
+int evs_profile_gemm_chain(evs_state* s, int32_t n, int32_t reps, float* ms_per_chain,
+                           int64_t* bytes_per_chain, int32_t* launches, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- misc */
 const char* evs_last_error(void);

@@ -593,3 +593,30 @@ def test_round_batch_equals_separate_rounds_bitwise(mode):
         l2 = to_np(_verify(evs, bat[b], [pending[b]], V)[0])
         assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32)), b
         assert ref[b].check() == 0 and bat[b].check() == 0
+
+
+@pytest.mark.gpu
+def test_gemm_profiling_leaves_state_unchanged():
+    # evs_profile_gemms (each launch alone) and evs_profile_gemm_chain (the
+    # step's GEMMs back to back in one graph) report the same algorithmic
+    # bytes and leave the decoding state as it was: the next verify's logits
+    # equal those of an untouched copy bit for bit.
+    import hybrid_ssm_attention_gb300 as evs
+    shape = small_shape()
+    m = evs.Model(shape, synth.make_weights(shape, 53))
+    V, nb = shape.vocab, shape.n_block
+    a, b = evs.State(m, 256), evs.State(m, 256)
+    pr = [int(x) for x in synth.prompt(shape, 53, 2 * nb)]
+    for st in (a, b):
+        for s0 in range(0, len(pr), nb):
+            _verify(evs, st, pr[s0:s0 + nb], V)
+            evs.evs_commit(st, len(pr[s0:s0 + nb]))
+    ms, by = evs.evs_profile_gemms(a, nb)
+    c_ms, c_by, c_n = evs.evs_profile_gemm_chain(a, nb, 3)
+    assert c_n == len(by) == 4 * len(shape.layers) + 1
+    assert c_by == sum(by) and c_ms > 0 and all(x > 0 for x in ms)
+    nxt = [int(x) for x in synth.prompt(shape, 54, nb)]
+    l1 = to_np(_verify(evs, a, nxt, V)[0])
+    l2 = to_np(_verify(evs, b, nxt, V)[0])
+    assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32))
+    assert a.book() == b.book() and a.check() == 0
