@@ -116,16 +116,19 @@ __global__ void __launch_bounds__(256)
     const int p = base + q;
     wreg[q] = (p >= 0 && p < rows) ? ext_s[p * 32 + lane] : 0.f;
   }
+  // all NTOK rows in one block so the per-row FMA chains interleave (rows
+  // past the block read zero window values and are not stored)
+  float acc[NTOK];
 #pragma unroll
   for (int t = 0; t < NTOK; ++t) {
-    if (t < n) {
-      float acc = 0.f;
+    acc[t] = 0.f;
 #pragma unroll
-      for (int q = 0; q < JT; ++q)
-        if (j0 + q < Lf) acc = fmaf(hreg[q], wreg[t - q + JT - 1], acc);
-      part_s[(warp * n + t) * 32 + lane] = acc;
-    }
+    for (int q = 0; q < JT; ++q)
+      if (j0 + q < Lf) acc[t] = fmaf(hreg[q], wreg[t - q + JT - 1], acc[t]);
   }
+#pragma unroll
+  for (int t = 0; t < NTOK; ++t)
+    if (t < n) part_s[(warp * n + t) * 32 + lane] = acc[t];
   __syncthreads();
   for (int t = warp; t < n; t += NW) {
     float y = 0.f;
