@@ -206,7 +206,7 @@ class Model:
         sh, ar = self.shape, self.ar
         d, F, eps = sh.d_model, sh.d_ffn, sh.norm_eps
         xn = ar.r(rmsnorm(x, eps, ar))
-        u = ar.r(M["w_in"] @ xn)
+        u = ar.r(ar.mv(M["w_in"], xn))
         if M["kind"] == ATT:
             g = ar.r(self.attn_step(M, L, u, pos))
         else:
@@ -214,15 +214,15 @@ class Model:
             z = b * v
             y = self.fir_step(M, L, z) if M["kind"] in (SE, MR) else self.iir_step(M, L, z)
             g = ar.r(a * y)
-        x = x + M["w_out"] @ g
+        x = x + ar.mv(M["w_out"], g)
         xn = ar.r(rmsnorm(x, eps, ar))
-        gu = M["w_gu"] @ xn
+        gu = ar.mv(M["w_gu"], xn)
         h = ar.r(silu(gu[:F], ar) * gu[F:])
-        return x + M["w_down"] @ h
+        return x + ar.mv(M["w_down"], h)
 
     def head(self, x):
         """Final RMSNorm and LM head."""
-        return self.lm_head @ self.ar.r(rmsnorm(x, self.shape.norm_eps, self.ar))
+        return self.ar.mv(self.lm_head, self.ar.r(rmsnorm(x, self.shape.norm_eps, self.ar)))
 
     def step(self, st: State, token: int):
         """One native decode step: consumes ``token`` at position st.pos,

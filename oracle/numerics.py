@@ -32,12 +32,35 @@ class Arith:
         gated mixer output, attention output, MLP hidden), the in-projection
         outputs a|b|v and q|k|v, and the rotated q and k (k is what the KV
         cache holds).  Weights are bf16 values already.
+
+    ``order`` picks the summation order of the matrix-vector products:
+    ``"blas"`` (default) is numpy's ``W @ x``; ``"k64_reversed"`` forms the
+    partial products of 64-column blocks of W (each by ``W @ x``) and adds
+    them one at a time from the last block to the first.  Both are valid
+    orders of the same sum in the arithmetic dtype; comparing them measures
+    how far rounding alone moves the oracle's own results.
     """
 
-    def __init__(self, dtype=np.float64, bf16_points: bool = False):
+    ORDERS = ("blas", "k64_reversed")
+
+    def __init__(self, dtype=np.float64, bf16_points: bool = False, order: str = "blas"):
+        if order not in self.ORDERS:
+            raise ValueError(f"order must be one of {self.ORDERS}")
         self.dt = np.dtype(dtype)
         self.bf16 = bool(bf16_points)
         self.cdt = np.complex128 if self.dt == np.float64 else np.complex64
+        self.order = order
+
+    def mv(self, W, x):
+        """W [N][K] times x [K] in the arithmetic dtype, in this mode's order."""
+        if self.order == "blas":
+            return W @ x
+        K = W.shape[1]
+        acc = None
+        for b in reversed(range((K + 63) // 64)):
+            part = W[:, 64 * b:64 * b + 64] @ x[64 * b:64 * b + 64]
+            acc = part if acc is None else acc + part
+        return acc.astype(self.dt, copy=False)
 
     def r(self, x):
         """A bf16 storage point (identity unless bf16_points)."""

@@ -5,10 +5,15 @@ bf16 storage points; tolerance 2e-2 of max |ref| on logits.
 * small 6-layer bf16 stack (d 256): prefill, block verify, commit; GPU
   speculative == GPU native, bitwise, at every emitted position.
 * 7B-shaped stack (32 layers, d 4096, F 11008, vocab 512, gamma 12), at
-  full size from a synthesised state at context 1024: teacher-forced block
-  logits vs the oracle's 13 native steps; greedy decisions compared where
-  the oracle's top-2 gap exceeds 4x the observed logit error (non-ties).
+  full size from a synthesised state at context 1024: every layer's update
+  and retained state teacher-forced against the oracle (2e-2); free-running
+  logits within twice the oracle's own summation-order spread; greedy
+  decisions compared where the oracle's top-2 gap exceeds 4x the observed
+  logit error (non-ties).
 """
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -356,11 +361,16 @@ def test_7b_block_verify_full_size():
     residual stream entering layer l must reproduce the GPU's layer update
     (X_{l+1} - X_l) within 2e-2 of its max, and the per-position state the
     layer retained (FIR windows, IIR states, appended K/V) within 2e-2; the
-    head applied to the GPU's final stream reproduces the GPU logits.  The
-    free-running comparison (oracle's own 32 layers) compounds bf16 rounding
-    flips through depth (a 1e-6 input perturbation alone moves the oracle's
-    logits by ~2e-3), so it is held to 5e-2 and to identical greedy choices
-    wherever the oracle's top-2 gap exceeds 4x the observed error."""
+    head applied to the GPU's final stream reproduces the GPU logits.
+
+    The free-running comparison (the oracle's own 32 layers) compounds bf16
+    rounding flips through depth.  Its bound comes from the oracle alone:
+    tests/golden/spread_7b.json records how far the oracle's logits move on
+    this very block when only the summation order of its matrix-vector
+    products changes (two valid float32 evaluations, 2.4e-2).  The GPU is a
+    third valid order, so it is held to twice that spread (the triangle
+    inequality through the second oracle order) and to identical greedy
+    choices wherever the oracle's top-2 gap exceeds 4x the observed error."""
     import hybrid_ssm_attention_gb300 as evs
     from oracle.model import Model as OModel
     from oracle.numerics import Arith
@@ -413,8 +423,13 @@ def test_7b_block_verify_full_size():
     ost = om.state_from(Sf, P + 64)
     ref, _ = om.verify(ost, toks)
     err = rel_err(got, ref)
-    print(f"per-layer teacher-forced max err {max(worst):.3e}; free-running logits err {err:.3e}")
-    assert err <= 5e-2, err
+    spread = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                         "spread_7b.json")))
+    assert spread["workload"]["block_tokens"] == toks and spread["workload"]["weights_seed"] == 3
+    bound = 2 * spread["rel_err_logits"]
+    print(f"per-layer teacher-forced max err {max(worst):.3e}; free-running logits err {err:.3e} "
+          f"(oracle order spread {spread['rel_err_logits']:.3e}, bound {bound:.3e})")
+    assert err <= bound, (err, bound)
     gap_tol = 4 * np.abs(got - ref).max()
     for i in range(n):
         srt = np.sort(ref[i])

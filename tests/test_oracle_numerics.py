@@ -42,3 +42,21 @@ def test_arith_points():
     assert a32.r(1.0 + 2.0 ** -9) == 1.0
     a64 = Arith(np.float64)
     assert a64.r(1.0 + 2.0 ** -30) == 1.0 + 2.0 ** -30
+
+
+def test_matvec_orders_agree():
+    # the two summation orders are the same sum: exact on integer-valued
+    # data (every partial sum representable), and within float64 rounding
+    # of each other on random data
+    g = np.random.default_rng(4)
+    W = g.integers(-50, 50, size=(37, 200)).astype(np.float64)
+    x = g.integers(-50, 50, size=200).astype(np.float64)
+    a, b = Arith(np.float64), Arith(np.float64, order="k64_reversed")
+    assert np.array_equal(a.mv(W, x), b.mv(W, x))
+    assert np.array_equal(a.mv(W, x), np.array([sum(int(W[i, k]) * int(x[k]) for k in range(200))
+                                                for i in range(37)], dtype=np.float64))
+    W = g.standard_normal((64, 300))
+    x = g.standard_normal(300)
+    np.testing.assert_allclose(b.mv(W, x), a.mv(W, x), rtol=1e-12, atol=1e-12)
+    c = Arith(np.float32, order="k64_reversed")
+    assert c.mv(W.astype(np.float32), x.astype(np.float32)).dtype == np.float32
