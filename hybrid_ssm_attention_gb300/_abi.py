@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(HERE, "libevs.so")
 
 EVS_OK, EVS_ERR_ARG, EVS_ERR_STATE, EVS_ERR_CAPACITY = 0, 1, 2, 3
 EVS_ERR_OOM, EVS_ERR_CUDA, EVS_ERR_DEVICE, EVS_ERR_UNSUPPORTED = 4, 5, 6, 7
-EVS_DEV_BAD_TOKEN, EVS_DEV_KV_OVERFLOW, EVS_DEV_BAD_KEEP, EVS_DEV_TIMEOUT = 1, 2, 4, 8
+EVS_DEV_BAD_TOKEN, EVS_DEV_KV_OVERFLOW, EVS_DEV_BAD_KEEP, EVS_DEV_TIMEOUT, EVS_DEV_BAD_PROBS = 1, 2, 4, 8, 16
 EVS_F32, EVS_BF16 = 0, 1
 EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_LAYER_ATTN = 0, 1, 2
 EVS_GREEDY, EVS_SAMPLE = 0, 1

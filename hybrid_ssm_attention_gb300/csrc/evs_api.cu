@@ -402,7 +402,7 @@ int enqueue_round(evs_state* s, const int32_t* tokens, int n, float* logits, con
     CUDA_TRY(launch_probs(Lc, logits, n, V, r.T, r.top_k, r.p));
     P = r.p;
   }
-  CUDA_TRY(launch_accept(Lc, P, r.q, r.drafts, r.u, n, V, r.mode, r.acc, r.otok));
+  CUDA_TRY(launch_accept(Lc, P, r.q, r.drafts, r.u, n, V, r.mode, r.acc, r.otok, s->book));
   CUDA_TRY(launch_commit(Lc, s->book, 0, r.acc, 0));
   return EVS_OK;
 }
@@ -419,9 +419,9 @@ int enqueue_round_batch(evs_state* const* states, const SeqRows& sr, const int32
     CUDA_TRY(launch_probs(Lc, logits, sr.row0[sr.nseq], V, r.T, r.top_k, r.p));
     P = r.p;
   }
-  CUDA_TRY(launch_accept_batch(Lc, P, r.q, r.drafts, r.u, sr, V, r.mode, r.acc, r.otok));
   SeqPtrs<evs_book*> books{};
   for (int b = 0; b < sr.nseq; ++b) books.p[b] = states[b]->book;
+  CUDA_TRY(launch_accept_batch(Lc, P, r.q, r.drafts, r.u, sr, V, r.mode, r.acc, r.otok, books));
   CUDA_TRY(launch_commit_batch(Lc, books, sr.nseq, r.acc));
   return EVS_OK;
 }
@@ -1324,6 +1324,13 @@ extern "C" int evs_op_gemm_static(const void* W, const void* X, int32_t N, int32
   } else {
     CUDA_TRY(launch_gemm_simt(Lc, dtype, W, X, K, P, K));
   }
+  // The flag lives in the library's array, out of the caller's reach: read
+  // it back here (a 4-byte copy into this stack frame, no allocation) so a
+  // pipeline wait that gave up is reported by this call.
+  int flag = 0;
+  CUDA_TRY(cudaMemcpyAsync(&flag, err_flag, sizeof(int), cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  if (flag) return fail(EVS_ERR_DEVICE, "device status 0x%x (a GEMM pipeline wait gave up; Y is incomplete)", flag);
   return EVS_OK;
 }
 

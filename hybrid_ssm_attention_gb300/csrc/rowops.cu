@@ -220,40 +220,117 @@ __global__ void mlp_act_kernel(const __grid_constant__ Src gu, int F, int il, T*
   h[(size_t)t * F + j] = from_f<T>(silu_f(gt) * up);
 }
 
-// One CTA per row.  top-k by rank: entry j is kept iff fewer than k entries
-// beat it (larger value, or equal value at a lower index).
+// Orderable key of a float: a larger value has a larger key; -0 and +0
+// share one key (they compare equal).
+__device__ __forceinline__ unsigned int ord_key(float x) {
+  if (x == 0.f) x = 0.f;
+  const unsigned int b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Inclusive prefix sum of v over the block in thread order (blockDim.x a
+// multiple of 32, at most 1024); scratch >= 32 ints.
+__device__ int block_scan_incl(int v, int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += scratch[w];
+  __syncthreads();
+  return v + base;
+}
+
+// One CTA per row.  top-k: the k-th largest logit is found by radix select
+// over the four bytes of its orderable key (a 256-bin histogram per byte,
+// O(V) work); entries above it are kept, and of the entries equal to it the
+// lowest-indexed ones fill the remaining places (ties to the lower index).
 __global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, float T, int k, float* p) {
   extern __shared__ float sm[];
   __shared__ float scratch[32];
+  __shared__ int iscr[32];
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned int s_prefix;
+  __shared__ int s_remain, s_eq;
   float* l_s = sm;        // [V]
   float* w_s = sm + V;    // [V]
-  const int t = blockIdx.x;
+  const int t = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
   pdl_trigger();
   pdl_wait();
-  for (int j = threadIdx.x; j < V; j += blockDim.x) l_s[j] = logits[(size_t)t * V + j];
+  for (int j = tid; j < V; j += nth) l_s[j] = logits[(size_t)t * V + j];
   __syncthreads();
   const bool use_k = k > 0 && k < V;
-  float mx = -INFINITY;
-  for (int j = threadIdx.x; j < V; j += blockDim.x) {
-    bool keep = true;
-    if (use_k) {
-      const float lj = l_s[j];
-      int rank = 0;
-      for (int l = 0; l < V; ++l) rank += (l_s[l] > lj) || (l_s[l] == lj && l < j);
-      keep = rank < k;
+  unsigned int kth = 0;  // key of the k-th largest entry (0: keep every entry)
+  int need_eq = 0, n_eq = 0;
+  if (use_k) {
+    unsigned int prefix = 0, mask = 0;
+    int remain = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += nth) hist[i] = 0;
+      __syncthreads();
+      for (int j = tid; j < V; j += nth) {
+        const unsigned int key = ord_key(l_s[j]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        // the digit holding the remain-th largest of the entries matching prefix
+        int acc = 0, D = 255;
+        for (; D > 0; --D) {
+          if (acc + (int)hist[D] >= remain) break;
+          acc += (int)hist[D];
+        }
+        s_prefix = prefix | ((unsigned int)D << shift);
+        s_remain = remain - acc;
+        s_eq = (int)hist[D];
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      remain = s_remain;
+      mask |= 255u << shift;
+      __syncthreads();
     }
-    w_s[j] = keep ? 1.f : 0.f;
-    if (keep) mx = fmaxf(mx, l_s[j]);
+    kth = prefix;
+    need_eq = remain;  // entries equal to kth to keep (k - remain entries lie above it)
+    n_eq = s_eq;       // entries equal to kth in all
+  }
+  float mx = -INFINITY;
+  if (!use_k || need_eq == n_eq) {
+    // no tie straddles the cut: keep every entry at or above the k-th key
+    for (int j = tid; j < V; j += nth) {
+      const bool keep = !use_k || ord_key(l_s[j]) >= kth;
+      w_s[j] = keep ? 1.f : 0.f;
+      if (keep) mx = fmaxf(mx, l_s[j]);
+    }
+  } else {
+    // ties at the cut: rank the equal entries by index (thread i owns the
+    // contiguous index range [i*seg, (i+1)*seg), ranks by a block scan)
+    const int seg = (V + nth - 1) / nth;
+    const int j0 = min(V, tid * seg), j1 = min(V, j0 + seg);
+    int c = 0;
+    for (int j = j0; j < j1; ++j) c += ord_key(l_s[j]) == kth;
+    int rank = block_scan_incl(c, iscr) - c;  // equal entries before this range
+    for (int j = j0; j < j1; ++j) {
+      const unsigned int key = ord_key(l_s[j]);
+      bool keep = key > kth;
+      if (key == kth) keep = rank++ < need_eq;
+      w_s[j] = keep ? 1.f : 0.f;
+      if (keep) mx = fmaxf(mx, l_s[j]);
+    }
   }
   mx = block_reduce(mx, MaxF(), scratch);
   float sum = 0.f;
-  for (int j = threadIdx.x; j < V; j += blockDim.x) {
+  for (int j = tid; j < V; j += nth) {
     const float w = w_s[j] != 0.f ? expf((l_s[j] - mx) / T) : 0.f;
     w_s[j] = w;
     sum += w;
   }
   sum = block_reduce(sum, AddF(), scratch);
-  for (int j = threadIdx.x; j < V; j += blockDim.x) p[(size_t)t * V + j] = w_s[j] / sum;
+  for (int j = tid; j < V; j += nth) p[(size_t)t * V + j] = w_s[j] / sum;
 }
 
 // argmax over a row by one warp, same ties rule (lowest index); all-NaN -> 0
@@ -314,9 +391,12 @@ __device__ int ladder_find(const unsigned int* W, int V, unsigned long long thr,
 // One CTA per sequence b of sr: its rows r0 = sr.row0[b] .. + n - 1 of p,
 // q, drafts and u (row r0 + i of q / drafts: draft i + 1); results to
 // out_a[b], out_tok[b].
+// books.p[b] (may be null): sequence b's bookkeeping, whose status gets
+// EVS_DEV_BAD_PROBS when a sampled row has no integer mass.
 __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float* q, const int32_t* drafts,
                                                      const float* u, const __grid_constant__ SeqRows sr, int V,
-                                                     int mode, int32_t* out_a, int32_t* out_tok) {
+                                                     int mode, int32_t* out_a, int32_t* out_tok,
+                                                     const __grid_constant__ SeqPtrs<evs_book*> books) {
   extern __shared__ unsigned int Wsm[];  // [V], then s_arg[n], s_ok[n]
   __shared__ unsigned long long us[256];
   __shared__ int found;
@@ -375,9 +455,23 @@ __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float
       S = block_reduce(loc, AddU(), us);
     }
     __syncthreads();
-    const unsigned long long U = (unsigned long long)(unsigned int)(u[gamma] * 16777216.0f);
+    // floor(u 2^24), held below 2^24 so that u = 1 (outside [0, 1)) still
+    // lands on the last entry with mass
+    const unsigned long long U =
+        min((unsigned long long)(unsigned int)(u[gamma] * 16777216.0f), 16777215ull);
     const unsigned long long thr = (U * S) >> 24;
     token = ladder_find(Wsm, V, thr, us, &found);
+    if (token < 0) {
+      // neither the residual nor p_a has integer mass (a NaN or all-zero
+      // row): the row's argmax stands in, and the state is flagged
+      if (warp == 0) {
+        const int am = warp_argmax(pa, V);
+        if (lane == 0) found = am;
+      }
+      __syncthreads();
+      token = found;
+      if (threadIdx.x == 0 && books.p[b]) set_status(books.p[b], EVS_DEV_BAD_PROBS);
+    }
   }
   if (threadIdx.x == 0) {
     out_a[0] = a;
@@ -490,12 +584,13 @@ cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, 
 }
 
 cudaError_t launch_accept(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
-                          const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok) {
-  return launch_accept_batch(L, p, q, drafts, u, one_seq(n), V, mode, acc, tok);
+                          const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok, evs_book* book) {
+  return launch_accept_batch(L, p, q, drafts, u, one_seq(n), V, mode, acc, tok, one_ptr(book));
 }
 
 cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
-                                const float* u, const SeqRows& sr, int V, int mode, int32_t* acc, int32_t* tok) {
+                                const float* u, const SeqRows& sr, int V, int mode, int32_t* acc, int32_t* tok,
+                                const SeqPtrs<evs_book*>& books) {
   int nmax = 0;
   for (int b = 0; b < sr.nseq; ++b) nmax = std::max(nmax, sr.row0[b + 1] - sr.row0[b]);
   const size_t smem = sizeof(unsigned int) * V + 2 * sizeof(int) * nmax;
@@ -504,7 +599,7 @@ cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float*
     cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch(L, accept_kernel, dim3(sr.nseq), dim3(256), smem, p, q, drafts, u, sr, V, mode, acc, tok);
+  return launch(L, accept_kernel, dim3(sr.nseq), dim3(256), smem, p, q, drafts, u, sr, V, mode, acc, tok, books);
 }
 
 cudaError_t launch_commit_batch(const LaunchCtx& L, const SeqPtrs<evs_book*>& books, int nseq, const int32_t* acc) {

@@ -64,7 +64,9 @@ enum {
   EVS_DEV_BAD_TOKEN = 1,   /* a token id outside [0, vocab) */
   EVS_DEV_KV_OVERFLOW = 2, /* an append past ctx_max */
   EVS_DEV_BAD_KEEP = 4,    /* commit keep outside [0, pending n] */
-  EVS_DEV_TIMEOUT = 8      /* a bounded pipeline wait gave up */
+  EVS_DEV_TIMEOUT = 8,     /* a bounded pipeline wait gave up */
+  EVS_DEV_BAD_PROBS = 16   /* a sampled row had no mass (NaN or all entries below 2^-24):
+                              its argmax was emitted instead (evs_round / evs_round_batch) */
 };
 
 enum { EVS_F32 = 0, EVS_BF16 = 1 };
@@ -259,7 +261,11 @@ int evs_probs(const float* logits_dev, int32_t n, int32_t V, float T,
  * sample((p_a - q_{a+1})^+, u_{n-1}) (falls back to p_a if that residual has
  * no integer mass); if all accepted a = n-1 and the token is argmax p_a /
  * sample(p_a, u_{n-1}).  sample(w,u) is the inverse CDF over integer weights
- * floor(w_j 2^24): exact and independent of summation order.
+ * floor(w_j 2^24): exact and independent of summation order.  A uniform
+ * of 1 or more is taken as the largest float32 below 1.  A row with no
+ * integer mass at all (NaN or all entries below 2^-24, never a valid
+ * distribution) yields its argmax instead; evs_round / evs_round_batch
+ * then also set EVS_DEV_BAD_PROBS in the state's status.
  * Writes out_accepted_dev[0] = a and out_token_dev[0] = token. */
 int evs_accept(const float* p_dev, const float* q_dev, const int32_t* drafts_dev,
                const float* u_dev, int32_t n, int32_t V, int32_t mode,
@@ -342,16 +348,22 @@ int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max, int64_t ct
 int evs_op_commit(evs_book* book_dev, int32_t keep, int32_t n, cudaStream_t stream);
 /* Skinny GEMM Y[n][N] = X[n][K] W^T (weight-streaming path; tensor cores
  * for bf16).  W [N][K], X [n][K] storage dtype, n <= 16; Y float32.
- * scratch: evs_op_gemm_scratch_bytes. */
+ * scratch: evs_op_gemm_scratch_bytes.  Synchronizes stream once before the
+ * launch (slot-table upload); the GEMM itself runs asynchronously.  The
+ * int at byte offset evs_op_gemm_scratch_bytes(N, K, dtype) - 256 of
+ * scratch is the launch's device status: zeroed before the launch, it holds
+ * EVS_DEV_TIMEOUT afterwards if a bounded pipeline wait gave up (Y is then
+ * incomplete); the caller reads it after the stream completes. */
 size_t evs_op_gemm_scratch_bytes(int32_t N, int32_t K, int32_t dtype);
 int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
                 int32_t dtype, float* y_dev, void* scratch_dev, size_t scratch_bytes,
                 cudaStream_t stream);
 /* The same GEMM without caller scratch: an engineering entry point with no
  * counterpart in the pages.  Same arguments (minus the scratch), layout,
- * results and errors as evs_op_gemm, but it allocates no device memory: its
- * partial slots, slot table, arrival counters and error flag live in one
- * library-owned device array of EVS_OP_GEMM_STATIC_SCRATCH_BYTES per device.
+ * results and argument errors as evs_op_gemm, but it allocates no device
+ * memory: its partial slots, slot table, arrival counters and error flag
+ * live in one library-owned device array of EVS_OP_GEMM_STATIC_SCRATCH_BYTES
+ * per device.
  * It serves callers that must not allocate on their path (a serving loop
  * that forbids allocation once running; a plug-in whose host framework owns
  * all device memory).  A shape whose scratch need (evs_op_gemm_scratch_bytes)
@@ -359,9 +371,12 @@ int evs_op_gemm(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int3
  * array's address is looked up on the first call on each device: make that
  * call outside stream capture.  Each call clears the counters and the error
  * flag with memsets and synchronizes `stream` after uploading the slot
- * table, as evs_op_gemm does.  Calls share the array: calls that overlap in
- * time on one device (other streams or host threads) race, so the caller
- * serializes them. */
+ * table, as evs_op_gemm does.  Because the device status sits in the
+ * library's array, the call also waits for the GEMM and reads the status
+ * back (synchronous): a bounded pipeline wait that gave up returns
+ * EVS_ERR_DEVICE (Y incomplete).  Calls share the array: calls that
+ * overlap in time on one device (other streams or host threads) race, so
+ * the caller serializes them. */
 #define EVS_OP_GEMM_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
 int evs_op_gemm_static(const void* w_dev, const void* x_dev, int32_t N, int32_t K, int32_t n,
                        int32_t dtype, float* y_dev, cudaStream_t stream);
