@@ -244,6 +244,15 @@ def draft_uniforms(seed: int, rounds: int, gamma: int) -> np.ndarray:
     return g.random((rounds, gamma))
 
 
+def logit_noise(seed: int, rounds: int, gamma: int, vocab: int, std: float = 0.5) -> np.ndarray:
+    """Noise of the noise drafter: float32 [rounds][gamma][vocab] ~ N(0, std)
+    (std is the standard deviation).  The drafter proposes draft i from
+    q_i = softmax(top-k(target logits along the draft path + noise[i])); the
+    arithmetic of that softmax lives with the caller, the draws here."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 13])))
+    return _normal_f32(g, (rounds, gamma, vocab), std)
+
+
 def keep_draws(seed: int, rounds: int, n: int, kind: str = "uniform") -> np.ndarray:
     """Commit lengths: U{0..n} or Geometric(1/3) on {1, 2, ...} clipped to n."""
     g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 5])))

@@ -50,3 +50,33 @@ def book_zero(t):
     b = t.zeros(8, dtype=t.int32, device="cuda")
     b[4] = -1
     return b
+
+
+def noise_drafts(evs, st, snap, pending, noise, du, T=1.0, top_k=4):
+    """The noise drafter: gamma = len(du) drafts along its own path.
+
+    Draft i + 1 is drawn (inverse CDF, uniform du[i]) from q_i, the
+    library's top-k softmax at temperature T of the target's native logits
+    after the path so far plus noise[i] (N(0, 0.5) draws from the input
+    generators).  The native steps run on st itself between a snapshot of
+    its recurrent state and the restore (KV rows they append lie beyond the
+    committed length and are rewritten by the next verify).  Returns
+    (drafts, q as a [gamma][V] numpy array, q as a device tensor)."""
+    import synth
+    t = torch()
+    gamma, V = noise.shape
+    st.snapshot_into(snap)
+    lg = t.empty((1, V), dtype=t.float32, device="cuda")
+    tk = t.empty(1, dtype=t.int32, device="cuda")
+    qd = t.empty((gamma, V), dtype=t.float32, device="cuda")
+    drafts, cur = [], int(pending)
+    for i in range(gamma):
+        tk.fill_(cur)
+        evs.evs_verify_block(st, tk, 1, lg)
+        evs.evs_commit(st, 1)
+        noisy = up((to_np(lg)[0] + noise[i]).astype(np.float32)[None])
+        evs.evs_probs(noisy, 1, V, T, top_k, qd[i:i + 1])
+        cur = synth.draw_from(to_np(qd[i]), float(du[i]))
+        drafts.append(cur)
+    snap.snapshot_into(st)
+    return drafts, to_np(qd), qd

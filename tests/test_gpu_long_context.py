@@ -73,3 +73,147 @@ def test_attention_op_262144_cache_sampled_heads():
         evs.evs_op_commit(book, keep, n)
         pos += keep
         assert int(book[0].item()) == pos
+
+
+def _kv_layer_from_synth(seed, P, H, Dh):
+    """All heads of one attention layer's cache rows [P][H][Dh] (bf16 patterns)."""
+    k = np.empty((P, H, Dh), np.uint16)
+    v = np.empty((P, H, Dh), np.uint16)
+    for h in range(H):
+        k[:, h], v[:, h] = synth.kv_head(seed, h, P, Dh)
+    return k, v
+
+
+@pytest.mark.gpu
+def test_7b_stack_262144_context_rounds():
+    """The full 7B-shaped stack at 262,144 cached positions (long-context
+    configuration): one traced block verify of 13 tokens from a synthesised
+    state, then greedy and sampled (T = 1, top_k = 4) rounds whose commit
+    lengths are drawn geometric with mean 3.
+
+    The first attention layer's cache holds N(0, 1) rows from the input
+    generators for every head; the other four attention layers hold device
+    filler (their values reach the checks only through the residual stream,
+    which the checks take from the GPU).  Teacher-forced against the oracle:
+    every Hyena layer's update and retained state, the first attention
+    layer's update over all 32 heads and 262,157 keys, its appended rows,
+    and the head; each round's accept decision on the GPU's p, q, u."""
+    import hybrid_ssm_attention_gb300 as evs
+    from oracle.model import LayerState, Model as OModel
+    from oracle.sampling import GREEDY, SAMPLE, accept
+    t = torch()
+    shape = synth.stack_7b()
+    H, Dh, d, V = shape.n_heads, shape.head_dim, shape.d_model, shape.vocab
+    P, n, R = 262144, shape.n_block, 4
+    ctx = P + 64
+    seed = 4
+    W = synth.make_weights(shape, seed)
+    m = evs.Model(shape, W)
+    st = evs.State(m, ctx)
+    S = synth.synth_state(shape, seed, 0)  # FIR windows and IIR states (no KV rows)
+    att = [i for i, (k, _) in enumerate(shape.layers) if k == "ATT"]
+    checked = att[0]
+    gen = t.Generator(device="cuda").manual_seed(seed)
+    kb, vb = _kv_layer_from_synth(seed, P, H, Dh)
+    for li, (kind, param) in enumerate(shape.layers):
+        v = st.view(li)
+        L = S["layers"][li]
+        if kind in ("SE", "MR"):
+            wrap(v.fir_ext[0], (param - 1 + v.n_max, d))[:param - 1] = up(L["window"])
+        elif kind == "LI":
+            wrap(v.iir_all[0], (v.n_max, d, param, 2))[0] = up(L["s"]).view(d, param, 2)
+        else:
+            kc = wrap(v.k_cache, (H, ctx, Dh), "<i2").view(t.bfloat16)
+            vc = wrap(v.v_cache, (H, ctx, Dh), "<i2").view(t.bfloat16)
+            if li == checked:
+                for h in range(H):
+                    kc[h, :P] = up(np.ascontiguousarray(kb[:, h]))
+                    vc[h, :P] = up(np.ascontiguousarray(vb[:, h]))
+            else:
+                kc.normal_(generator=gen)
+                vc.normal_(generator=gen)
+    t.cuda.synchronize()
+    st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
+    toks = [int(x) for x in synth.prompt(shape, seed, n)]
+    tt = t.tensor(np.asarray(toks, np.int32), device="cuda")
+    lg = t.empty((n, V), dtype=t.float32, device="cuda")
+    p = t.empty((n, V), dtype=t.float32, device="cuda")
+    trace = t.empty((len(shape.layers) + 1, n, d), dtype=t.float32, device="cuda")
+    evs.evs_verify_block_trace(st, tt, n, lg, trace)
+    X, got = to_np(trace), to_np(lg)
+    book = st.book()
+    assert book["pending_n"] == n and book["status"] == 0
+    ret = {}
+    for li, (kind, param) in enumerate(shape.layers):
+        v = st.view(li)
+        if kind in ("SE", "MR"):
+            ret[li] = to_np(wrap(v.fir_ext[1 - book["fir_bank"]], (param - 1 + v.n_max, d)))
+        elif kind == "LI":
+            ret[li] = to_np(wrap(v.iir_all[1 - book["iir_bank"]], (v.n_max, d, param, 2)))
+        elif li == checked:
+            kc = wrap(v.k_cache, (H, ctx, Dh), "<i2").view(t.bfloat16)
+            vc = wrap(v.v_cache, (H, ctx, Dh), "<i2").view(t.bfloat16)
+            ret[li] = (to_np(kc[:, P:P + n]).transpose(1, 0, 2), to_np(vc[:, P:P + n]).transpose(1, 0, 2))
+    # rounds: accept (greedy, then sampled), commit a drawn geometric keep
+    keeps = synth.keep_draws(seed, R, n, kind="geometric")
+    q = synth.fixed_logit_drafter(seed, n - 1, V)
+    U = synth.uniforms(seed, R, n)
+    acc = t.zeros(1, dtype=t.int32, device="cuda")
+    tok = t.zeros(1, dtype=t.int32, device="cuda")
+    pos = P
+    for r in range(R):
+        if r > 0:
+            toks_r = [int(x) for x in synth.prompt(shape, seed + 10 * r, n)]
+            evs.evs_verify_block(st, t.tensor(np.asarray(toks_r, np.int32), device="cuda"), n, lg)
+        else:
+            toks_r = toks
+        if r % 2 == 0:
+            evs.evs_accept(lg, None, t.tensor(np.asarray(toks_r[1:], np.int32), device="cuda"), None, n, V,
+                           evs.EVS_GREEDY, acc, tok)
+            want = accept(to_np(lg), None, toks_r[1:], np.zeros(n, np.float32), GREEDY)
+        else:
+            evs.evs_probs(lg, n, V, 1.0, 4, p)
+            evs.evs_accept(p, up(q), t.tensor(np.asarray(toks_r[1:], np.int32), device="cuda"), up(U[r]), n, V,
+                           evs.EVS_SAMPLE, acc, tok)
+            want = accept(to_np(p), q, toks_r[1:], U[r], SAMPLE)
+        assert (int(acc.item()), int(tok.item())) == want, r
+        evs.evs_commit(st, int(keeps[r]))
+        pos += int(keeps[r])
+        assert st.book()["pos"] == pos
+    assert st.check() == 0
+    st.close()
+    m.close()
+    # the oracle, teacher-forced on the GPU's residual stream
+    Wf = synth.weights_f32(W)
+    del W
+    om = OModel(shape, Wf, Arith(np.float32, bf16_points=True))
+    del Wf
+    for li, (M, (kind, param)) in enumerate(zip(om.layers, shape.layers)):
+        Ls = S["layers"][li]
+        if kind in ("SE", "MR"):
+            L = LayerState(kind, window=Ls["window"].astype(np.float32).copy())
+        elif kind == "LI":
+            L = LayerState(kind, s=Ls["s"].astype(np.complex64).copy())
+        elif li == checked:
+            K = np.zeros((P + n, H, Dh), np.float32)
+            Vv = np.zeros((P + n, H, Dh), np.float32)
+            K[:P], Vv[:P] = _f(kb), _f(vb)
+            L = LayerState(kind, K=K, V=Vv, length=P)
+        else:
+            continue
+        d_ref, d_gpu = [], []
+        for i in range(n):
+            x_out = om.layer_forward(M, L, X[li][i].copy(), P + i)
+            d_ref.append(x_out - X[li][i])
+            d_gpu.append(X[li + 1][i] - X[li][i])
+            if kind in ("SE", "MR"):
+                assert rel_err(ret[li][i + 1:i + param], L.window) <= 2e-2, (li, i)
+            elif kind == "LI":
+                Rr = ret[li][i]
+                assert rel_err(Rr[..., 0], L.s.real) <= 2e-2 and rel_err(Rr[..., 1], L.s.imag) <= 2e-2, (li, i)
+        if kind == "ATT":
+            assert rel_err(ret[li][0], L.K[P:P + n]) <= 2e-2 and rel_err(ret[li][1], L.V[P:P + n]) <= 2e-2
+        e = rel_err(np.stack(d_gpu), np.stack(d_ref))
+        assert e <= 2e-2, (li, kind, e)
+    head = np.stack([om.head(X[-1][i]) for i in range(n)])
+    assert rel_err(got, head) <= 1e-3

@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import rel_err, to_np, torch, up, wrap
+from gpu_util import noise_drafts, rel_err, to_np, torch, up, wrap
 
 TOL = 2e-2
 
@@ -635,3 +635,84 @@ def test_gemm_profiling_leaves_state_unchanged():
     l2 = to_np(_verify(evs, b, nxt, V)[0])
     assert np.array_equal(l1.view(np.uint32), l2.view(np.uint32))
     assert a.book() == b.book() and a.check() == 0
+
+
+@pytest.mark.gpu
+def test_7b_sampled_rounds_noise_drafter():
+    """Full-size 7B-shaped stack, sampled decoding (T = 1.0, top_k = 4, the
+    model card's "Library" defaults) with the noise drafter: q_i = top-4
+    softmax of the target's native logits along the draft path plus
+    N(0, 0.5) noise.  Two rounds from a synthesised state at context 1024,
+    each one graph launch (verify, top-k distribution, accept, commit).
+
+    Checked: the GPU's p equals the top-k softmax of its own logits (support
+    exact, values within 2e-6); the accept decision and output token equal
+    the oracle's rule on the GPU's p, q and uniforms bit for bit; the
+    logits of each round are within the free-running bound of the oracle's
+    block verify along the same tokens (from the committed state the
+    accept left), and the GPU's top-4 support equals the oracle's on every
+    row whose 4th / 5th logit gap exceeds 4x the observed logit error."""
+    import hybrid_ssm_attention_gb300 as evs
+    from oracle.model import Model as OModel
+    from oracle.numerics import Arith
+    from oracle.sampling import SAMPLE, accept, topk_probs
+    t = torch()
+    shape = synth.stack_7b()
+    P, n, V, gamma = 1024, shape.n_block, shape.vocab, shape.gamma
+    R = 2
+    W = synth.make_weights(shape, 3)
+    S = synth.synth_state(shape, 3, P)
+    m = evs.Model(shape, W)
+    st, snap = evs.State(m, P + 64), evs.State(m, P + 64)
+    _load_synth_state(evs, shape, st, S, P)
+    noise = synth.logit_noise(4, R, gamma, V)
+    du = synth.draft_uniforms(4, R, gamma)
+    U = synth.uniforms(4, R, n)
+    pending = int(synth.prompt(shape, 4, 1)[0])
+    lg = t.empty((n, V), dtype=t.float32, device="cuda")
+    p = t.empty((n, V), dtype=t.float32, device="cuda")
+    acc = t.zeros(1, dtype=t.int32, device="cuda")
+    tok = t.zeros(1, dtype=t.int32, device="cuda")
+    rounds = []
+    for r in range(R):
+        drafts, qh, qd = noise_drafts(evs, st, snap, pending, noise[r], du[r])
+        block = [pending] + drafts
+        tt = t.tensor(np.asarray(block, np.int32), device="cuda")
+        u = t.tensor(U[r], device="cuda")
+        evs.evs_round(st, tt, n, lg, p, qd, u, 1.0, 4, evs.EVS_SAMPLE, acc, tok)
+        L, Pg = to_np(lg), to_np(p)
+        a, x = int(acc.item()), int(tok.item())
+        want_p = np.stack([topk_probs(row, 1.0, 4, dtype=np.float32) for row in L])
+        assert np.array_equal(Pg > 0, want_p > 0) and np.abs(Pg - want_p).max() <= 2e-6
+        assert (a, x) == accept(Pg, qh, drafts, U[r], SAMPLE), r
+        rounds.append((block, L, Pg, a))
+        pending = x
+    assert st.check() == 0
+    assert st.book()["pos"] == P + sum(a + 1 for _, _, _, a in rounds)
+    st.close()
+    snap.close()
+    m.close()
+    Wf = synth.weights_f32(W)
+    del W
+    om = OModel(shape, Wf, Arith(np.float32, bf16_points=True))
+    del Wf
+    Sf = dict(S)
+    Sf["layers"] = [dict(L, k=None if L["k"] is None else synth.bf16_bits_to_f32(L["k"]),
+                         v=None if L["v"] is None else synth.bf16_bits_to_f32(L["v"])) for L in S["layers"]]
+    ost = om.state_from(Sf, P + 64)
+    spread = json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                         "spread_7b.json")))
+    bound = 2 * spread["rel_err_logits"]
+    for r, (block, L, Pg, a) in enumerate(rounds):
+        ref, rec = om.verify(ost, block)
+        err = rel_err(L, ref)
+        assert err <= bound, (r, err, bound)
+        gap_tol = 4 * np.abs(L - ref).max()
+        checked = 0
+        for i in range(n):
+            srt = np.sort(ref[i])[::-1]
+            if srt[3] - srt[4] > gap_tol:
+                assert np.array_equal(Pg[i] > 0, topk_probs(ref[i], 1.0, 4, dtype=np.float32) > 0), (r, i)
+                checked += 1
+        print(f"round {r}: accepted {a} of {gamma}, logits err {err:.3e}, support checked on {checked} rows")
+        ost = OModel.commit(ost, rec, a + 1)
