@@ -51,12 +51,19 @@ def parse():
     ap.add_argument("--seed", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-replay", action="store_true")
     ap.add_argument("--no-batch", action="store_true")
-    ap.add_argument("--long-gen", type=int, default=0,
+    ap.add_argument("--long-gen", type=int, default=4096,
                     help="also generate this many tokens natively and speculatively (drafts with random "
-                         "corrupted tails) and report whether the two sequences are identical")
+                         "corrupted tails) and report whether the two sequences are identical (0: skip)")
+    ap.add_argument("--no-sampled", action="store_true")
+    ap.add_argument("--no-long-context", action="store_true")
+    ap.add_argument("--long-context", type=int, default=262144, help="cached positions of the long-context rounds")
+    ap.add_argument("--cpu-one-thread-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--case", nargs="+", metavar=("KIND", "ARG"),
+                    help="instead of the benchmark, launch one small profiler case and exit: "
+                         "gemm N K n | fir L d n | iir M d n | attn P n | stack L n | batch L B n")
+    ap.add_argument("--reps", type=int, default=4, help="repetitions of a --case launch")
     return ap.parse_args()
 
 
@@ -156,9 +163,9 @@ class ClockSampler:
 
 
 # DRAM traffic per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum,
-# averaged over the 129 weight GEMMs of a step) from the ncu capture summarised
-# in profiles/gemm_tc_7b_packed_weight_stream.md; valid only for the kernel
-# source it was taken on (sha256 prefix of gemm.cu), else reported as null.
+# averaged over the 129 weight GEMMs of a step) from one ncu capture of the
+# weight-streaming GEMM; valid only for the kernel source it was taken on
+# (sha256 prefix of gemm.cu), else reported as null.
 GEMM_TRAFFIC = {"gemm_cu_sha256": "f6ea79a125047c1a", "bytes_per_launch": 100.85e6}
 
 
@@ -200,45 +207,142 @@ def step_bytes(shape, P, n):
     return b
 
 
+WORKLOAD = ("7B-shaped hybrid stack: 32 layers (FIR7/FIR128/IIR16, attention every 6th), d_model 4096, MLP 11008, "
+            "vocab 512, bf16 weights 12.96 GB; 1024-token ACGT prompt; gamma=12; identity drafter, greedy")
+
+
+def config(args, world, n, rounds):
+    return {"workload": WORKLOAD, "gamma": 12, "context_start": args.prompt, "generated_tokens": n * rounds,
+            "l2": "inputs larger than L2 (13 GB of weights per step), no flush",
+            "parallelism": f"replicas x{world}"}
+
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer and part codes, plus the kernel's model string if any)."""
+    fields = {}
+    try:
+        for ln in open("/proc/cpuinfo"):
+            k, _, v = ln.partition(":")
+            fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    for k in ("model name", "cpu model", "hardware"):
+        if fields.get(k):
+            return fields[k]
+    if "cpu implementer" in fields:
+        return f"Arm CPU implementer {fields['cpu implementer']} part {fields.get('cpu part', '?')}"
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def blas_threads():
+    """Threads the oracle's matrix products run on (the BLAS pool)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
 # ------------------------------------------------------------------ oracle timing
-def oracle_tokens_per_s(shape, W, seed, P, steps, warm=1):
-    """The CPU oracle (fp32 with bf16 storage points) on a bounded sample:
-    `steps` native steps from a synthesised state at context P."""
+def oracle_round_tokens_per_s(shape, W, seed, P, rounds, native_steps, warm=0):
+    """The oracle's own speculative round on the same workload: a verify of
+    the 13-token identity-drafter block (13 native steps on a copy, every
+    position's state recorded), the accept rule and the commit; plus
+    `native_steps` plain native steps.  The identity drafts (the oracle's own
+    greedy continuation) are made outside the timed part, as on the GPU.
+    Returns tok/s of the rounds (emitted tokens / round time), seconds per
+    round and seconds per native step."""
     import synth
+    from oracle.decode import native_generate
     from oracle.model import Model as OModel
     from oracle.numerics import Arith
+    from oracle.sampling import GREEDY, accept
     om = OModel(shape, synth.weights_f32(W), Arith(np.float32, bf16_points=True))
     S = synth.synth_state(shape, seed, P)
     S["layers"] = [dict(L, k=None if L["k"] is None else synth.bf16_bits_to_f32(L["k"]),
                         v=None if L["v"] is None else synth.bf16_bits_to_f32(L["v"])) for L in S["layers"]]
-    st = om.state_from(S, P + warm + steps + 1)
-    toks = [int(x) for x in synth.prompt(shape, seed, warm + steps)]
-    for t in toks[:warm]:
-        om.step(st, t)
+    n = shape.n_block
+    st = om.state_from(S, P + 2 * n * (warm + rounds + 1) + native_steps + 2)
+    pend = int(synth.prompt(shape, seed, 1)[0])
     t0 = time.perf_counter()
-    for t in toks[warm:]:
-        om.step(st, t)
-    dt = time.perf_counter() - t0
-    return steps / dt, dt
+    native_generate(om, st.copy(), pend, native_steps)
+    t_native = (time.perf_counter() - t0) / max(native_steps, 1)
+    t_round, emitted = 0.0, 0
+    for r in range(warm + rounds):
+        drafts, _ = native_generate(om, st.copy(), pend, n - 1)
+        t0 = time.perf_counter()
+        logits, rec = om.verify(st, [pend] + drafts)
+        a, tok = accept(logits, None, drafts, np.zeros(n, np.float32), GREEDY)
+        st = OModel.commit(st, rec, a + 1)
+        if r >= warm:
+            t_round += time.perf_counter() - t0
+            emitted += a + 1
+        pend = tok
+    if rounds == 0:
+        return None, None, t_native
+    return emitted / t_round, t_round / rounds, t_native
+
+
+def cpu_baseline(args, shape, W):
+    """The oracle as the reported CPU baseline: all host cores, then one
+    thread (a child process with one BLAS thread), on bounded samples."""
+    rounds = 1
+    tps, t_round, t_native = oracle_round_tokens_per_s(shape, W, args.seed, args.prompt, rounds, 2)
+    out = {"value": tps, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+           "cpu": cpu_model(), "host_cores": os.cpu_count(),
+           "sample": f"{rounds} oracle round (13-token identity-drafter block verify = 13 native steps on a copy, "
+                     f"accept, commit) + 2 native steps of the same stack at context {args.prompt}, fp32 with bf16 "
+                     f"storage points; value = 13 tokens / round time",
+           "round_s": t_round, "native_step_s": t_native}
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-one-thread-child", "--seed",
+                            str(args.seed), "--prompt", str(args.prompt)], env=env, capture_output=True, text=True,
+                           timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out["one_thread"] = one
+    except Exception as e:  # reported, not fatal: the all-cores figure stands
+        out["one_thread"] = {"error": str(e)[:200]}
+    return out
+
+
+def run_cpu_one_thread_child(args):
+    import synth
+    shape = synth.stack_7b()
+    W = synth.make_weights(shape, args.seed)
+    _, _, t_native = oracle_round_tokens_per_s(shape, W, args.seed, args.prompt, 0, 1)
+    print(json.dumps({"tok_s": 1.0 / t_native, "native_step_s": t_native, "threads": blas_threads(),
+                      "sample": "1 oracle native step (a round of 13 costs 13 of them)"}))
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step one oracle round of the
+    GPU arm's workload (identity-drafter block verify of 13 tokens, accept,
+    commit), drafts made outside the timed part; rank 0 only."""
     if rank != 0:
         return
     import synth
     shape = synth.stack_7b()
     W = synth.make_weights(shape, args.seed)
-    tps, dt = oracle_tokens_per_s(shape, W, args.seed, args.prompt, args.steps, warm=args.warmup)
-    cores = os.cpu_count()
+    n = shape.n_block
+    tps, t_round, t_native = oracle_round_tokens_per_s(shape, W, args.seed, args.prompt, args.steps, 1,
+                                                       warm=args.warmup)
+    sample = (f"{args.steps} oracle rounds after {args.warmup} warm-up rounds (13-token identity-drafter block "
+              f"verify, accept, commit; fp32 with bf16 storage points) from context {args.prompt}")
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_round,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": "7B-shaped hybrid stack, gamma=12, context 1024",
-                       "note": "one step = one oracle native step (1 of a round's 13 positions)"},
-            "cpu_baseline": {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{args.steps} oracle native steps after {args.warmup} warm-up, "
-                                       f"fp32 with bf16 storage points, context {args.prompt}"},
+            "data": "synthetic", "config": config(args, world, n, args.warmup + args.steps),
+            "cpu_baseline": {"value": tps, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "cpu": cpu_model(), "sample": sample, "native_step_s": t_native},
             "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -359,6 +463,292 @@ def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, y, rounds=24,
         for st in states:
             st.close()
     return out
+
+
+def noise_drafts(evs, torch, st, snap, pending, noise, du, dev, T=1.0, top_k=4):
+    """The noise drafter (outside every timed region): draft i + 1 is drawn
+    (inverse CDF, uniform du[i]) from q_i, the library's top-k softmax of the
+    target's native logits along the draft path plus noise[i].  The native
+    steps run on st between a snapshot of its recurrent state and the
+    restore; the KV rows they append lie beyond the committed length and are
+    rewritten by the next verify.  Returns (drafts, q on the device)."""
+    import synth
+    gamma, V = noise.shape
+    st.snapshot_into(snap)
+    lg = torch.empty((1, V), dtype=torch.float32, device=dev)
+    tk = torch.empty(1, dtype=torch.int32, device=dev)
+    q = torch.empty((gamma, V), dtype=torch.float32, device=dev)
+    drafts, cur = [], int(pending)
+    for i in range(gamma):
+        tk.fill_(cur)
+        evs.evs_verify_block(st, tk, 1, lg)
+        evs.evs_commit(st, 1)
+        noisy = torch.from_numpy((lg.cpu().numpy()[0] + noise[i]).astype(np.float32)[None]).to(dev)
+        evs.evs_probs(noisy, 1, V, T, top_k, q[i:i + 1])
+        cur = synth.draw_from(q[i].cpu().numpy(), float(du[i]))
+        drafts.append(cur)
+    snap.snapshot_into(st)
+    return drafts, q
+
+
+def sampled_rounds(evs, torch, model, shape, post_prompt, ctx, dev, pending, seed, rounds=8, warm=2):
+    """Sampled decoding (T = 1.0, top_k = 4) with the noise drafter (q = top-4
+    softmax of the target's logits along the draft path plus N(0, 0.5)
+    noise), from the post-prompt state.  A first pass alternates drafter and
+    round (each round one graph launch: verify, target distribution, accept,
+    commit), recording every round's block, q and uniforms; the timed pass
+    restores the post-prompt state and runs the same rounds back to back
+    (their results repeat the first pass bit for bit, asserted), with CUDA
+    events around the whole sequence, as the greedy measurement does."""
+    import synth
+    n, V, gamma = shape.n_block, shape.vocab, shape.gamma
+    st, snap = evs.State(model, ctx), evs.State(model, ctx)
+    post_prompt.clone_into(st)
+    R = warm + rounds
+    noise = synth.logit_noise(seed, R, gamma, V)
+    du = synth.draft_uniforms(seed, R, gamma)
+    U = torch.from_numpy(synth.uniforms(seed, R, n)).to(dev)
+    lg = torch.empty((n, V), dtype=torch.float32, device=dev)
+    p = torch.empty((n, V), dtype=torch.float32, device=dev)
+    q = torch.empty((gamma, V), dtype=torch.float32, device=dev)
+    u = torch.empty(n, dtype=torch.float32, device=dev)
+    acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    toks = torch.empty(n, dtype=torch.int32, device=dev)
+    blocks = torch.empty((R, n), dtype=torch.int32, device=dev)
+    qs = torch.empty((R, gamma, V), dtype=torch.float32, device=dev)
+    results, draft_s = [], 0.0
+    for r in range(R):
+        t0 = time.perf_counter()
+        drafts, qr = noise_drafts(evs, torch, st, snap, pending, noise[r], du[r], dev)
+        torch.cuda.synchronize()
+        draft_s += time.perf_counter() - t0 if r >= warm else 0.0
+        blocks[r].copy_(torch.tensor([pending] + drafts, dtype=torch.int32))
+        qs[r].copy_(qr)
+        toks.copy_(blocks[r])
+        q.copy_(qs[r])
+        u.copy_(U[r])
+        evs.evs_round(st, toks, n, lg, p, q, u, 1.0, 4, evs.EVS_SAMPLE, acc, tok)
+        results.append((int(acc.item()), int(tok.item())))
+        pending = results[-1][1]
+    # timed pass: the same rounds back to back from the post-prompt state
+    post_prompt.clone_into(st)
+    acc_log = torch.zeros((R, 2), dtype=torch.int32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for r in range(R):
+        if r == warm:
+            torch.cuda.synchronize()
+            e0.record()
+        toks.copy_(blocks[r])
+        q.copy_(qs[r])
+        u.copy_(U[r])
+        evs.evs_round(st, toks, n, lg, p, q, u, 1.0, 4, evs.EVS_SAMPLE, acc, tok)
+        acc_log[r, 0:1].copy_(acc)
+        acc_log[r, 1:2].copy_(tok)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    replay = [tuple(int(x) for x in row) for row in acc_log.cpu().numpy()]
+    ok = st.check() == 0 and replay == results
+    st.close()
+    snap.close()
+    accepted = [a for a, _ in results[warm:]]
+    emitted = sum(a + 1 for a in accepted)
+    return {"value": emitted / (ms / 1e3), "unit": UNIT, "rounds": rounds, "ms_per_round": ms / rounds,
+            "mean_accepted_per_round": float(np.mean(accepted)), "accepted": accepted,
+            "replay_identical_and_status_ok": ok, "drafter_ms_per_round_host": 1e3 * draft_s / rounds,
+            "note": "T=1.0, top_k=4; noise drafter q_i = top-4 softmax(target logits along the draft path + "
+                    "N(0, 0.5)); rounds (one graph each: verify 13, probs, accept, commit) timed back to back "
+                    "with CUDA events on a replay of the drafter-driven pass; drafter untimed (12 native "
+                    "steps + host draws per round)"}
+
+
+def long_context_rounds(evs, torch, model, shape, P, seed, dev, peak, rounds=6, warm=2):
+    """The same stack over a synthesised long context: FIR windows and IIR
+    states from the input generators, every attention layer's cache holding
+    P rows of device filler N(0, 1) (the values do not change the work).
+    Each round is a verify of 13 tokens, the accept rule (greedy, then
+    sampled at T = 1, top_k = 4) and a commit of a length drawn geometric
+    with mean 3; rounds run back to back, timed with CUDA events."""
+    import synth
+    n, V, d = shape.n_block, shape.vocab, shape.d_model
+    H, Dh = shape.n_heads, shape.head_dim
+    ctx = P + n * 2 * (warm + rounds) + n
+    st = evs.State(model, ctx)
+    S = synth.synth_state(shape, seed, 0)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    for li, (kind, param) in enumerate(shape.layers):
+        v = st.view(li)
+        L = S["layers"][li]
+        if kind in ("SE", "MR"):
+            w = torch.from_numpy(L["window"]).to(dev)
+            _dev_view(torch, v.fir_ext[0], (param - 1 + v.n_max, d), torch.float32)[:param - 1] = w
+        elif kind == "LI":
+            s2 = torch.from_numpy(np.ascontiguousarray(L["s"]).view(np.float32)).to(dev)
+            _dev_view(torch, v.iir_all[0], (v.n_max, d * param * 2), torch.float32)[0] = s2.reshape(-1)
+        else:
+            for ptr in (v.k_cache, v.v_cache):
+                _dev_view(torch, ptr, (H, ctx, Dh), torch.bfloat16).normal_(generator=gen)
+    torch.cuda.synchronize()
+    st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
+    keeps = synth.keep_draws(seed, 2 * (warm + rounds), n, kind="geometric")
+    q = torch.from_numpy(synth.fixed_logit_drafter(seed, n - 1, V)).to(dev)
+    U = torch.from_numpy(synth.uniforms(seed, 2 * (warm + rounds), n)).to(dev)
+    toks = torch.from_numpy(synth.prompt(shape, seed, 2 * (warm + rounds) * n).reshape(-1, n)).to(dev)
+    lg = torch.empty((n, V), dtype=torch.float32, device=dev)
+    p = torch.empty((n, V), dtype=torch.float32, device=dev)
+    acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+    k = 0
+    for mode in ("greedy", "sampled"):
+        # rounds back to back (the commit lengths are known on the host, so
+        # nothing waits between rounds); events around the timed rounds
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kept = 0
+        for r in range(warm + rounds):
+            if r == warm:
+                torch.cuda.synchronize()
+                e0.record()
+            tk = toks[k]
+            evs.evs_verify_block(st, tk, n, lg)
+            if mode == "greedy":
+                evs.evs_accept(lg, None, tk[1:], None, n, V, evs.EVS_GREEDY, acc, tok)
+            else:
+                evs.evs_probs(lg, n, V, 1.0, 4, p)
+                evs.evs_accept(p, q, tk[1:], U[k], n, V, evs.EVS_SAMPLE, acc, tok)
+            evs.evs_commit(st, int(keeps[k]))
+            if r >= warm:
+                kept += int(keeps[k])
+            k += 1
+        e1.record()
+        torch.cuda.synchronize()
+        t_round = e0.elapsed_time(e1)
+        out[mode] = {"ms_per_round": t_round / rounds, "tok_s": kept / (t_round / 1e3), "mean_keep": kept / rounds}
+    book = st.book()
+    ok = st.check() == 0
+    st.close()
+    sb = step_bytes(shape, P + n, n)
+    ms = out["greedy"]["ms_per_round"]
+    out.update({"context": P, "rounds_per_mode": rounds, "status_ok": ok, "pos_end": book["pos"],
+                "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms / 1e3) / 1e9,
+                             "frac": sb / (ms / 1e3) / 1e9 / peak},
+                "note": "commit lengths drawn geometric (mean 3) override the accept result; attention caches "
+                        "are device filler N(0,1), FIR/IIR state synthesised; verify (graph) + accept + commit "
+                        "per round, rounds back to back"})
+    return out
+
+
+def _dev_view(torch, ptr, shape, dtype):
+    """Zero-copy torch view of library-owned device memory (state setup)."""
+    class _A:
+        pass
+    a = _A()
+    ts = {torch.float32: "<f4", torch.bfloat16: "<i2"}[dtype]
+    a.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": ts, "data": (int(ptr), False), "version": 3,
+                                  "strides": None}
+    t = torch.as_tensor(a, device="cuda")
+    return t.view(torch.bfloat16) if dtype == torch.bfloat16 else t
+
+
+def run_case(args):
+    """Small, self-contained launches of one kernel for profiler captures.
+
+    gemm N K n     bf16 tensor-core GEMM of a [N][K] weight (N(0, 0.02)) against
+                   n tokens, --reps times; the default 22016 x 4096 weight
+                   (180 MB) is larger than L2, so each launch streams it from HBM
+    fir L d n      FIR mixer (L taps, d channels, n block rows), fresh inputs per rep
+    iir M d n      IIR mixer (M poles)
+    attn P n       split-KV attention over P cached positions (32 x 128, chunks of 64)
+    stack L n      the first L layers of the 7B-shaped stack with the library's
+                   packed weights: one warm-up verify of n tokens, then every
+                   weight GEMM of a step once more, each launched alone
+    batch L B n    the first L layers, B sequences of n rows verified in one
+                   batched pass, each committing its block; --reps times
+    """
+    import torch
+
+    import hybrid_ssm_attention_gb300 as evs
+    from hybrid_ssm_attention_gb300 import build as b
+    b.build()
+    kind, cargs = args.case[0], [int(x) for x in args.case[1:]]
+    if kind not in ("gemm", "fir", "iir", "attn", "stack", "batch"):
+        raise SystemExit(f"unknown case {kind}")
+
+    class a:
+        pass
+    a.kind, a.args, a.reps = kind, cargs, args.reps
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(0)
+    book = torch.zeros(8, dtype=torch.int32, device=dev)
+    book[4] = -1
+    if a.kind == "batch":
+        import synth
+        L, B, n = (a.args + [2, 8, 13][len(a.args):])[:3]
+        full = synth.stack_7b()
+        shape = synth.ModelShape(name=f"7b-first-{L}", vocab=full.vocab, d_model=full.d_model,
+                                 layers=full.layers[:L], n_heads=full.n_heads, head_dim=full.head_dim,
+                                 d_ffn=full.d_ffn, gamma=full.gamma, dtype="bf16", pole_mag=full.pole_mag)
+        m = evs.Model(shape, synth.make_weights(shape, 3))
+        sts = [evs.State(m, 256) for _ in range(B)]
+        toks = torch.tensor([65 + (i % 4) for i in range(B * n)], dtype=torch.int32, device=dev)
+        lg = torch.empty((B * n, shape.vocab), device=dev)
+        for _ in range(a.reps):
+            evs.evs_verify_batch(sts, toks, [n] * B, lg)
+            for st in sts:
+                evs.evs_commit(st, n)
+    elif a.kind == "stack":
+        import synth
+        L, n = (a.args + [2, 13][len(a.args):])[:2]
+        full = synth.stack_7b()
+        shape = synth.ModelShape(name=f"7b-first-{L}", vocab=full.vocab, d_model=full.d_model,
+                                 layers=full.layers[:L], n_heads=full.n_heads, head_dim=full.head_dim,
+                                 d_ffn=full.d_ffn, gamma=full.gamma, dtype="bf16", pole_mag=full.pole_mag)
+        m = evs.Model(shape, synth.make_weights(shape, 3))
+        st = evs.State(m, 256)
+        toks = torch.tensor([65 + (i % 4) for i in range(n)], dtype=torch.int32, device=dev)
+        lg = torch.empty((n, shape.vocab), device=dev)
+        evs.evs_verify_block(st, toks, n, lg)
+        evs.evs_commit(st, n)
+        evs.evs_profile_gemms(st, n)
+    elif a.kind == "gemm":
+        N, K, n = (a.args + [22016, 4096, 13][len(a.args):])[:3]
+        W = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        X = torch.randn(n, K, device=dev, generator=g).to(torch.bfloat16)
+        y = torch.empty(n, N, device=dev)
+        s = torch.empty(evs.evs_op_gemm_scratch_bytes(N, K, evs.EVS_BF16), dtype=torch.uint8, device=dev)
+        for _ in range(a.reps):
+            evs.evs_op_gemm(W, X, N, K, n, evs.EVS_BF16, y, s)
+    elif a.kind in ("fir", "iir"):
+        P, d, n = (a.args + [128 if a.kind == "fir" else 16, 4096, 13][len(a.args):])[:3]
+        abv = torch.randn(n, 3 * d, device=dev, generator=g).to(torch.bfloat16)
+        gout = torch.empty(n, d, device=dev, dtype=torch.bfloat16)
+        for r in range(a.reps):
+            if a.kind == "fir":
+                e0 = torch.randn(P - 1 + n, d, device=dev, generator=g)
+                e1 = torch.empty_like(e0)
+                taps = torch.randn(P, d, device=dev, generator=g)
+                evs.evs_op_fir(P, d, n, n, evs.EVS_BF16, abv, taps, e0, e1, book, gout)
+            else:
+                s0 = torch.randn(n, d, P, 2, device=dev, generator=g)
+                s1 = torch.empty_like(s0)
+                lam = torch.rand(d, P, 2, device=dev, generator=g) * 0.7
+                res = torch.randn(d, P, 2, device=dev, generator=g) * 0.25
+                evs.evs_op_iir(P, d, n, n, evs.EVS_BF16, abv, lam, res, s0, s1, book, gout)
+    else:
+        P, n = (a.args + [8192, 13][len(a.args):])[:2]
+        H, Dh, chunk = 32, 128, 64
+        ctx = P + n
+        kc = torch.randn(H, ctx, Dh, device=dev, generator=g).to(torch.bfloat16)
+        vc = torch.randn(H, ctx, Dh, device=dev, generator=g).to(torch.bfloat16)
+        qkv = torch.randn(n, 3 * H * Dh, device=dev, generator=g).to(torch.bfloat16)
+        gout = torch.empty(n, H * Dh, device=dev, dtype=torch.bfloat16)
+        s = torch.empty(evs.evs_op_attention_scratch_bytes(H, Dh, ctx, chunk, n), dtype=torch.uint8, device=dev)
+        book[0] = P
+        for _ in range(a.reps):
+            evs.evs_op_attention(H, Dh, n, n, ctx, chunk, 10000.0, evs.EVS_BF16, qkv, kc, vc, book, gout, s)
+    torch.cuda.synchronize()
+    print("profile case done:", a.kind, a.args)
 
 
 def run_evs(args, rank, world, local):
@@ -524,27 +914,27 @@ def run_evs(args, rank, world, local):
     if args.long_gen > 0:
         longgen = long_generation(evs, torch, model, shape, prompt, args.long_gen, args.seed + 100, dev)
 
+    sampled = None
+    if not args.no_sampled:
+        sampled = sampled_rounds(evs, torch, model, shape, snap, ctx, dev, prompt[-1], args.seed + 1)
+
+    longctx = None
+    if not args.no_long_context:
+        longctx = long_context_rounds(evs, torch, model, shape, args.long_context, args.seed + 1, dev, peak)
+
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
         st.close()
         snap.close()
         model.close()
         torch.cuda.empty_cache()
-        tps, dt = oracle_tokens_per_s(shape, W, args.seed, P0, args.cpu_steps)
-        cpu = {"value": tps, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{args.cpu_steps} oracle native steps (1 token each) of the same stack at context "
-                         f"{P0}, fp32 with bf16 storage points, after 1 warm-up step"}
+        cpu = cpu_baseline(args, shape, W)
     if rank != 0:
         return
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "7B-shaped hybrid stack: 32 layers (FIR7/FIR128/IIR16, attention every 6th), "
-                                   "d_model 4096, MLP 11008, vocab 512, bf16 weights 12.96 GB; 1024-token ACGT "
-                                   "prompt; gamma=12; identity drafter, greedy",
-                       "gamma": 12, "context_start": P0, "generated_tokens": n * rounds,
-                       "l2": "inputs larger than L2 (13 GB of weights per step), no flush",
-                       "parallelism": f"replicas x{world}"},
+            "config": config(args, world, n, rounds),
             "verify_round_us": 1e3 * ms_per_step,
             "native_step_us": 1e3 * native_step_ms,
             "identity_overhead": ms_per_step / (n * native_step_ms),
@@ -552,7 +942,7 @@ def run_evs(args, rank, world, local):
             "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms_per_step / 1e3) / 1e9,
                          "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "snapshot_replay": replay,
-            "long_generation": longgen, "batched_verify": batched,
+            "long_generation": longgen, "batched_verify": batched, "sampled": sampled, "long_context": longctx,
             "gpu_launches": int(launches),
             "clocks": clk}
     print(json.dumps(line), flush=True)
@@ -560,6 +950,12 @@ def run_evs(args, rank, world, local):
 
 def main():
     args = parse()
+    if args.cpu_one_thread_child:
+        run_cpu_one_thread_child(args)
+        return
+    if args.case:
+        run_case(args)
+        return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

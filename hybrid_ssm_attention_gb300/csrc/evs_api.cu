@@ -537,10 +537,9 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
   m->n_max = cfg->gamma_max + 1;
   m->has_attn = false;
   {
-    const char* pk = getenv("EVS_WPACK");
     const char* fz = getenv("EVS_FUSE");
     const char* sw = getenv("EVS_SWIGLU");
-    m->packed = m->tc && !(pk && pk[0] == '0') && cfg->d_ffn % (TILE_M / 2) == 0;
+    m->packed = m->tc && cfg->d_ffn % (TILE_M / 2) == 0;
     m->swiglu = m->packed && sw && sw[0] == '1';
     // fp32 rows staged by TMA need 16-byte row strides
     m->fuse = m->packed && cfg->d_model % 4 == 0 && fz && fz[0] == '1';
@@ -595,8 +594,7 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
     size_t tb = 0;
     m->ws_bytes = 0;
     for (int k = 0; k < 5; ++k) {
-      const char* cl_env = getenv("EVS_GEMM_CLUSTER");
-      const bool allow_cl = m->tc && !(cl_env && cl_env[0] == '0');
+      const bool allow_cl = m->tc;
       const bool resid = k == 1 || k == 3;
       const int cl = allow_cl && !(resid && m->slots_resid) ? gemm_cluster_choice(shapes[k][0], shapes[k][1], m->num_sms)
                                                             : 0;
@@ -611,11 +609,6 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
       if (m->tc)
         plans[k].P.stages =
             std::min(plans[k].P.stages, gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA));
-      // EVS_GEMM_STAGES overrides the ring depth, clamped to what fits
-      const char* st_env = getenv("EVS_GEMM_STAGES");
-      if (st_env && m->tc)
-        plans[k].P.stages = std::max(2, std::min(gemm_stages_for(plans[k].P.cl, m->fuse ? bs[k] : GEMM_B_TMA),
-                                                 atoi(st_env)));
       // stream-K twin over the same CTA unit ranges (G = T * cl for a
       // cluster plan), for passes of more than NTOK rows
       GemmPlan& q = plans[5 + k];
@@ -715,12 +708,10 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   s->uid = ++g_state_uid;
   s->ctx_max = ctx_max;
   s->use_graphs = true;
-  const char* pdl_env = getenv("EVS_PDL");
-  s->pdl = !(pdl_env && pdl_env[0] == '0');
-  const char* pf_env = getenv("EVS_PREFETCH_UNITS");
+  s->pdl = true;
   // 4 units (64 KB) per CTA, 9.7 MB in all: measured best on the 7B-shaped
   // step (deeper prefetches compete with the running GEMM's own stream)
-  s->pf_units = pf_env ? std::max(0, atoi(pf_env)) : 4;
+  s->pf_units = 4;
   const evs_config& c = m->cfg;
   const int d = c.d_model, F = c.d_ffn, nm = m->n_max;
   const size_t es = esize(c.dtype);

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import book_zero, rel_err, to_np, torch, up
+from gpu_util import book_zero, rel_err, to_np, torch, up, wrap
 from oracle.model import attend, rope
 from oracle.numerics import Arith, round_bf16
 
