@@ -57,6 +57,7 @@ def parse():
                     help="also generate this many tokens natively and speculatively (drafts with random "
                          "corrupted tails) and report whether the two sequences are identical (0: skip)")
     ap.add_argument("--no-sampled", action="store_true")
+    ap.add_argument("--no-drafter", action="store_true")
     ap.add_argument("--no-long-context", action="store_true")
     ap.add_argument("--long-context", type=int, default=262144, help="cached positions of the long-context rounds")
     ap.add_argument("--cpu-one-thread-child", action="store_true", help=argparse.SUPPRESS)
@@ -563,6 +564,55 @@ def sampled_rounds(evs, torch, model, shape, post_prompt, ctx, dev, pending, see
                     "steps + host draws per round)"}
 
 
+def drafter_rounds(evs, torch, dev, seed, prompt_len, rounds=16, warm=4):
+    """The drafter side, as a timing stand-in (no trained drafter exists):
+    per round the trunk stand-in (one attention layer at d_model 1024,
+    random init) scores the gamma draft slots in one verify pass and commits
+    the pending token, then the Markov head kernel draws the gamma drafts
+    from its rows (T = 1, top_k = 4).  Rounds back to back; CUDA events
+    around each part of each round, read at the end."""
+    import synth
+    shape = synth.drafter_trunk_standin()
+    gamma, V = shape.gamma, shape.vocab
+    m = evs.Model(shape, synth.make_weights(shape, seed))
+    st = evs.State(m, prompt_len + warm + rounds + 2 * gamma)
+    pr = torch.from_numpy(synth.prompt(shape, seed, prompt_len)).to(dev)
+    lg = torch.empty((gamma, V), dtype=torch.float32, device=dev)
+    for s0 in range(0, prompt_len - 1, gamma):
+        k = min(gamma, prompt_len - 1 - s0)
+        evs.evs_verify_block(st, pr[s0:s0 + k], k, lg[:k])
+        evs.evs_commit(st, k)
+    M = torch.from_numpy(synth.markov_matrix(seed, V)).to(dev)
+    U = torch.from_numpy(synth.uniforms(seed, warm + rounds, gamma)).to(dev)
+    toks = torch.from_numpy(synth.prompt(shape, seed + 1, (warm + rounds) * gamma).reshape(-1, gamma)).to(dev)
+    d = torch.zeros(gamma, dtype=torch.int32, device=dev)
+    q = torch.empty((gamma, V), dtype=torch.float32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(rounds)]
+    torch.cuda.synchronize()
+    for r in range(warm + rounds):
+        e = ev[r - warm] if r >= warm else None
+        if e:
+            e[0].record()
+        evs.evs_verify_block(st, toks[r], gamma, lg)
+        evs.evs_commit(st, 1)
+        if e:
+            e[1].record()
+        evs.evs_markov_draft(lg, M, V, toks[r, :1], U[r], gamma, 1.0, 4, evs.EVS_SAMPLE, d, q)
+        if e:
+            e[2].record()
+    torch.cuda.synchronize()
+    trunk = sum(e[0].elapsed_time(e[1]) for e in ev) / rounds
+    head = sum(e[1].elapsed_time(e[2]) for e in ev) / rounds
+    total = ev[0][0].elapsed_time(ev[-1][2]) / rounds
+    ok = st.check() == 0
+    st.close()
+    m.close()
+    return {"us_per_round": 1e3 * total, "trunk_us": 1e3 * trunk, "markov_head_us": 1e3 * head, "status_ok": ok,
+            "note": "timing stand-in, random init: trunk = one attention layer at d_model 1024 (8x128 heads, MLP "
+                    "4096, vocab 512) scoring 12 slots in one verify pass; Markov head = the evs_markov_draft "
+                    "kernel (12 sequential top-4 draws over trunk row + V x V Markov row)"}
+
+
 def long_context_rounds(evs, torch, model, shape, P, seed, dev, peak, rounds=6, warm=2):
     """The same stack over a synthesised long context: FIR windows and IIR
     states from the input generators, every attention layer's cache holding
@@ -914,6 +964,10 @@ def run_evs(args, rank, world, local):
     if args.long_gen > 0:
         longgen = long_generation(evs, torch, model, shape, prompt, args.long_gen, args.seed + 100, dev)
 
+    drafter = None
+    if not args.no_drafter:
+        drafter = drafter_rounds(evs, torch, dev, args.seed + 2, P0)
+
     sampled = None
     if not args.no_sampled:
         sampled = sampled_rounds(evs, torch, model, shape, snap, ctx, dev, prompt[-1], args.seed + 1)
@@ -943,6 +997,7 @@ def run_evs(args, rank, world, local):
                          "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "snapshot_replay": replay,
             "long_generation": longgen, "batched_verify": batched, "sampled": sampled, "long_context": longctx,
+            "drafter": drafter,
             "gpu_launches": int(launches),
             "clocks": clk}
     print(json.dumps(line), flush=True)

@@ -20,7 +20,7 @@ from ._abi import (EVS_BF16, EVS_ERR_ARG, EVS_ERR_CAPACITY, EVS_ERR_CUDA, EVS_ER
                    EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
-           "evs_commit", "evs_commit_dev", "evs_round", "evs_round_batch", "evs_op_fir", "evs_op_iir",
+           "evs_commit", "evs_commit_dev", "evs_markov_draft", "evs_round", "evs_round_batch", "evs_op_fir", "evs_op_iir",
            "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_verify_batch",
            "evs_kernel_launches"]
 
@@ -213,6 +213,14 @@ def evs_probs(logits, n: int, V: int, T: float, top_k: int, p, stream=None):
 def evs_accept(p, q, drafts, u, n: int, V: int, mode: int, out_accepted, out_token, stream=None):
     _check(lib().evs_accept(_ptr(p), _ptr(q), _ptr(drafts), _ptr(u), int(n), int(V), int(mode),
                             _ptr(out_accepted), _ptr(out_token), _stream(stream)), "evs_accept")
+
+
+def evs_markov_draft(trunk_logits, markov, V: int, prev, u, gamma: int, T: float, top_k: int, mode: int, drafts, q,
+                     stream=None):
+    """Drafter-side Markov head: gamma sequential draws from trunk rows plus Markov rows."""
+    _check(lib().evs_markov_draft(_ptr(trunk_logits), _ptr(markov), int(V), _ptr(prev), _ptr(u), int(gamma),
+                                  float(T), int(top_k), int(mode), _ptr(drafts), _ptr(q), _stream(stream)),
+           "evs_markov_draft")
 
 
 def evs_commit(state: State, keep: int, stream=None):

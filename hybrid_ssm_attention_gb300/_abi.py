@@ -73,6 +73,7 @@ PROTOTYPES = {
     "evs_verify_batch": (i32, [vp, i32, vp, vp, vp, vp]),
     "evs_probs": (i32, [vp, i32, i32, f32, i32, vp, vp]),
     "evs_accept": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]),
+    "evs_markov_draft": (i32, [vp, vp, i32, vp, vp, i32, f32, i32, i32, vp, vp, vp]),
     "evs_commit": (i32, [vp, i32, vp]),
     "evs_commit_dev": (i32, [vp, vp, vp]),
     "evs_round": (i32, [vp, vp, i32, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),

@@ -1030,6 +1030,19 @@ extern "C" int evs_accept(const float* p, const float* q, const int32_t* drafts,
   return EVS_OK;
 }
 
+extern "C" int evs_markov_draft(const float* trunk, const float* markov, int32_t V, const int32_t* prev,
+                                const float* u, int32_t gamma, float T, int32_t top_k, int32_t mode, int32_t* drafts,
+                                float* q, cudaStream_t stream) {
+  if (!trunk || !markov || !prev || !drafts || !q) return fail(EVS_ERR_ARG, "null argument");
+  if (V < 1 || V > 8192 || gamma < 1 || gamma > 64) return fail(EVS_ERR_ARG, "V or gamma out of range");
+  if (mode != EVS_GREEDY && mode != EVS_SAMPLE) return fail(EVS_ERR_ARG, "mode must be EVS_GREEDY or EVS_SAMPLE");
+  if (mode == EVS_SAMPLE && !u) return fail(EVS_ERR_ARG, "sample mode needs u");
+  if (!(T > 0.f)) return fail(EVS_ERR_ARG, "temperature must be > 0");
+  LaunchCtx Lc{stream, false};
+  CUDA_TRY(launch_markov_draft(Lc, trunk, markov, V, prev, u, gamma, T, top_k, mode, drafts, q));
+  return EVS_OK;
+}
+
 extern "C" int evs_commit(evs_state* s, int32_t keep, cudaStream_t stream) {
   if (!s) return fail(EVS_ERR_ARG, "null state");
   if (!s->host_pending) return fail(EVS_ERR_STATE, "commit without a pending verify");

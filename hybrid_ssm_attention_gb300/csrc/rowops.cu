@@ -245,58 +245,57 @@ __device__ int block_scan_incl(int v, int* scratch) {
   return v + base;
 }
 
-// One CTA per row.  top-k: the k-th largest logit is found by radix select
-// over the four bytes of its orderable key (a 256-bin histogram per byte,
-// O(V) work); entries above it are kept, and of the entries equal to it the
-// lowest-indexed ones fill the remaining places (ties to the lower index).
-__global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, float T, int k, float* p) {
-  extern __shared__ float sm[];
-  __shared__ float scratch[32];
-  __shared__ int iscr[32];
-  __shared__ unsigned int hist[256];
-  __shared__ unsigned int s_prefix;
-  __shared__ int s_remain, s_eq;
-  float* l_s = sm;        // [V]
-  float* w_s = sm + V;    // [V]
-  const int t = blockIdx.x, tid = threadIdx.x, nth = blockDim.x;
-  pdl_trigger();
-  pdl_wait();
-  for (int j = tid; j < V; j += nth) l_s[j] = logits[(size_t)t * V + j];
-  __syncthreads();
+// Shared scratch of row_topk_softmax.
+struct TopkScratch {
+  float f[32];
+  int i[32];
+  unsigned int hist[256];
+  unsigned int prefix;
+  int remain, eq;
+};
+
+// Top-k softmax of the row l_s[V] (shared memory, written and synchronised
+// by the caller) by the whole block: w_s[j] = p_j.  The k-th largest logit
+// is found by radix select over the four bytes of its orderable key (a
+// 256-bin histogram per byte, O(V) work); entries above it are kept, and of
+// the entries equal to it the lowest-indexed ones fill the remaining places
+// (ties to the lower index).  k <= 0 or k >= V keeps every entry.
+__device__ void row_topk_softmax(const float* l_s, float* w_s, int V, float T, int k, TopkScratch& ts) {
+  const int tid = threadIdx.x, nth = blockDim.x;
   const bool use_k = k > 0 && k < V;
-  unsigned int kth = 0;  // key of the k-th largest entry (0: keep every entry)
+  unsigned int kth = 0;  // key of the k-th largest entry
   int need_eq = 0, n_eq = 0;
   if (use_k) {
     unsigned int prefix = 0, mask = 0;
     int remain = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += nth) hist[i] = 0;
+      for (int i = tid; i < 256; i += nth) ts.hist[i] = 0;
       __syncthreads();
       for (int j = tid; j < V; j += nth) {
         const unsigned int key = ord_key(l_s[j]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        if ((key & mask) == prefix) atomicAdd(&ts.hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
       if (tid == 0) {
         // the digit holding the remain-th largest of the entries matching prefix
         int acc = 0, D = 255;
         for (; D > 0; --D) {
-          if (acc + (int)hist[D] >= remain) break;
-          acc += (int)hist[D];
+          if (acc + (int)ts.hist[D] >= remain) break;
+          acc += (int)ts.hist[D];
         }
-        s_prefix = prefix | ((unsigned int)D << shift);
-        s_remain = remain - acc;
-        s_eq = (int)hist[D];
+        ts.prefix = prefix | ((unsigned int)D << shift);
+        ts.remain = remain - acc;
+        ts.eq = (int)ts.hist[D];
       }
       __syncthreads();
-      prefix = s_prefix;
-      remain = s_remain;
+      prefix = ts.prefix;
+      remain = ts.remain;
       mask |= 255u << shift;
       __syncthreads();
     }
     kth = prefix;
     need_eq = remain;  // entries equal to kth to keep (k - remain entries lie above it)
-    n_eq = s_eq;       // entries equal to kth in all
+    n_eq = ts.eq;      // entries equal to kth in all
   }
   float mx = -INFINITY;
   if (!use_k || need_eq == n_eq) {
@@ -313,7 +312,7 @@ __global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, 
     const int j0 = min(V, tid * seg), j1 = min(V, j0 + seg);
     int c = 0;
     for (int j = j0; j < j1; ++j) c += ord_key(l_s[j]) == kth;
-    int rank = block_scan_incl(c, iscr) - c;  // equal entries before this range
+    int rank = block_scan_incl(c, ts.i) - c;  // equal entries before this range
     for (int j = j0; j < j1; ++j) {
       const unsigned int key = ord_key(l_s[j]);
       bool keep = key > kth;
@@ -322,15 +321,31 @@ __global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, 
       if (keep) mx = fmaxf(mx, l_s[j]);
     }
   }
-  mx = block_reduce(mx, MaxF(), scratch);
+  mx = block_reduce(mx, MaxF(), ts.f);
   float sum = 0.f;
   for (int j = tid; j < V; j += nth) {
     const float w = w_s[j] != 0.f ? expf((l_s[j] - mx) / T) : 0.f;
     w_s[j] = w;
     sum += w;
   }
-  sum = block_reduce(sum, AddF(), scratch);
-  for (int j = tid; j < V; j += nth) p[(size_t)t * V + j] = w_s[j] / sum;
+  sum = block_reduce(sum, AddF(), ts.f);
+  for (int j = tid; j < V; j += nth) w_s[j] = w_s[j] / sum;
+  __syncthreads();
+}
+
+// One CTA per row: the target distribution (temperature, top-k).
+__global__ void __launch_bounds__(256) probs_kernel(const float* logits, int V, float T, int k, float* p) {
+  extern __shared__ float sm[];
+  __shared__ TopkScratch ts;
+  float* l_s = sm;        // [V]
+  float* w_s = sm + V;    // [V]
+  const int t = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  for (int j = threadIdx.x; j < V; j += blockDim.x) l_s[j] = logits[(size_t)t * V + j];
+  __syncthreads();
+  row_topk_softmax(l_s, w_s, V, T, k, ts);
+  for (int j = threadIdx.x; j < V; j += blockDim.x) p[(size_t)t * V + j] = w_s[j];
 }
 
 // argmax over a row by one warp, same ties rule (lowest index); all-NaN -> 0
@@ -461,6 +476,7 @@ __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float
         min((unsigned long long)(unsigned int)(u[gamma] * 16777216.0f), 16777215ull);
     const unsigned long long thr = (U * S) >> 24;
     token = ladder_find(Wsm, V, thr, us, &found);
+    __syncthreads();  // every thread has read found before it is reused
     if (token < 0) {
       // neither the residual nor p_a has integer mass (a NaN or all-zero
       // row): the row's argmax stands in, and the state is flagged
@@ -476,6 +492,63 @@ __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float
   if (threadIdx.x == 0) {
     out_a[0] = a;
     out_tok[0] = token;
+  }
+}
+
+// Drafter-side Markov head (preprint abstract, contribution (ii); model
+// card, drafter description): the gamma drafts are drawn one after another in
+// one CTA.  Slot i's logits are the trunk's row i plus row prev of the V x V
+// Markov matrix, prev being the pending token for the first slot and the
+// previous draft after it; q_i is their top-k softmax at temperature T and
+// the draft is q_i's integer-ladder sample with uniform u[i] (greedy: the
+// argmax of the logits, lowest index on ties).  A pending token outside
+// [0, V) selects row 0.
+__global__ void __launch_bounds__(256) markov_draft_kernel(const float* trunk, const float* M, int V,
+                                                           const int32_t* prev_dev, const float* u, int gamma,
+                                                           float T, int k, int mode, int32_t* drafts, float* q) {
+  extern __shared__ float sm[];
+  __shared__ TopkScratch ts;
+  __shared__ unsigned long long us[256];
+  __shared__ int found;
+  float* l_s = sm;                                           // [V] logits of the slot
+  float* w_s = sm + V;                                       // [V] q of the slot
+  unsigned int* Wl = reinterpret_cast<unsigned int*>(sm + 2 * V);  // [V] ladder weights
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  int prev = prev_dev[0];
+  if (prev < 0 || prev >= V) prev = 0;
+  for (int i = 0; i < gamma; ++i) {
+    const float* mr = M + (size_t)prev * V;
+    const float* tr = trunk + (size_t)i * V;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) l_s[j] = __fadd_rn(tr[j], mr[j]);
+    __syncthreads();
+    row_topk_softmax(l_s, w_s, V, T, k, ts);
+    for (int j = threadIdx.x; j < V; j += blockDim.x) q[(size_t)i * V + j] = w_s[j];
+    int d = -1;
+    if (mode == EVS_SAMPLE) {
+      unsigned long long loc = 0;
+      for (int j = threadIdx.x; j < V; j += blockDim.x) {
+        Wl[j] = ladder_weight(w_s[j]);
+        loc += Wl[j];
+      }
+      const unsigned long long S = block_reduce(loc, AddU(), us);
+      __syncthreads();
+      const unsigned long long U = min((unsigned long long)(unsigned int)(u[i] * 16777216.0f), 16777215ull);
+      d = ladder_find(Wl, V, (U * S) >> 24, us, &found);
+      __syncthreads();  // every thread has read found before it is reused
+    }
+    if (d < 0) {  // greedy, or a row without integer mass
+      if (warp == 0) {
+        const int am = warp_argmax(l_s, V);
+        if (lane == 0) found = am;
+      }
+      __syncthreads();
+      d = found;
+    }
+    if (threadIdx.x == 0) drafts[i] = d;
+    prev = d;
+    __syncthreads();  // every thread has read found and l_s before the next slot
   }
 }
 
@@ -600,6 +673,18 @@ cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float*
     if (e != cudaSuccess) return e;
   }
   return launch(L, accept_kernel, dim3(sr.nseq), dim3(256), smem, p, q, drafts, u, sr, V, mode, acc, tok, books);
+}
+
+cudaError_t launch_markov_draft(const LaunchCtx& L, const float* trunk, const float* M, int V, const int32_t* prev,
+                                const float* u, int gamma, float T, int top_k, int mode, int32_t* drafts, float* q) {
+  const size_t smem = sizeof(float) * 3 * V;
+  if (smem > 48 * 1024) {
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(markov_draft_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch(L, markov_draft_kernel, dim3(1), dim3(256), smem, trunk, M, V, prev, u, gamma, T, top_k, mode, drafts,
+                q);
 }
 
 cudaError_t launch_commit_batch(const LaunchCtx& L, const SeqPtrs<evs_book*>& books, int nseq, const int32_t* acc) {

@@ -271,6 +271,24 @@ int evs_accept(const float* p_dev, const float* q_dev, const int32_t* drafts_dev
                const float* u_dev, int32_t n, int32_t V, int32_t mode,
                int32_t* out_accepted_dev, int32_t* out_token_dev, cudaStream_t stream);
 
+/* Drafter-side Markov head ([abstract] (ii): a gamma-parallel drafter trunk
+ * with a full-matrix Markov head; model card, drafter description: a full
+ * V x V Markov head).  The trunk scores all gamma draft slots in one pass
+ * (trunk_logits_dev float32 [gamma][V], e.g. the logits of a verify of the
+ * drafter's own stack); the head then draws the drafts one after another:
+ * slot i's logits are trunk_logits[i] + markov_dev[prev_i] (row prev_i of
+ * float32 [V][V]), prev_0 = prev_dev[0] (the pending token; outside [0, V)
+ * selects row 0) and prev_{i+1} = draft i; q_i = softmax over the top_k
+ * largest of those logits at temperature T (as evs_probs), written to
+ * q_dev [gamma][V]; draft i = sample(q_i, u_dev[i]) with the accept rule's
+ * integer-ladder sampler (EVS_SAMPLE; a row without mass gives its argmax)
+ * or the argmax of the logits, lowest index on ties (EVS_GREEDY, u_dev
+ * unused, may be null), written to drafts_dev[i].  One CTA; V <= 8192,
+ * 1 <= gamma <= 64, T > 0. */
+int evs_markov_draft(const float* trunk_logits_dev, const float* markov_dev, int32_t V, const int32_t* prev_dev,
+                     const float* u_dev, int32_t gamma, float T, int32_t top_k, int32_t mode,
+                     int32_t* drafts_dev, float* q_dev, cudaStream_t stream);
+
 /* Commit ([abstract] (i): per-position state slicing with zero
  * recomputation).  keep in [0, n] tokens of the pending block are consumed:
  * FIR window <- ext rows [keep, keep+L-1); IIR state <- state after block

@@ -253,6 +253,20 @@ def logit_noise(seed: int, rounds: int, gamma: int, vocab: int, std: float = 0.5
     return _normal_f32(g, (rounds, gamma, vocab), std)
 
 
+def markov_matrix(seed: int, vocab: int, std: float = 1.0) -> np.ndarray:
+    """Random-init full V x V Markov matrix of the drafter head, float32 ~ N(0, std)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 14])))
+    return _normal_f32(g, (vocab, vocab), std)
+
+
+def drafter_trunk_standin(vocab: int = 512, gamma: int = 12) -> ModelShape:
+    """Timing stand-in for the drafter trunk (random init, no trained
+    weights exist): one attention layer at d_model 1024 (8 heads x 128,
+    MLP 4096), scoring gamma draft slots in one pass."""
+    return ModelShape(name="drafter-trunk-standin", vocab=vocab, d_model=1024, layers=[(ATT, 0)], n_heads=8,
+                      head_dim=128, d_ffn=4096, gamma=gamma, dtype="bf16")
+
+
 def keep_draws(seed: int, rounds: int, n: int, kind: str = "uniform") -> np.ndarray:
     """Commit lengths: U{0..n} or Geometric(1/3) on {1, 2, ...} clipped to n."""
     g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 5])))
