@@ -276,16 +276,37 @@ __device__ void row_topk_softmax(const float* l_s, float* w_s, int V, float T, i
         if ((key & mask) == prefix) atomicAdd(&ts.hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        // the digit holding the remain-th largest of the entries matching prefix
-        int acc = 0, D = 255;
-        for (; D > 0; --D) {
-          if (acc + (int)ts.hist[D] >= remain) break;
-          acc += (int)ts.hist[D];
+      if (tid < 32) {
+        // the digit D holding the remain-th largest of the entries matching
+        // prefix: count(bins > D) < remain <= count(bins >= D).  Lane l owns
+        // bins 8l .. 8l+7; a suffix sum over the lanes finds the one lane
+        // whose bins hold D, which scans its eight bins from the top.
+        const int lane = tid;
+        int c[8], tot = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tot += c[e] = (int)ts.hist[8 * lane + e];
+        int suf = tot;  // bins of lanes >= lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_down_sync(0xffffffffu, suf, o);
+          if (lane + o < 32) suf += y;
         }
-        ts.prefix = prefix | ((unsigned int)D << shift);
-        ts.remain = remain - acc;
-        ts.eq = (int)ts.hist[D];
+        int acc = suf - tot;  // bins of lanes above this one
+        if (acc < remain && remain <= acc + tot) {
+          int D = 8 * lane, eq = c[0];
+#pragma unroll
+          for (int e = 7; e >= 0; --e) {
+            if (acc + c[e] >= remain) {
+              D = 8 * lane + e;
+              eq = c[e];
+              break;
+            }
+            acc += c[e];
+          }
+          ts.prefix = prefix | ((unsigned int)D << shift);
+          ts.remain = remain - acc;
+          ts.eq = eq;
+        }
       }
       __syncthreads();
       prefix = ts.prefix;
