@@ -186,6 +186,10 @@ class State:
     def use_graphs(self, on: bool):
         _check(lib().evs_state_use_graphs(self.handle, int(bool(on))), "evs_state_use_graphs")
 
+    def use_engine(self, on: bool):
+        """Single-sequence verifies through the persistent engine (on by default where the model allows)."""
+        _check(lib().evs_state_use_engine(self.handle, int(bool(on))), "evs_state_use_engine")
+
     def clone_into(self, dst: "State", stream=None):
         _check(lib().evs_state_clone(self.handle, dst.handle, _stream(stream)), "evs_state_clone")
 

@@ -68,6 +68,7 @@ PROTOTYPES = {
     "evs_state_book_write": (i32, [vp, C.POINTER(evs_book), vp]),
     "evs_state_check": (i32, [vp, vp, C.POINTER(i32)]),
     "evs_state_use_graphs": (i32, [vp, i32]),
+    "evs_state_use_engine": (i32, [vp, i32]),
     "evs_verify_block": (i32, [vp, vp, i32, vp, vp]),
     "evs_verify_block_trace": (i32, [vp, vp, i32, vp, vp, vp]),
     "evs_verify_batch": (i32, [vp, i32, vp, vp, vp, vp]),

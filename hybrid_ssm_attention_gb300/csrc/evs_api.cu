@@ -168,6 +168,20 @@ struct evs_state {
   unsigned long long* trace;  // EVS_TRACE builds: GEMM timeline slots
   int cta_slot = -1;          // EVS_TRACE builds: GEMM launch with per-CTA timeline
   cudaStream_t cap;
+  // Persistent engine (single-sequence bf16 verifies): the phase program,
+  // its counters and the spans it is cut into by the attention mixers
+  struct EngSeg {
+    int ph0, ph1;
+    int attn_layer;   // the attention layer whose mixer follows the span, or -1
+    float* attn_ws;   // that layer's in-projection slots
+  };
+  bool engine_ok = false;
+  bool use_engine = false;
+  EngPhase* eng_prog = nullptr;
+  std::vector<EngSeg> eng_segs;
+  int* eng_cnt = nullptr;
+  size_t eng_cnt_bytes = 0;
+  int eng_row_floats = 0;
   std::vector<GraphEntry> graphs;
   unsigned long long tick;
   std::vector<void*> allocs;
@@ -198,6 +212,207 @@ int dmalloc(evs_state* s, void** p, size_t bytes) {
   }
   s->allocs.push_back(*p);
   s->alloc_bytes += bytes;
+  return EVS_OK;
+}
+
+// ------------------------------------------------------------------ engine
+// Whether the persistent engine can run this model: the bf16 packed path with
+// every stream-K GEMM leaving slots to its consumers, FIR filters of at most
+// 128 taps, and the head's stream-K view over its cluster plan.
+static bool engine_eligible(const evs_model* m) {
+  const evs_config& c = m->cfg;
+  if (!(m->tc && m->packed && m->slots && m->slots_resid) || m->fuse || m->swiglu) return false;
+  if (m->p_in.cl || m->p_out.cl || m->p_gu.cl || m->p_down.cl) return false;
+  if (m->p_in.max_cnt > SLOTS_MIX_MAX || m->p_gu.max_cnt > SLOTS_MIX_MAX || m->p_out.max_cnt > SLOTS_RESID_MAX ||
+      m->p_down.max_cnt > SLOTS_RESID_MAX || m->q_head.max_cnt > 8)
+    return false;
+  if (m->q_head.G != m->p_head.G || m->q_head.U != m->p_head.U) return false;
+  if (c.d_model % TILE_M || c.d_model / TILE_M > RESID_TILES_ROW || c.d_ffn % TILE_K || c.vocab % TILE_M) return false;
+  if (m->p_in.G > m->num_sms || m->p_out.G > m->num_sms || m->p_gu.G > m->num_sms || m->p_down.G > m->num_sms)
+    return false;
+  for (const LayerW& L : m->L)
+    if (L.kind == EVS_LAYER_FIR && L.param > 128) return false;
+  return true;
+}
+
+// The phase program of a state: every GEMM and row phase of a verify in
+// order, cut into spans at the attention mixers.  cnt == nullptr counts the
+// counters the program needs (*ncnt) without building it.
+static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, std::vector<evs_state::EngSeg>* segs,
+                           size_t* ncnt, int* row_floats) {
+  const evs_model* m = s->m;
+  const evs_config& c = m->cfg;
+  const int d = c.d_model, F = c.d_ffn, V = c.vocab;
+  size_t k = 0;
+  auto take = [&](int n) -> int* {
+    int* p = cnt ? cnt + k : nullptr;
+    k += n;
+    return p;
+  };
+  int wsi = 0;
+  std::vector<EngPhase>& ph = *out;
+  ph.clear();
+  segs->clear();
+  *row_floats = 0;
+  auto gemm = [&](const Partials& P, const uint8_t* wpk, int bmap, int* ready, int target) -> EngPhase& {
+    EngPhase e{};
+    e.kind = ENG_GEMM;
+    e.G = P.G;
+    e.KB = P.KB;
+    e.T = (P.N + TILE_M - 1) / TILE_M;
+    e.U = P.U;
+    e.bmap = bmap;
+    e.target = ready ? target : 0;
+    e.wpk = wpk;
+    e.tab = P.tab;
+    e.ws = s->ws[(wsi++) & 1];
+    e.cnt = take(e.T);
+    e.ready = ready;
+    ph.push_back(e);
+    return ph.back();
+  };
+  auto row = [&](int kind, int items, const EngPhase& src) -> EngPhase& {
+    EngPhase e{};
+    e.kind = kind;
+    e.G = items;
+    e.tab = src.tab;
+    e.ws = src.ws;
+    e.cnt = src.cnt;
+    e.ready = take(1);
+    ph.push_back(e);
+    return ph.back();
+  };
+  // residual add + RMSNorm after an out / down GEMM; returns the counter the
+  // normalised rows raise
+  auto resid_norm = [&](const EngPhase& g) -> int* {
+    EngPhase& r = row(ENG_RESID, d / TILE_M, g);
+    r.X = s->X;
+    r.ss = s->ss;
+    int* done = r.ready;
+    EngPhase e{};
+    e.kind = ENG_NORM;
+    e.G = d / TILE_K;
+    e.wait = done;
+    e.target = d / TILE_M;
+    e.ready = take(1);
+    e.X = s->X;
+    e.ss = s->ss;
+    e.out = s->xn;
+    e.out_ld = d;
+    ph.push_back(e);
+    return e.ready;
+  };
+  int* xn_ready = nullptr;  // the first in-projection reads the embedding kernel's rows
+  int seg0 = 0;
+  int* g_ready = nullptr;
+  int g_target = 0;
+  for (size_t i = 0; i < m->L.size(); ++i) {
+    const LayerW& w = m->L[i];
+    const LayerS& st = s->S[i];
+    EngPhase in = gemm(m->p_in, w.pk_in, ENG_B_XN, xn_ready, d / TILE_K);
+    if (w.kind == EVS_LAYER_ATTN) {
+      segs->push_back({seg0, (int)ph.size(), (int)i, in.ws});
+      seg0 = (int)ph.size();
+      g_ready = nullptr;  // the attention kernels finish before the next span starts
+      g_target = 0;
+    } else {
+      const bool fir = w.kind == EVS_LAYER_FIR;
+      const int items = fir ? d / 32 : d / (256 / w.param);
+      EngPhase& mx = row(fir ? ENG_FIR : ENG_IIR, items, in);
+      mx.L = w.param;
+      mx.p0 = fir ? w.taps : w.lam;
+      mx.p1 = fir ? nullptr : w.res;
+      mx.bank0 = fir ? st.ext[0] : st.st[0];
+      mx.bank1 = fir ? st.ext[1] : st.st[1];
+      mx.out = s->g;
+      mx.out_ld = d;
+      g_ready = mx.ready;
+      g_target = items;
+      *row_floats = std::max(*row_floats, engine_row_floats(mx.kind, w.param));
+    }
+    EngPhase out_g = gemm(m->p_out, w.pk_out, ENG_B_G, g_ready, g_target);
+    int* xr = resid_norm(out_g);
+    EngPhase gu = gemm(m->p_gu, w.pk_gu, ENG_B_XN, xr, d / TILE_K);
+    EngPhase& act = row(ENG_ACT, gu.T, gu);
+    act.out = s->h;
+    act.out_ld = F;
+    int* h_ready = act.ready;
+    const int h_items = act.G;
+    EngPhase dn = gemm(m->p_down, w.pk_down, ENG_B_H, h_ready, h_items);
+    xn_ready = resid_norm(dn);
+  }
+  // the head's stream-K view (G = tiles x cluster ranks, the packed order of its cluster plan)
+  EngPhase hd = gemm(m->q_head, m->pk_head, ENG_B_XN, xn_ready, d / TILE_K);
+  EngPhase& lg = row(ENG_LOGITS, V / TILE_M, hd);
+  lg.ready = nullptr;
+  segs->push_back({seg0, (int)ph.size(), -1, nullptr});
+  *ncnt = k + 1;  // + the abort flag
+}
+
+static int build_engine(evs_state* s) {
+  s->engine_ok = false;
+  s->use_engine = false;
+  if (!engine_eligible(s->m)) return EVS_OK;
+  std::vector<EngPhase> prog;
+  std::vector<evs_state::EngSeg> segs;
+  size_t ncnt = 0;
+  int rf = 0;
+  engine_program(s, nullptr, &prog, &segs, &ncnt, &rf);
+  void* cnt = nullptr;
+  EVS_TRY(dmalloc(s, &cnt, sizeof(int) * ncnt));
+  engine_program(s, static_cast<int*>(cnt), &prog, &segs, &ncnt, &rf);
+  if (engine_smem(rf) > 232448) return EVS_OK;
+  void* dprog = nullptr;
+  EVS_TRY(dmalloc(s, &dprog, sizeof(EngPhase) * prog.size()));
+  CUDA_TRY(cudaMemcpy(dprog, prog.data(), sizeof(EngPhase) * prog.size(), cudaMemcpyHostToDevice));
+  s->eng_prog = static_cast<EngPhase*>(dprog);
+  s->eng_segs = segs;
+  s->eng_cnt = static_cast<int*>(cnt);
+  s->eng_cnt_bytes = sizeof(int) * ncnt;
+  s->eng_row_floats = rf;
+  s->engine_ok = true;
+  s->use_engine = true;
+  return EVS_OK;
+}
+
+// One verify of a single sequence's block through the engine: counters
+// cleared, embedding + first norm, then every span as one persistent launch
+// with the attention mixers between spans.
+static int enqueue_verify_engine(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc) {
+  const evs_model* m = s->m;
+  const evs_config& c = m->cfg;
+  CUDA_TRY(cudaMemsetAsync(s->eng_cnt, 0, s->eng_cnt_bytes, Lc.stream));
+  const SeqRows sr = one_seq(n);
+  CUDA_TRY(launch_embed_norm(Lc, c.dtype, m->embed, tokens, sr, c.d_model, c.vocab, c.norm_eps, s->X, s->xn,
+                             one_ptr(s->book)));
+  const LaunchCtx Le{Lc.stream, false};
+  for (const auto& sg : s->eng_segs) {
+    EngArgs a{};
+    a.prog = s->eng_prog;
+    a.ph0 = sg.ph0;
+    a.ph1 = sg.ph1;
+    a.n = n;
+    a.d = c.d_model;
+    a.eps = c.norm_eps;
+    a.gabort = s->eng_cnt + s->eng_cnt_bytes / sizeof(int) - 1;
+    a.book = s->book;
+    a.logits = logits;
+    a.V = c.vocab;
+    a.row_floats = s->eng_row_floats;
+    CUDA_TRY(launch_engine(Le, s->m_xn, s->m_g, s->m_h, a, m->num_sms));
+    if (sg.attn_layer >= 0) {
+      const LayerS& st = s->S[sg.attn_layer];
+      AttnSeq as{};
+      as.kc.p[0] = st.kc;
+      as.vc.p[0] = st.vc;
+      as.book.p[0] = s->book;
+      as.part_o.p[0] = s->ab.part_o;
+      as.part_ml.p[0] = s->ab.part_ml;
+      MixSrc src{s->fin, 3 * c.d_model, 1, sg.attn_ws, m->p_in.tab, NTOK};
+      CUDA_TRY(launch_attention(Lc, c.dtype, src, c.n_heads, c.head_dim, sr, s->ctx_max, c.attn_chunk, as, s->ab,
+                                s->g));
+    }
+  }
   return EVS_OK;
 }
 
@@ -380,6 +595,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
 
 int enqueue_verify(evs_state* s, const int32_t* tokens, int n, float* logits, const LaunchCtx& Lc,
                    float* trace = nullptr) {
+  if (s->use_engine && !trace) return enqueue_verify_engine(s, tokens, n, logits, Lc);
   return enqueue_verify(&s, one_seq(n), tokens, logits, Lc, trace);
 }
 
@@ -786,6 +1002,7 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   cudaMemset(s->g, 0, es * R * d);
   cudaMemset(s->h, 0, es * R * F);
   r = evs_state_reset(s, 0);
+  if (r == EVS_OK) r = build_engine(s);
   if (r == EVS_OK) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) r = fail(EVS_ERR_CUDA, "state init: %s", cudaGetErrorString(e));
@@ -878,6 +1095,17 @@ extern "C" int evs_state_check(evs_state* s, cudaStream_t stream, int32_t* statu
 extern "C" int evs_state_use_graphs(evs_state* s, int32_t enable) {
   if (!s) return fail(EVS_ERR_ARG, "null state");
   s->use_graphs = enable != 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_state_use_engine(evs_state* s, int32_t enable) {
+  if (!s) return fail(EVS_ERR_ARG, "null state");
+  if (enable && !s->engine_ok) return fail(EVS_ERR_UNSUPPORTED, "the persistent engine does not take this model");
+  if ((enable != 0) != s->use_engine) {
+    for (auto& g : s->graphs) cudaGraphExecDestroy(g.exec);  // captured with the other path
+    s->graphs.clear();
+  }
+  s->use_engine = enable != 0;
   return EVS_OK;
 }
 
@@ -1558,6 +1786,12 @@ extern "C" int64_t evs_kernel_launches(void) { return g_launches.load(); }
 extern "C" int32_t evs_verify_kernel_count(const evs_state* s, int32_t n) {
   (void)n;
   if (!s) return -1;
+  if (s->use_engine) {
+    // embed, one engine launch per span, three attention kernels per attention layer
+    int k = 1 + (int)s->eng_segs.size();
+    for (const auto& L : s->m->L) k += L.kind == EVS_LAYER_ATTN ? 3 : 0;
+    return k;
+  }
   int k = 1 + 2;  // embed, head GEMM, logits
   // per layer: 4 GEMMs + the mixer (3 kernels for attention), plus two
   // RMSNorm kernels and the activation kernel unless the GEMMs do that work

@@ -203,6 +203,16 @@ int evs_state_book_write(evs_state* s, const evs_book* in_host, cudaStream_t str
 int evs_state_check(evs_state* s, cudaStream_t stream, int32_t* status_host);
 /* Capture verify / commit sequences in CUDA graphs (default on). */
 int evs_state_use_graphs(evs_state* s, int32_t enable);
+/* Run single-sequence verifies through the persistent engine (default on
+ * where the model allows it: bf16 storage, FIR filters of at most 128
+ * taps): one kernel per span of layers between attention mixers, in which
+ * the weight GEMMs stream without stopping at layer boundaries and the row
+ * work between them (mixers, residual add + RMSNorm, SiLU-and-multiply,
+ * logits) runs on other warps of the same CTAs.  Results equal the separate
+ * kernels' bit for bit.  Traced and batched verifies always use the
+ * separate kernels.  EVS_ERR_UNSUPPORTED when enabling it for a model it
+ * does not take. */
+int evs_state_use_engine(evs_state* s, int32_t enable);
 
 /* ---------------------------------------------------------------- path */
 /* Block verify ([abstract] (i); [implemented]; [prereq1]).

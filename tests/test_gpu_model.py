@@ -296,8 +296,10 @@ def test_fused_norm_and_activation_equal_separate_kernels_bitwise(which, monkeyp
     states = [evs.State(m, 256) for m in models]
     nb = shape.n_block
     L = len(shape.layers)
+    states[0].use_engine(False)  # kernel counts of the separate-kernel path
     counts = [evs.evs_verify_kernel_count(st, nb) for st in states]
     assert counts[0] - counts[1] == L and counts[1] - counts[2] == 2 * L
+    states[0].use_engine(True)  # the default model's verifies run through the engine
     prompt = [int(x) for x in synth.prompt(shape, 21, 3 * nb + 5)]
     for s0 in range(0, len(prompt), nb):
         chunk = prompt[s0:s0 + nb]
