@@ -33,7 +33,9 @@ namespace evs {
 namespace {
 
 constexpr int E_S = 8;             // ring stages (weight + activation tile each)
-constexpr int E_PF = 8;            // units prefetched into L2 beyond the ring
+constexpr int E_SLOG = 3;          // log2(E_S)
+static_assert((1 << E_SLOG) == E_S, "ring depth is a power of two");
+constexpr int E_PF = 16;           // units kept prefetched into L2 beyond the ring
 constexpr int E_THREADS = 512;
 constexpr int E_EPI0 = 4;          // first epilogue warp (warps 4..7 own TMEM lane quarters 0..3)
 constexpr int E_ROW0 = 8;          // first row-work warp
@@ -46,6 +48,23 @@ constexpr uint64_t E_WAIT_NS = 2000000000ull;  // bound on any wait
 constexpr size_t E_BAR_OFF = (size_t)E_S * (EA_BYTES + EB_BYTES);
 constexpr size_t E_ROW_OFF = (E_BAR_OFF + (3 * E_S + 5) * 8 + 64 + 127) & ~(size_t)127;
 constexpr size_t E_FIXED = 1024 + E_ROW_OFF;
+
+// Timeline hooks, compiled in only for profiling builds (EVS_ENGINE_TRACE):
+// per CTA and program phase, the time of event ev (producer first / last
+// unit, activation readiness, first / last MMA, last epilogue count, first
+// row item start / last row item end).
+#ifdef EVS_ENGINE_TRACE
+constexpr int ETR_CTAS = 160, ETR_PHASES = 512, ETR_EV = 16;
+__device__ unsigned long long g_etrace[(size_t)ETR_CTAS * ETR_PHASES * ETR_EV];
+#define ETR(ph, ev)                                                                                             \
+  do {                                                                                                          \
+    if (c < ETR_CTAS && (ph) < ETR_PHASES) g_etrace[((size_t)c * ETR_PHASES + (ph)) * ETR_EV + (ev)] = gtimer(); \
+  } while (0)
+#else
+#define ETR(ph, ev) \
+  do {              \
+  } while (0)
+#endif
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -131,34 +150,6 @@ __device__ __forceinline__ void unit_range(const EngPhase& P, int c, long long* 
   }
 }
 
-// Cursor over this CTA's weight units across the GEMM phases [ph, ph1).
-struct UnitCursor {
-  int ph, ph1, c;
-  long long u, ue;
-  const uint8_t* wp;
-  size_t step;
-  const EngPhase* prog;
-  __device__ bool seek(int from) {
-    for (ph = from; ph < ph1; ++ph) {
-      const EngPhase& P = prog[ph];
-      if (P.kind != ENG_GEMM) continue;
-      long long ub;
-      unit_range(P, c, &ub, &ue);
-      if (ub < ue) {
-        u = ub;
-        wp = P.wpk + (size_t)c * EA_BYTES;
-        step = (size_t)P.G * EA_BYTES;
-        return true;
-      }
-    }
-    return false;
-  }
-  __device__ bool next() {
-    wp += step;
-    return ++u < ue || seek(ph + 1);
-  }
-};
-
 // ------------------------------------------------------------------ row work
 // Items of the row phases.  Each is done by the 256 row-work threads of one
 // CTA (rt = their index); the arithmetic and its order are those of the
@@ -167,12 +158,26 @@ struct UnitCursor {
 // Waits (one thread) until every contributor of the listed tiles of the
 // GEMM whose slots a row phase reads has finished; the row threads proceed
 // together.
+#ifdef EVS_ENGINE_TRACE
+__device__ int g_trace_ph[ETR_CTAS];  // the row phase each CTA is working on
+#define ETR_ROW(ev)                                             \
+  do {                                                          \
+    const int c = blockIdx.x;                                   \
+    if (threadIdx.x == E_ROW0 * 32 && c < ETR_CTAS) ETR(g_trace_ph[c], ev); \
+  } while (0)
+#else
+#define ETR_ROW(ev) \
+  do {              \
+  } while (0)
+#endif
+
 __device__ bool row_wait_tiles(const EngPhase& P, const int* tiles, int k, Abort ab, volatile int* s_flag) {
   const int rt = threadIdx.x - E_ROW0 * 32;
   if (rt == 0) {
     bool ok = true;
     for (int i = 0; i < k && ok; ++i) ok = e_count_wait(P.cnt + tiles[i], __ldg(&P.tab[tiles[i]].y), ab);
     *s_flag = ok ? 1 : 0;
+    ETR_ROW(8);
   }
   row_sync();
   const bool ok = *s_flag != 0;
@@ -182,9 +187,14 @@ __device__ bool row_wait_tiles(const EngPhase& P, const int* tiles, int k, Abort
 // All row threads' outputs of an item are written: make them visible to the
 // async proxy (TMA readers), then count the item.
 __device__ void row_signal(int* counter, bool tma_readers) {
+  ETR_ROW(9);
   if (tma_readers) fence_proxy_async_global();
+  ETR_ROW(10);
   row_sync();
-  if (threadIdx.x == E_ROW0 * 32) red_release_add(counter, 1);
+  if (threadIdx.x == E_ROW0 * 32) {
+    red_release_add(counter, 1);
+    ETR_ROW(11);
+  }
 }
 
 // FIR mixer for 32 channels (fir_kernel's arithmetic; the taps are split
@@ -279,50 +289,58 @@ __device__ bool fir_item(const EngPhase& P, int j, int n, int d, const evs_book*
   return true;
 }
 
-// IIR modal mixer for 256 / M channels (iir_kernel's arithmetic).
-template <int M>
+// IIR modal mixer for NS blocks of 256 / M channels (iir_kernel's
+// arithmetic); thread (cl, m) runs pole m of channel cl of every block, the
+// blocks' recurrences interleaved.
+template <int M, int NS>
 __device__ bool iir_item(const EngPhase& P, int j, int n, int d, const evs_book* book, float* sm, Abort ab,
                          volatile int* s_flag) {
-  constexpr int CPB = 256 / M;
-  float* z_s = sm;               // [NTOK][CPB]
-  float* a_s = sm + NTOK * CPB;  // [NTOK][CPB]
+  constexpr int CPB = 256 / M, CH = NS * CPB;
+  float* z_s = sm;             // [NTOK][CH]
+  float* a_s = sm + NTOK * CH; // [NTOK][CH]
   const int rt = threadIdx.x - E_ROW0 * 32;
   const int cl = rt / M, m = rt % M;
-  const int c0 = j * CPB, c = c0 + cl;
+  const int c0 = j * CH;
   const float2* lam = reinterpret_cast<const float2*>(P.p0);
   const float2* res = reinterpret_cast<const float2*>(P.p1);
-  const float2 L = lam[(size_t)c * M + m];
-  const float2 R = res[(size_t)c * M + m];
   const int bank = book->iir_bank, slot = book->iir_slot;
   const float2* cur = reinterpret_cast<const float2*>(bank ? P.bank1 : P.bank0);
   float2* dst = reinterpret_cast<float2*>(bank ? P.bank0 : P.bank1);
-  float2 s = make_float2(0.f, 0.f);
-  if (slot >= 0) s = cur[((size_t)slot * d + c) * M + m];
-  const int cc = c0 + rt % CPB;
+  float2 L[NS], R[NS], s[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int c = c0 + k * CPB + cl;
+    L[k] = lam[(size_t)c * M + m];
+    R[k] = res[(size_t)c * M + m];
+    s[k] = slot >= 0 ? cur[((size_t)slot * d + c) * M + m] : make_float2(0.f, 0.f);
+  }
   const int tiles[3] = {c0 / TILE_M, (d + c0) / TILE_M, (2 * d + c0) / TILE_M};
   if (!row_wait_tiles(P, tiles, 3, ab, s_flag)) return false;
   const SrcSlots src{P.ws, P.tab, NTOK};
-  const auto ca = src.at(cc), cb = src.at(d + cc), cv = src.at(2 * d + cc);
-  for (int e = rt; e < n * CPB; e += 256) {
-    const int t = e / CPB;
-    const float a = stored<bf16>(src.get(ca, t, cc));
-    const float b = stored<bf16>(src.get(cb, t, d + cc));
-    const float v = stored<bf16>(src.get(cv, t, 2 * d + cc));
-    a_s[t * CPB + e % CPB] = a;
-    z_s[t * CPB + e % CPB] = b * v;
+  for (int e = rt; e < n * CH; e += E_ROWT) {
+    const int t = e / CH, cc = c0 + e % CH;
+    const float a = stored<bf16>(src.get(src.at(cc), t, cc));
+    const float b = stored<bf16>(src.get(src.at(d + cc), t, d + cc));
+    const float v = stored<bf16>(src.get(src.at(2 * d + cc), t, 2 * d + cc));
+    a_s[t * CH + e % CH] = a;
+    z_s[t * CH + e % CH] = b * v;
   }
   row_sync();
   bf16* g = static_cast<bf16*>(P.out);
   for (int t = 0; t < n; ++t) {
-    const float z = z_s[t * CPB + cl];
-    const float sr = fmaf(L.x, s.x, fmaf(-L.y, s.y, z));
-    const float si = fmaf(L.x, s.y, L.y * s.x);
-    s = make_float2(sr, si);
-    dst[((size_t)t * d + c) * M + m] = s;
-    float y = fmaf(R.x, s.x, -R.y * s.y);
 #pragma unroll
-    for (int o = M / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-    if (m == 0) g[(size_t)t * d + c] = __float2bfloat16_rn(a_s[t * CPB + cl] * y);
+    for (int k = 0; k < NS; ++k) {
+      const int ci = k * CPB + cl, c = c0 + ci;
+      const float z = z_s[t * CH + ci];
+      const float sr = fmaf(L[k].x, s[k].x, fmaf(-L[k].y, s[k].y, z));
+      const float si = fmaf(L[k].x, s[k].y, L[k].y * s[k].x);
+      s[k] = make_float2(sr, si);
+      dst[((size_t)t * d + c) * M + m] = s[k];
+      float y = fmaf(R[k].x, s[k].x, -R[k].y * s[k].y);
+#pragma unroll
+      for (int o = M / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+      if (m == 0) g[(size_t)t * d + c] = __float2bfloat16_rn(a_s[t * CH + ci] * y);
+    }
   }
   row_signal(P.ready, true);
   row_sync();
@@ -331,50 +349,52 @@ __device__ bool iir_item(const EngPhase& P, int j, int n, int d, const evs_book*
 
 // Residual add of one 128-column tile from the out / down GEMM's slots and
 // the tile's per-row sum of squares (resid_norm_kernel's arithmetic: lane l
-// owns columns 4l .. 4l+3, the squares meet in the GEMM epilogue's order).
-__device__ bool resid_item(const EngPhase& P, int t, int n, int d, Abort ab, volatile int* s_flag) {
+// owns columns 4l .. 4l+3, the squares meet in the GEMM epilogue's order);
+// then, once every tile of the rows is added, the RMSNorm of this tile: the
+// row's sum of squares is its tile sums added in tile order.
+__device__ bool resid_item(const EngPhase& P, int t, int n, int d, float eps, Abort ab, volatile int* s_flag) {
   if (!row_wait_tiles(P, &t, 1, ab, s_flag)) return false;
   const int rt = threadIdx.x - E_ROW0 * 32, lane = rt & 31, warp = rt >> 5;
   const SrcSlots src{P.ws, P.tab, NTOK};
-  const int col = t * TILE_M + 4 * lane;
-  const SrcSlots::Col c = src.at(col);
-  const size_t stride = (size_t)src.rows * TILE_M;
-  for (int r = warp; r < n; r += E_ROWW) {
-    float* xr = P.X + (size_t)r * d + col;
-    const float* p = c.p + (size_t)r * TILE_M;
-    float4 x = __ldcg(reinterpret_cast<const float4*>(xr));
-    const float4 v0 = __ldcg(reinterpret_cast<const float4*>(p));
-    float4 a[SLOTS_RESID_MAX];
+  {
+    const int col = t * TILE_M + 4 * lane;
+    const SrcSlots::Col c = src.at(col);
+    const size_t stride = (size_t)src.rows * TILE_M;
+    for (int r = warp; r < n; r += E_ROWW) {
+      float* xr = P.X + (size_t)r * d + col;
+      const float* p = c.p + (size_t)r * TILE_M;
+      float4 x = __ldcg(reinterpret_cast<const float4*>(xr));
+      const float4 v0 = __ldcg(reinterpret_cast<const float4*>(p));
+      float4 a[SLOTS_RESID_MAX];
 #pragma unroll
-    for (int q = 1; q < SLOTS_RESID_MAX; ++q)
-      a[q] = c.cnt > q ? __ldcg(reinterpret_cast<const float4*>(p + q * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 1; q < SLOTS_RESID_MAX; ++q)
+        a[q] = c.cnt > q ? __ldcg(reinterpret_cast<const float4*>(p + q * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int q = 1; q < SLOTS_RESID_MAX; ++q) v.x += a[q].x, v.y += a[q].y, v.z += a[q].z, v.w += a[q].w;
-    x.x += v0.x + v.x;
-    x.y += v0.y + v.y;
-    x.z += v0.z + v.z;
-    x.w += v0.w + v.w;
-    __stcg(reinterpret_cast<float4*>(xr), x);
-    float q4[4] = {x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w};
+      for (int q = 1; q < SLOTS_RESID_MAX; ++q) v.x += a[q].x, v.y += a[q].y, v.z += a[q].z, v.w += a[q].w;
+      x.x += v0.x + v.x;
+      x.y += v0.y + v.y;
+      x.z += v0.z + v.z;
+      x.w += v0.w + v.w;
+      __stcg(reinterpret_cast<float4*>(xr), x);
+      float q4[4] = {x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w};
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1)  // column xor 16, 8, 4
+      for (int o = 4; o > 0; o >>= 1)  // column xor 16, 8, 4
 #pragma unroll
-      for (int k = 0; k < 4; ++k) q4[k] += __shfl_xor_sync(0xffffffffu, q4[k], o);
-    const float wsum = (q4[0] + q4[2]) + (q4[1] + q4[3]);  // column xor 2, then 1
-    const float w1 = __shfl_sync(0xffffffffu, wsum, 8), w2 = __shfl_sync(0xffffffffu, wsum, 16);
-    const float w3 = __shfl_sync(0xffffffffu, wsum, 24);
-    if (lane == 0) __stcg(P.ss + (size_t)t * ROWS_MAX + r, ((wsum + w1) + w2) + w3);
+        for (int k = 0; k < 4; ++k) q4[k] += __shfl_xor_sync(0xffffffffu, q4[k], o);
+      const float wsum = (q4[0] + q4[2]) + (q4[1] + q4[3]);  // column xor 2, then 1
+      const float w1 = __shfl_sync(0xffffffffu, wsum, 8), w2 = __shfl_sync(0xffffffffu, wsum, 16);
+      const float w3 = __shfl_sync(0xffffffffu, wsum, 24);
+      if (lane == 0) __stcg(P.ss + (size_t)t * ROWS_MAX + r, ((wsum + w1) + w2) + w3);
+    }
   }
-  row_signal(P.ready, false);
-  return true;
-}
-
-// RMSNorm of 64 columns of every row once all tiles are added: the row's sum
-// of squares is its tile sums added in tile order (as resid_norm_kernel).
-__device__ bool norm_item(const EngPhase& P, int kb, int n, int d, float eps, Abort ab, volatile int* s_flag) {
-  const int rt = threadIdx.x - E_ROW0 * 32;
-  if (rt == 0) *s_flag = e_count_wait(P.wait, P.target, ab) ? 1 : 0;
+  row_sync();
+  if (rt == 0) {
+    ETR_ROW(12);
+    red_release_add(P.done, 1);
+    *s_flag = e_count_wait(P.done, d / TILE_M, ab) ? 1 : 0;
+    ETR_ROW(13);
+  }
   row_sync();
   const bool ok = *s_flag != 0;
   row_sync();
@@ -385,33 +405,40 @@ __device__ bool norm_item(const EngPhase& P, int kb, int n, int d, float eps, Ab
     float tot = 0.f;
     for (int k = 0; k < ntiles; ++k) tot += __ldcg(P.ss + (size_t)k * ROWS_MAX + r);
     const float den = sqrtf(tot / (float)d + eps), rden = 1.f / den;
-    const int col = kb * TILE_K + 4 * q;
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(P.X + (size_t)r * d + col));
+    const int col = t * TILE_M + 8 * q;
+    const float4 x0 = __ldcg(reinterpret_cast<const float4*>(P.X + (size_t)r * d + col));
+    const float4 x1 = __ldcg(reinterpret_cast<const float4*>(P.X + (size_t)r * d + col + 4));
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
     bf16* xo = static_cast<bf16*>(P.out) + (size_t)r * P.out_ld + col;
-    xo[0] = __float2bfloat16_rn(div_row(x.x, den, rden));
-    xo[1] = __float2bfloat16_rn(div_row(x.y, den, rden));
-    xo[2] = __float2bfloat16_rn(div_row(x.z, den, rden));
-    xo[3] = __float2bfloat16_rn(div_row(x.w, den, rden));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xo[k] = __float2bfloat16_rn(div_row(xs[k], den, rden));
   }
   row_signal(P.ready, true);
   return true;
 }
 
-// SiLU-and-multiply of gate/up tile t (the packed gate/up rows interleave 64
-// gate and 64 up rows per tile): h columns 64t .. 64t+63.
-__device__ bool act_item(const EngPhase& P, int t, int n, Abort ab, volatile int* s_flag) {
-  if (!row_wait_tiles(P, &t, 1, ab, s_flag)) return false;
+// SiLU-and-multiply of gate/up tiles j*sub .. j*sub+sub-1 (the packed
+// gate/up rows interleave 64 gate and 64 up rows per tile): tile t gives h
+// columns 64t .. 64t+63 (mlp_act_kernel's arithmetic).
+__device__ bool act_item(const EngPhase& P, int j, int n, Abort ab, volatile int* s_flag) {
+  int tiles[2];
+  int k = 0;
+  for (; k < P.sub && j * P.sub + k < P.T; ++k) tiles[k] = j * P.sub + k;
+  if (!row_wait_tiles(P, tiles, k, ab, s_flag)) return false;
   const int rt = threadIdx.x - E_ROW0 * 32;
   const int r = rt >> 4, q = rt & 15;
   if (r < n) {
     const SrcSlots src{P.ws, P.tab, NTOK};
     bf16* h = static_cast<bf16*>(P.out) + (size_t)r * P.out_ld;
+    for (int i = 0; i < k; ++i) {
+      const int t = tiles[i];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int jj = 4 * q + k;                 // column within the tile's 64 outputs
-      const int gj = t * TILE_M + jj, uj = gj + TILE_M / 2;
-      const float gt = src.get(src.at(gj), r, gj), up = src.get(src.at(uj), r, uj);
-      h[t * (TILE_M / 2) + jj] = __float2bfloat16_rn(silu_f(gt) * up);
+      for (int e = 0; e < 4; ++e) {
+        const int jj = 4 * q + e;  // column within the tile's 64 outputs
+        const int gj = t * TILE_M + jj, uj = gj + TILE_M / 2;
+        const float gt = src.get(src.at(gj), r, gj), up = src.get(src.at(uj), r, uj);
+        h[t * (TILE_M / 2) + jj] = __float2bfloat16_rn(silu_f(gt) * up);
+      }
     }
   }
   row_signal(P.ready, true);
@@ -427,6 +454,11 @@ __device__ bool logits_item(const EngPhase& P, int t, int n, float* logits, int 
   const SrcSlots::Col c = src.at(col);
   for (int r = rt >> 7; r < n; r += E_ROWT / TILE_M) logits[(size_t)r * V + col] = src.get<8>(c, r, col);
   return true;
+}
+
+template <int M>
+__device__ bool iir_sub(const EngPhase& P, int j, const EngArgs& a, float* sm, Abort ab, volatile int* f) {
+  return P.sub == 2 ? iir_item<M, 2>(P, j, a.n, a.d, a.book, sm, ab, f) : iir_item<M, 1>(P, j, a.n, a.d, a.book, sm, ab, f);
 }
 
 __device__ bool row_item(const EngPhase& P, int j, const EngArgs& a, float* sm, Abort ab, volatile int* f) {
@@ -445,15 +477,14 @@ __device__ bool row_item(const EngPhase& P, int j, const EngArgs& a, float* sm, 
     }
     case ENG_IIR:
       switch (P.L) {
-        case 1: return iir_item<1>(P, j, a.n, a.d, a.book, sm, ab, f);
-        case 2: return iir_item<2>(P, j, a.n, a.d, a.book, sm, ab, f);
-        case 4: return iir_item<4>(P, j, a.n, a.d, a.book, sm, ab, f);
-        case 8: return iir_item<8>(P, j, a.n, a.d, a.book, sm, ab, f);
-        case 16: return iir_item<16>(P, j, a.n, a.d, a.book, sm, ab, f);
-        default: return iir_item<32>(P, j, a.n, a.d, a.book, sm, ab, f);
+        case 1: return iir_sub<1>(P, j, a, sm, ab, f);
+        case 2: return iir_sub<2>(P, j, a, sm, ab, f);
+        case 4: return iir_sub<4>(P, j, a, sm, ab, f);
+        case 8: return iir_sub<8>(P, j, a, sm, ab, f);
+        case 16: return iir_sub<16>(P, j, a, sm, ab, f);
+        default: return iir_sub<32>(P, j, a, sm, ab, f);
       }
-    case ENG_RESID: return resid_item(P, j, a.n, a.d, ab, f);
-    case ENG_NORM: return norm_item(P, j, a.n, a.d, a.eps, ab, f);
+    case ENG_RESID: return resid_item(P, j, a.n, a.d, a.eps, ab, f);
     case ENG_ACT: return act_item(P, j, a.n, ab, f);
     case ENG_LOGITS: return logits_item(P, j, a.n, a.logits, a.V, ab, f);
     default: return true;
@@ -472,6 +503,7 @@ __global__ void __launch_bounds__(E_THREADS, 1)
   volatile int* abort_local = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // epilogue
   volatile int* s_row = reinterpret_cast<volatile int*>(tmem_slot + 3);  // row work
+  volatile int* s_prod = reinterpret_cast<volatile int*>(tmem_slot + 4); // units the producer has issued
   float* row_sm = reinterpret_cast<float*>(smem + E_ROW_OFF);
   auto w_full = [&](int s) { return smem_u32(bars + s); };
   auto b_full = [&](int s) { return smem_u32(bars + E_S + s); };
@@ -496,6 +528,7 @@ __global__ void __launch_bounds__(E_THREADS, 1)
     }
     mbar_init(drain, 1);
     *abort_local = 0;
+    *s_prod = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&m_xn)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&m_g)) : "memory");
@@ -513,30 +546,61 @@ __global__ void __launch_bounds__(E_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- weight producer
+    // ---------------- weight producer: tight loop, one bulk copy per unit
     const uint64_t pol = policy_evict_first();
-    UnitCursor ld{0, a.ph1, c, 0, 0, nullptr, 0, prog};
-    bool more = ld.seek(a.ph0);
-    UnitCursor pf = ld;
-    bool pf_more = more;
-    for (int k = 0; k < E_S && pf_more; ++k) pf_more = pf.next();
-    for (int k = 0; k < E_PF && pf_more; ++k) {
-      bulk_prefetch_l2(pf.wp, EA_BYTES);
-      pf_more = pf.next();
-    }
     long long i = 0;
-    for (; more; ++i) {
-      const int s = (int)(i % E_S);
-      if (i >= E_S && !e_mbar_wait(empty(s), (uint32_t)((i / E_S) - 1) & 1, ab)) break;
-      mbar_expect_tx(w_full(s), EA_BYTES);
-      bulk_load(smem_u32(sA + s * EA_BYTES), ld.wp, EA_BYTES, w_full(s), pol);
-      if (pf_more) {
-        bulk_prefetch_l2(pf.wp, EA_BYTES);
-        pf_more = pf.next();
+    bool stop = false;
+    for (int ph = a.ph0; ph < a.ph1 && !stop; ++ph) {
+      const EngPhase& P = prog[ph];
+      if (P.kind != ENG_GEMM) continue;
+      long long ub, ue;
+      unit_range(P, c, &ub, &ue);
+      if (ub >= ue) continue;
+      const uint8_t* wp = P.wpk + (size_t)c * EA_BYTES;
+      const size_t step = (size_t)P.G * EA_BYTES;
+      ETR(ph, 0);
+      for (long long u = ub; u < ue; ++u, ++i) {
+        const int s = (int)(i & (E_S - 1));
+        if (i >= E_S && !e_mbar_wait(empty(s), (uint32_t)((i >> E_SLOG) - 1) & 1, ab)) {
+          stop = true;
+          break;
+        }
+        mbar_expect_tx(w_full(s), EA_BYTES);
+        bulk_load(smem_u32(sA + s * EA_BYTES), wp, EA_BYTES, w_full(s), pol);
+        wp += step;
+        *s_prod = (int)(i + 1);
       }
-      more = ld.next();
+      ETR(ph, 1);
     }
-    for (long long j = i > E_S ? i - E_S : 0; j < i; ++j) drain_wait(w_full((int)(j % E_S)), (uint32_t)(j / E_S) & 1);
+    for (long long j = i > E_S ? i - E_S : 0; j < i; ++j)
+      drain_wait(w_full((int)(j & (E_S - 1))), (uint32_t)(j >> E_SLOG) & 1);
+  } else if (warp == 3 && lane == 0) {
+    // ---------------- L2 prefetch: the units E_S .. E_S + E_PF - 1 beyond the
+    // producer's front, so a stall of the ring does not stop the HBM stream
+    long long i = 0;
+    bool stop = false;
+    const uint64_t t0 = gtimer();
+    for (int ph = a.ph0; ph < a.ph1 && !stop; ++ph) {
+      const EngPhase& P = prog[ph];
+      if (P.kind != ENG_GEMM) continue;
+      long long ub, ue;
+      unit_range(P, c, &ub, &ue);
+      if (ub >= ue) continue;
+      const uint8_t* wp = P.wpk + (size_t)c * EA_BYTES;
+      const size_t step = (size_t)P.G * EA_BYTES;
+      for (long long u = ub; u < ue; ++u, ++i, wp += step) {
+        if (i < E_S) continue;  // the ring's first fill
+        while (i >= (long long)*s_prod + E_S + E_PF) {
+          if (aborted(ab) || gtimer() - t0 > E_WAIT_NS) {
+            stop = true;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (stop) break;
+        bulk_prefetch_l2(wp, EA_BYTES);
+      }
+    }
   } else if (warp == 2 && lane == 0) {
     // ---------------- activation loader
     const uint64_t pol = policy_evict_last();
@@ -552,18 +616,25 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         if (!e_count_wait(P.ready, P.target, ab)) break;
         fence_proxy_async_global();
       }
+      ETR(ph, 2);
       const CUtensorMap* map = P.bmap == ENG_B_XN ? &m_xn : P.bmap == ENG_B_G ? &m_g : &m_h;
+      const int KB = P.KB;
+      int kb = (int)(ub % KB);
       for (long long u = ub; u < ue; ++u, ++i) {
-        const int s = (int)(i % E_S);
-        if (i >= E_S && !e_mbar_wait(empty(s), (uint32_t)((i / E_S) - 1) & 1, ab)) {
+        const int s = (int)(i & (E_S - 1));
+        if (i >= E_S && !e_mbar_wait(empty(s), (uint32_t)((i >> E_SLOG) - 1) & 1, ab)) {
           ok = false;
           break;
         }
         mbar_expect_tx(b_full(s), EB_BYTES);
-        tma_load_2d(smem_u32(sB + s * EB_BYTES), map, b_full(s), (int)(u % P.KB) * TILE_K, 0, pol);
+        tma_load_2d(smem_u32(sB + s * EB_BYTES), map, b_full(s), kb * TILE_K, 0, pol);
+        if (u == ub) ETR(ph, 8);
+        if (u == ub + 7) ETR(ph, 9);
+        if (++kb == KB) kb = 0;
       }
     }
-    for (long long j = i > E_S ? i - E_S : 0; j < i; ++j) drain_wait(b_full((int)(j % E_S)), (uint32_t)(j / E_S) & 1);
+    for (long long j = i > E_S ? i - E_S : 0; j < i; ++j)
+      drain_wait(b_full((int)(j & (E_S - 1))), (uint32_t)(j >> E_SLOG) & 1);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     const uint64_t ad0 = sw128_desc(smem_u32(sA)), bd0 = sw128_desc(smem_u32(sB));
@@ -591,13 +662,24 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         const uint32_t dt = tmem + (uint32_t)(b * NTOK);
         bool first = true;
         for (; u < seg_end; ++u, ++i) {
-          const int s = (int)(i % E_S);
-          const uint32_t par = (uint32_t)(i / E_S) & 1;
-          if (!e_mbar_wait(w_full(s), par, ab) || !e_mbar_wait(b_full(s), par, ab)) {
+          const int s = (int)(i & (E_S - 1));
+          const uint32_t par = (uint32_t)(i >> E_SLOG) & 1;
+          if (!e_mbar_wait(w_full(s), par, ab)) {
             ok = false;
             break;
           }
+          if (u == ub) ETR(ph, 10);
+          if (!e_mbar_wait(b_full(s), par, ab)) {
+            ok = false;
+            break;
+          }
+          if (u == ub) ETR(ph, 11);
+          if (u == ub + 1) ETR(ph, 12);
+          if (u == ub + 4) ETR(ph, 13);
           tc_fence_after();
+          if (u == ub) ETR(ph, 3);
+          if (u == ub + E_S) ETR(ph, 6);
+          if (u == ub + E_S + E_PF) ETR(ph, 7);
           const uint64_t ad = ad0 + (uint64_t)(s * (EA_BYTES >> 4));
           const uint64_t bd = bd0 + (uint64_t)(s * (EB_BYTES >> 4));
 #pragma unroll
@@ -607,6 +689,7 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         }
         if (ok) mma_commit(acc_full(b));
       }
+      ETR(ph, 4);
     }
     mma_commit(drain);
     drain_wait(drain, 0);
@@ -642,16 +725,31 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         for (int t = 0; t < NTOK; ++t)
           if (t < a.n) __stcg(dst + t * TILE_M, v[t]);
         epi_sync();
-        if (g == 0) red_release_add(P.cnt + tile, 1);
+        if (g == 0) {
+          red_release_add(P.cnt + tile, 1);
+          ETR(ph, 5);
+        }
       }
     }
   } else if (warp >= E_ROW0) {
     // ---------------- row work
-    bool ok = true;
-    for (int ph = a.ph0; ph < a.ph1 && ok; ++ph) {
+    for (int ph = a.ph0; ph < a.ph1; ++ph) {
       const EngPhase& P = prog[ph];
       if (P.kind == ENG_GEMM) continue;
-      for (int j = c; j < P.G && ok; j += gridDim.x) ok = row_item(P, j, a, row_sm, ab, s_row);
+#ifdef EVS_ENGINE_TRACE
+      if (threadIdx.x == E_ROW0 * 32 && c < ETR_CTAS) g_trace_ph[c] = ph;
+      if (threadIdx.x == E_ROW0 * 32) ETR(ph, 6);
+#endif
+      for (int j = c; j < P.G; j += gridDim.x)
+        if (!row_item(P, j, a, row_sm, ab, s_row)) break;
+      if (threadIdx.x == E_ROW0 * 32) ETR(ph, 7);
+      // all row warps leave the phase together and agree whether to go on
+      row_sync();
+      if (threadIdx.x == E_ROW0 * 32) *s_row = aborted(ab) ? 0 : 1;
+      row_sync();
+      const bool go = *s_row != 0;
+      row_sync();
+      if (!go) break;
     }
   }
 
@@ -666,12 +764,23 @@ __global__ void __launch_bounds__(E_THREADS, 1)
 
 }  // namespace
 
-int engine_row_floats(int kind, int param) {
+#ifdef EVS_ENGINE_TRACE
+// profiling builds only: copies the timeline out and clears it
+extern "C" int evs_engine_trace_read(unsigned long long* out_host) {
+  const size_t bytes = sizeof(g_etrace);
+  if (cudaMemcpyFromSymbol(out_host, g_etrace, bytes) != cudaSuccess) return 5;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_etrace) != cudaSuccess || cudaMemset(p, 0, bytes) != cudaSuccess) return 5;
+  return 0;
+}
+#endif
+
+int engine_row_floats(int kind, int param, int sub) {
   if (kind == ENG_FIR) {
     const int NW = param < 8 ? param : 8;
     return 32 * ((param - 1 + NTOK) + NTOK + param + NW * NTOK);
   }
-  if (kind == ENG_IIR) return 2 * NTOK * (256 / param);
+  if (kind == ENG_IIR) return 2 * NTOK * sub * (256 / param);
   return 0;
 }
 

@@ -219,17 +219,28 @@ int dmalloc(evs_state* s, void** p, size_t bytes) {
 // Whether the persistent engine can run this model: the bf16 packed path with
 // every stream-K GEMM leaving slots to its consumers, FIR filters of at most
 // 128 taps, and the head's stream-K view over its cluster plan.
+// The stream-K plan the engine runs a weight matrix with: the plan itself,
+// or for a cluster plan its stream-K twin, which gives every CTA the same
+// units (so the packed order is the same) and sums the same partials in the
+// same order (cluster ranks = slots).
+static const Partials& eng_plan(const Partials& p, const Partials& q) { return p.cl == 0 ? p : q; }
+
 static bool engine_eligible(const evs_model* m) {
   const evs_config& c = m->cfg;
   if (!(m->tc && m->packed && m->slots && m->slots_resid) || m->fuse || m->swiglu) return false;
-  if (m->p_in.cl || m->p_out.cl || m->p_gu.cl || m->p_down.cl) return false;
-  if (m->p_in.max_cnt > SLOTS_MIX_MAX || m->p_gu.max_cnt > SLOTS_MIX_MAX || m->p_out.max_cnt > SLOTS_RESID_MAX ||
-      m->p_down.max_cnt > SLOTS_RESID_MAX || m->q_head.max_cnt > 8)
+  const Partials& pin = eng_plan(m->p_in, m->q_in);
+  const Partials& pout = eng_plan(m->p_out, m->q_out);
+  const Partials& pgu = eng_plan(m->p_gu, m->q_gu);
+  const Partials& pdn = eng_plan(m->p_down, m->q_down);
+  const Partials& phd = eng_plan(m->p_head, m->q_head);
+  if (pin.max_cnt > SLOTS_MIX_MAX || pgu.max_cnt > SLOTS_MIX_MAX || pout.max_cnt > SLOTS_RESID_MAX ||
+      pdn.max_cnt > SLOTS_RESID_MAX || phd.max_cnt > 8)
     return false;
-  if (m->q_head.G != m->p_head.G || m->q_head.U != m->p_head.U) return false;
+  const Partials* all[5] = {&pin, &pout, &pgu, &pdn, &phd};
+  const Partials* own[5] = {&m->p_in, &m->p_out, &m->p_gu, &m->p_down, &m->p_head};
+  for (int k = 0; k < 5; ++k)
+    if (all[k]->G > m->num_sms || all[k]->G != own[k]->G || all[k]->U != own[k]->U) return false;
   if (c.d_model % TILE_M || c.d_model / TILE_M > RESID_TILES_ROW || c.d_ffn % TILE_K || c.vocab % TILE_M) return false;
-  if (m->p_in.G > m->num_sms || m->p_out.G > m->num_sms || m->p_gu.G > m->num_sms || m->p_down.G > m->num_sms)
-    return false;
   for (const LayerW& L : m->L)
     if (L.kind == EVS_LAYER_FIR && L.param > 128) return false;
   return true;
@@ -282,25 +293,16 @@ static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, s
     ph.push_back(e);
     return ph.back();
   };
-  // residual add + RMSNorm after an out / down GEMM; returns the counter the
-  // normalised rows raise
+  // residual add + RMSNorm after an out / down GEMM (one item per 128-column
+  // tile); returns the counter the normalised tiles raise
   auto resid_norm = [&](const EngPhase& g) -> int* {
     EngPhase& r = row(ENG_RESID, d / TILE_M, g);
+    r.done = take(1);
     r.X = s->X;
     r.ss = s->ss;
-    int* done = r.ready;
-    EngPhase e{};
-    e.kind = ENG_NORM;
-    e.G = d / TILE_K;
-    e.wait = done;
-    e.target = d / TILE_M;
-    e.ready = take(1);
-    e.X = s->X;
-    e.ss = s->ss;
-    e.out = s->xn;
-    e.out_ld = d;
-    ph.push_back(e);
-    return e.ready;
+    r.out = s->xn;
+    r.out_ld = d;
+    return r.ready;
   };
   int* xn_ready = nullptr;  // the first in-projection reads the embedding kernel's rows
   int seg0 = 0;
@@ -309,7 +311,7 @@ static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, s
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& w = m->L[i];
     const LayerS& st = s->S[i];
-    EngPhase in = gemm(m->p_in, w.pk_in, ENG_B_XN, xn_ready, d / TILE_K);
+    EngPhase in = gemm(eng_plan(m->p_in, m->q_in), w.pk_in, ENG_B_XN, xn_ready, d / TILE_M);
     if (w.kind == EVS_LAYER_ATTN) {
       segs->push_back({seg0, (int)ph.size(), (int)i, in.ws});
       seg0 = (int)ph.size();
@@ -317,9 +319,14 @@ static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, s
       g_target = 0;
     } else {
       const bool fir = w.kind == EVS_LAYER_FIR;
-      const int items = fir ? d / 32 : d / (256 / w.param);
+      // IIR items take two blocks of 256 / M channels when one block each
+      // would leave CTAs with two items
+      const int cpb = fir ? 32 : 256 / w.param;
+      const int sub = !fir && d / cpb > m->num_sms && d % (2 * cpb) == 0 && 2 * cpb <= TILE_M ? 2 : 1;
+      const int items = d / (cpb * sub);
       EngPhase& mx = row(fir ? ENG_FIR : ENG_IIR, items, in);
       mx.L = w.param;
+      mx.sub = sub;
       mx.p0 = fir ? w.taps : w.lam;
       mx.p1 = fir ? nullptr : w.res;
       mx.bank0 = fir ? st.ext[0] : st.st[0];
@@ -328,21 +335,24 @@ static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, s
       mx.out_ld = d;
       g_ready = mx.ready;
       g_target = items;
-      *row_floats = std::max(*row_floats, engine_row_floats(mx.kind, w.param));
+      *row_floats = std::max(*row_floats, engine_row_floats(mx.kind, w.param, sub));
     }
-    EngPhase out_g = gemm(m->p_out, w.pk_out, ENG_B_G, g_ready, g_target);
+    EngPhase out_g = gemm(eng_plan(m->p_out, m->q_out), w.pk_out, ENG_B_G, g_ready, g_target);
     int* xr = resid_norm(out_g);
-    EngPhase gu = gemm(m->p_gu, w.pk_gu, ENG_B_XN, xr, d / TILE_K);
-    EngPhase& act = row(ENG_ACT, gu.T, gu);
+    EngPhase gu = gemm(eng_plan(m->p_gu, m->q_gu), w.pk_gu, ENG_B_XN, xr, d / TILE_M);
+    // two gate/up tiles per item when one each would leave CTAs with two items
+    const int asub = gu.T > m->num_sms ? 2 : 1;
+    EngPhase& act = row(ENG_ACT, (gu.T + asub - 1) / asub, gu);
+    act.sub = asub;
+    act.T = gu.T;
     act.out = s->h;
     act.out_ld = F;
     int* h_ready = act.ready;
     const int h_items = act.G;
-    EngPhase dn = gemm(m->p_down, w.pk_down, ENG_B_H, h_ready, h_items);
+    EngPhase dn = gemm(eng_plan(m->p_down, m->q_down), w.pk_down, ENG_B_H, h_ready, h_items);
     xn_ready = resid_norm(dn);
   }
-  // the head's stream-K view (G = tiles x cluster ranks, the packed order of its cluster plan)
-  EngPhase hd = gemm(m->q_head, m->pk_head, ENG_B_XN, xn_ready, d / TILE_K);
+  EngPhase hd = gemm(eng_plan(m->p_head, m->q_head), m->pk_head, ENG_B_XN, xn_ready, d / TILE_M);
   EngPhase& lg = row(ENG_LOGITS, V / TILE_M, hd);
   lg.ready = nullptr;
   segs->push_back({seg0, (int)ph.size(), -1, nullptr});
@@ -371,7 +381,7 @@ static int build_engine(evs_state* s) {
   s->eng_cnt_bytes = sizeof(int) * ncnt;
   s->eng_row_floats = rf;
   s->engine_ok = true;
-  s->use_engine = true;
+  s->use_engine = false;  // opt-in: measured slower than the separate kernels (see evs_state_use_engine)
   return EVS_OK;
 }
 
@@ -408,7 +418,7 @@ static int enqueue_verify_engine(evs_state* s, const int32_t* tokens, int n, flo
       as.book.p[0] = s->book;
       as.part_o.p[0] = s->ab.part_o;
       as.part_ml.p[0] = s->ab.part_ml;
-      MixSrc src{s->fin, 3 * c.d_model, 1, sg.attn_ws, m->p_in.tab, NTOK};
+      MixSrc src{s->fin, 3 * c.d_model, 1, sg.attn_ws, eng_plan(m->p_in, m->q_in).tab, NTOK};
       CUDA_TRY(launch_attention(Lc, c.dtype, src, c.n_heads, c.head_dim, sr, s->ctx_max, c.attn_chunk, as, s->ab,
                                 s->g));
     }

@@ -203,15 +203,21 @@ int evs_state_book_write(evs_state* s, const evs_book* in_host, cudaStream_t str
 int evs_state_check(evs_state* s, cudaStream_t stream, int32_t* status_host);
 /* Capture verify / commit sequences in CUDA graphs (default on). */
 int evs_state_use_graphs(evs_state* s, int32_t enable);
-/* Run single-sequence verifies through the persistent engine (default on
- * where the model allows it: bf16 storage, FIR filters of at most 128
- * taps): one kernel per span of layers between attention mixers, in which
- * the weight GEMMs stream without stopping at layer boundaries and the row
- * work between them (mixers, residual add + RMSNorm, SiLU-and-multiply,
- * logits) runs on other warps of the same CTAs.  Results equal the separate
- * kernels' bit for bit.  Traced and batched verifies always use the
- * separate kernels.  EVS_ERR_UNSUPPORTED when enabling it for a model it
- * does not take. */
+/* Run single-sequence verifies through the persistent engine (off by
+ * default; available where the model allows it: bf16 storage, FIR filters of
+ * at most 128 taps): one kernel per span of layers between attention
+ * mixers, in which the weight GEMMs stream without stopping at layer
+ * boundaries and the row work between them (mixers, residual add + RMSNorm,
+ * SiLU-and-multiply, logits) runs on other warps of the same CTAs,
+ * synchronised through counters in global memory.  Results equal the
+ * separate kernels' bit for bit.  On the 7B-shaped stack it is slower than
+ * the separate kernels with programmatic dependent launch (3.2 against
+ * 2.73 ms per round of 13): each SM takes in weight units at about its
+ * share of the HBM bandwidth and no faster, so the stream cannot catch up
+ * after a stall, and a layer boundary handed over through global counters
+ * takes longer than a kernel boundary.  Traced and batched verifies always
+ * use the separate kernels.  EVS_ERR_UNSUPPORTED when enabling it for a
+ * model it does not take. */
 int evs_state_use_engine(evs_state* s, int32_t enable);
 
 /* ---------------------------------------------------------------- path */

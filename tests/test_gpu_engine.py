@@ -63,6 +63,7 @@ def test_engine_equals_separate_kernels_bitwise(which):
     m = evs.Model(shape, W)
     V, nb = shape.vocab, shape.n_block
     eng, sep = evs.State(m, 512), evs.State(m, 512)
+    eng.use_engine(True)
     sep.use_engine(False)
     assert evs.evs_verify_kernel_count(eng, nb) < evs.evs_verify_kernel_count(sep, nb)
     prompt = [int(x) for x in synth.prompt(shape, 81, 3 * nb + 4)]
@@ -117,6 +118,7 @@ def test_engine_7b_rounds_equal_separate_kernels_bitwise():
     m = evs.Model(shape, W)
     V, nb = shape.vocab, shape.n_block
     eng, sep = evs.State(m, 256), evs.State(m, 256)
+    eng.use_engine(True)
     sep.use_engine(False)
     prompt = [int(x) for x in synth.prompt(shape, 3, 64)]
     for s0 in range(0, len(prompt), nb):
