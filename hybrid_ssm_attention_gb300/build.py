@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libevs.so")
-SOURCES = ["gemm.cu", "engine.cu", "mixers.cu", "rowops.cu", "evs_api.cu"]
+SOURCES = ["gemm.cu", "engine.cu", "mixers.cu", "attention.cu", "rowops.cu", "evs_api.cu"]
 HEADERS = ["evs_internal.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",

@@ -71,6 +71,8 @@ struct LayerS {
   float* st[2];
   void* kc;
   void* vc;
+  const CUtensorMap* kmap;  // device tensor maps of kc / vc (bf16 caches), else null
+  const CUtensorMap* vmap;
 };
 
 struct GraphEntry {
@@ -393,7 +395,8 @@ static int enqueue_verify_engine(evs_state* s, const int32_t* tokens, int n, flo
   const evs_config& c = m->cfg;
   CUDA_TRY(cudaMemsetAsync(s->eng_cnt, 0, s->eng_cnt_bytes, Lc.stream));
   const SeqRows sr = one_seq(n);
-  CUDA_TRY(launch_embed_norm(Lc, c.dtype, m->embed, tokens, sr, c.d_model, c.vocab, c.norm_eps, s->X, s->xn,
+  CUDA_TRY(launch_embed_norm(LaunchCtx{Lc.stream, false}, c.dtype, m->embed, tokens, sr, c.d_model, c.vocab,
+                             c.norm_eps, s->X, s->xn,
                              one_ptr(s->book)));
   const LaunchCtx Le{Lc.stream, false};
   for (const auto& sg : s->eng_segs) {
@@ -415,6 +418,9 @@ static int enqueue_verify_engine(evs_state* s, const int32_t* tokens, int n, flo
       AttnSeq as{};
       as.kc.p[0] = st.kc;
       as.vc.p[0] = st.vc;
+      as.kmap.p[0] = st.kmap;
+      as.vmap.p[0] = st.vmap;
+      as.arrivals.p[0] = s->ab.arrivals;
       as.book.p[0] = s->book;
       as.part_o.p[0] = s->ab.part_o;
       as.part_ml.p[0] = s->ab.part_ml;
@@ -538,7 +544,10 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
     books.p[b] = states[b]->book;
     cbooks.p[b] = states[b]->book;
   }
-  CUDA_TRY(launch_embed_norm(Lc, dt, m->embed, tokens, sr, d, V, eps, s->X, s->xn, books));
+  // The first kernel of a verify waits for all earlier work (no programmatic
+  // overlap): later kernels read the committed state (lengths, banks, cache
+  // rows) before their own dependency wait.
+  CUDA_TRY(launch_embed_norm(LaunchCtx{Lc.stream, false}, dt, m->embed, tokens, sr, d, V, eps, s->X, s->xn, books));
   if (trace) CUDA_TRY(cudaMemcpyAsync(trace, s->X, xbytes, cudaMemcpyDeviceToDevice, Lc.stream));
   const bool fz = m->fuse, sg = m->swiglu;
   for (size_t i = 0; i < m->L.size(); ++i) {
@@ -565,6 +574,9 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       for (int b = 0; b < nseq; ++b) {
         as.kc.p[b] = states[b]->S[i].kc;
         as.vc.p[b] = states[b]->S[i].vc;
+        as.kmap.p[b] = states[b]->S[i].kmap;
+        as.vmap.p[b] = states[b]->S[i].vmap;
+        as.arrivals.p[b] = states[b]->ab.arrivals;
         as.book.p[b] = states[b]->book;
         as.part_o.p[b] = states[b]->ab.part_o;
         as.part_ml.p[b] = states[b]->ab.part_ml;
@@ -991,6 +1003,35 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
       ALLOC(st.vc, es * (size_t)c.n_heads * ctx_max * c.head_dim);
     }
   }
+  if (m->has_attn && attn_tma_eligible(c.dtype, c.n_heads, c.head_dim, ctx_max)) {
+    // tensor maps of every attention cache, encoded once (the caches never move)
+    std::vector<CUtensorMap> maps;
+    char err[256] = {0};
+    for (const LayerS& st : s->S) {
+      if (!st.kc) continue;
+      CUtensorMap km, vm;
+      if (!encode_kv_maps(&km, &vm, st.kc, st.vc, c.n_heads, c.head_dim, ctx_max, err, sizeof err)) {
+        state_free(s);
+        return fail(EVS_ERR_CUDA, "KV tensor map: %s", err);
+      }
+      maps.push_back(km);
+      maps.push_back(vm);
+    }
+    CUtensorMap* dmaps = nullptr;
+    ALLOC(dmaps, sizeof(CUtensorMap) * maps.size());
+    cudaError_t e = cudaMemcpy(dmaps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      state_free(s);
+      return fail(EVS_ERR_CUDA, "KV tensor map upload: %s", cudaGetErrorString(e));
+    }
+    int j = 0;
+    for (LayerS& st : s->S) {
+      if (!st.kc) continue;
+      st.kmap = dmaps + 2 * j;
+      st.vmap = dmaps + 2 * j + 1;
+      ++j;
+    }
+  }
 #undef ALLOC
   if (m->tc) {
     char err[256] = {0};
@@ -1042,6 +1083,7 @@ extern "C" int evs_state_reset(evs_state* s, cudaStream_t stream) {
   }
   LaunchCtx Lc{stream, false};
   CUDA_TRY(cudaMemsetAsync(s->cnt, 0, sizeof(int) * s->cnt_len, stream));
+  if (s->m->has_attn) CUDA_TRY(cudaMemsetAsync(s->ab.arrivals, 0, sizeof(int) * s->m->cfg.n_heads, stream));
   CUDA_TRY(launch_book_set(Lc, s->book, initial_book()));
   s->host_pos = 0;
   s->host_pos_known = true;
@@ -1420,6 +1462,20 @@ extern "C" int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max,
   AttnSeq as{};
   as.kc.p[0] = kc;
   as.vc.p[0] = vc;
+  if (attn_tma_eligible(dtype, H, Dh, ctx_max)) {
+    // tensor maps of the caller's caches into the scratch (synchronous: the
+    // host copies live on this stack frame)
+    CUtensorMap maps[2];
+    char err[256] = {0};
+    if (!encode_kv_maps(&maps[0], &maps[1], kc, vc, H, Dh, ctx_max, err, sizeof err))
+      return fail(EVS_ERR_ARG, "KV tensor map: %s", err);
+    CUDA_TRY(cudaMemcpyAsync(B.maps, maps, sizeof maps, cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(cudaMemsetAsync(B.arrivals, 0, sizeof(int) * H, stream));
+    CUDA_TRY(cudaStreamSynchronize(stream));
+    as.kmap.p[0] = B.maps;
+    as.vmap.p[0] = B.maps + 1;
+    as.arrivals.p[0] = B.arrivals;
+  }
   as.book.p[0] = book;
   as.part_o.p[0] = B.part_o;
   as.part_ml.p[0] = B.part_ml;
@@ -1796,16 +1852,18 @@ extern "C" int64_t evs_kernel_launches(void) { return g_launches.load(); }
 extern "C" int32_t evs_verify_kernel_count(const evs_state* s, int32_t n) {
   (void)n;
   if (!s) return -1;
+  const evs_config& c = s->m->cfg;
+  const int ak = attn_kernels(c.dtype, c.n_heads, c.head_dim, s->ctx_max);
   if (s->use_engine) {
-    // embed, one engine launch per span, three attention kernels per attention layer
+    // embed, one engine launch per span, the attention kernels of each attention layer
     int k = 1 + (int)s->eng_segs.size();
-    for (const auto& L : s->m->L) k += L.kind == EVS_LAYER_ATTN ? 3 : 0;
+    for (const auto& L : s->m->L) k += L.kind == EVS_LAYER_ATTN ? ak : 0;
     return k;
   }
   int k = 1 + 2;  // embed, head GEMM, logits
-  // per layer: 4 GEMMs + the mixer (3 kernels for attention), plus two
+  // per layer: 4 GEMMs + the mixer (2 or 3 kernels for attention), plus two
   // RMSNorm kernels and the activation kernel unless the GEMMs do that work
   for (const auto& L : s->m->L)
-    k += 4 + (s->m->fuse ? 0 : 2) + (s->m->swiglu ? 0 : 1) + (L.kind == EVS_LAYER_ATTN ? 3 : 1);
+    k += 4 + (s->m->fuse ? 0 : 2) + (s->m->swiglu ? 0 : 1) + (L.kind == EVS_LAYER_ATTN ? ak : 1);
   return k;
 }

@@ -9,7 +9,10 @@
 //  IIR  (modal Hyena filter): s_t = lam * s_{t-1} + z_t per channel and pole,
 //       y_t = Re sum_m R_m s_t[m]; all n states go to the spare bank.
 //  ATTN rotary q/k, append k/v at rows pos..pos+n-1 (append-only cache),
-//       split-KV block-causal attention with a fixed-order combine.
+//       split-KV block-causal attention with a fixed-order combine.  Here:
+//       the SIMT path for float caches and head dims without tensor maps;
+//       bf16 caches at Dh 64 / 128 take the tensor-map kernel (attention.cu)
+//       and share the combine.
 //
 // Every mixer first forms its inputs from the in-projection (GEMM partials
 // or a plain matrix) with the storage rounding of the path.
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ attention
 // (1) rotary embedding + append: grid (n, H), Dh/2 threads, one rotation pair each.
 template <typename T, typename Src>
-__global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const double* inv_freq,
+__global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const uint64_t* turn_fx,
                                 const __grid_constant__ SeqRows sr, const __grid_constant__ SeqPtrs<T*> kcs,
                                 const __grid_constant__ SeqPtrs<T*> vcs, float* qbuf,
                                 const __grid_constant__ SeqPtrs<evs_book*> books) {
@@ -208,16 +211,9 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const
   const int d = H * Dh;
   pdl_trigger();
   // the position is fixed for the whole verify: the rotation is computed
-  // while the in-projection still runs.  Angle pos * base^(-2i/Dh) in
-  // double (table built on the host in double), reduced to [-pi, pi] in
-  // double, then sin / cos in float.
+  // while the in-projection still runs
   const long long pos = (long long)book->pos + t;
-  const double TWO_PI = 6.283185307179586476925287;
-  const double ang = (double)pos * inv_freq[i];
-  const double turns = rint(ang * (1.0 / TWO_PI));
-  const float red = (float)fma(-turns, TWO_PI, ang);
-  float sn, cs;
-  sincosf(red, &sn, &cs);
+  const float2 c = rope_cs(pos, turn_fx[i]);
   const int col = h * Dh + i;
   const auto cq1 = src.at(col), cq2 = src.at(col + half), ck1 = src.at(d + col), ck2 = src.at(d + col + half);
   const auto cv1 = src.at(2 * d + col), cv2 = src.at(2 * d + col + half);
@@ -229,8 +225,8 @@ __global__ void qkv_rope_kernel(Src src, int H, int Dh, long long ctx_max, const
   const float q1 = stored<T>(src.get(cq1, r, col)), q2 = stored<T>(src.get(cq2, r, col + half));
   const float k1 = stored<T>(src.get(ck1, r, d + col)), k2 = stored<T>(src.get(ck2, r, d + col + half));
   const float v1 = stored<T>(src.get(cv1, r, 2 * d + col)), v2 = stored<T>(src.get(cv2, r, 2 * d + col + half));
-  const float rq1 = q1 * cs - q2 * sn, rq2 = q1 * sn + q2 * cs;
-  const float rk1 = k1 * cs - k2 * sn, rk2 = k1 * sn + k2 * cs;
+  const float rq1 = rot_lo(q1, q2, c), rq2 = rot_hi(q1, q2, c);
+  const float rk1 = rot_lo(k1, k2, c), rk2 = rot_hi(k1, k2, c);
   const size_t row = ((size_t)h * ctx_max + pos) * Dh;
   kc[row + i] = from_f<T>(rk1);
   kc[row + i + half] = from_f<T>(rk2);
@@ -446,270 +442,6 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// (2b) split-KV attention on tensor cores (bf16 caches): grid (splits, H),
-// 4 warps.  Split s owns keys [s*span, (s+1)*span) of head h (span fixed per
-// state, so a query's key partition never depends on the block size n).
-// Keys stream through a 3-stage cp.async ring of 64-key stages (K and V rows
-// of 2*DH bytes, 16-byte chunks XOR-swizzled by row so ldmatrix is
-// conflict-free); warp w takes keys 16w..16w+15 of each stage:
-//   S = Q K^T  (mma.sync m16n8k16, Q rows = the block's queries, bf16),
-//   online softmax per query row (running max / sum, fp32),
-//   O += P V   (P rounded to bf16 as the A operand, V by ldmatrix.trans).
-// The four warps' (m, l, O) merge in warp order into one partial per split.
-constexpr int AT_WARPS = 4, AT_STAGE = 64, AT_NST = 3;
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
-}
-__device__ __forceinline__ void mma_16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-template <int DH>
-__host__ __device__ constexpr size_t attn_mma_smem() {
-  return (size_t)AT_NST * 2 * AT_STAGE * DH * 2;  // K and V stages (the warp merge reuses them)
-}
-
-template <int DH>
-__global__ void __launch_bounds__(AT_WARPS * 32)
-    attn_mma_kernel(const float* __restrict__ qbuf, const __grid_constant__ SeqPtrs<const bf16*> kcs,
-                    const __grid_constant__ SeqPtrs<const bf16*> vcs, int H, const __grid_constant__ SeqRows sr,
-                    long long ctx_max, const __grid_constant__ SeqPtrs<const evs_book*> books, int span, int nsplit_max,
-                    const __grid_constant__ SeqPtrs<float*> part_os, const __grid_constant__ SeqPtrs<float*> part_mls) {
-  static_assert(DH % 16 == 0 && DH <= 256, "head dim");
-  constexpr int RB = DH * 2;                  // bytes per key row
-  constexpr int CPR = DH / 8;                 // 16-byte chunks per row
-  constexpr int SWZ = CPR < 8 ? CPR - 1 : 7;  // XOR mask of the chunk index
-  constexpr int STAGE_B = AT_STAGE * RB;      // one of K / V for a stage
-  constexpr int KS = DH / 16;                 // k-steps of Q K^T
-  constexpr int NT = DH / 8;                  // 8-dim output tiles
-  extern __shared__ __align__(128) unsigned char at_sm[];
-  const int h = blockIdx.y, sp = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int g = lane >> 2, t4 = lane & 3;
-  // this CTA's sequence (blockIdx.z): its queries are block rows [r0, r0 + n)
-  const int sq = blockIdx.z, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
-  const bf16* kc = kcs.p[sq];
-  const bf16* vc = vcs.p[sq];
-  const evs_book* book = books.p[sq];
-  float* part_o = part_os.p[sq];
-  float* part_ml = part_mls.p[sq];
-  pdl_trigger();
-  const long long pos = book->pos;
-  const long long total = min(pos + n, ctx_max);
-  const long long k_begin = (long long)sp * span;
-  const long long k_end = min(k_begin + span, total);
-  const int nstage = k_end > k_begin ? (int)((k_end - k_begin + AT_STAGE - 1) / AT_STAGE) : 0;
-  const bf16* kh = kc + (size_t)h * ctx_max * DH;
-  const bf16* vh = vc + (size_t)h * ctx_max * DH;
-  // committed keys do not change in this verify: warm L2 with the first
-  // stages while the preceding kernels finish
-  if (tid == 0 && nstage > 0) {
-    const long long pre_end = min(k_begin + (long long)AT_NST * AT_STAGE, min(pos, k_end));
-    if (pre_end > k_begin) {
-      const unsigned bytes = (unsigned)((pre_end - k_begin) * RB);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kh + k_begin * DH), "r"(bytes) : "memory");
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vh + k_begin * DH), "r"(bytes) : "memory");
-    }
-  }
-  pdl_wait();
-  if (sp * (long long)span >= total) return;  // this split holds no key of the block
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(at_sm);
-  auto stage_k = [&](int st) { return sbase + (uint32_t)(st % AT_NST) * 2 * STAGE_B; };
-  auto stage_v = [&](int st) { return stage_k(st) + STAGE_B; };
-  // stage st: keys k_begin + 64 st ..; rows past k_end: K left as is (masked),
-  // V zeroed (P = 0 must not meet a non-finite value)
-  auto issue = [&](int st) {
-    if (st < nstage) {
-      const long long key0 = k_begin + (long long)st * AT_STAGE;
-      unsigned char* kd = at_sm + (st % AT_NST) * 2 * STAGE_B;
-      unsigned char* vd = kd + STAGE_B;
-      for (int e = tid; e < AT_STAGE * CPR; e += AT_WARPS * 32) {
-        const int r = e / CPR, c = e % CPR;
-        const int off = r * RB + ((c ^ (r & SWZ)) << 4);
-        const long long key = key0 + r;
-        if (key < k_end) {
-          cp_async16(kd + off, kh + key * DH + c * 8);
-          cp_async16(vd + off, vh + key * DH + c * 8);
-        } else {
-          *reinterpret_cast<uint4*>(vd + off) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-    }
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int st = 0; st < AT_NST - 1; ++st) issue(st);
-
-  // Q as the A operand: rows g and g+8 (queries), k-step kk
-  uint32_t qa[KS][4];
-  {
-    const float* q0 = qbuf + ((size_t)(r0 + g) * H + h) * DH;
-    const float* q1 = qbuf + ((size_t)(r0 + g + 8) * H + h) * DH;
-    const bool ok0 = g < n, ok1 = g + 8 < n;
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      const int c0 = kk * 16 + 2 * t4;
-      qa[kk][0] = ok0 ? pack_bf16(q0[c0], q0[c0 + 1]) : 0u;
-      qa[kk][1] = ok1 ? pack_bf16(q1[c0], q1[c0 + 1]) : 0u;
-      qa[kk][2] = ok0 ? pack_bf16(q0[c0 + 8], q0[c0 + 9]) : 0u;
-      qa[kk][3] = ok1 ? pack_bf16(q1[c0 + 8], q1[c0 + 9]) : 0u;
-    }
-  }
-  const float scale = rsqrtf((float)DH);
-  float o[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g, g+8 (l: this thread's share)
-  const long long lim0 = pos + g, lim1 = pos + g + 8;         // last key each row may see
-
-  for (int st = 0; st < nstage; ++st) {
-    issue(st + AT_NST - 1);
-    cp_async_wait_group<AT_NST - 1>();
-    __syncthreads();
-    const long long kw = k_begin + (long long)st * AT_STAGE + 16 * w;  // this warp's first key
-    if (kw < k_end) {
-      // S = Q K^T for 16 keys: two 8-key tiles
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint32_t kb = stage_k(st);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int mi = lane >> 3;
-        const int r = 16 * w + ((mi >> 1) << 3) + (lane & 7);
-        const int c = 2 * kk + (mi & 1);
-        uint32_t b[4];
-        ldsm_x4(kb + r * RB + ((c ^ (r & SWZ)) << 4), b);
-        mma_16816(sc[0], qa[kk], b[0], b[1]);
-        mma_16816(sc[1], qa[kk], b[2], b[3]);
-      }
-      // mask, running max, probabilities
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const long long key = kw + 8 * j + 2 * t4 + (e & 1);
-          const bool ok = key < k_end && key <= ((e >> 1) ? lim1 : lim0);
-          sc[j][e] = ok ? sc[j][e] * scale : -INFINITY;
-          if (e >> 1) mx1 = fmaxf(mx1, sc[j][e]); else mx0 = fmaxf(mx0, sc[j][e]);
-        }
-#pragma unroll
-      for (int x = 1; x < 4; x <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
-      }
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = n0 == -INFINITY ? 1.f : expf(m0 - n0);
-      const float a1 = n1 == -INFINITY ? 1.f : expf(m1 - n1);
-      m0 = n0;
-      m1 = n1;
-      float p[2][4];
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float mm = (e >> 1) ? n1 : n0;
-          p[j][e] = sc[j][e] == -INFINITY ? 0.f : expf(sc[j][e] - mm);
-          if (e >> 1) ps1 += p[j][e]; else ps0 += p[j][e];
-        }
-      l0 = l0 * a0 + ps0;
-      l1 = l1 * a1 + ps1;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        o[j][0] *= a0;
-        o[j][1] *= a0;
-        o[j][2] *= a1;
-        o[j][3] *= a1;
-      }
-      // O += P V: P (16 queries x 16 keys) as the A operand
-      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]),
-                              pack_bf16(p[1][0], p[1][1]), pack_bf16(p[1][2], p[1][3])};
-      const uint32_t vb = stage_v(st);
-#pragma unroll
-      for (int jd = 0; jd < NT; jd += 2) {
-        const int mi = lane >> 3;
-        const int r = 16 * w + ((mi & 1) << 3) + (lane & 7);
-        const int c = jd + (mi >> 1);
-        uint32_t b[4];
-        ldsm_x4_t(vb + r * RB + ((c ^ (r & SWZ)) << 4), b);
-        mma_16816(o[jd], pa, b[0], b[1]);
-        mma_16816(o[jd + 1], pa, b[2], b[3]);
-      }
-    }
-    __syncthreads();  // the stage buffer is refilled by the next iteration's issue
-  }
-  cp_async_wait_group<0>();
-  __syncthreads();
-  // row sums over the quad, then merge the four warps in order
-#pragma unroll
-  for (int x = 1; x < 4; x <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
-  }
-  float* mw = reinterpret_cast<float*>(at_sm);  // [4][16] max, [4][16] sum, [4][16][DH] O
-  float* lw = mw + AT_WARPS * 16;
-  float* ow = lw + AT_WARPS * 16;
-  if (t4 == 0) {
-    mw[w * 16 + g] = m0;
-    mw[w * 16 + g + 8] = m1;
-    lw[w * 16 + g] = l0;
-    lw[w * 16 + g + 8] = l1;
-  }
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    float* r0 = ow + ((size_t)w * 16 + g) * DH + 8 * j + 2 * t4;
-    float* r1 = r0 + 8 * DH;
-    r0[0] = o[j][0];
-    r0[1] = o[j][1];
-    r1[0] = o[j][2];
-    r1[1] = o[j][3];
-  }
-  __syncthreads();
-  for (int e = tid; e < n * DH; e += AT_WARPS * 32) {
-    const int t = e / DH, dd = e % DH;
-    float M = -INFINITY;
-#pragma unroll
-    for (int v = 0; v < AT_WARPS; ++v) M = fmaxf(M, mw[v * 16 + t]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int v = 0; v < AT_WARPS; ++v) {
-      const float mv = mw[v * 16 + t];
-      if (mv == -INFINITY) continue;
-      const float f = expf(mv - M);
-      L = fmaf(lw[v * 16 + t], f, L);
-      O = fmaf(ow[((size_t)v * 16 + t) * DH + dd], f, O);
-    }
-    part_o[(((size_t)h * nsplit_max + sp) * NTOK + t) * DH + dd] = O;
-    if (dd == 0) {
-      float* ml = part_ml + (((size_t)h * nsplit_max + sp) * NTOK + t) * 2;
-      ml[0] = M;
-      ml[1] = L;
-    }
-  }
-}
-
 // (3) combine: grid (n, H), Dh threads; splits in ascending order.
 template <typename T>
 __global__ void attn_combine_kernel(const __grid_constant__ SeqPtrs<const float*> part_os,
@@ -834,21 +566,6 @@ cudaError_t attn_split_launch(const LaunchCtx& L, int H, const SeqRows& sr, long
 template <typename T, int DH>
 cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, const SeqRows& sr, long long ctx_max, int chunk,
                                 const AttnSeq& as, const AttnBufs& B) {
-  if constexpr (sizeof(T) == 2) {
-    // bf16 caches: tensor-core kernel (the chunk only shapes the span)
-    constexpr size_t smem = attn_mma_smem<DH>();
-    auto k = attn_mma_kernel<DH>;
-    static bool attr_set = false;
-    if (!attr_set && smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
-    if (B.span % AT_STAGE) return cudaErrorInvalidValue;
-    return launch(L, k, dim3(B.nsplit_max, H, sr.nseq), dim3(AT_WARPS * 32), smem, (const float*)B.qbuf,
-                  cast_ptrs<const bf16*>(as.kc, sr.nseq), cast_ptrs<const bf16*>(as.vc, sr.nseq), H, sr, ctx_max,
-                  cast_ptrs<const evs_book*>(as.book, sr.nseq), B.span, B.nsplit_max, as.part_o, as.part_ml);
-  }
   switch (chunk) {
     case 32: return attn_split_launch<T, DH, 32>(L, H, sr, ctx_max, as, B);
     case 64: return attn_split_launch<T, DH, 64>(L, H, sr, ctx_max, as, B);
@@ -858,12 +575,21 @@ cudaError_t attn_split_dispatch(const LaunchCtx& L, int H, const SeqRows& sr, lo
   }
 }
 
+template <typename T>
+cudaError_t combine_launch(const LaunchCtx& L, int H, int Dh, const SeqRows& sr, long long ctx_max, const AttnSeq& as,
+                           const AttnBufs& B, void* g) {
+  const int rows = sr.row0[sr.nseq];
+  return launch(L, attn_combine_kernel<T>, dim3(rows, H), dim3(Dh), 0, cast_ptrs<const float*>(as.part_o, sr.nseq),
+                cast_ptrs<const float*>(as.part_ml, sr.nseq), H, Dh, sr, B.span, ctx_max,
+                cast_ptrs<const evs_book*>(as.book, sr.nseq), B.nsplit_max, (T*)g);
+}
+
 template <typename T, typename Src>
 cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, const SeqRows& sr, long long ctx_max, int chunk,
                         const AttnSeq& as, const AttnBufs& B, void* g) {
   const int rows = sr.row0[sr.nseq];
   cudaError_t e = launch(L, qkv_rope_kernel<T, Src>, dim3(rows, H), dim3(Dh / 2), 0, s, H, Dh, ctx_max,
-                         (const double*)B.inv_freq, sr, cast_ptrs<T*>(as.kc, sr.nseq), cast_ptrs<T*>(as.vc, sr.nseq),
+                         (const uint64_t*)B.turn_fx, sr, cast_ptrs<T*>(as.kc, sr.nseq), cast_ptrs<T*>(as.vc, sr.nseq),
                          B.qbuf, as.book);
   if (e != cudaSuccess) return e;
   switch (Dh) {
@@ -873,9 +599,7 @@ cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, const SeqRows&
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch(L, attn_combine_kernel<T>, dim3(rows, H), dim3(Dh), 0, cast_ptrs<const float*>(as.part_o, sr.nseq),
-                cast_ptrs<const float*>(as.part_ml, sr.nseq), H, Dh, sr, B.span, ctx_max,
-                cast_ptrs<const evs_book*>(as.book, sr.nseq), B.nsplit_max, (T*)g);
+  return combine_launch<T>(L, H, Dh, sr, ctx_max, as, B, g);
 }
 
 }  // namespace
@@ -910,11 +634,11 @@ cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, const S
   return iir_dispatch<float>(L, sf, d, sr, M, lam, res, st0, st1, book, g);
 }
 
-// Key span of a split: max(chunk, 64) * 2^j, the smallest with at most
+// Key span of a split: max(chunk, 128) * 2^j, the smallest with at most
 // ATTN_SPLITS_MAX splits over ctx_max.  Fixed per cache, so the partition
 // of a query's keys never depends on the block size.
 long long attn_span(long long ctx_max, int chunk) {
-  long long span = std::max(chunk, 64);
+  long long span = std::max(chunk, 128);
   while ((ctx_max + span - 1) / span > ATTN_SPLITS_MAX) span *= 2;
   return span;
 }
@@ -922,8 +646,9 @@ long long attn_span(long long ctx_max, int chunk) {
 size_t attn_scratch_bytes(int H, int Dh, long long ctx_max, int chunk) {
   const long long nsplit = (ctx_max + attn_span(ctx_max, chunk) - 1) / attn_span(ctx_max, chunk);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al(sizeof(double) * (Dh / 2)) + al(sizeof(float) * ROWS_MAX * H * Dh) +
-         al(sizeof(float) * H * nsplit * NTOK * Dh) + al(sizeof(float) * H * nsplit * NTOK * 2);
+  return al(sizeof(uint64_t) * (Dh / 2)) + al(sizeof(float) * ROWS_MAX * H * Dh) +
+         al(sizeof(float) * H * nsplit * NTOK * Dh) + al(sizeof(float) * H * nsplit * NTOK * 2) +
+         al(2 * sizeof(CUtensorMap)) + al(sizeof(int) * H);
 }
 
 void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int chunk, AttnBufs* out) {
@@ -931,28 +656,61 @@ void attn_bufs_from_scratch(void* scratch, int H, int Dh, long long ctx_max, int
   const long long nsplit = (ctx_max + span - 1) / span;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* p = (char*)scratch;
-  out->inv_freq = (double*)p;
-  p += al(sizeof(double) * (Dh / 2));
+  out->turn_fx = (uint64_t*)p;
+  p += al(sizeof(uint64_t) * (Dh / 2));
   out->qbuf = (float*)p;
   p += al(sizeof(float) * ROWS_MAX * H * Dh);
   out->part_o = (float*)p;
   p += al(sizeof(float) * H * nsplit * NTOK * Dh);
   out->part_ml = (float*)p;
+  p += al(sizeof(float) * H * nsplit * NTOK * 2);
+  out->maps = (CUtensorMap*)p;
+  p += al(2 * sizeof(CUtensorMap));
+  out->arrivals = (int*)p;
   out->nsplit_max = (int)nsplit;
   out->span = (int)span;
 }
 
 cudaError_t fill_rope_table(const AttnBufs& B, int Dh, float rope_base, cudaStream_t stream) {
-  double tab[512];
+  uint64_t fx[512];
   if (Dh / 2 > 512) return cudaErrorInvalidValue;
-  for (int i = 0; i < Dh / 2; ++i) tab[i] = std::pow((double)rope_base, -2.0 * (double)i / (double)Dh);
-  cudaError_t e = cudaMemcpyAsync(B.inv_freq, tab, sizeof(double) * (Dh / 2), cudaMemcpyHostToDevice, stream);
+  const double TWO_PI = 6.283185307179586476925287;
+  for (int i = 0; i < Dh / 2; ++i) {
+    // turns per position base^(-2i/Dh) / (2 pi), scaled by 2^64 (below 2^64:
+    // the frequency is at most 1 < 2 pi); a double carries it to 2^-53
+    // relative, far below the float angle's resolution at any position
+    // below 2^31
+    const double f = std::pow((double)rope_base, -2.0 * (double)i / (double)Dh);
+    fx[i] = (uint64_t)std::ldexp(f / TWO_PI, 64);
+  }
+  cudaError_t e = cudaMemcpyAsync(B.turn_fx, fx, sizeof(uint64_t) * (Dh / 2), cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return e;
-  return cudaStreamSynchronize(stream);  // tab lives on this stack frame
+  return cudaStreamSynchronize(stream);  // fx lives on this stack frame
 }
 
 cudaError_t launch_attention(const LaunchCtx& L, int dtype, MixSrc src, int H, int Dh, const SeqRows& sr,
                              long long ctx_max, int chunk, const AttnSeq& as, const AttnBufs& B, void* g) {
+  if (attn_tma_eligible(dtype, H, Dh, ctx_max)) {
+    if (ctx_max > ATTN_SHORT_CACHE)
+      // long bf16 caches: rotary embedding, append, split-KV and the combine
+      // in one kernel
+      return launch_attn_tma(L, src, H, Dh, sr, ctx_max, as, B, g, true);
+    // short ones: a few stages per split, all splits at once; the three
+    // steps as separate kernels overlap better under dependent launch
+    const int rows = sr.row0[sr.nseq];
+    auto rope = [&](auto s) {
+      return launch(L, qkv_rope_kernel<bf16, decltype(s)>, dim3(rows, H), dim3(Dh / 2), 0, s, H, Dh, ctx_max,
+                    (const uint64_t*)B.turn_fx, sr, cast_ptrs<bf16*>(as.kc, sr.nseq),
+                    cast_ptrs<bf16*>(as.vc, sr.nseq), B.qbuf, as.book);
+    };
+    cudaError_t e = src.ws ? rope(SrcSlots{src.ws, src.tab, src.slot_rows})
+                           : src.f32 ? rope(SrcPlain<float>{(const float*)src.p, src.ld})
+                                     : rope(SrcPlain<bf16>{(const bf16*)src.p, src.ld});
+    if (e != cudaSuccess) return e;
+    e = launch_attn_tma(L, src, H, Dh, sr, ctx_max, as, B, g, false);
+    if (e != cudaSuccess) return e;
+    return combine_launch<bf16>(L, H, Dh, sr, ctx_max, as, B, g);
+  }
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (src.ws)
     return dtype == EVS_BF16 ? attention_t<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, H, Dh, sr, ctx_max,

@@ -1,7 +1,8 @@
 """Block-causal attention at long context (the long-context configuration:
 32 heads x 128, a cache of 262,144 committed positions ~ N(0, 1)) through
 the operator entry point, the launch configuration the model uses at that
-size (fixed key spans of 32,768 keys, nine splits per head).
+size (fixed key spans of 8,192 keys, 33 splits per head, 1,056 work units
+over one CTA per SM).
 
 The full cache is 4.3 GB; the oracle evaluates two sampled heads (0 and 29),
 whose rows are synthesised on the host, while the other heads' rows are

@@ -6,9 +6,9 @@ rotary and attention code.
   2e-2 of max |ref| (bf16 outputs); the retained per-position state (FIR
   ext rows, IIR states) within 1e-5 (fp32 state); then commit at a random
   keep and a second block from the sliced state.
-* Attention (32 heads x 128, KV cache of 8192 positions ~ N(0,1)): appended
-  rotated keys / values and the block-causal outputs, then commit and a
-  second block.
+* Attention (32 heads x 128 over 8192 cached positions; 8 x 64 over 3000;
+  4 x 32 over 700; caches ~ N(0,1)): appended rotated keys / values and the
+  block-causal outputs, then commit and a second block.
 * Skinny GEMM (tcgen05 path for bf16, SIMT path for f32) at every weight
   shape of the 7B-shaped stack, n = 1, 13, 16.
 Edge cases: n = 1, keep = 0, keep = n, window offset > 0, zero initial IIR.
@@ -123,10 +123,14 @@ def test_iir_op_block_and_slice():
 
 
 @pytest.mark.gpu
-def test_attention_op_8192_cache():
+@pytest.mark.parametrize("H,Dh,P,chunk", [(32, 128, 8192, 256), (8, 64, 3000, 64), (4, 32, 700, 32)])
+def test_attention_op_cache(H, Dh, P, chunk):
+    # Dh 128 / 64: the tensor-map kernel (Dh 64: one box per key row; the
+    # block at 3000 straddles the split boundary at 3008, span 64); Dh 32:
+    # the SIMT kernel on bf16 caches
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
-    H, Dh, P, n_max, chunk = 32, 128, 8192, 13, 256
+    n_max = 13
     d = H * Dh
     ctx = P + 3 * n_max
     ls = synth.layer_state(3, "ATT", 0, d, P=P, n_heads=H, head_dim=Dh)
