@@ -368,9 +368,16 @@ int evs_op_iir(int32_t M, int32_t d, int32_t n, int32_t n_max, int32_t dtype,
                cudaStream_t stream);
 /* Block-causal attention for one block: qkv_dev [n][3*H*Dh] (q|k|v, heads
  * contiguous) storage dtype; caches [H][ctx_max][Dh]; Dh in {32, 64, 128};
- * rotary embedding at positions pos..pos+n-1,
+ * rotary embedding at positions pos..pos+n-1 (angle pos * base^(-2i/Dh)
+ * reduced exactly in 64-bit fixed point, sin / cos in float),
  * k/v appended to the caches at those rows, query i attends rows
- * 0..pos+i.  Writes g_dev [n][H*Dh].  scratch: evs_op_attention_scratch_bytes. */
+ * 0..pos+i (EvSpark discussion post, "What we implemented").  Writes g_dev
+ * [n][H*Dh].  scratch: evs_op_attention_scratch_bytes, device memory the
+ * call fills (rotary table, tensor maps of the caches, zeroed counters)
+ * before its kernels, synchronously on the stream: not for stream capture.
+ * bf16 caches with Dh 64 / 128 stream K and V by tensor-map copies (caches
+ * 16-byte aligned); above 8192 positions one kernel also does the rotary
+ * embedding, the append and the fold of the key splits. */
 size_t evs_op_attention_scratch_bytes(int32_t H, int32_t Dh, int64_t ctx_max, int32_t chunk, int32_t n_max);
 int evs_op_attention(int32_t H, int32_t Dh, int32_t n, int32_t n_max, int64_t ctx_max,
                      int32_t chunk, float rope_base, int32_t dtype, const void* qkv_dev,

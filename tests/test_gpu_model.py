@@ -537,13 +537,15 @@ def _greedy_continuation(evs, st, tmp, first, k, V):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("mode", ["greedy", "sample"])
-def test_round_batch_equals_separate_rounds_bitwise(mode):
+@pytest.mark.parametrize("mode,ctx", [("greedy", 256), ("sample", 256), ("greedy", 9000), ("sample", 9000)])
+def test_round_batch_equals_separate_rounds_bitwise(mode, ctx):
     # evs_round_batch (one graph: batched verify, per-sequence probs / accept /
     # commit on the device) against each sequence's own evs_round, over
     # ragged blocks whose drafts follow the greedy continuation up to a
     # random cut: accepted counts, output tokens, logits, probabilities and
-    # the states' next results agree bit for bit.
+    # the states' next results agree bit for bit.  ctx 9000: caches above
+    # the short-cache size, so attention runs as one fused kernel that folds
+    # each head's splits itself (the committed lengths span several splits)
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
     shape = small_shape()
@@ -552,12 +554,13 @@ def test_round_batch_equals_separate_rounds_bitwise(mode):
     V, nmax = shape.vocab, shape.n_block
     g = np.random.default_rng(9)
     B = 4
-    ref = [evs.State(m, 256) for _ in range(B)]
-    bat = [evs.State(m, 256) for _ in range(B)]
-    tmp = evs.State(m, 256)
+    ref = [evs.State(m, ctx) for _ in range(B)]
+    bat = [evs.State(m, ctx) for _ in range(B)]
+    tmp = evs.State(m, ctx)
     pending = []
     for b in range(B):
-        pr = [int(x) for x in synth.prompt(shape, 80 + b, 6 + 4 * b)]
+        plen = 6 + 4 * b + (190 * b if ctx > 8192 else 0)
+        pr = [int(x) for x in synth.prompt(shape, 80 + b, plen)]
         for st in (ref[b], bat[b]):
             body = pr[:-1]
             for s0 in range(0, len(body), nmax):

@@ -123,11 +123,14 @@ def test_iir_op_block_and_slice():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("H,Dh,P,chunk", [(32, 128, 8192, 256), (8, 64, 3000, 64), (4, 32, 700, 32)])
+@pytest.mark.parametrize("H,Dh,P,chunk", [(32, 128, 8192, 256), (8, 64, 9210, 64), (8, 64, 3066, 64),
+                                           (4, 32, 700, 32)])
 def test_attention_op_cache(H, Dh, P, chunk):
-    # Dh 128 / 64: the tensor-map kernel (Dh 64: one box per key row; the
-    # block at 3000 straddles the split boundary at 3008, span 64); Dh 32:
-    # the SIMT kernel on bf16 caches
+    # Dh 128 / 64: the tensor-map kernel, fused with rotary / append / fold
+    # for caches above 8192 positions, between the rotary and combine kernels
+    # at or below (Dh 64: one box per key row; the first block straddles a
+    # split boundary: 9216 at span 256, 3072 at span 128); Dh 32: the SIMT
+    # kernel on bf16 caches
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
     n_max = 13
