@@ -167,7 +167,7 @@ class ClockSampler:
 # averaged over the 129 weight GEMMs of a step) from one ncu capture of the
 # weight-streaming GEMM; valid only for the kernel source it was taken on
 # (sha256 prefix of gemm.cu), else reported as null.
-GEMM_TRAFFIC = {"gemm_cu_sha256": "f6ea79a125047c1a", "bytes_per_launch": 100.85e6}
+GEMM_TRAFFIC = {"gemm_cu_sha256": "3399583022487da5", "bytes_per_launch": 100.94e6}
 
 
 def gemm_traffic():
@@ -631,8 +631,11 @@ def long_context_rounds(evs, torch, model, shape, P, seed, dev, peak, rounds=6, 
         v = st.view(li)
         L = S["layers"][li]
         if kind in ("SE", "MR"):
+            # the window is positions P-L+1 .. P-1, ring row p mod (L-1+n_max)
             w = torch.from_numpy(L["window"]).to(dev)
-            _dev_view(torch, v.fir_ext[0], (param - 1 + v.n_max, d), torch.float32)[:param - 1] = w
+            R = param - 1 + v.n_max
+            idx = torch.tensor([(P - param + 1 + r) % R for r in range(param - 1)], device=dev)
+            _dev_view(torch, v.fir_ring, (R, d), torch.float32)[idx] = w
         elif kind == "LI":
             s2 = torch.from_numpy(np.ascontiguousarray(L["s"]).view(np.float32)).to(dev)
             _dev_view(torch, v.iir_all[0], (v.n_max, d * param * 2), torch.float32)[0] = s2.reshape(-1)
@@ -640,7 +643,7 @@ def long_context_rounds(evs, torch, model, shape, P, seed, dev, peak, rounds=6, 
             for ptr in (v.k_cache, v.v_cache):
                 _dev_view(torch, ptr, (H, ctx, Dh), torch.bfloat16).normal_(generator=gen)
     torch.cuda.synchronize()
-    st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
+    st.set_book(pos=P, iir_bank=0, iir_slot=0, pending_n=0, status=0)
     keeps = synth.keep_draws(seed, 2 * (warm + rounds), n, kind="geometric")
     q = torch.from_numpy(synth.fixed_logit_drafter(seed, n - 1, V)).to(dev)
     U = torch.from_numpy(synth.uniforms(seed, 2 * (warm + rounds), n)).to(dev)
@@ -775,10 +778,10 @@ def run_case(args):
         gout = torch.empty(n, d, device=dev, dtype=torch.bfloat16)
         for r in range(a.reps):
             if a.kind == "fir":
-                e0 = torch.randn(P - 1 + n, d, device=dev, generator=g)
-                e1 = torch.empty_like(e0)
+                ring = torch.randn(P - 1 + n, d, device=dev, generator=g)
                 taps = torch.randn(P, d, device=dev, generator=g)
-                evs.evs_op_fir(P, d, n, n, evs.EVS_BF16, abv, taps, e0, e1, book, gout)
+                book[0] = 1000 + r  # the window wraps around the ring
+                evs.evs_op_fir(P, d, n, n, evs.EVS_BF16, abv, taps, ring, book, gout)
             else:
                 s0 = torch.randn(n, d, P, 2, device=dev, generator=g)
                 s1 = torch.empty_like(s0)

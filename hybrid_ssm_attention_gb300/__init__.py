@@ -252,9 +252,9 @@ def evs_round_batch(states, tokens, ns, logits, p, q, u, T: float, top_k: int, m
                                  _stream(stream)), "evs_round_batch")
 
 
-def evs_op_fir(L, d, n, n_max, dtype, abv, taps, ext0, ext1, book_dev, g, stream=None):
-    _check(lib().evs_op_fir(L, d, n, n_max, dtype, _ptr(abv), _ptr(taps), _ptr(ext0), _ptr(ext1),
-                            _ptr(book_dev), _ptr(g), _stream(stream)), "evs_op_fir")
+def evs_op_fir(L, d, n, n_max, dtype, abv, taps, ring, book_dev, g, stream=None):
+    _check(lib().evs_op_fir(L, d, n, n_max, dtype, _ptr(abv), _ptr(taps), _ptr(ring), _ptr(book_dev), _ptr(g),
+                            _stream(stream)), "evs_op_fir")
 
 
 def evs_op_iir(M, d, n, n_max, dtype, abv, lam, res, st0, st1, book_dev, g, stream=None):

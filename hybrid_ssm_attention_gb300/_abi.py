@@ -41,7 +41,7 @@ class evs_weights(C.Structure):
 
 
 class evs_book(C.Structure):
-    _fields_ = [("pos", i32), ("fir_bank", i32), ("fir_off", i32), ("iir_bank", i32),
+    _fields_ = [("pos", i32), ("reserved0", i32), ("reserved1", i32), ("iir_bank", i32),
                 ("iir_slot", i32), ("pending_n", i32), ("status", i32), ("reserved", i32)]
 
     def as_dict(self):
@@ -49,7 +49,7 @@ class evs_book(C.Structure):
 
 
 class evs_layer_view(C.Structure):
-    _fields_ = [("kind", i32), ("param", i32), ("fir_ext", vp * 2), ("iir_all", vp * 2),
+    _fields_ = [("kind", i32), ("param", i32), ("fir_ring", vp), ("reserved", vp), ("iir_all", vp * 2),
                 ("k_cache", vp), ("v_cache", vp), ("ctx_max", i64), ("n_max", i32)]
 
 
@@ -80,7 +80,7 @@ PROTOTYPES = {
     "evs_round": (i32, [vp, vp, i32, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
     "evs_round_batch": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
     "evs_profile_gemm_chain": (i32, [vp, i32, i32, C.POINTER(C.c_float), C.POINTER(i64), C.POINTER(i32), vp]),
-    "evs_op_fir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+    "evs_op_fir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
     "evs_op_iir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
     "evs_op_attention_scratch_bytes": (sz, [i32, i32, i64, i32, i32]),
     "evs_op_attention": (i32, [i32, i32, i32, i32, i64, i32, f32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),

@@ -209,9 +209,10 @@ __device__ bool fir_item(const EngPhase& P, int j, int n, int d, const evs_book*
   float* part_s = tap_s + Lf * 32; // [NW][n][32]
   const int rt = threadIdx.x - E_ROW0 * 32, lane = rt & 31, warp = rt >> 5;
   const int c0 = j * 32, c = c0 + lane;
-  const int bank = book->fir_bank, off = book->fir_off;
-  const float* src_ext = bank ? P.bank1 : P.bank0;
-  float* dst_ext = bank ? P.bank0 : P.bank1;
+  // the ring: the input of position p at row p mod R (fir_kernel's layout)
+  const long long pos = book->pos;
+  const int R = P.ring;
+  float* ring = P.bank0;
   bf16* g = static_cast<bf16*>(P.out);
   // taps and the committed window do not depend on the in-projection
   for (int e = rt; e < Lf * 8; e += E_ROWT) {
@@ -220,15 +221,12 @@ __device__ bool fir_item(const EngPhase& P, int j, int n, int d, const evs_book*
   }
   for (int e = rt; e < (Lf - 1) * 8; e += E_ROWT) {
     const int r = e >> 3, w = e & 7;
-    cp_async16(ext_s + r * 32 + w * 4, src_ext + (size_t)(off + r) * d + c0 + w * 4);
+    const long long p = pos - (Lf - 1) + r;  // rows before position 0 hold zeros
+    const int pr = (int)(p >= 0 ? p % R : p + R);
+    cp_async16(ext_s + r * 32 + w * 4, ring + (size_t)pr * d + c0 + w * 4);
   }
   cp_async_wait_all();
   row_sync();
-  for (int e = rt; e < (Lf - 1) * 8; e += E_ROWT) {
-    const int r = e >> 3, w = e & 7;
-    *reinterpret_cast<float4*>(dst_ext + (size_t)r * d + c0 + w * 4) =
-        *reinterpret_cast<const float4*>(ext_s + r * 32 + w * 4);
-  }
   const int tiles[3] = {c0 / TILE_M, (d + c0) / TILE_M, (2 * d + c0) / TILE_M};
   if (!row_wait_tiles(P, tiles, 3, ab, s_flag)) return false;
   const SrcSlots src{P.ws, P.tab, NTOK};
@@ -249,7 +247,7 @@ __device__ bool fir_item(const EngPhase& P, int j, int n, int d, const evs_book*
         const float a = stored<bf16>(av[k]), b = stored<bf16>(bv[k]), v = stored<bf16>(vv[k]);
         a_s[t * 32 + lane] = a;
         ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
-        dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
+        ring[(size_t)((pos + t) % R) * d + c] = b * v;
       }
     }
   }

@@ -67,7 +67,7 @@ struct LayerW {
 };
 
 struct LayerS {
-  float* ext[2];
+  float* ring;   // FIR inputs [L-1+n_max][d], position p at row p mod (L-1+n_max)
   float* st[2];
   void* kc;
   void* vc;
@@ -331,8 +331,9 @@ static void engine_program(evs_state* s, int* cnt, std::vector<EngPhase>* out, s
       mx.sub = sub;
       mx.p0 = fir ? w.taps : w.lam;
       mx.p1 = fir ? nullptr : w.res;
-      mx.bank0 = fir ? st.ext[0] : st.st[0];
-      mx.bank1 = fir ? st.ext[1] : st.st[1];
+      mx.bank0 = fir ? st.ring : st.st[0];
+      mx.bank1 = fir ? nullptr : st.st[1];
+      mx.ring = fir ? w.param - 1 + m->n_max : 0;
       mx.out = s->g;
       mx.out_ld = d;
       g_ready = mx.ready;
@@ -562,9 +563,9 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       EVS_TRY(gemm(m->p_in, w.m_in, w.pk_in, w.w_in, s->m_xn, s->xn, d, GEMM_FINAL, s->fin, 3 * d, GEMM_B_TMA, &src));
     (void)st;
     if (w.kind == EVS_LAYER_FIR) {
-      SeqPtrs<float*> e0{}, e1{};
-      for (int b = 0; b < nseq; ++b) e0.p[b] = states[b]->S[i].ext[0], e1.p[b] = states[b]->S[i].ext[1];
-      CUDA_TRY(launch_fir(Lc, dt, src, d, sr, w.param, w.taps, e0, e1, cbooks, s->g));
+      SeqPtrs<float*> rings{};
+      for (int b = 0; b < nseq; ++b) rings.p[b] = states[b]->S[i].ring;
+      CUDA_TRY(launch_fir(Lc, dt, src, d, sr, w.param, w.param - 1 + m->n_max, w.taps, rings, cbooks, s->g));
     } else if (w.kind == EVS_LAYER_IIR) {
       SeqPtrs<float*> s0{}, s1{};
       for (int b = 0; b < nseq; ++b) s0.p[b] = states[b]->S[i].st[0], s1.p[b] = states[b]->S[i].st[1];
@@ -995,7 +996,7 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
     st = LayerS{};
     const LayerW& L = m->L[i];
     if (L.kind == EVS_LAYER_FIR) {
-      for (int b = 0; b < 2; ++b) ALLOC(st.ext[b], sizeof(float) * (size_t)(L.param - 1 + nm) * d);
+      ALLOC(st.ring, sizeof(float) * (size_t)(L.param - 1 + nm) * d);
     } else if (L.kind == EVS_LAYER_IIR) {
       for (int b = 0; b < 2; ++b) ALLOC(st.st[b], sizeof(float) * 2 * (size_t)nm * d * L.param);
     } else {
@@ -1077,9 +1078,9 @@ extern "C" int evs_state_reset(evs_state* s, cudaStream_t stream) {
   const evs_model* m = s->m;
   for (size_t i = 0; i < m->L.size(); ++i) {
     const LayerW& L = m->L[i];
-    if (L.kind == EVS_LAYER_FIR)
-      for (int b = 0; b < 2; ++b)
-        CUDA_TRY(cudaMemsetAsync(s->S[i].ext[b], 0, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * m->cfg.d_model, stream));
+    if (L.kind == EVS_LAYER_FIR)  // positions before 0 read as zero inputs
+      CUDA_TRY(cudaMemsetAsync(s->S[i].ring, 0, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * m->cfg.d_model,
+                               stream));
   }
   LaunchCtx Lc{stream, false};
   CUDA_TRY(cudaMemsetAsync(s->cnt, 0, sizeof(int) * s->cnt_len, stream));
@@ -1097,8 +1098,8 @@ extern "C" int evs_state_layer_view(const evs_state* s, int32_t layer, evs_layer
   const LayerS& st = s->S[layer];
   out->kind = s->m->L[layer].kind;
   out->param = s->m->L[layer].param;
-  out->fir_ext[0] = st.ext[0];
-  out->fir_ext[1] = st.ext[1];
+  out->fir_ring = st.ring;
+  out->reserved = nullptr;
   out->iir_all[0] = st.st[0];
   out->iir_all[1] = st.st[1];
   out->k_cache = st.kc;
@@ -1123,8 +1124,8 @@ extern "C" int evs_state_book_read(const evs_state* s, evs_book* out, cudaStream
 
 extern "C" int evs_state_book_write(evs_state* s, const evs_book* in, cudaStream_t stream) {
   if (!s || !in) return fail(EVS_ERR_ARG, "null argument");
-  if (in->pos < 0 || in->pos > s->ctx_max || (in->fir_bank & ~1) || (in->iir_bank & ~1) ||
-      in->iir_slot < -1 || in->iir_slot >= s->m->n_max || in->fir_off < 0 || in->fir_off > s->m->n_max ||
+  if (in->pos < 0 || in->pos > s->ctx_max || in->reserved0 || in->reserved1 || (in->iir_bank & ~1) ||
+      in->iir_slot < -1 || in->iir_slot >= s->m->n_max ||
       in->pending_n < 0 || in->pending_n > s->m->n_max)
     return fail(EVS_ERR_ARG, "book field out of range");
   LaunchCtx Lc{stream, false};
@@ -1173,9 +1174,8 @@ extern "C" int evs_state_snapshot(const evs_state* src, evs_state* dst, cudaStre
     const LayerW& L = m->L[i];
     const LayerS &a = src->S[i], &z = dst->S[i];
     if (L.kind == EVS_LAYER_FIR) {
-      for (int k = 0; k < 2; ++k)
-        CUDA_TRY(cudaMemcpyAsync(z.ext[k], a.ext[k], sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
-                                 cudaMemcpyDeviceToDevice, stream));
+      CUDA_TRY(cudaMemcpyAsync(z.ring, a.ring, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
+                               cudaMemcpyDeviceToDevice, stream));
     } else if (L.kind == EVS_LAYER_IIR) {
       for (int k = 0; k < 2; ++k)
         CUDA_TRY(cudaMemcpyAsync(z.st[k], a.st[k], sizeof(float) * 2 * (size_t)m->n_max * c.d_model * L.param,
@@ -1201,9 +1201,8 @@ extern "C" int evs_state_clone(const evs_state* src, evs_state* dst, cudaStream_
     const LayerW& L = m->L[i];
     const LayerS &a = src->S[i], &z = dst->S[i];
     if (L.kind == EVS_LAYER_FIR) {
-      for (int k = 0; k < 2; ++k)
-        CUDA_TRY(cudaMemcpyAsync(z.ext[k], a.ext[k], sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
-                                 cudaMemcpyDeviceToDevice, stream));
+      CUDA_TRY(cudaMemcpyAsync(z.ring, a.ring, sizeof(float) * (size_t)(L.param - 1 + m->n_max) * c.d_model,
+                               cudaMemcpyDeviceToDevice, stream));
     } else if (L.kind == EVS_LAYER_IIR) {
       for (int k = 0; k < 2; ++k)
         CUDA_TRY(cudaMemcpyAsync(z.st[k], a.st[k], sizeof(float) * 2 * (size_t)m->n_max * c.d_model * L.param,
@@ -1413,15 +1412,14 @@ extern "C" int evs_round_batch(evs_state* const* states, int32_t nseq, const int
 
 // =================================================================== operators
 extern "C" int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_t dtype, const void* abv,
-                          const float* taps, float* e0, float* e1, const evs_book* book, void* g,
-                          cudaStream_t stream) {
-  if (!abv || !taps || !e0 || !e1 || !book || !g) return fail(EVS_ERR_ARG, "null argument");
+                          const float* taps, float* ring, const evs_book* book, void* g, cudaStream_t stream) {
+  if (!abv || !taps || !ring || !book || !g) return fail(EVS_ERR_ARG, "null argument");
   if (L < 1 || L > 256 || d < 32 || d % 32 || n < 1 || n > NTOK || n > n_max)
     return fail(EVS_ERR_ARG, "bad FIR shape");
   if (dtype != EVS_BF16 && dtype != EVS_F32) return fail(EVS_ERR_ARG, "bad dtype");
   LaunchCtx Lc{stream, false};
-  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, one_seq(n), L, taps, one_ptr(e0),
-                      one_ptr(e1), one_ptr(book), g));
+  CUDA_TRY(launch_fir(Lc, dtype, MixSrc{abv, 3 * d, dtype == EVS_F32}, d, one_seq(n), L, L - 1 + n_max, taps,
+                      one_ptr(ring), one_ptr(book), g));
   return EVS_OK;
 }
 

@@ -2,10 +2,11 @@
 // state after every block position ("What we implemented" in the EvSpark
 // discussion post; author's reply, prerequisite 1):
 //
-//  FIR  (short / medium Hyena filter): the window of the last L-1 inputs and
-//       the block's n new inputs form one "ext" buffer [L-1+n][d]; position
-//       i's window is ext rows [i+1, i+L).  The kernel writes ext to the
-//       spare bank, so commit only moves an offset.
+//  FIR  (short / medium Hyena filter): the inputs live in a ring of
+//       R = L-1+n_max rows, position p at row p mod R.  The committed window
+//       is positions pos-L+1 .. pos-1; the kernel writes the block's inputs
+//       at positions pos .. pos+n-1, so every block position's window is in
+//       place and commit only moves pos (no copy).
 //  IIR  (modal Hyena filter): s_t = lam * s_{t-1} + z_t per channel and pole,
 //       y_t = Re sum_m R_m s_t[m]; all n states go to the spare bank.
 //  ATTN rotary q/k, append k/v at rows pos..pos+n-1 (append-only cache),
@@ -36,18 +37,18 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // ------------------------------------------------------------------ FIR
 // Block = 32 channels x NW warps; warp w sums taps [w*J, (w+1)*J), J = JT.
 // Each lane keeps its J taps and the J + 15 window values they touch in
-// registers.
+// registers.  Shared rows: the window (positions pos-L+1 .. pos-1) followed
+// by the block's inputs.
 template <typename T, typename Src, int JT>
 __global__ void __launch_bounds__(256)
-    fir_kernel(Src src, int d, int Lf, const float* __restrict__ taps, const __grid_constant__ SeqRows sr,
-               const __grid_constant__ SeqPtrs<float*> ext0s, const __grid_constant__ SeqPtrs<float*> ext1s,
-               const __grid_constant__ SeqPtrs<const evs_book*> books, T* g) {
+    fir_kernel(Src src, int d, int Lf, int R, const float* __restrict__ taps, const __grid_constant__ SeqRows sr,
+               const __grid_constant__ SeqPtrs<float*> rings, const __grid_constant__ SeqPtrs<const evs_book*> books,
+               T* g) {
   extern __shared__ float sm[];
   const int NW = blockDim.x >> 5;
-  // this CTA's sequence: block rows [r0, r0 + n), its own banks and bookkeeping
+  // this CTA's sequence: block rows [r0, r0 + n), its own ring and bookkeeping
   const int sq = blockIdx.y, r0 = sr.row0[sq], n = sr.row0[sq + 1] - r0;
-  float* ext0 = ext0s.p[sq];
-  float* ext1 = ext1s.p[sq];
+  float* ring = rings.p[sq];
   const evs_book* book = books.p[sq];
   const int rows = Lf - 1 + n;
   float* ext_s = sm;                       // [rows][32]
@@ -58,12 +59,9 @@ __global__ void __launch_bounds__(256)
   const int c0 = blockIdx.x * 32, c = c0 + lane;
 
   pdl_trigger();
-  // Taps, the committed window and its copy into the spare bank do not
-  // depend on the in-projection: done while the preceding GEMM still runs
-  // (the bank / offset are fixed for the whole verify).
-  const int bank = book->fir_bank, off = book->fir_off;
-  const float* src_ext = bank ? ext1 : ext0;
-  float* dst_ext = bank ? ext0 : ext1;
+  // Taps and the committed window do not depend on the in-projection: loaded
+  // while the preceding GEMM still runs (pos is fixed for the whole verify).
+  const long long pos = book->pos;
   // rows of 32 channels = 128 bytes = 8 x 16-byte pieces, all copies in flight at once
   const int nthr = blockDim.x;
   for (int e = threadIdx.x; e < Lf * 8; e += nthr) {
@@ -72,16 +70,13 @@ __global__ void __launch_bounds__(256)
   }
   for (int e = threadIdx.x; e < (Lf - 1) * 8; e += nthr) {
     const int r = e >> 3, w = e & 7;
-    cp_async16(ext_s + r * 32 + w * 4, src_ext + (size_t)(off + r) * d + c0 + w * 4);
+    const long long p = pos - (Lf - 1) + r;  // >= -(Lf - 1) > -R: rows before position 0 hold zeros
+    const int pr = (int)(p >= 0 ? p % R : p + R);
+    cp_async16(ext_s + r * 32 + w * 4, ring + (size_t)pr * d + c0 + w * 4);
   }
   const auto ca = src.at(c), cb = src.at(d + c), cv = src.at(2 * d + c);
   cp_async_wait_all();
   __syncthreads();
-  for (int e = threadIdx.x; e < (Lf - 1) * 8; e += nthr) {
-    const int r = e >> 3, w = e & 7;
-    *reinterpret_cast<float4*>(dst_ext + (size_t)r * d + c0 + w * 4) =
-        *reinterpret_cast<const float4*>(ext_s + r * 32 + w * 4);
-  }
   pdl_wait();
   // three of this warp's rows at a time, all reads issued before any use
   // (rows past the block re-read its last row and are dropped)
@@ -101,7 +96,7 @@ __global__ void __launch_bounds__(256)
         const float a = stored<T>(av[k]), b = stored<T>(bv[k]), v = stored<T>(vv[k]);
         a_s[t * 32 + lane] = a;
         ext_s[(Lf - 1 + t) * 32 + lane] = b * v;
-        dst_ext[(size_t)(Lf - 1 + t) * d + c] = b * v;
+        ring[(size_t)((pos + t) % R) * d + c] = b * v;
       }
     }
   }
@@ -485,15 +480,14 @@ static int max_rows(const SeqRows& sr) {
 }
 
 template <typename T, typename Src>
-cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, const SeqRows& sr, int Lf, const float* taps,
-                         const SeqPtrs<float*>& e0, const SeqPtrs<float*>& e1, const SeqPtrs<const evs_book*>& book,
-                         void* g) {
+cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, const SeqRows& sr, int Lf, int R, const float* taps,
+                         const SeqPtrs<float*>& rings, const SeqPtrs<const evs_book*>& book, void* g) {
   const int NW = std::min(8, Lf);
   int J = 1;
   while (J * NW < Lf) J <<= 1;  // taps per warp, a power of two <= 32 (Lf <= 256)
   const int n = max_rows(sr);
   const size_t smem = sizeof(float) * 32 * ((Lf - 1 + n) + n + Lf + NW * n);
-  void (*k)(Src, int, int, const float*, SeqRows, SeqPtrs<float*>, SeqPtrs<float*>, SeqPtrs<const evs_book*>, T*);
+  void (*k)(Src, int, int, int, const float*, SeqRows, SeqPtrs<float*>, SeqPtrs<const evs_book*>, T*);
   switch (J) {
     case 1: k = fir_kernel<T, Src, 1>; break;
     case 2: k = fir_kernel<T, Src, 2>; break;
@@ -503,11 +497,12 @@ cudaError_t fir_dispatch(const LaunchCtx& L, Src s, int d, const SeqRows& sr, in
     case 32: k = fir_kernel<T, Src, 32>; break;
     default: return cudaErrorInvalidValue;
   }
+  if (R < Lf - 1 + n) return cudaErrorInvalidValue;  // the window and the block must not alias
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch(L, k, dim3(d / 32, sr.nseq), dim3(32 * NW), smem, s, d, Lf, taps, sr, e0, e1, book, (T*)g);
+  return launch(L, k, dim3(d / 32, sr.nseq), dim3(32 * NW), smem, s, d, Lf, R, taps, sr, rings, book, (T*)g);
 }
 
 template <typename T, typename Src, int M>
@@ -604,19 +599,19 @@ cudaError_t attention_t(const LaunchCtx& L, Src s, int H, int Dh, const SeqRows&
 
 }  // namespace
 
-cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, const SeqRows& sr, int Lf,
-                       const float* taps, const SeqPtrs<float*>& ext0, const SeqPtrs<float*>& ext1,
-                       const SeqPtrs<const evs_book*>& book, void* g) {
+cudaError_t launch_fir(const LaunchCtx& L, int dtype, MixSrc src, int d, const SeqRows& sr, int Lf, int R,
+                       const float* taps, const SeqPtrs<float*>& rings, const SeqPtrs<const evs_book*>& book,
+                       void* g) {
   const SrcPlain<float> sf{(const float*)src.p, src.ld};
   if (src.ws)
-    return dtype == EVS_BF16 ? fir_dispatch<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, d, sr, Lf, taps, ext0,
-                                                  ext1, book, g)
+    return dtype == EVS_BF16 ? fir_dispatch<bf16>(L, SrcSlots{src.ws, src.tab, src.slot_rows}, d, sr, Lf, R, taps,
+                                                  rings, book, g)
                              : cudaErrorInvalidValue;
   if (dtype == EVS_BF16)
-    return src.f32 ? fir_dispatch<bf16>(L, sf, d, sr, Lf, taps, ext0, ext1, book, g)
-                   : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, Lf, taps, ext0,
-                                        ext1, book, g);
-  return fir_dispatch<float>(L, sf, d, sr, Lf, taps, ext0, ext1, book, g);
+    return src.f32 ? fir_dispatch<bf16>(L, sf, d, sr, Lf, R, taps, rings, book, g)
+                   : fir_dispatch<bf16>(L, SrcPlain<bf16>{(const bf16*)src.p, src.ld}, d, sr, Lf, R, taps, rings,
+                                        book, g);
+  return fir_dispatch<float>(L, sf, d, sr, Lf, R, taps, rings, book, g);
 }
 
 cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, const SeqRows& sr, int M,

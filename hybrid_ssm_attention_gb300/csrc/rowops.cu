@@ -582,8 +582,7 @@ __device__ void commit_one(evs_book* book, int keep, int n_explicit) {
     book->pending_n = 0;
     return;
   }
-  book->fir_bank ^= 1;
-  book->fir_off = keep;
+  // FIR windows follow pos (ring rows by absolute position)
   if (keep > 0) {
     book->iir_bank ^= 1;
     book->iir_slot = keep - 1;

@@ -142,14 +142,16 @@ int evs_model_create(const evs_config* cfg, const evs_weights* w, evs_model** ou
 int evs_model_destroy(evs_model* m);
 
 /* ---------------------------------------------------------------- state */
-/* Device-resident bookkeeping of one decoding state.  FIR windows and IIR
- * states live in two banks per layer: a verify reads the current bank and
- * writes its per-position results to the other; commit flips banks and
- * moves offsets, so slicing copies nothing ([implemented]).              */
+/* Device-resident bookkeeping of one decoding state.  Commit copies nothing
+ * ([implemented]): FIR inputs live in one ring per layer indexed by absolute
+ * position, so moving pos moves every window; IIR states live in two banks
+ * per layer, a verify reads the current bank and writes its per-position
+ * states to the other, and commit flips the bank and picks the slot.     */
 typedef struct evs_book {
-  int32_t pos;        /* committed tokens = valid KV rows = next position */
-  int32_t fir_bank;   /* bank holding the current FIR windows */
-  int32_t fir_off;    /* window = rows [fir_off, fir_off + L - 1) of that bank */
+  int32_t pos;        /* committed tokens = valid KV rows = next position; the
+                         FIR input of position p is ring row p mod (L-1+n_max) */
+  int32_t reserved0;  /* zero */
+  int32_t reserved1;  /* zero */
   int32_t iir_bank;   /* bank holding the current IIR states */
   int32_t iir_slot;   /* slot within that bank, -1 = the zero initial state */
   int32_t pending_n;  /* block size awaiting commit, 0 if none */
@@ -158,13 +160,18 @@ typedef struct evs_book {
 } evs_book;
 
 /* Per-layer state buffers (device pointers owned by the state):
- *  FIR : fir_ext[b]  float32 [L-1+n_max][d]  - window followed by block z
+ *  FIR : fir_ring  float32 [L-1+n_max][d] - the input z of position p at row
+ *        p mod (L-1+n_max); the window of the committed state (the last L-1
+ *        inputs) is positions pos-L+1 .. pos-1, zero before position 0.  A
+ *        verify of n tokens writes positions pos .. pos+n-1 and leaves the
+ *        window of every block position in place.
  *  IIR : iir_all[b]  float32 [n_max][d][M][2] - state after each block position
  *  ATTN: k_cache, v_cache [H][ctx_max][Dh] storage dtype (head-major, so a
  *        head's keys stream contiguously)                               */
 typedef struct evs_layer_view {
   int32_t kind, param;
-  float* fir_ext[2];
+  float* fir_ring;
+  void* reserved;
   float* iir_all[2];
   void* k_cache;
   void* v_cache;
@@ -173,8 +180,8 @@ typedef struct evs_layer_view {
 } evs_layer_view;
 
 /* Allocates all state for up to ctx_max positions (KV caches for attention
- * layers, two FIR / IIR banks per Hyena layer, activations, workspaces) and
- * resets it.  Synchronous. */
+ * layers, a FIR ring / two IIR banks per Hyena layer, activations,
+ * workspaces) and resets it.  Synchronous. */
 int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out);
 int evs_state_destroy(evs_state* s);
 /* Zero windows / states, empty caches, position 0.  Enqueued on stream. */
@@ -350,13 +357,14 @@ int evs_round_batch(evs_state* const* states_host, int32_t nseq, const int32_t* 
  * of GEMM partial sums.  For operator-level parity and timing.            */
 
 /* Hyena FIR mixer for one block ([systems], [prereq1]).
- * abv_dev [n][3d] storage dtype (a|b|v), taps [L][d], ext banks
- * [L-1+n_max][d] float32, book_dev: fir_bank / fir_off / pos are read,
- * nothing written.  Writes g_dev [n][d] storage dtype = a * (h (*) (b*v))
- * and ext rows [0, L-1+n) of bank 1-fir_bank.  Needs d % 32 == 0 and
- * 1 <= L <= 256. */
+ * abv_dev [n][3d] storage dtype (a|b|v), taps [L][d], ring_dev
+ * [L-1+n_max][d] float32 (the input of position p at row p mod (L-1+n_max),
+ * the window being positions pos-L+1 .. pos-1; rows before position 0 must
+ * be zero), book_dev: pos is read, nothing written.  Writes g_dev [n][d]
+ * storage dtype = a * (h (*) (b*v)) and the block's inputs b*v at positions
+ * pos .. pos+n-1 of the ring.  Needs d % 32 == 0 and 1 <= L <= 256. */
 int evs_op_fir(int32_t L, int32_t d, int32_t n, int32_t n_max, int32_t dtype,
-               const void* abv_dev, const float* taps_dev, float* ext0_dev, float* ext1_dev,
+               const void* abv_dev, const float* taps_dev, float* ring_dev,
                const evs_book* book_dev, void* g_dev, cudaStream_t stream);
 /* Hyena modal IIR mixer for one block.  State banks [n_max][d][M][2];
  * reads the state at (iir_bank, iir_slot), writes the n per-position states

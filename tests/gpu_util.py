@@ -80,3 +80,19 @@ def noise_drafts(evs, st, snap, pending, noise, du, T=1.0, top_k=4):
         drafts.append(cur)
     snap.snapshot_into(st)
     return drafts, to_np(qd), qd
+
+
+def fir_ext(ring, L, n_max, pos, n):
+    """Positions pos-L+1 .. pos+n-1 of a FIR ring [L-1+n_max][d] (position p at
+    row p mod (L-1+n_max)): the committed window followed by a block's n inputs,
+    so row i+1 .. i+L-1 is the window after block position i."""
+    R = L - 1 + n_max
+    return ring[[p % R for p in range(pos - L + 1, pos + n)]]
+
+
+def fir_set_window(ring_t, L, n_max, pos, window_t):
+    """Place the window of a state at position pos (positions pos-L+1 .. pos-1)."""
+    t = torch()
+    R = L - 1 + n_max
+    idx = t.tensor([(pos - L + 1 + r) % R for r in range(L - 1)], device=ring_t.device)
+    ring_t[idx] = window_t

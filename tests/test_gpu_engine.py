@@ -41,8 +41,7 @@ def _state_bits(shape, st):
     for li, (kind, param) in enumerate(shape.layers):
         v = st.view(li)
         if kind in ("SE", "MR"):
-            for b in (0, 1):
-                out.append(to_np(wrap(v.fir_ext[b], (param - 1 + v.n_max, d))).view(np.uint32))
+            out.append(to_np(wrap(v.fir_ring, (param - 1 + v.n_max, d))).view(np.uint32))
         elif kind == "LI":
             for b in (0, 1):
                 out.append(to_np(wrap(v.iir_all[b], (v.n_max, d, param, 2))).view(np.uint32))

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import book_zero, rel_err, to_np, torch, up, wrap
+from gpu_util import book_zero, fir_ext, fir_set_window, rel_err, to_np, torch, up, wrap
 from oracle.model import attend, rope
 from oracle.numerics import Arith, round_bf16
 
@@ -120,7 +120,7 @@ def test_7b_stack_262144_context_rounds():
         v = st.view(li)
         L = S["layers"][li]
         if kind in ("SE", "MR"):
-            wrap(v.fir_ext[0], (param - 1 + v.n_max, d))[:param - 1] = up(L["window"])
+            fir_set_window(wrap(v.fir_ring, (param - 1 + v.n_max, d)), param, v.n_max, P, up(L["window"]))
         elif kind == "LI":
             wrap(v.iir_all[0], (v.n_max, d, param, 2))[0] = up(L["s"]).view(d, param, 2)
         else:
@@ -134,7 +134,7 @@ def test_7b_stack_262144_context_rounds():
                 kc.normal_(generator=gen)
                 vc.normal_(generator=gen)
     t.cuda.synchronize()
-    st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
+    st.set_book(pos=P, iir_bank=0, iir_slot=0, pending_n=0, status=0)
     toks = [int(x) for x in synth.prompt(shape, seed, n)]
     tt = t.tensor(np.asarray(toks, np.int32), device="cuda")
     lg = t.empty((n, V), dtype=t.float32, device="cuda")
@@ -148,7 +148,7 @@ def test_7b_stack_262144_context_rounds():
     for li, (kind, param) in enumerate(shape.layers):
         v = st.view(li)
         if kind in ("SE", "MR"):
-            ret[li] = to_np(wrap(v.fir_ext[1 - book["fir_bank"]], (param - 1 + v.n_max, d)))
+            ret[li] = fir_ext(to_np(wrap(v.fir_ring, (param - 1 + v.n_max, d))), param, v.n_max, P, n)
         elif kind == "LI":
             ret[li] = to_np(wrap(v.iir_all[1 - book["iir_bank"]], (v.n_max, d, param, 2)))
         elif li == checked:

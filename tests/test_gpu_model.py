@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import noise_drafts, rel_err, to_np, torch, up, wrap
+from gpu_util import fir_ext, fir_set_window, noise_drafts, rel_err, to_np, torch, up, wrap
 
 TOL = 2e-2
 
@@ -322,7 +322,7 @@ def _load_synth_state(evs, shape, st, S, P):
         L = S["layers"][li]
         d = shape.d_model
         if kind in ("SE", "MR"):
-            wrap(v.fir_ext[0], (param - 1 + v.n_max, d))[:param - 1] = up(L["window"])
+            fir_set_window(wrap(v.fir_ring, (param - 1 + v.n_max, d)), param, v.n_max, P, up(L["window"]))
         elif kind == "LI":
             wrap(v.iir_all[0], (v.n_max, d, param, 2))[0] = up(L["s"]).view(d, param, 2)
         else:
@@ -332,11 +332,12 @@ def _load_synth_state(evs, shape, st, S, P):
             kc[:, :P] = up(L["k"]).transpose(0, 1)
             vc[:, :P] = up(L["v"]).transpose(0, 1)
     t.cuda.synchronize()
-    st.set_book(pos=P, fir_bank=0, fir_off=0, iir_bank=0, iir_slot=0, pending_n=0, status=0)
+    st.set_book(pos=P, iir_bank=0, iir_slot=0, pending_n=0, status=0)
 
 
 def _retained_np(shape, st, P, n):
-    """Copies of the per-position state a verify left in the spare banks."""
+    """Copies of the per-position state a verify left: FIR positions P-L+1 ..
+    P+n-1 from the ring (window then inputs), IIR states from the spare bank."""
     t = torch()
     book = st.book()
     out = {}
@@ -344,7 +345,7 @@ def _retained_np(shape, st, P, n):
         v = st.view(li)
         d = shape.d_model
         if kind in ("SE", "MR"):
-            out[li] = to_np(wrap(v.fir_ext[1 - book["fir_bank"]], (param - 1 + v.n_max, d)))
+            out[li] = fir_ext(to_np(wrap(v.fir_ring, (param - 1 + v.n_max, d))), param, v.n_max, P, n)
         elif kind == "LI":
             out[li] = to_np(wrap(v.iir_all[1 - book["iir_bank"]], (v.n_max, d, param, 2)))
         else:

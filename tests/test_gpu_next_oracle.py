@@ -24,7 +24,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import rel_err, to_np, torch, wrap
+from gpu_util import fir_ext, rel_err, to_np, torch, wrap
 
 TOL = 2e-2
 
@@ -71,8 +71,7 @@ def _check_committed_state(shape, st, ost, what):
         v = st.view(li)
         ref = ost.layers[li]
         if kind in ("SE", "MR"):
-            ext = to_np(wrap(v.fir_ext[book["fir_bank"]], (param - 1 + v.n_max, d)))
-            got = ext[book["fir_off"]:book["fir_off"] + param - 1]
+            got = fir_ext(to_np(wrap(v.fir_ring, (param - 1 + v.n_max, d))), param, v.n_max, book["pos"], 0)
             assert rel_err(got, ref.window) <= TOL, (what, li)
         elif kind == "LI":
             if book["iir_slot"] < 0:

@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import book_zero, rel_err, to_np, torch, up, wrap
+from gpu_util import book_zero, fir_ext, fir_set_window, rel_err, to_np, torch, up, wrap
 from oracle.model import LayerState, Model as OModel, attend, rope
 from oracle.numerics import Arith, round_bf16
 
@@ -39,27 +39,30 @@ def _f(bits):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("L", [7, 128])
-def test_fir_op_block_and_slice(L):
+@pytest.mark.parametrize("L,pos0", [(7, 40), (128, 300), (7, 2)])
+def test_fir_op_block_and_slice(L, pos0):
+    # The ring holds the input of position p at row p mod (L-1+n_max): at
+    # pos0 = 300 with L = 128 the window wraps around the ring; at pos0 = 2
+    # the window reaches before position 0 (zero rows, never written).
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
     n_max, d = 13, D
     taps = synth.mixer_params(1, "MR", L, d)["taps"]
-    win = synth.layer_state(1, "MR", L, d)["window"]
-    off = 3
-    ext0 = t.zeros((L - 1 + n_max, d), dtype=t.float32, device="cuda")
-    ext1 = t.zeros_like(ext0)
-    ext0[off:off + L - 1] = up(win)
+    win = synth.layer_state(1, "MR", L, d)["window"].copy()
+    win[:max(0, L - 1 - pos0)] = 0.0
+    ring = t.zeros((L - 1 + n_max, d), dtype=t.float32, device="cuda")
+    fir_set_window(ring, L, n_max, pos0, up(win))
     book = book_zero(t)
-    book[2] = off
+    book[0] = pos0
     taps_d = up(taps)
     ops = _Ops()
     st = LayerState("MR", window=win.copy())
     rng = np.random.default_rng(L)
+    pos = pos0
     for rnd, n in enumerate((13, 1, 13)):
         abv = _abv(10 + rnd, n, d)
         g = t.empty((n, d), dtype=t.bfloat16, device="cuda")
-        evs.evs_op_fir(L, d, n, n_max, evs.EVS_BF16, up(abv), taps_d, ext0, ext1, book, g)
+        evs.evs_op_fir(L, d, n, n_max, evs.EVS_BF16, up(abv), taps_d, ring, book, g)
         a, b, v = _f(abv[:, :d]), _f(abv[:, d:2 * d]), _f(abv[:, 2 * d:])
         recs, gref = [], []
         work = LayerState("MR", window=st.window.copy())
@@ -69,16 +72,15 @@ def test_fir_op_block_and_slice(L):
             gref.append(round_bf16(a[i] * y))
             recs.append(work.window.copy())
         assert rel_err(to_np(g), np.stack(gref)) <= 2e-2
-        bank = int(book[1].item())
-        ext = to_np(ext1 if bank == 0 else ext0)
+        ext = fir_ext(to_np(ring), L, n_max, pos, n)
         for i in range(n):
             assert np.array_equal(ext[i + 1:i + L], recs[i]), (rnd, i)
         keep = int(rng.integers(0, n + 1)) if rnd != 1 else 0
         evs.evs_op_commit(book, keep, n)
         if keep:
             st.window = recs[keep - 1]
-        bk = book.cpu().numpy()
-        assert bk[1] == 1 - bank and bk[2] == keep
+        pos += keep
+        assert int(book[0].item()) == pos
 
 
 @pytest.mark.gpu

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import rel_err, to_np, torch, wrap
+from gpu_util import fir_ext, rel_err, to_np, torch, wrap
 
 TOL = 1e-5
 
@@ -44,7 +44,7 @@ def _check_retained(shape, st, book, records, n):
         v = st.view(li)
         if kind in ("SE", "MR"):
             L = param
-            ext = to_np(wrap(v.fir_ext[1 - book["fir_bank"]], (L - 1 + v.n_max, d)))
+            ext = fir_ext(to_np(wrap(v.fir_ring, (L - 1 + v.n_max, d))), L, v.n_max, book["pos"], n)
             for i in range(n):
                 assert rel_err(ext[i + 1:i + L], records[i].layers[li].window) <= TOL
         elif kind == "LI":
