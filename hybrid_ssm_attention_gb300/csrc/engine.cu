@@ -49,23 +49,6 @@ constexpr size_t E_BAR_OFF = (size_t)E_S * (EA_BYTES + EB_BYTES);
 constexpr size_t E_ROW_OFF = (E_BAR_OFF + (3 * E_S + 5) * 8 + 64 + 127) & ~(size_t)127;
 constexpr size_t E_FIXED = 1024 + E_ROW_OFF;
 
-// Timeline hooks, compiled in only for profiling builds (EVS_ENGINE_TRACE):
-// per CTA and program phase, the time of event ev (producer first / last
-// unit, activation readiness, first / last MMA, last epilogue count, first
-// row item start / last row item end).
-#ifdef EVS_ENGINE_TRACE
-constexpr int ETR_CTAS = 160, ETR_PHASES = 512, ETR_EV = 16;
-__device__ unsigned long long g_etrace[(size_t)ETR_CTAS * ETR_PHASES * ETR_EV];
-#define ETR(ph, ev)                                                                                             \
-  do {                                                                                                          \
-    if (c < ETR_CTAS && (ph) < ETR_PHASES) g_etrace[((size_t)c * ETR_PHASES + (ph)) * ETR_EV + (ev)] = gtimer(); \
-  } while (0)
-#else
-#define ETR(ph, ev) \
-  do {              \
-  } while (0)
-#endif
-
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -158,18 +141,6 @@ __device__ __forceinline__ void unit_range(const EngPhase& P, int c, long long* 
 // Waits (one thread) until every contributor of the listed tiles of the
 // GEMM whose slots a row phase reads has finished; the row threads proceed
 // together.
-#ifdef EVS_ENGINE_TRACE
-__device__ int g_trace_ph[ETR_CTAS];  // the row phase each CTA is working on
-#define ETR_ROW(ev)                                             \
-  do {                                                          \
-    const int c = blockIdx.x;                                   \
-    if (threadIdx.x == E_ROW0 * 32 && c < ETR_CTAS) ETR(g_trace_ph[c], ev); \
-  } while (0)
-#else
-#define ETR_ROW(ev) \
-  do {              \
-  } while (0)
-#endif
 
 __device__ bool row_wait_tiles(const EngPhase& P, const int* tiles, int k, Abort ab, volatile int* s_flag) {
   const int rt = threadIdx.x - E_ROW0 * 32;
@@ -177,7 +148,6 @@ __device__ bool row_wait_tiles(const EngPhase& P, const int* tiles, int k, Abort
     bool ok = true;
     for (int i = 0; i < k && ok; ++i) ok = e_count_wait(P.cnt + tiles[i], __ldg(&P.tab[tiles[i]].y), ab);
     *s_flag = ok ? 1 : 0;
-    ETR_ROW(8);
   }
   row_sync();
   const bool ok = *s_flag != 0;
@@ -187,13 +157,10 @@ __device__ bool row_wait_tiles(const EngPhase& P, const int* tiles, int k, Abort
 // All row threads' outputs of an item are written: make them visible to the
 // async proxy (TMA readers), then count the item.
 __device__ void row_signal(int* counter, bool tma_readers) {
-  ETR_ROW(9);
   if (tma_readers) fence_proxy_async_global();
-  ETR_ROW(10);
   row_sync();
   if (threadIdx.x == E_ROW0 * 32) {
     red_release_add(counter, 1);
-    ETR_ROW(11);
   }
 }
 
@@ -388,10 +355,8 @@ __device__ bool resid_item(const EngPhase& P, int t, int n, int d, float eps, Ab
   }
   row_sync();
   if (rt == 0) {
-    ETR_ROW(12);
     red_release_add(P.done, 1);
     *s_flag = e_count_wait(P.done, d / TILE_M, ab) ? 1 : 0;
-    ETR_ROW(13);
   }
   row_sync();
   const bool ok = *s_flag != 0;
@@ -556,7 +521,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
       if (ub >= ue) continue;
       const uint8_t* wp = P.wpk + (size_t)c * EA_BYTES;
       const size_t step = (size_t)P.G * EA_BYTES;
-      ETR(ph, 0);
       for (long long u = ub; u < ue; ++u, ++i) {
         const int s = (int)(i & (E_S - 1));
         if (i >= E_S && !e_mbar_wait(empty(s), (uint32_t)((i >> E_SLOG) - 1) & 1, ab)) {
@@ -568,7 +532,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         wp += step;
         *s_prod = (int)(i + 1);
       }
-      ETR(ph, 1);
     }
     for (long long j = i > E_S ? i - E_S : 0; j < i; ++j)
       drain_wait(w_full((int)(j & (E_S - 1))), (uint32_t)(j >> E_SLOG) & 1);
@@ -614,7 +577,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         if (!e_count_wait(P.ready, P.target, ab)) break;
         fence_proxy_async_global();
       }
-      ETR(ph, 2);
       const CUtensorMap* map = P.bmap == ENG_B_XN ? &m_xn : P.bmap == ENG_B_G ? &m_g : &m_h;
       const int KB = P.KB;
       int kb = (int)(ub % KB);
@@ -626,8 +588,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         }
         mbar_expect_tx(b_full(s), EB_BYTES);
         tma_load_2d(smem_u32(sB + s * EB_BYTES), map, b_full(s), kb * TILE_K, 0, pol);
-        if (u == ub) ETR(ph, 8);
-        if (u == ub + 7) ETR(ph, 9);
         if (++kb == KB) kb = 0;
       }
     }
@@ -666,18 +626,11 @@ __global__ void __launch_bounds__(E_THREADS, 1)
             ok = false;
             break;
           }
-          if (u == ub) ETR(ph, 10);
           if (!e_mbar_wait(b_full(s), par, ab)) {
             ok = false;
             break;
           }
-          if (u == ub) ETR(ph, 11);
-          if (u == ub + 1) ETR(ph, 12);
-          if (u == ub + 4) ETR(ph, 13);
           tc_fence_after();
-          if (u == ub) ETR(ph, 3);
-          if (u == ub + E_S) ETR(ph, 6);
-          if (u == ub + E_S + E_PF) ETR(ph, 7);
           const uint64_t ad = ad0 + (uint64_t)(s * (EA_BYTES >> 4));
           const uint64_t bd = bd0 + (uint64_t)(s * (EB_BYTES >> 4));
 #pragma unroll
@@ -687,7 +640,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         }
         if (ok) mma_commit(acc_full(b));
       }
-      ETR(ph, 4);
     }
     mma_commit(drain);
     drain_wait(drain, 0);
@@ -725,7 +677,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
         epi_sync();
         if (g == 0) {
           red_release_add(P.cnt + tile, 1);
-          ETR(ph, 5);
         }
       }
     }
@@ -734,13 +685,8 @@ __global__ void __launch_bounds__(E_THREADS, 1)
     for (int ph = a.ph0; ph < a.ph1; ++ph) {
       const EngPhase& P = prog[ph];
       if (P.kind == ENG_GEMM) continue;
-#ifdef EVS_ENGINE_TRACE
-      if (threadIdx.x == E_ROW0 * 32 && c < ETR_CTAS) g_trace_ph[c] = ph;
-      if (threadIdx.x == E_ROW0 * 32) ETR(ph, 6);
-#endif
       for (int j = c; j < P.G; j += gridDim.x)
         if (!row_item(P, j, a, row_sm, ab, s_row)) break;
-      if (threadIdx.x == E_ROW0 * 32) ETR(ph, 7);
       // all row warps leave the phase together and agree whether to go on
       row_sync();
       if (threadIdx.x == E_ROW0 * 32) *s_row = aborted(ab) ? 0 : 1;
@@ -761,17 +707,6 @@ __global__ void __launch_bounds__(E_THREADS, 1)
 }
 
 }  // namespace
-
-#ifdef EVS_ENGINE_TRACE
-// profiling builds only: copies the timeline out and clears it
-extern "C" int evs_engine_trace_read(unsigned long long* out_host) {
-  const size_t bytes = sizeof(g_etrace);
-  if (cudaMemcpyFromSymbol(out_host, g_etrace, bytes) != cudaSuccess) return 5;
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_etrace) != cudaSuccess || cudaMemset(p, 0, bytes) != cudaSuccess) return 5;
-  return 0;
-}
-#endif
 
 int engine_row_floats(int kind, int param, int sub) {
   if (kind == ENG_FIR) {

@@ -167,8 +167,6 @@ struct evs_state {
   CUtensorMap m_xf;  // fp32 X [ROWS_MAX][d] (RMSNorm converter source, 16-row boxes)
   bool use_graphs, pdl;
   int pf_units;  // next-weight L2 prefetch per CTA (units of 128x64)
-  unsigned long long* trace;  // EVS_TRACE builds: GEMM timeline slots
-  int cta_slot = -1;          // EVS_TRACE builds: GEMM launch with per-CTA timeline
   cudaStream_t cap;
   // Persistent engine (single-sequence bf16 verifies): the phase program,
   // its counters and the spans it is cut into by the attention mixers
@@ -518,11 +516,6 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
     P.nKB = np->KB;
     P.nU = np->U;
     P.ncl = np->cl;
-#ifdef EVS_TRACE
-    P.trace = s->trace;
-    P.trace_slot = gk - 1;
-    P.cta_slot = s->cta_slot;
-#endif
     if (out) {
       *out = MixSrc{fin, ld, 1};
       if (mode == GEMM_SLOTS) {
@@ -973,9 +966,6 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   ALLOC(s->ss, sizeof(float) * R * ((d + TILE_M - 1) / TILE_M));
   s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
   ALLOC(s->cnt, sizeof(int) * s->cnt_len);
-#ifdef EVS_TRACE
-  ALLOC(s->trace, sizeof(unsigned long long) * (6 * 1024 + 4 * 1024 + 512));
-#endif
   size_t wsb = 0;
   wsb = m->ws_bytes;
   ALLOC(s->ws[0], wsb);
@@ -1802,39 +1792,6 @@ extern "C" int evs_profile_gemm_chain(evs_state* s, int32_t n, int32_t reps, flo
   *launches = (int32_t)calls.size();
   return EVS_OK;
 }
-
-#ifdef EVS_TRACE
-// Timeline of the GEMM launches since the previous call: out[6k..6k+5] =
-// {first entry, first dependency release, last exit, first MMA, last
-// accumulator drain, last fixup end} of the k-th GEMM; re-arms the slots.
-extern "C" int evs_trace_read(evs_state* s, unsigned long long* out, int32_t max_slots) {
-  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
-  const int k = std::min(max_slots, 1024);
-  CUDA_TRY(cudaDeviceSynchronize());
-  CUDA_TRY(cudaMemcpy(out, s->trace, sizeof(unsigned long long) * 6 * k, cudaMemcpyDeviceToHost));
-  std::vector<unsigned long long> init(6 * 1024);
-  for (int i = 0; i < 1024; ++i) {
-    init[6 * i] = init[6 * i + 1] = init[6 * i + 3] = ~0ull;
-    init[6 * i + 2] = init[6 * i + 4] = init[6 * i + 5] = 0;
-  }
-  CUDA_TRY(cudaMemcpy(s->trace, init.data(), sizeof(unsigned long long) * 6 * 1024, cudaMemcpyHostToDevice));
-  return EVS_OK;
-}
-// Per-CTA timeline {first MMA, SM id, last accumulator read, end}
-// of GEMM launch `slot` of later verifies: out[4c..4c+3] for CTA c < 1024;
-// then out[4096 + 256 w + 64 k + i]: CTA (w ? 100 : 0), unit i < 64, event k
-// (0 issue, 1 converter saw its rows, 2 B tile ready, 3 MMA start).
-// Reads the previous recording, then arms slot for the next ones.
-extern "C" int evs_trace_cta(evs_state* s, int32_t slot, unsigned long long* out) {
-  if (!s || !out) return fail(EVS_ERR_ARG, "null argument");
-  CUDA_TRY(cudaDeviceSynchronize());
-  CUDA_TRY(cudaMemcpy(out, s->trace + 6 * 1024, sizeof(unsigned long long) * (4 * 1024 + 512),
-                      cudaMemcpyDeviceToHost));
-  CUDA_TRY(cudaMemset(s->trace + 6 * 1024, 0, sizeof(unsigned long long) * (4 * 1024 + 512)));
-  s->cta_slot = slot;
-  return EVS_OK;
-}
-#endif
 
 extern "C" int evs_selftest_wait_timeout(int32_t* status_dev, int64_t limit_ns, cudaStream_t stream) {
   if (!status_dev) return fail(EVS_ERR_ARG, "null status");

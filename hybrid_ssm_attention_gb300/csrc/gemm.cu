@@ -283,28 +283,15 @@ __device__ void tile_done(const Partials& P, int tile, int row, volatile int* s_
   if (row == 0) P.cnt[tile] = 0;
 }
 
-
-#ifdef EVS_TRACE
-// unit-level timeline of CTAs 0 and 100 of the per-CTA traced launch:
-// [which][kind][unit < 64], kind 0 issue, 1 converter saw full, 2 ready, 3 MMA start
-#define UNIT_TRACE(kind, i)                                                                        \
-  do {                                                                                             \
-    if (P.trace && P.trace_slot == P.cta_slot && (c == 0 || c == 100) && (i) < 64)                 \
-      P.trace[6 * 1024 + 4 * 1024 + (c == 0 ? 0 : 256) + (kind) * 64 + (int)(i)] = gtimer();       \
-  } while (0)
-#else
-#define UNIT_TRACE(kind, i) \
-  do {                      \
-  } while (0)
-#endif
-
 // At most 144 registers a thread (no spills): a 320-thread block then leaves
 // a 256-thread, 72-register mixer CTA room on the SM to start its prologue
 // while the GEMM drains.
 // MC: several 16-row chunks (P.nt > 1); a separate instance so that the
-// one-chunk kernel keeps its register allocation.
+// one-chunk kernel keeps its register allocation.  It holds the wider
+// epilogue's state in 168 registers (no spills; a 72-register mixer CTA
+// still fits beside it).
 template <bool MC>
-__global__ void __maxnreg__(144)
+__global__ void __maxnreg__(MC ? 168 : 144)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const __grid_constant__ CUtensorMap nmap, Partials P, int* err_flag) {
   extern __shared__ uint8_t smem_raw[];
@@ -374,9 +361,6 @@ __global__ void __maxnreg__(144)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
-#ifdef EVS_TRACE
-    if (P.trace) atomicMin(P.trace + 6 * P.trace_slot, gtimer());
-#endif
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (!P.wpk) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
@@ -425,16 +409,12 @@ __global__ void __maxnreg__(144)
     int kb = kb0, t = t0;
     const uint8_t* wp = wp0;
     for (int i = 0; i < pre; ++i) {
-      UNIT_TRACE(0, i);
       mbar_expect_tx(full0 + 8 * i, stage_tx);
       load_w(i, kb, t, wp);
       if (++kb == KB) kb = 0, ++t;
       if (wp) wp += wstep;
     }
     pdl_wait();  // activations are written by the preceding kernel
-#ifdef EVS_TRACE
-    if (P.trace) atomicMin(P.trace + 6 * P.trace_slot + 1, gtimer());
-#endif
     for (int i = 0, k2 = kb0; i < pre; ++i) {
       load_b(i, k2);
       if (++k2 == KB) k2 = 0;
@@ -447,7 +427,6 @@ __global__ void __maxnreg__(144)
     long long i = pre;
     for (; i < nunits; ++i) {
       if (!mbar_wait(empty0 + 8 * s, ph, abort_flag)) break;
-      UNIT_TRACE(0, i);
       mbar_expect_tx(full0 + 8 * s, stage_tx);
       load_w(s, kb, t, wp);
       load_b(s, kb);
@@ -511,29 +490,17 @@ __global__ void __maxnreg__(144)
           break;
         }
         tc_fence_after();
-        UNIT_TRACE(3, i);
         const uint64_t ad = ad0 + (uint64_t)(s * (A_BYTES >> 4));
         const uint64_t bd = bd0 + (uint64_t)(s * (BST >> 4));
 #pragma unroll
         for (int k = 0; k < TILE_K / 16; ++k)  // 16 bf16 = 32 bytes per MMA step along K
           mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-#ifdef EVS_TRACE
-        if (i == 0 && P.trace) atomicMin(P.trace + 6 * P.trace_slot + 3, gtimer());
-        if (i == 0 && P.trace && P.trace_slot == P.cta_slot && c < 1024) P.trace[6 * 1024 + 4 * c] = gtimer();
-#endif
         first = false;
         mma_commit(empty0 + 8 * s);
         if (++s == STAGES) s = 0, ph ^= 1;
       }
       if (ok) mma_commit(acc_full(b));
     }
-#ifdef EVS_TRACE
-    if (P.trace && P.trace_slot == P.cta_slot && c < 1024) {
-      unsigned smid;
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      P.trace[6 * 1024 + 4 * c + 1] = smid;
-    }
-#endif
     // wait for every issued MMA before TMEM is released
     mma_commit(drain);
     volatile int local_abort = 0;
@@ -569,11 +536,6 @@ __global__ void __maxnreg__(144)
         tc_fence_before();
         mbar_arrive(acc_empty(b));
       }
-#ifdef EVS_TRACE
-      if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 4, gtimer());
-      if (g == 0 && seg == nseg - 1 && P.trace && P.trace_slot == P.cta_slot && c < 1024)
-        P.trace[6 * 1024 + 4 * c + 2] = gtimer();
-#endif
       if (clmode) {
         // ranks 1..cl-1 send their column to rank 0's shared memory
         if (crank == 0) {
@@ -610,9 +572,6 @@ __global__ void __maxnreg__(144)
         mbar_arrive(acc_empty(b));
       }
       if (P.mode != GEMM_SLOTS) tile_done<true, MC>(P, tile, row, s_flag, s_red, s_xch);
-#ifdef EVS_TRACE
-      if (g == 0 && seg == nseg - 1 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 5, gtimer());
-#endif
     }
   } else if (warp >= 6 && P.bsrc != GEMM_B_TMA) {
     // ---------------- B-tile converters: fp32 residual rows (staged by TMA)
@@ -650,7 +609,6 @@ __global__ void __maxnreg__(144)
     uint32_t ph = 0;
     for (long long i = 0; i < nunits; ++i) {
       if (!warp_wait(full(s), ph, abort_flag)) break;
-      if (w == 0 && lane == 0) UNIT_TRACE(1, i);
       const int col = kb * TILE_K + 4 * cq;  // first of this lane's four columns
       const float* raw = reinterpret_cast<const float*>(sR + s * RAW) + 4 * cq;
       uint8_t* dstB = sB + s * B_BYTES + (cq & 1) * 8;
@@ -677,7 +635,6 @@ __global__ void __maxnreg__(144)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(ready(s));
-      if (w == 0 && lane == 0) UNIT_TRACE(2, i);
       if (++s == STAGES) s = 0, ph ^= 1;
       if (++kb == P.KB) kb = 0;
     }
@@ -710,13 +667,6 @@ __global__ void __maxnreg__(144)
         for (int j = 0; j < NTOK; ++j) vkeep[j] = vkeep[j] + acc[j];
       }
       tile_output<true>(P, first_tile, row, vkeep, s_red, s_xch, have_x ? xpre : nullptr);
-#ifdef EVS_TRACE
-      if (threadIdx.x == 64 && P.trace) {
-        const unsigned long long now = gtimer();
-        atomicMax(P.trace + 6 * P.trace_slot + 5, now);
-        atomicMax(P.trace + 6 * P.trace_slot + 2, now);  // the kernel's real end
-      }
-#endif
     }
   }
   if (warp == 1) {
@@ -724,10 +674,6 @@ __global__ void __maxnreg__(144)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(err_flag, EVS_DEV_TIMEOUT);
-#ifdef EVS_TRACE
-  if (threadIdx.x == 0 && P.trace) atomicMax(P.trace + 6 * P.trace_slot + 2, gtimer());
-  if (threadIdx.x == 0 && P.trace && P.trace_slot == P.cta_slot && c < 1024) P.trace[6 * 1024 + 4 * c + 3] = gtimer();
-#endif
 }
 
 // SIMT variant with the same unit schedule and partial layout (float32
