@@ -17,7 +17,8 @@ import numpy as np
 from . import _abi
 from ._abi import (EVS_BF16, EVS_ERR_ARG, EVS_ERR_CAPACITY, EVS_ERR_CUDA, EVS_ERR_DEVICE,  # noqa: F401
                    EVS_ERR_OOM, EVS_ERR_STATE, EVS_ERR_UNSUPPORTED, EVS_F32, EVS_GREEDY, EVS_LAYER_ATTN,
-                   EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_SAMPLE, evs_book, evs_layer_view)
+                   EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_OPT_GEMM_SUMS_SLOTS, EVS_OPT_NORM_IN_GEMM,
+                   EVS_OPT_SWIGLU_EPILOGUE, EVS_SAMPLE, evs_book, evs_layer_view)
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
            "evs_commit", "evs_commit_dev", "evs_markov_draft", "evs_round", "evs_round_batch", "evs_op_fir", "evs_op_iir",
@@ -81,7 +82,7 @@ class Model:
     d_ffn, gamma, dtype ("bf16" | "f32"), attn_chunk, rope_base, norm_eps;
     ``weights`` is the dict layout of the synthetic-input module (numpy)."""
 
-    def __init__(self, shape, weights: dict):
+    def __init__(self, shape, weights: dict, options: int = 0):
         self.shape = shape
         self.dtype = EVS_BF16 if shape.dtype == "bf16" else EVS_F32
         self.tensors = []
@@ -93,7 +94,7 @@ class Model:
         cfg = _abi.evs_config(vocab=shape.vocab, d_model=shape.d_model, n_layers=nl,
                               n_heads=shape.n_heads, head_dim=shape.head_dim, d_ffn=shape.d_ffn,
                               gamma_max=shape.gamma, dtype=self.dtype, attn_chunk=shape.attn_chunk,
-                              rope_base=shape.rope_base, norm_eps=shape.norm_eps,
+                              rope_base=shape.rope_base, norm_eps=shape.norm_eps, options=int(options),
                               layer_kind_host=kinds, layer_param_host=params)
         lw = (_abi.evs_layer_weights * nl)()
         for i, L in enumerate(weights["layers"]):

@@ -17,6 +17,7 @@ EVS_DEV_BAD_TOKEN, EVS_DEV_KV_OVERFLOW, EVS_DEV_BAD_KEEP, EVS_DEV_TIMEOUT, EVS_D
 EVS_F32, EVS_BF16 = 0, 1
 EVS_LAYER_FIR, EVS_LAYER_IIR, EVS_LAYER_ATTN = 0, 1, 2
 EVS_GREEDY, EVS_SAMPLE = 0, 1
+EVS_OPT_SWIGLU_EPILOGUE, EVS_OPT_NORM_IN_GEMM, EVS_OPT_GEMM_SUMS_SLOTS = 1, 2, 4
 
 ERR_NAMES = {0: "EVS_OK", 1: "EVS_ERR_ARG", 2: "EVS_ERR_STATE", 3: "EVS_ERR_CAPACITY",
              4: "EVS_ERR_OOM", 5: "EVS_ERR_CUDA", 6: "EVS_ERR_DEVICE", 7: "EVS_ERR_UNSUPPORTED"}
@@ -27,7 +28,7 @@ vp, i32, i64, f32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_size_t
 class evs_config(C.Structure):
     _fields_ = [("vocab", i32), ("d_model", i32), ("n_layers", i32), ("n_heads", i32),
                 ("head_dim", i32), ("d_ffn", i32), ("gamma_max", i32), ("dtype", i32),
-                ("attn_chunk", i32), ("rope_base", f32), ("norm_eps", f32),
+                ("attn_chunk", i32), ("rope_base", f32), ("norm_eps", f32), ("options", i32),
                 ("layer_kind_host", C.POINTER(i32)), ("layer_param_host", C.POINTER(i32))]
 
 

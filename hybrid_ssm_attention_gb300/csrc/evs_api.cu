@@ -120,9 +120,9 @@ struct evs_model {
   bool packed;
   // Opt-in fusions of the small elementwise kernels into the GEMMs (packed
   // weights only), bit-identical to the separate kernels:
-  //  swiglu (EVS_SWIGLU=1): the gate/up GEMM applies SiLU-and-multiply in
+  //  swiglu (EVS_OPT_SWIGLU_EPILOGUE): the gate/up GEMM applies SiLU-and-multiply in
   //    its epilogue (no activation kernel);
-  //  fuse (EVS_FUSE=1): the GEMMs that read RMSNorm output build their B
+  //  fuse (EVS_OPT_NORM_IN_GEMM): the GEMMs that read RMSNorm output build their B
   //    tiles from the fp32 residual rows (no normalisation kernels).
   // Both measured slower on the 7B-shaped stack: with a small kernel in
   // between, the next GEMM's CTAs are resident and loading weights before
@@ -133,7 +133,7 @@ struct evs_model {
   bool fuse;
   // stream-K in-projection and gate/up GEMMs leave their partial slots to
   // the consuming mixer / activation kernel (GEMM_SLOTS): no fixup tail
-  // (bf16; EVS_SLOTS=0 keeps the GEMM-side fixup)
+  // (bf16; EVS_OPT_GEMM_SUMS_SLOTS keeps the GEMM-side fixup)
   bool slots;
   // out / down GEMMs too (stream-K on every SM instead of cluster split-K),
   // the residual add and its sums of squares done by resid_norm (fused
@@ -484,7 +484,7 @@ int enqueue_verify(evs_state* const* states, const SeqRows& sr, const int32_t* t
       for (int k = 0; k < 5; ++k)
         if (&plan == one[k]) P = *many[k];
       if (P.cl != 0 || bsrc != GEMM_B_TMA || !m->tc)
-        return fail(EVS_ERR_UNSUPPORTED, "passes of more than %d rows need the bf16 path without EVS_FUSE", NTOK);
+        return fail(EVS_ERR_UNSUPPORTED, "passes of more than %d rows need the bf16 path without EVS_OPT_NORM_IN_GEMM", NTOK);
       P.stages = std::min(P.stages, gemm_stages_for(0, GEMM_B_TMA, nt));
     }
     P.nt = nt;
@@ -769,14 +769,12 @@ extern "C" int evs_model_create(const evs_config* cfg, const evs_weights* w, evs
   m->n_max = cfg->gamma_max + 1;
   m->has_attn = false;
   {
-    const char* fz = getenv("EVS_FUSE");
-    const char* sw = getenv("EVS_SWIGLU");
+    const int opt = cfg->options;
     m->packed = m->tc && cfg->d_ffn % (TILE_M / 2) == 0;
-    m->swiglu = m->packed && sw && sw[0] == '1';
+    m->swiglu = m->packed && (opt & EVS_OPT_SWIGLU_EPILOGUE);
     // fp32 rows staged by TMA need 16-byte row strides
-    m->fuse = m->packed && cfg->d_model % 4 == 0 && fz && fz[0] == '1';
-    const char* sl = getenv("EVS_SLOTS");
-    m->slots = m->tc && !(sl && sl[0] == '0');
+    m->fuse = m->packed && cfg->d_model % 4 == 0 && (opt & EVS_OPT_NORM_IN_GEMM);
+    m->slots = m->tc && !(opt & EVS_OPT_GEMM_SUMS_SLOTS);
     m->slots_resid = m->slots && resid_norm_ok(cfg->d_model);
   }
   const int d = cfg->d_model, F = cfg->d_ffn, V = cfg->vocab;

@@ -86,6 +86,18 @@ enum { EVS_GREEDY = 0, EVS_SAMPLE = 1 };
  * MLP    W_down (silu(W_gate xn) * W_up xn); head logits = W_lm RMSNorm(x).
  * bf16 storage needs d_model, 2*d_ffn, vocab multiples of 128 and
  * d_model, d_ffn multiples of 64; f32 storage has no such limit.        */
+/* Alternative kernel arrangements of the bf16 path, each bit-for-bit equal to
+ * the default and measured slower on the 7B-shaped round; for comparison.
+ *  EVS_OPT_SWIGLU_EPILOGUE: SiLU-and-multiply in the gate/up GEMM's epilogue
+ *    (gate / up rows interleaved by 64 in the packed weights).
+ *  EVS_OPT_NORM_IN_GEMM: the RMSNorm of each GEMM input built by the GEMM's
+ *    own B-tile converters from the fp32 residual rows (passes of at most
+ *    16 rows).
+ *  EVS_OPT_GEMM_SUMS_SLOTS: every GEMM sums its split-K partials itself
+ *    (the last contributor of a tile; out / down on 4-CTA clusters) instead
+ *    of leaving them to the consuming kernel. */
+enum { EVS_OPT_SWIGLU_EPILOGUE = 1, EVS_OPT_NORM_IN_GEMM = 2, EVS_OPT_GEMM_SUMS_SLOTS = 4 };
+
 typedef struct evs_config {
   int32_t vocab;
   int32_t d_model;
@@ -98,6 +110,7 @@ typedef struct evs_config {
   int32_t attn_chunk;     /* keys per split-KV chunk: 32, 64, 128 or 256 */
   float rope_base;        /* e.g. 10000 */
   float norm_eps;         /* e.g. 1e-6 */
+  int32_t options;        /* EVS_OPT_* bits, 0 = the default (fastest measured) kernels */
   const int32_t* layer_kind_host;   /* [n_layers] EVS_LAYER_* */
   const int32_t* layer_param_host;  /* [n_layers] */
 } evs_config;
@@ -247,7 +260,7 @@ int evs_verify_block(evs_state* s, const int32_t* tokens_dev, int32_t n,
  * states_host [nseq] (1 <= nseq <= 16): distinct states of one model and one
  * ctx_max, none with a pending verify; n_host [nseq]: block lengths, each in
  * [1, gamma_max+1], summing to at most 128 (EVS_BATCH_ROWS_MAX) on the bf16
- * path, at most 16 for float32 models and with EVS_FUSE=1
+ * path, at most 16 for float32 models and with EVS_OPT_NORM_IN_GEMM
  * (EVS_ERR_UNSUPPORTED between 17 and 128); tokens_dev: the blocks back to
  * back (sequence 0's n_host[0] tokens first); logits_dev [sum n][V] in the
  * same row order.  The weight GEMMs take all rows in one pass (16-row

@@ -56,5 +56,5 @@ def test_struct_layouts_match_header():
     import ctypes
     import hybrid_ssm_attention_gb300._abi as abi
     assert ctypes.sizeof(abi.evs_book) == 32
-    assert ctypes.sizeof(abi.evs_config) == 11 * 4 + 4 + 16   # 11 ints/floats, pad, 2 pointers
+    assert ctypes.sizeof(abi.evs_config) == 12 * 4 + 16   # 12 ints / floats, 2 pointers
     assert ctypes.sizeof(abi.evs_layer_weights) == 7 * 8

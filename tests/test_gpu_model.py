@@ -39,7 +39,7 @@ def _verify(evs, st, toks, V):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("slots", ["1", "0"])
-def test_small_bf16_stack_matches_oracle(slots, monkeypatch):
+def test_small_bf16_stack_matches_oracle(slots):
     # slots "1": GEMMs leave partial slots to the consuming kernels (default);
     # "0": every GEMM sums its own slots (cluster split-K out / down)
     import hybrid_ssm_attention_gb300 as evs
@@ -47,9 +47,7 @@ def test_small_bf16_stack_matches_oracle(slots, monkeypatch):
     from oracle.numerics import Arith
     shape = small_shape()
     W = synth.make_weights(shape, 11)
-    monkeypatch.setenv("EVS_SLOTS", slots)
-    m = evs.Model(shape, W)
-    monkeypatch.delenv("EVS_SLOTS")
+    m = evs.Model(shape, W, options=0 if slots == "1" else evs.EVS_OPT_GEMM_SUMS_SLOTS)
     st = evs.State(m, 512)
     om = OModel(shape, synth.weights_f32(W), Arith(np.float32, bf16_points=True))
     ost = om.new_state(512)
@@ -275,24 +273,16 @@ def wide_shape():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("which", ["small", "wide"])
-def test_fused_norm_and_activation_equal_separate_kernels_bitwise(which, monkeypatch):
+def test_fused_norm_and_activation_equal_separate_kernels_bitwise(which):
     # The three ways of running RMSNorm and SiLU-and-multiply agree bit for
     # bit: separate kernels (default), SwiGLU in the gate/up GEMM's epilogue
-    # (EVS_SWIGLU=1), and RMSNorm built inside the consuming GEMMs as well
-    # (EVS_FUSE=1)
+    # (EVS_OPT_SWIGLU_EPILOGUE), and RMSNorm built inside the consuming GEMMs
+    # as well (EVS_OPT_NORM_IN_GEMM)
     import hybrid_ssm_attention_gb300 as evs
     shape = small_shape() if which == "small" else wide_shape()
     W = synth.make_weights(shape, 21)
-
-    def model(**env):
-        for k, v in env.items():
-            monkeypatch.setenv(k, v)
-        m = evs.Model(shape, W)
-        for k in env:
-            monkeypatch.delenv(k)
-        return m
-
-    models = [model(), model(EVS_SWIGLU="1"), model(EVS_SWIGLU="1", EVS_FUSE="1")]
+    sw, nrm = evs.EVS_OPT_SWIGLU_EPILOGUE, evs.EVS_OPT_NORM_IN_GEMM
+    models = [evs.Model(shape, W), evs.Model(shape, W, options=sw), evs.Model(shape, W, options=sw | nrm)]
     states = [evs.State(m, 256) for m in models]
     nb = shape.n_block
     L = len(shape.layers)
@@ -493,7 +483,7 @@ def test_batches_beyond_16_rows_equal_separate_bitwise(which):
 
 
 @pytest.mark.gpu
-def test_batch_row_limits(monkeypatch):
+def test_batch_row_limits():
     # More than 128 rows is an argument error; 17..128 rows need the bf16
     # path without the fused RMSNorm converter (EVS_ERR_UNSUPPORTED otherwise,
     # and nothing is left pending on the states).
@@ -517,9 +507,7 @@ def test_batch_row_limits(monkeypatch):
     attempt(evs.Model(small, W), (small.n_block,) * 10, evs.EVS_ERR_ARG)  # 130 rows
     tiny = synth.tiny()
     attempt(evs.Model(tiny, synth.make_weights(tiny, 7)), (tiny.n_block,) * 4, evs.EVS_ERR_UNSUPPORTED)
-    monkeypatch.setenv("EVS_FUSE", "1")
-    fused = evs.Model(small, W)
-    monkeypatch.delenv("EVS_FUSE")
+    fused = evs.Model(small, W, options=evs.EVS_OPT_NORM_IN_GEMM)
     attempt(fused, (small.n_block, small.n_block), evs.EVS_ERR_UNSUPPORTED)
 
 
