@@ -12,7 +12,7 @@
 // follows from the committed lengths, read on the device) and runs first the
 // units whose keys are all committed, then those holding the block's keys.
 //
-// Roles of a CTA (288 threads):
+// Roles of a CTA (MW math warps + 2):
 //  * warp 8 streams K and V through a ring of 64-key stages (128 KB), each
 //    stage two tensor-map loads per 64 dimensions (128-byte swizzle), one
 //    mbarrier pair per stage, without draining between units.  Committed
@@ -27,11 +27,14 @@
 //      S = Q K^T (mma.sync m16n8k16, bf16), mask, online softmax in fp32
 //      in base 2, O += P V (P rounded to bf16 as the A operand, V by
 //      ldmatrix.trans);
-//    at the unit's end the eight warps merge in warp order into the split's
-//    partial (max, sum of exp, unnormalised output) and count it in the
-//    head's arrival counter; the CTA that brings the count to the head's
-//    number of splits folds the partials in ascending split order into the
-//    mixer output and resets the counter (no CTA waits for another).
+//    at the unit's end they deposit their (max, sum, O) in shared memory and
+//    go on with the next unit.
+//  * a merge warp folds each deposit in warp order into the split's partial
+//    (max, sum of exp, unnormalised output) while the math warps stream, and
+//    counts it in the head's arrival counter; the CTA that brings the count
+//    to the head's number of splits folds the partials, after its last unit,
+//    in ascending split order into the mixer output and resets the counter
+//    (no CTA waits for another).
 // Rows of a stage past the split's end are masked (K) or zeroed in shared
 // memory by the warp that owns them (V), so P = 0 never meets a non-finite
 // value.  Every mbarrier wait is bounded; on expiry the CTA raises
@@ -57,7 +60,11 @@ constexpr int AK_BOX = 64;    // elements of one 128-byte swizzled box row
 template <int DH, int MW>
 struct AkLayout {
   static constexpr int MATH_THREADS = MW * 32;
-  static constexpr int THREADS = MATH_THREADS + 32;        // + one producer warp
+  // long caches (MW = 8): a merge warp folds each unit's warp states while
+  // the math warps stream the next unit; short caches (a unit or two per
+  // CTA, the merge on the critical path): the math warps merge themselves
+  static constexpr bool MERGE_WARP = MW == 8;
+  static constexpr int THREADS = MATH_THREADS + (MERGE_WARP ? 64 : 32);  // + producer (+ merge) warp
   static constexpr int GROUPS = MW / AK_GROUP_WARPS;
   static constexpr int HALVES = DH / AK_BOX;               // boxes per key row
   static constexpr uint32_t BOX_B = AK_STAGE * 128;        // one box: 64 rows x 128 bytes
@@ -71,12 +78,25 @@ struct AkLayout {
   static constexpr uint32_t ML_B = 3 * MW * 16 * 4;
   static constexpr uint32_t OW_B = MW * 16 * QP * 4;
   static constexpr uint32_t BAR_B = (2 * NST + 1) * 8;
-  static constexpr size_t SMEM = 1024 + RING_B + Q_B + ML_B + OW_B + BAR_B + 16;
+  // then the fold list (host-sized: at most one entry per unit of a CTA)
+  static constexpr uint32_t FOLD_OFF = RING_B + Q_B + ML_B + OW_B + BAR_B + 16;
+  static constexpr size_t SMEM = 1024 + FOLD_OFF;  // without the fold list
 };
 
 template <int NTHR>
 __device__ __forceinline__ void math_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NTHR) : "memory");
+}
+// Hand-offs between the math warps and the merge warp (NTHR = both): id 2
+// "the merge area is free", id 3 "a unit's state is deposited", id 4 "every
+// unit is merged and counted"; one side arrives, the other waits.
+template <int ID, int NTHR>
+__device__ __forceinline__ void hand_wait() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(NTHR) : "memory");
+}
+template <int ID, int NTHR>
+__device__ __forceinline__ void hand_arrive() {
+  asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(NTHR) : "memory");
 }
 // math_sync that also returns whether v held on any math thread (the same
 // answer on all of them, so branches on it stay uniform)
@@ -246,8 +266,9 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
                     const __grid_constant__ SeqPtrs<const CUtensorMap*> vms,
                     const __grid_constant__ SeqPtrs<evs_book*> books, int span, int nsplit_max,
                     const __grid_constant__ SeqPtrs<float*> part_os, const __grid_constant__ SeqPtrs<float*> part_mls,
-                    const __grid_constant__ SeqPtrs<int*> arrivals, bf16* __restrict__ gout) {
+                    const __grid_constant__ SeqPtrs<int*> arrivals, bf16* __restrict__ gout, int fold_cap) {
   using LY = AkLayout<DH, MW>;
+  static_assert(FUSED == LY::MERGE_WARP, "the fused kernel runs with the merge warp");
   constexpr int NST = LY::NST;
   constexpr int QP = LY::QP;
   constexpr int MT = LY::MATH_THREADS;
@@ -262,8 +283,9 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
   float* ow = reinterpret_cast<float*>(sm + LY::RING_B + LY::Q_B + LY::ML_B);  // [MW][16][QP] O
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::RING_B + LY::Q_B + LY::ML_B + LY::OW_B);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NST + 1);
+  int* fold_list = reinterpret_cast<int*>(sm + LY::FOLD_OFF);  // [fold_cap] (sequence << 16 | head)
   __shared__ long long s_pos[MAX_SEQ], s_tot[MAX_SEQ];
-  __shared__ int s_act[MAX_SEQ], s_pref[MAX_SEQ + 1], s_last;
+  __shared__ int s_act[MAX_SEQ], s_pref[MAX_SEQ + 1], s_nfold;
   const uint32_t ring = smem_u32(sm);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -279,6 +301,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     }
     mbar_init(app, MT);
     *abort_flag = 0;
+    s_nfold = 0;
     // committed lengths are fixed for the whole verify (commit runs after it)
     int acc = 0;
     for (int q = 0; q < sr.nseq; ++q) {
@@ -328,6 +351,76 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       if ((int)decode(u).fresh == pass) return;
     }
   };
+  constexpr int HT = MT + 32;  // math warps + merge warp
+  if (LY::MERGE_WARP && warp == MW + 1) {
+    // ---------------- merge warp: each unit's deposit -> the split's partial
+    int pass = 0, u = ub - 1;
+    advance(pass, u);
+    if (u < ue) hand_arrive<2, HT>();  // the merge area starts free
+    while (u < ue) {
+      const AkUnit x = decode(u);
+      const int n = sr.row0[x.sq + 1] - sr.row0[x.sq];
+      int npass = pass, nu = u;
+      advance(npass, nu);
+      hand_wait<3, HT>();
+      // per (row, warp): the warp's weight exp2(m_v - M), M the row's merged
+      // max (0 for a warp that saw no key of the row)
+      for (int q = lane; q < 16 * MW; q += 32) {
+        const int t = q / MW, v = q % MW;
+        float M = -INFINITY;
+#pragma unroll
+        for (int vv = 0; vv < MW; ++vv) M = fmaxf(M, mw[vv * 16 + t]);
+        const float mv = mw[v * 16 + t];
+        fw[v * 16 + t] = mv == -INFINITY ? 0.f : exp2f(mv - M);
+      }
+      __syncwarp();
+      const bool good = !*abort_flag;
+      float* part_o = part_os.p[x.sq];
+      float* part_ml = part_mls.p[x.sq];
+      if (good) {
+        for (int e = lane; e < n * DH; e += 32) {
+          const int t = e / DH, dd = e % DH;
+          float O = 0.f;
+#pragma unroll
+          for (int v = 0; v < MW; ++v) O = fmaf(ow[((size_t)v * 16 + t) * QP + dd], fw[v * 16 + t], O);
+          const size_t base = ((size_t)x.h * nsplit_max + x.sp) * NTOK + t;
+          part_o[base * DH + dd] = O;
+          if (dd == 0) {
+            float M = -INFINITY, L = 0.f;
+#pragma unroll
+            for (int v = 0; v < MW; ++v) {
+              M = fmaxf(M, mw[v * 16 + t]);
+              L = fmaf(lw[v * 16 + t], fw[v * 16 + t], L);
+            }
+            part_ml[base * 2] = M * AK_LN2;
+            part_ml[base * 2 + 1] = L;
+          }
+        }
+      }
+      __syncwarp();
+      if (nu < ue) hand_arrive<2, HT>();  // the next unit may deposit
+      if (FUSED && good) {
+        // count the split; the last one of the head is folded after this
+        // CTA's last unit
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          int* cnt = arrivals.p[x.sq] + x.h;
+          if (atomicAdd(cnt, 1) == s_act[x.sq] - 1) {
+            __threadfence();  // the other splits' partials are read after this
+            *cnt = 0;  // every split of the head has counted: ready for the next pass
+            if (s_nfold < fold_cap) fold_list[s_nfold++] = (x.sq << 16) | x.h;
+            else *abort_flag = 1;  // cannot happen with the host's capacity
+          }
+        }
+      }
+      pass = npass;
+      u = nu;
+    }
+    hand_arrive<4, HT>();
+    return;
+  }
+
   if (warp == MW) {
     // ---------------- producer: one thread streams the CTA's stages
     if (lane != 0) return;
@@ -575,12 +668,14 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       if (ok && lane == 0) mbar_arrive(empty(s));
     }
     gi += nst;
-    // row sums over the quad, then the MW warps merge in warp order
+    // row sums over the quad, then (max, sum, O) into the merge area for the
+    // merge warp
 #pragma unroll
     for (int xo = 1; xo < 4; xo <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, xo);
       l1 += __shfl_xor_sync(0xffffffffu, l1, xo);
     }
+    if (LY::MERGE_WARP) hand_wait<2, HT>();
     if (t4 == 0) {
       mw[warp * 16 + g] = m0;
       mw[warp * 16 + g + 8] = m1;
@@ -593,9 +688,12 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       *reinterpret_cast<float2*>(q0) = make_float2(o[jj][0], o[jj][1]);
       *reinterpret_cast<float2*>(q0 + 8 * QP) = make_float2(o[jj][2], o[jj][3]);
     }
+    if (LY::MERGE_WARP) {
+      hand_arrive<3, HT>();
+      continue;
+    }
+    // without a merge warp: the math warps merge the unit in warp order
     math_sync<MT>();
-    // per (row, warp): the warp's weight exp2(m_v - M), M the row's merged
-    // max (0 for a warp that saw no key of the row)
     if (ctid < 16 * MW) {
       const int t = ctid / MW, v = ctid % MW;
       float M = -INFINITY;
@@ -627,91 +725,87 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
         }
       }
     }
-    // count the split; the last one of the head folds them all (skipped
-    // by every math thread once any wait of the CTA gave up)
-    if (FUSED && !math_any<MT>(!ok)) {
-      float* part_o = part_os.p[x.sq];
-      float* part_ml = part_mls.p[x.sq];
-      __threadfence();
-      math_sync<MT>();
-      if (ctid == 0) {
-        int* cnt = arrivals.p[x.sq] + x.h;
-        const bool last = atomicAdd(cnt, 1) == s_act[x.sq] - 1;
-        if (last) *cnt = 0;  // every split of the head has counted: ready for the next pass
-        s_last = last;
+    math_sync<MT>();  // the merge area is rewritten by the next unit
+  }
+  if (!LY::MERGE_WARP) {
+    if (!ok && ctid == 0)
+      for (int q = 0; q < sr.nseq; ++q) set_status(books.p[q], EVS_DEV_TIMEOUT);
+    return;
+  }
+  // every unit merged and counted; the heads whose last split finished here
+  // are folded: per query row t the splits holding keys <= its position,
+  // their weights exp(m_c - M) and l_c (the merge area is free: [16][64]
+  // each, then the row sums [16]), all loads of a phase in flight
+  hand_wait<4, HT>();
+  for (int f = 0; f < s_nfold; ++f) {
+    const int sq = fold_list[f] >> 16, h = fold_list[f] & 0xffff;
+    const int n = sr.row0[sq + 1] - sr.row0[sq], r0 = sr.row0[sq];
+    const long long pos = s_pos[sq];
+    __threadfence();
+    float* wt = ow;
+    float* lc = ow + 16 * ATTN_SPLITS_MAX;
+    float* lt = lc + 16 * ATTN_SPLITS_MAX;
+    const float* pml = part_mls.p[sq] + ((size_t)h * nsplit_max) * NTOK * 2;
+    const float* po = part_os.p[sq] + ((size_t)h * nsplit_max) * NTOK * DH;
+    for (int tb = 0; tb < 16; tb += MT / 16) {
+      const int t = tb + (ctid >> 4), l16 = ctid & 15;  // 16 threads per row, every lane shuffles
+      const int nc = t < n ? (int)(min(pos + t, ctx_max - 1) / span) + 1 : 0;
+      float2 ml[ATTN_SPLITS_MAX / 16];
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < ATTN_SPLITS_MAX / 16; ++k) {
+        const int c = l16 + 16 * k;
+        ml[k] = c < nc ? __ldcg(reinterpret_cast<const float2*>(pml + ((size_t)c * NTOK + t) * 2))
+                       : make_float2(-INFINITY, 0.f);
+        M = fmaxf(M, ml[k].x);
       }
-      math_sync<MT>();
-      if (s_last) {
-        __threadfence();
-        // per query row t: the splits holding keys <= its position, their
-        // weights exp(m_c - M) and l_c (the merge area is free: [16][64]
-        // each, then the row sums [16]), all loads of a phase in flight
-        float* wt = ow;
-        float* lc = ow + 16 * ATTN_SPLITS_MAX;
-        float* lt = lc + 16 * ATTN_SPLITS_MAX;
-        const float* pml = part_ml + ((size_t)x.h * nsplit_max) * NTOK * 2;
-        const float* po = part_o + ((size_t)x.h * nsplit_max) * NTOK * DH;
-        for (int tb = 0; tb < 16; tb += MT / 16) {
-          const int t = tb + (ctid >> 4), l16 = ctid & 15;  // 16 threads per row, every lane shuffles
-          const int nc = t < n ? (int)(min(pos + t, ctx_max - 1) / span) + 1 : 0;
-          float2 ml[ATTN_SPLITS_MAX / 16];
-          float M = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < ATTN_SPLITS_MAX / 16; ++k) {
-            const int c = l16 + 16 * k;
-            ml[k] = c < nc ? __ldcg(reinterpret_cast<const float2*>(pml + ((size_t)c * NTOK + t) * 2))
-                           : make_float2(-INFINITY, 0.f);
-            M = fmaxf(M, ml[k].x);
-          }
+      for (int xo = 8; xo > 0; xo >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, xo));
 #pragma unroll
-          for (int xo = 8; xo > 0; xo >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, xo));
-#pragma unroll
-          for (int k = 0; k < ATTN_SPLITS_MAX / 16; ++k) {
-            const int c = l16 + 16 * k;
-            if (c < nc) {
-              wt[t * ATTN_SPLITS_MAX + c] = ml[k].x == -INFINITY ? 0.f : expf(ml[k].x - M);
-              lc[t * ATTN_SPLITS_MAX + c] = ml[k].y;
-            }
-          }
-        }
-        math_sync<MT>();
-        if (ctid < n) {  // the sum of l_c weights in split order
-          const int t = ctid;
-          const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
-          float l = 0.f;
-          for (int c = 0; c < nc; ++c) {
-            const float w = wt[t * ATTN_SPLITS_MAX + c];
-            if (w != 0.f) l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
-          }
-          lt[t] = l;
-        }
-        math_sync<MT>();
-        // outputs four dims per thread, each summed over the splits in order
-        for (int e = ctid; e < n * (DH / 4); e += MT) {
-          const int t = e / (DH / 4), d4 = 4 * (e % (DH / 4));
-          const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
-          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-          for (int c = 0; c < nc; ++c) {
-            const float w = wt[t * ATTN_SPLITS_MAX + c];
-            const float4 oc = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4));
-            if (w != 0.f) {
-              o.x = fmaf(oc.x, w, o.x);
-              o.y = fmaf(oc.y, w, o.y);
-              o.z = fmaf(oc.z, w, o.z);
-              o.w = fmaf(oc.w, w, o.w);
-            }
-          }
-          const float l = lt[t];
-          __nv_bfloat162 lo = __floats2bfloat162_rn(o.x / l, o.y / l), hi = __floats2bfloat162_rn(o.z / l, o.w / l);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(gout + (size_t)(r0 + t) * H * DH + x.h * DH + d4) = pk;
+      for (int k = 0; k < ATTN_SPLITS_MAX / 16; ++k) {
+        const int c = l16 + 16 * k;
+        if (c < nc) {
+          wt[t * ATTN_SPLITS_MAX + c] = ml[k].x == -INFINITY ? 0.f : expf(ml[k].x - M);
+          lc[t * ATTN_SPLITS_MAX + c] = ml[k].y;
         }
       }
     }
-    math_sync<MT>();  // the merge area is rewritten by the next unit
+    math_sync<MT>();
+    if (ctid < n) {  // the sum of l_c weights in split order
+      const int t = ctid;
+      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
+      float l = 0.f;
+      for (int c = 0; c < nc; ++c) {
+        const float w = wt[t * ATTN_SPLITS_MAX + c];
+        if (w != 0.f) l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
+      }
+      lt[t] = l;
+    }
+    math_sync<MT>();
+    // outputs four dims per thread, each summed over the splits in order
+    for (int e = ctid; e < n * (DH / 4); e += MT) {
+      const int t = e / (DH / 4), d4 = 4 * (e % (DH / 4));
+      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+      for (int c = 0; c < nc; ++c) {
+        const float w = wt[t * ATTN_SPLITS_MAX + c];
+        const float4 oc = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4));
+        if (w != 0.f) {
+          o.x = fmaf(oc.x, w, o.x);
+          o.y = fmaf(oc.y, w, o.y);
+          o.z = fmaf(oc.z, w, o.z);
+          o.w = fmaf(oc.w, w, o.w);
+        }
+      }
+      const float l = lt[t];
+      __nv_bfloat162 lo = __floats2bfloat162_rn(o.x / l, o.y / l), hi = __floats2bfloat162_rn(o.z / l, o.w / l);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(gout + (size_t)(r0 + t) * H * DH + h * DH + d4) = pk;
+    }
+    math_sync<MT>();  // the area is rewritten by the next fold
   }
   if (!ok && ctid == 0)
     for (int q = 0; q < sr.nseq; ++q) set_status(books.p[q], EVS_DEV_TIMEOUT);
@@ -722,15 +816,18 @@ cudaError_t attn_tma_launch_t(const LaunchCtx& L, Src s, int H, const SeqRows& s
                               const AttnSeq& as, const AttnBufs& B, void* g) {
   using LY = AkLayout<DH, MW>;
   auto k = attn_tma_kernel<Src, DH, MW, FUSED>;
-  const size_t smem = LY::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long units = (long long)sr.nseq * H * B.nsplit_max;
   const int grid = (int)std::max(1LL, std::min<long long>(units, (long long)sms * (MW == 8 ? 1 : 2)));
+  // a CTA folds at most the heads of its own units
+  const int fold_cap = (int)((units + grid - 1) / grid) + 1;
+  const size_t smem = LY::SMEM + sizeof(int) * fold_cap;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   SeqPtrs<bf16*> kc{}, vc{};
   SeqPtrs<const CUtensorMap*> km{}, vm{};
   for (int b = 0; b < sr.nseq; ++b) {
@@ -741,7 +838,7 @@ cudaError_t attn_tma_launch_t(const LaunchCtx& L, Src s, int H, const SeqRows& s
   }
   return launch(L, k, dim3(grid), dim3(LY::THREADS), smem, s, H, ctx_max, (const uint64_t*)B.turn_fx,
                 (const float*)B.qbuf, sr, kc, vc, km,
-                vm, as.book, B.span, B.nsplit_max, as.part_o, as.part_ml, as.arrivals, (bf16*)g);
+                vm, as.book, B.span, B.nsplit_max, as.part_o, as.part_ml, as.arrivals, (bf16*)g, fold_cap);
 }
 
 template <typename Src>
