@@ -588,9 +588,8 @@ def drafter_rounds(evs, torch, dev, seed, prompt_len, rounds=16, warm=4):
     d = torch.zeros(gamma, dtype=torch.int32, device=dev)
     q = torch.empty((gamma, V), dtype=torch.float32, device=dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(rounds)]
-    torch.cuda.synchronize()
-    for r in range(warm + rounds):
-        e = ev[r - warm] if r >= warm else None
+
+    def one(r, e):
         if e:
             e[0].record()
         evs.evs_verify_block(st, toks[r], gamma, lg)
@@ -600,6 +599,16 @@ def drafter_rounds(evs, torch, dev, seed, prompt_len, rounds=16, warm=4):
         evs.evs_markov_draft(lg, M, V, toks[r, :1], U[r], gamma, 1.0, 4, evs.EVS_SAMPLE, d, q)
         if e:
             e[2].record()
+
+    for r in range(warm):
+        one(r, None)
+    torch.cuda.synchronize()
+    # the device sleeps while the host queues every timed round behind it,
+    # so the events time the device, not the Python calls between them
+    torch.cuda._sleep(100_000_000)
+    for r in range(rounds):
+        one(warm + r, ev[r])
+    queued_ahead = not ev[-1][2].query()
     torch.cuda.synchronize()
     trunk = sum(e[0].elapsed_time(e[1]) for e in ev) / rounds
     head = sum(e[1].elapsed_time(e[2]) for e in ev) / rounds
@@ -608,9 +617,12 @@ def drafter_rounds(evs, torch, dev, seed, prompt_len, rounds=16, warm=4):
     st.close()
     m.close()
     return {"us_per_round": 1e3 * total, "trunk_us": 1e3 * trunk, "markov_head_us": 1e3 * head, "status_ok": ok,
+            "queued_ahead": queued_ahead,
             "note": "timing stand-in, random init: trunk = one attention layer at d_model 1024 (8x128 heads, MLP "
                     "4096, vocab 512) scoring 12 slots in one verify pass; Markov head = the evs_markov_draft "
-                    "kernel (12 sequential top-4 draws over trunk row + V x V Markov row)"}
+                    "kernel (12 sequential top-4 draws over trunk row + V x V Markov row); the rounds are queued "
+                    "behind a device sleep, so the events time the device (queued_ahead: the host had queued "
+                    "the last round before the device reached it)"}
 
 
 def long_context_rounds(evs, torch, model, shape, P, seed, dev, peak, rounds=6, warm=2):

@@ -573,6 +573,356 @@ __global__ void __launch_bounds__(256) markov_draft_kernel(const float* trunk, c
   }
 }
 
+// The same draft chain for 0 < top_k <= 8 and V <= 8192, with the support
+// found by merging sorted lists instead of a radix select.  Order: larger
+// logit first, lower index on ties (the oracle's stable order; a NaN never
+// enters).  Each of the 256 threads keeps the best KM of its strided entries
+// j = tid + 256 e in registers; a butterfly over the warp merges the lists of
+// lane pairs (the better half of a bitonic merge), the 8 warp lists meet in
+// shared memory behind one barrier and every thread merges them itself.  So
+// every thread holds the support, sorted: its softmax, the integer ladder in
+// index order and the next draft are computed by each thread from registers,
+// and the Markov row of that draft is loaded without a further barrier.
+constexpr int MK_THREADS = 256, MK_WARPS = MK_THREADS / 32;
+
+__device__ __forceinline__ bool mk_better(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// v/ix (sorted, best first) <- the best KM of v/ix and ov/oi (both sorted)
+template <int KM>
+__device__ __forceinline__ void mk_merge(float (&v)[KM], int (&ix)[KM], const float (&ov)[KM], const int (&oi)[KM]) {
+#pragma unroll
+  for (int r = 0; r < KM; ++r)
+    if (mk_better(ov[KM - 1 - r], oi[KM - 1 - r], v[r], ix[r])) {
+      v[r] = ov[KM - 1 - r];
+      ix[r] = oi[KM - 1 - r];
+    }
+  // v is now bitonic (worse towards the middle): half-cleaners sort it
+#pragma unroll
+  for (int h = KM / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int r = 0; r < KM; ++r)
+      if ((r & h) == 0 && mk_better(v[r + h], ix[r + h], v[r], ix[r])) {
+        const float tv = v[r];
+        const int ti = ix[r];
+        v[r] = v[r + h];
+        ix[r] = ix[r + h];
+        v[r + h] = tv;
+        ix[r + h] = ti;
+      }
+}
+
+template <int KM, int EM>
+__global__ void __launch_bounds__(MK_THREADS) markov_draft_topk_kernel(
+    const float* __restrict__ trunk, const float* __restrict__ M, int V, const int32_t* prev_dev,
+    const float* __restrict__ u, int gamma, float T, int k, int mode, int32_t* drafts, float* q) {
+  __shared__ float lv[2][MK_WARPS][KM];
+  __shared__ int li[2][MK_WARPS][KM];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int NONE = 0x7fffffff;
+  pdl_trigger();
+  pdl_wait();
+  int prev = prev_dev[0];
+  if (prev < 0 || prev >= V) prev = 0;
+  float tr[EM];
+#pragma unroll
+  for (int e = 0; e < EM; ++e) {
+    const int j = tid + MK_THREADS * e;
+    tr[e] = (j < V && gamma > 0) ? trunk[j] : 0.f;
+  }
+  for (int i = 0; i < gamma; ++i) {
+    const float* mr = M + (size_t)prev * V;
+    const float* tn = trunk + (size_t)(i + 1) * V;
+    float l[EM], tnx[EM];
+#pragma unroll
+    for (int e = 0; e < EM; ++e) {
+      const int j = tid + MK_THREADS * e;
+      l[e] = j < V ? __fadd_rn(tr[e], mr[j]) : 0.f;
+      tnx[e] = (j < V && i + 1 < gamma) ? tn[j] : 0.f;
+    }
+    float v[KM];
+    int ix[KM];
+#pragma unroll
+    for (int r = 0; r < KM; ++r) {
+      v[r] = -INFINITY;
+      ix[r] = NONE;
+    }
+#pragma unroll
+    for (int e = 0; e < EM; ++e) {
+      float x = l[e];
+      int j = tid + MK_THREADS * e;
+      if (j < V && mk_better(x, j, v[KM - 1], ix[KM - 1])) {
+#pragma unroll
+        for (int r = 0; r < KM; ++r)
+          if (mk_better(x, j, v[r], ix[r])) {
+            const float tv = v[r];
+            const int ti = ix[r];
+            v[r] = x;
+            ix[r] = j;
+            x = tv;
+            j = ti;
+          }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov[KM];
+      int oi[KM];
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        ov[r] = __shfl_xor_sync(0xffffffffu, v[r], o);
+        oi[r] = __shfl_xor_sync(0xffffffffu, ix[r], o);
+      }
+      mk_merge<KM>(v, ix, ov, oi);
+    }
+    const int b = i & 1;  // the barrier of slot i-1 ended every read of buffer b from slot i-2
+    if (lane < KM) {
+#pragma unroll
+      for (int r = 0; r < KM; ++r)
+        if (r == lane) {
+          lv[b][warp][r] = v[r];
+          li[b][warp][r] = ix[r];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < MK_WARPS; ++w) {
+      if (w == warp) continue;
+      float ov[KM];
+      int oi[KM];
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        ov[r] = lv[b][w][r];
+        oi[r] = li[b][w][r];
+      }
+      mk_merge<KM>(v, ix, ov, oi);
+    }
+    // the support: the first k entries; softmax of (l - max) / T over it
+    const float mx = v[0];
+    float w[KM], sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < KM; ++r) {
+      w[r] = (r < k && ix[r] != NONE) ? expf((v[r] - mx) / T) : 0.f;
+      sum += w[r];
+    }
+#pragma unroll
+    for (int r = 0; r < KM; ++r) w[r] = w[r] / sum;
+    int d = -1;
+    if (mode == EVS_SAMPLE) {
+      unsigned int W[KM];
+      unsigned long long S = 0;
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        W[r] = ladder_weight(w[r]);
+        S += W[r];
+      }
+      const unsigned long long U = min((unsigned long long)(unsigned int)(u[i] * 16777216.0f), 16777215ull);
+      const unsigned long long thr = (U * S) >> 24;
+      // the ladder in index order: entry r holds [pre_r, pre_r + W_r)
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        unsigned long long pre = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < KM; ++s2)
+          if (ix[s2] < ix[r]) pre += W[s2];
+        if (W[r] > 0 && pre <= thr && thr < pre + W[r]) d = ix[r];
+      }
+    }
+    if (d < 0) d = ix[0] == NONE ? 0 : ix[0];  // greedy, or no integer mass: the argmax
+#pragma unroll
+    for (int e = 0; e < EM; ++e) {
+      const int j = tid + MK_THREADS * e;
+      if (j < V) {
+        float qv = 0.f;
+#pragma unroll
+        for (int r = 0; r < KM; ++r)
+          if (ix[r] == j) qv = w[r];
+        q[(size_t)i * V + j] = qv;
+      }
+    }
+    if (tid == 0) drafts[i] = d;
+    prev = d;
+#pragma unroll
+    for (int e = 0; e < EM; ++e) tr[e] = tnx[e];
+  }
+}
+
+// The top_k <= 8 chain by one warp when V <= 1024 and V % 4 == 0 (rows of
+// whole float4s): lane l owns the NPL contiguous entries from l * NPL.  An
+// entry's order is its orderable 32-bit key (NaN -> 0, never chosen), ties
+// to the lower index; a support round is one warp max of the lanes' best
+// keys, a ballot for the lowest lane holding it (lowest lane = lowest
+// index), and a rescan by that lane alone.  The support then sits in every
+// lane's registers, and so do its softmax, the ladder draw and the next
+// draft: the next Markov row is requested before this slot's q is stored
+// (greedy: right after the first round, the draft being the argmax).
+__device__ __forceinline__ unsigned int mk_key(float x) { return x != x ? 0u : ord_key(x); }
+
+__device__ __forceinline__ float mk_val(unsigned int key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+template <int NPL>
+__device__ __forceinline__ void mk_load_row(float (&x)[NPL], const float* __restrict__ row, int j0, int V) {
+#pragma unroll
+  for (int c = 0; c < NPL / 4; ++c) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j0 + 4 * c < V) f = *reinterpret_cast<const float4*>(row + j0 + 4 * c);
+    x[4 * c] = f.x;
+    x[4 * c + 1] = f.y;
+    x[4 * c + 2] = f.z;
+    x[4 * c + 3] = f.w;
+  }
+}
+
+// this lane's best key and the lowest entry holding it (key 0: none)
+template <int NPL>
+__device__ __forceinline__ void mk_lane_best(const unsigned int (&key)[NPL], unsigned int& bk, int& be) {
+  unsigned int t[NPL];
+#pragma unroll
+  for (int e = 0; e < NPL; ++e) t[e] = key[e];
+#pragma unroll
+  for (int h = NPL / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int e = 0; e < h; ++e) t[e] = max(t[e], t[e + h]);
+  bk = t[0];
+  unsigned int m = 0;
+#pragma unroll
+  for (int e = 0; e < NPL; ++e) m |= (key[e] == bk ? 1u : 0u) << e;
+  be = __ffs(m) - 1;
+}
+
+template <int KM, int NPL>
+__global__ void __launch_bounds__(32) markov_draft_warp_kernel(
+    const float* __restrict__ trunk, const float* __restrict__ M, int V, const int32_t* prev_dev,
+    const float* __restrict__ u, int gamma, float T, int k, int mode, int32_t* drafts, float* q) {
+  constexpr int NONE = 0x7fffffff;
+  const int lane = threadIdx.x, j0 = lane * NPL;
+  const int nown = max(0, min(NPL, V - j0));
+  pdl_trigger();
+  pdl_wait();
+  int prev = prev_dev[0];
+  if (prev < 0 || prev >= V) prev = 0;
+  float tr[NPL], x[NPL];
+  if (gamma > 0) {
+    mk_load_row<NPL>(tr, trunk, j0, V);
+    mk_load_row<NPL>(x, M + (size_t)prev * V, j0, V);
+  }
+  for (int i = 0; i < gamma; ++i) {
+    const bool more = i + 1 < gamma;
+    float tn[NPL];
+    if (more) mk_load_row<NPL>(tn, trunk + (size_t)(i + 1) * V, j0, V);
+    const float ui = u[i];
+    unsigned int key[NPL];
+#pragma unroll
+    for (int e = 0; e < NPL; ++e) key[e] = e < nown ? mk_key(__fadd_rn(tr[e], x[e])) : 0u;
+    unsigned int bk;
+    int be;
+    mk_lane_best<NPL>(key, bk, be);
+    unsigned int sk[KM];
+    int si[KM];
+    int d = -1;
+#pragma unroll
+    for (int r = 0; r < KM; ++r) {
+      sk[r] = 0u;
+      si[r] = NONE;
+      if (r < k) {
+        const unsigned int mk = __reduce_max_sync(0xffffffffu, bk);
+        if (mk != 0u) {
+          const int wl = __ffs(__ballot_sync(0xffffffffu, bk == mk)) - 1;
+          sk[r] = mk;
+          si[r] = wl * NPL + __shfl_sync(0xffffffffu, be, wl);
+          if (r + 1 < k) {
+            if (lane == wl) {
+#pragma unroll
+              for (int e = 0; e < NPL; ++e)
+                if (e == be) key[e] = 0u;
+              mk_lane_best<NPL>(key, bk, be);
+            }
+          }
+        }
+      }
+      if (r == 0 && mode != EVS_SAMPLE) {
+        d = si[0] == NONE ? 0 : si[0];
+        if (more) mk_load_row<NPL>(x, M + (size_t)d * V, j0, V);
+      }
+    }
+    float w[KM], sum = 0.f;
+    const float mx = mk_val(sk[0]);
+#pragma unroll
+    for (int r = 0; r < KM; ++r) {
+      w[r] = sk[r] != 0u ? expf((mk_val(sk[r]) - mx) / T) : 0.f;
+      sum += w[r];
+    }
+#pragma unroll
+    for (int r = 0; r < KM; ++r) w[r] = w[r] / sum;
+    if (mode == EVS_SAMPLE) {
+      unsigned int W[KM];
+      unsigned long long S = 0;
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        W[r] = ladder_weight(w[r]);
+        S += W[r];
+      }
+      const unsigned long long U = min((unsigned long long)(unsigned int)(ui * 16777216.0f), 16777215ull);
+      const unsigned long long thr = (U * S) >> 24;
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        unsigned long long pre = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < KM; ++s2)
+          if (si[s2] < si[r]) pre += W[s2];
+        if (W[r] > 0 && pre <= thr && thr < pre + W[r]) d = si[r];
+      }
+      if (d < 0) d = si[0] == NONE ? 0 : si[0];  // no integer mass: the argmax
+      if (more) mk_load_row<NPL>(x, M + (size_t)d * V, j0, V);
+    }
+    // q: this lane's entries zero, then its support entries (same thread,
+    // so the later store wins)
+    float* qr = q + (size_t)i * V;
+#pragma unroll
+    for (int c = 0; c < NPL / 4; ++c)
+      if (j0 + 4 * c < V) *reinterpret_cast<float4*>(qr + j0 + 4 * c) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < KM; ++r)
+      if (si[r] != NONE && (unsigned int)(si[r] - j0) < (unsigned int)NPL) qr[si[r]] = w[r];
+    if (lane == 0) drafts[i] = d;
+    if (more) {
+#pragma unroll
+      for (int e = 0; e < NPL; ++e) tr[e] = tn[e];
+    }
+  }
+}
+
+template <int KM, int NPL>
+static cudaError_t launch_markov_warp(const LaunchCtx& L, const float* trunk, const float* M, int V,
+                                      const int32_t* prev, const float* u, int gamma, float T, int k, int mode,
+                                      int32_t* drafts, float* q) {
+  return launch(L, markov_draft_warp_kernel<KM, NPL>, dim3(1), dim3(32), 0, trunk, M, V, prev, u, gamma, T, k, mode,
+                drafts, q);
+}
+
+template <int KM>
+static cudaError_t launch_markov_topk(const LaunchCtx& L, const float* trunk, const float* M, int V, const int32_t* prev,
+                                      const float* u, int gamma, float T, int k, int mode, int32_t* drafts, float* q) {
+  const bool al16 = ((reinterpret_cast<uintptr_t>(trunk) | reinterpret_cast<uintptr_t>(M) |
+                      reinterpret_cast<uintptr_t>(q)) & 15) == 0;
+  if (V % 4 == 0 && al16) {
+    if (V <= 128) return launch_markov_warp<KM, 4>(L, trunk, M, V, prev, u, gamma, T, k, mode, drafts, q);
+    if (V <= 512) return launch_markov_warp<KM, 16>(L, trunk, M, V, prev, u, gamma, T, k, mode, drafts, q);
+    if (V <= 1024) return launch_markov_warp<KM, 32>(L, trunk, M, V, prev, u, gamma, T, k, mode, drafts, q);
+  }
+  if (V <= 2 * MK_THREADS)
+    return launch(L, markov_draft_topk_kernel<KM, 2>, dim3(1), dim3(MK_THREADS), 0, trunk, M, V, prev, u, gamma, T,
+                  k, mode, drafts, q);
+  if (V <= 8 * MK_THREADS)
+    return launch(L, markov_draft_topk_kernel<KM, 8>, dim3(1), dim3(MK_THREADS), 0, trunk, M, V, prev, u, gamma, T,
+                  k, mode, drafts, q);
+  return launch(L, markov_draft_topk_kernel<KM, 32>, dim3(1), dim3(MK_THREADS), 0, trunk, M, V, prev, u, gamma, T, k,
+                mode, drafts, q);
+}
+
 // Commit: keep = *acc_dev + 1 when acc_dev is given, else keep_host.
 // n_explicit > 0 replaces book->pending_n (bare-book operator use).
 __device__ void commit_one(evs_book* book, int keep, int n_explicit) {
@@ -697,6 +1047,10 @@ cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float*
 
 cudaError_t launch_markov_draft(const LaunchCtx& L, const float* trunk, const float* M, int V, const int32_t* prev,
                                 const float* u, int gamma, float T, int top_k, int mode, int32_t* drafts, float* q) {
+  if (top_k > 0 && top_k < V && top_k <= 8 && V <= 32 * MK_THREADS) {
+    if (top_k <= 4) return launch_markov_topk<4>(L, trunk, M, V, prev, u, gamma, T, top_k, mode, drafts, q);
+    return launch_markov_topk<8>(L, trunk, M, V, prev, u, gamma, T, top_k, mode, drafts, q);
+  }
   const size_t smem = sizeof(float) * 3 * V;
   if (smem > 48 * 1024) {
     if (smem > 200 * 1024) return cudaErrorInvalidValue;

@@ -4,8 +4,11 @@ Each slot's q equals the oracle's top-k softmax of the trunk row plus the
 Markov row of the previous token (support exact, values within 2e-6); each
 draft equals the oracle's decision on that same q and uniform (integer-ladder
 sample, bit-exact) or, greedy, the oracle's argmax; the greedy chain equals
-the oracle's whole chain.  Vocab 16, 512 and 8192; top_k 0, 4 and V - 1;
-T 1 and 0.7; a one-hot Markov chain; a pending token outside the vocabulary.
+the oracle's whole chain.  Vocab 16, 510, 512, 1000, 2000 and 8192; top_k
+0, 1, 4, 7 and V - 1 (top_k 1 .. 8: the one-warp kernel for V <= 1024 and
+V % 4 == 0, the merged-list kernel otherwise; other top_k: the radix
+select); T 1, 0.8 and 0.7; integer logits whose ties straddle the top-k cut;
+a one-hot Markov chain; a pending token outside the vocabulary.
 The drafter trunk stand-in (one attention layer at d_model 1024) scores the
 gamma slots in one verify pass whose rows feed the kernel.
 """
@@ -29,7 +32,7 @@ def _gpu(evs, trunk, M, prev, u, T, k, mode):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("V", [16, 512, 8192])
+@pytest.mark.parametrize("V", [16, 510, 512, 1000, 2000, 8192])
 def test_markov_draft_matches_oracle(V):
     import hybrid_ssm_attention_gb300 as evs
     g = np.random.default_rng(V + 1)
@@ -39,7 +42,7 @@ def test_markov_draft_matches_oracle(V):
         trunk = (g.standard_normal((gamma, V)) * 2).astype(np.float32)
         prev = int(g.integers(0, V))
         u = g.random(gamma).astype(np.float32)
-        for T, k in ((1.0, 4), (0.7, 0), (1.0, V - 1)):
+        for T, k in ((1.0, 4), (0.7, 0), (1.0, V - 1), (0.8, 7), (1.0, 1)):
             for mode in (SAMPLE, GREEDY):
                 d, q = _gpu(evs, trunk, M, prev, u, T, k, mode)
                 p = prev
@@ -53,6 +56,36 @@ def test_markov_draft_matches_oracle(V):
                     p = d[i]
                 if mode == GREEDY:
                     assert d == markov_draft(trunk, M, prev, u, T, k, GREEDY)[0]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("V", [16, 510, 1000, 2000, 8192])
+def test_markov_draft_ties_take_lower_indices(V):
+    # small integer logits: most entries tie with others, and ties straddle
+    # the top-k cut; the support keeps the lower indices (the oracle's
+    # stable order) for every k, in both kernels (k <= 8 and k = V - 1)
+    import hybrid_ssm_attention_gb300 as evs
+    g = np.random.default_rng(V + 3)
+    gamma = 12
+    M = g.integers(-2, 3, (V, V)).astype(np.float32)
+    for k in (1, 3, 4, 8, V - 1):
+        trunk = g.integers(-1, 2, (gamma, V)).astype(np.float32)
+        prev = int(g.integers(0, V))
+        u = g.random(gamma).astype(np.float32)
+        for mode in (SAMPLE, GREEDY):
+            d, q = _gpu(evs, trunk, M, prev, u, 1.0, k, mode)
+            want_d, want_q = markov_draft(trunk, M, prev, u, 1.0, k, GREEDY) if mode == GREEDY else (None, None)
+            p = prev
+            for i in range(gamma):
+                logits = trunk[i] + M[p]
+                ref = topk_probs(logits, 1.0, k, dtype=np.float32)
+                assert np.array_equal(q[i] > 0, ref > 0), (k, mode, i)
+                assert np.abs(q[i] - ref).max() <= 2e-6
+                want = argmax_low(logits) if mode == GREEDY else sample(q[i], u[i])
+                assert d[i] == want, (k, mode, i)
+                p = d[i]
+            if mode == GREEDY:
+                assert d == want_d
 
 
 @pytest.mark.gpu
