@@ -31,7 +31,9 @@
 //    go on with the next unit.
 //  * a merge warp folds each deposit in warp order into the split's partial
 //    (max, sum of exp, unnormalised output) while the math warps stream, and
-//    counts it in the head's arrival counter; the CTA that brings the count
+//    counts it in the head's arrival counter (the CTA's last unit, with no
+//    stream left to overlap, is merged and counted by the math warps
+//    themselves, eight warps instead of one); the CTA that brings the count
 //    to the head's number of splits folds the partials, after its last unit,
 //    in ascending split order into the mixer output and resets the counter
 //    (no CTA waits for another).
@@ -97,6 +99,31 @@ __device__ __forceinline__ void hand_wait() {
 template <int ID, int NTHR>
 __device__ __forceinline__ void hand_arrive() {
   asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(NTHR) : "memory");
+}
+// Four output dims of query row t merged over the MW warp states in warp
+// order (O = sum_v w_v O_v, one fused multiply-add per warp and dim, as a
+// scalar loop would) and stored as one float4.
+template <int MW, int QP>
+__device__ __forceinline__ void merge_dims(const float* ow, const float* fw, int t, int dd, float* dst) {
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int v = 0; v < MW; ++v) {
+    const float4 a = *reinterpret_cast<const float4*>(ow + ((size_t)v * 16 + t) * QP + dd);
+    const float w = fw[v * 16 + t];
+    O.x = fmaf(a.x, w, O.x);
+    O.y = fmaf(a.y, w, O.y);
+    O.z = fmaf(a.z, w, O.z);
+    O.w = fmaf(a.w, w, O.w);
+  }
+  *reinterpret_cast<float4*>(dst) = O;
+}
+// o / l rounded to bf16, four dims stored as one 8-byte word
+__device__ __forceinline__ void store_out4(bf16* dst, float4 o, float l) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(o.x / l, o.y / l), hi = __floats2bfloat162_rn(o.z / l, o.w / l);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = pk;
 }
 // math_sync that also returns whether v held on any math thread (the same
 // answer on all of them, so branches on it stay uniform)
@@ -362,6 +389,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       const int n = sr.row0[x.sq + 1] - sr.row0[x.sq];
       int npass = pass, nu = u;
       advance(npass, nu);
+      if (nu >= ue) break;  // the CTA's last unit: the math warps merge it themselves
       hand_wait<3, HT>();
       // per (row, warp): the warp's weight exp2(m_v - M), M the row's merged
       // max (0 for a warp that saw no key of the row)
@@ -378,13 +406,10 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       float* part_o = part_os.p[x.sq];
       float* part_ml = part_mls.p[x.sq];
       if (good) {
-        for (int e = lane; e < n * DH; e += 32) {
-          const int t = e / DH, dd = e % DH;
-          float O = 0.f;
-#pragma unroll
-          for (int v = 0; v < MW; ++v) O = fmaf(ow[((size_t)v * 16 + t) * QP + dd], fw[v * 16 + t], O);
+        for (int e = lane; e < n * (DH / 4); e += 32) {
+          const int t = e / (DH / 4), dd = 4 * (e % (DH / 4));
           const size_t base = ((size_t)x.h * nsplit_max + x.sp) * NTOK + t;
-          part_o[base * DH + dd] = O;
+          merge_dims<MW, QP>(ow, fw, t, dd, part_o + base * DH + dd);
           if (dd == 0) {
             float M = -INFINITY, L = 0.f;
 #pragma unroll
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
         }
       }
       __syncwarp();
-      if (nu < ue) hand_arrive<2, HT>();  // the next unit may deposit
+      hand_arrive<2, HT>();  // the next unit may deposit
       if (FUSED && good) {
         // count the split; the last one of the head is folded after this
         // CTA's last unit
@@ -531,9 +556,13 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
   int gi = 0;  // ring stages so far
   bool ok = true;
   const float c2 = rsqrtf((float)DH) * AK_LOG2E;
+  int last_sq = -1, last_h = 0;  // the last unit, when the math warps merged it
   for (; u < ue; advance(pass, u)) {
     const AkUnit x = decode(u);
     const int n = sr.row0[x.sq + 1] - sr.row0[x.sq], r0 = sr.row0[x.sq];
+    int lpass = pass, lu = u;
+    advance(lpass, lu);
+    const bool last = lu >= ue;
     const long long pos = s_pos[x.sq];
     if (x.h != cur_h || x.sq != cur_sq) {
       queries(x);
@@ -688,11 +717,12 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       *reinterpret_cast<float2*>(q0) = make_float2(o[jj][0], o[jj][1]);
       *reinterpret_cast<float2*>(q0 + 8 * QP) = make_float2(o[jj][2], o[jj][3]);
     }
-    if (LY::MERGE_WARP) {
+    if (LY::MERGE_WARP && !last) {
       hand_arrive<3, HT>();
       continue;
     }
-    // without a merge warp: the math warps merge the unit in warp order
+    // without a merge warp, and for the CTA's last unit (the merge warp
+    // would be the tail): the math warps merge the unit in warp order
     math_sync<MT>();
     if (ctid < 16 * MW) {
       const int t = ctid / MW, v = ctid % MW;
@@ -706,13 +736,10 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     if (ok) {
       float* part_o = part_os.p[x.sq];
       float* part_ml = part_mls.p[x.sq];
-      for (int e = ctid; e < n * DH; e += MT) {
-        const int t = e / DH, dd = e % DH;
-        float O = 0.f;
-#pragma unroll
-        for (int v = 0; v < MW; ++v) O = fmaf(ow[((size_t)v * 16 + t) * QP + dd], fw[v * 16 + t], O);
+      for (int e = ctid; e < n * (DH / 4); e += MT) {
+        const int t = e / (DH / 4), dd = 4 * (e % (DH / 4));
         const size_t base = ((size_t)x.h * nsplit_max + x.sp) * NTOK + t;
-        part_o[base * DH + dd] = O;
+        merge_dims<MW, QP>(ow, fw, t, dd, part_o + base * DH + dd);
         if (dd == 0) {
           float M = -INFINITY, L = 0.f;
 #pragma unroll
@@ -724,6 +751,11 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
           part_ml[base * 2 + 1] = L;
         }
       }
+    }
+    if (LY::MERGE_WARP) {
+      __threadfence();  // the partial is visible before the split is counted
+      last_sq = x.sq;
+      last_h = x.h;
     }
     math_sync<MT>();  // the merge area is rewritten by the next unit
   }
@@ -737,6 +769,18 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
   // their weights exp(m_c - M) and l_c (the merge area is free: [16][64]
   // each, then the row sums [16]), all loads of a phase in flight
   hand_wait<4, HT>();
+  if (last_sq >= 0 && ctid == 0 && !*abort_flag) {
+    // count the last split (after the merge warp's counts: one writer of the
+    // fold list at a time)
+    int* cnt = arrivals.p[last_sq] + last_h;
+    if (atomicAdd(cnt, 1) == s_act[last_sq] - 1) {
+      __threadfence();
+      *cnt = 0;
+      if (s_nfold < fold_cap) fold_list[s_nfold++] = (last_sq << 16) | last_h;
+      else *abort_flag = 1;
+    }
+  }
+  math_sync<MT>();
   for (int f = 0; f < s_nfold; ++f) {
     const int sq = fold_list[f] >> 16, h = fold_list[f] & 0xffff;
     const int n = sr.row0[sq + 1] - sr.row0[sq], r0 = sr.row0[sq];
@@ -744,9 +788,24 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     __threadfence();
     float* wt = ow;
     float* lc = ow + 16 * ATTN_SPLITS_MAX;
-    float* lt = lc + 16 * ATTN_SPLITS_MAX;
     const float* pml = part_mls.p[sq] + ((size_t)h * nsplit_max) * NTOK * 2;
     const float* po = part_os.p[sq] + ((size_t)h * nsplit_max) * NTOK * DH;
+    const int items = n * (DH / 4);  // four output dims each
+    auto item_of = [&](int e, int& t, int& d4, int& nc) {
+      t = e / (DH / 4);
+      d4 = 4 * (e % (DH / 4));
+      nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
+    };
+    // the first 16 splits of this thread's first item are requested now:
+    // they do not depend on the weights computed next
+    float4 pre[16];
+    {
+      int t, d4, nc;
+      item_of(ctid < items ? ctid : 0, t, d4, nc);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        pre[c] = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)min(c, nc - 1) * NTOK + t) * DH + d4));
+    }
     for (int tb = 0; tb < 16; tb += MT / 16) {
       const int t = tb + (ctid >> 4), l16 = ctid & 15;  // 16 threads per row, every lane shuffles
       const int nc = t < n ? (int)(min(pos + t, ctx_max - 1) / span) + 1 : 0;
@@ -771,39 +830,33 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       }
     }
     math_sync<MT>();
-    if (ctid < n) {  // the sum of l_c weights in split order
-      const int t = ctid;
-      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
-      float l = 0.f;
-      for (int c = 0; c < nc; ++c) {
-        const float w = wt[t * ATTN_SPLITS_MAX + c];
-        if (w != 0.f) l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
-      }
-      lt[t] = l;
-    }
-    math_sync<MT>();
-    // outputs four dims per thread, each summed over the splits in order
-    for (int e = ctid; e < n * (DH / 4); e += MT) {
-      const int t = e / (DH / 4), d4 = 4 * (e % (DH / 4));
-      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
+    // each item summed over the splits in order, and with it the row's
+    // l = sum_c w_c l_c in the same order
+    for (int e = ctid; e < items; e += MT) {
+      int t, d4, nc;
+      item_of(e, t, d4, nc);
       float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-      for (int c = 0; c < nc; ++c) {
+      float l = 0.f;
+      auto acc = [&](const float4& a, int c) {
         const float w = wt[t * ATTN_SPLITS_MAX + c];
-        const float4 oc = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4));
         if (w != 0.f) {
-          o.x = fmaf(oc.x, w, o.x);
-          o.y = fmaf(oc.y, w, o.y);
-          o.z = fmaf(oc.z, w, o.z);
-          o.w = fmaf(oc.w, w, o.w);
+          o.x = fmaf(a.x, w, o.x);
+          o.y = fmaf(a.y, w, o.y);
+          o.z = fmaf(a.z, w, o.z);
+          o.w = fmaf(a.w, w, o.w);
+          l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
         }
+      };
+      int c = 0;
+      if (e == ctid) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (k < nc) acc(pre[k], k);
+        c = 16;
       }
-      const float l = lt[t];
-      __nv_bfloat162 lo = __floats2bfloat162_rn(o.x / l, o.y / l), hi = __floats2bfloat162_rn(o.z / l, o.w / l);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(gout + (size_t)(r0 + t) * H * DH + h * DH + d4) = pk;
+#pragma unroll 16
+      for (; c < nc; ++c) acc(__ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4)), c);
+      store_out4(gout + (size_t)(r0 + t) * H * DH + h * DH + d4, o, l);
     }
     math_sync<MT>();  // the area is rewritten by the next fold
   }
