@@ -199,13 +199,11 @@ struct AkRows {
 // both rounded to bf16 and stored at positions pos + t.
 template <typename Src, int DH, int NTHR>
 __device__ __forceinline__ void append_rows(const Src& src, int d, int h, int r0, long long pos, int t0, int t1,
-                                            long long ctx_max, const uint64_t* turn_fx, bf16* kc, bf16* vc,
-                                            int ctid) {
+                                            long long ctx_max, uint64_t fx, bf16* kc, bf16* vc, int ctid) {
   using R = AkRows<DH, NTHR>;
   constexpr int HALF = R::HALF;
-  const int i = ctid % HALF, tb = t0 + ctid / HALF;
+  const int i = ctid % HALF, tb = t0 + ctid / HALF;  // fx: the angle step of dimension pair i
   const int col = h * DH + i;
-  const uint64_t fx = turn_fx[i];
   const auto ck1 = src.at(d + col), ck2 = src.at(d + col + HALF);
   const auto cv1 = src.at(2 * d + col), cv2 = src.at(2 * d + col + HALF);
   // at most four rows of each stream in flight per thread
@@ -251,9 +249,13 @@ struct QueryRows {
       q2[k] = src.get(cb, r0 + t, col + R::HALF);
     }
   }
-  __device__ __forceinline__ void finish(long long pos, int n, const uint64_t* turn_fx, float* q, int ctid) const {
-    const int i = ctid % R::HALF, tb = ctid / R::HALF;
-    const uint64_t fx = turn_fx[i];
+  // this thread's rotary angle step (a constant table: read before the
+  // dependency wait)
+  __device__ __forceinline__ static uint64_t angle_step(const uint64_t* turn_fx, int ctid) {
+    return turn_fx[ctid % R::HALF];
+  }
+  __device__ __forceinline__ void finish(long long pos, int n, uint64_t fx, float* q, int ctid) const {
+    const int tb = ctid / R::HALF, i = ctid % R::HALF;
 #pragma unroll
     for (int k = 0; k < R::K; ++k) {
       const int t = tb + k * R::RPP;
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
   const int d = H * DH;
   int pass = 0, u = ub - 1;
   advance(pass, u);  // the first unit in processing order
+  const uint64_t fx = FUSED ? QueryRows<Src, DH, QP, MT>::angle_step(turn_fx, ctid) : 0;
   pdl_wait();
   QueryRows<Src, DH, QP, MT> qr;
   int cur_h = -1, cur_sq = -1;
@@ -508,7 +511,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     const int n = sr.row0[x.sq + 1] - sr.row0[x.sq], r0 = sr.row0[x.sq];
     if (FUSED) {
       qr.load(src, x.h, r0, n, ctid);
-      qr.finish(s_pos[x.sq], n, turn_fx, q_s, ctid);
+      qr.finish(s_pos[x.sq], n, QueryRows<Src, DH, QP, MT>::angle_step(turn_fx, ctid), q_s, ctid);
     } else {
       for (int e = ctid; e < 16 * DH; e += MT) {
         const int t = e / DH, dd = e % DH;
@@ -539,14 +542,14 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     if (!x.fresh) continue;
     const long long pos = s_pos[x.sq];
     const int t0 = (int)(max(x.k0, pos) - pos), t1 = (int)(x.k1 - pos);
-    append_rows<Src, DH, MT>(src, d, x.h, sr.row0[x.sq], pos, t0, t1, ctx_max, turn_fx, kcs.p[x.sq], vcs.p[x.sq], ctid);
+    append_rows<Src, DH, MT>(src, d, x.h, sr.row0[x.sq], pos, t0, t1, ctx_max, fx, kcs.p[x.sq], vcs.p[x.sq], ctid);
   }
   // the producer's tensor-map loads (async proxy) read these rows next
   asm volatile("fence.proxy.async.global;" ::: "memory");
   mbar_arrive(app);
   if (u < ue) {
     const AkUnit x = decode(u);
-    qr.finish(s_pos[x.sq], sr.row0[x.sq + 1] - sr.row0[x.sq], turn_fx, q_s, ctid);
+    qr.finish(s_pos[x.sq], sr.row0[x.sq + 1] - sr.row0[x.sq], fx, q_s, ctid);
     cur_h = x.h;
     cur_sq = x.sq;
   }
@@ -788,24 +791,9 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     __threadfence();
     float* wt = ow;
     float* lc = ow + 16 * ATTN_SPLITS_MAX;
+    float* lt = lc + 16 * ATTN_SPLITS_MAX;
     const float* pml = part_mls.p[sq] + ((size_t)h * nsplit_max) * NTOK * 2;
     const float* po = part_os.p[sq] + ((size_t)h * nsplit_max) * NTOK * DH;
-    const int items = n * (DH / 4);  // four output dims each
-    auto item_of = [&](int e, int& t, int& d4, int& nc) {
-      t = e / (DH / 4);
-      d4 = 4 * (e % (DH / 4));
-      nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
-    };
-    // the first 16 splits of this thread's first item are requested now:
-    // they do not depend on the weights computed next
-    float4 pre[16];
-    {
-      int t, d4, nc;
-      item_of(ctid < items ? ctid : 0, t, d4, nc);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pre[c] = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)min(c, nc - 1) * NTOK + t) * DH + d4));
-    }
     for (int tb = 0; tb < 16; tb += MT / 16) {
       const int t = tb + (ctid >> 4), l16 = ctid & 15;  // 16 threads per row, every lane shuffles
       const int nc = t < n ? (int)(min(pos + t, ctx_max - 1) / span) + 1 : 0;
@@ -830,33 +818,48 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
       }
     }
     math_sync<MT>();
-    // each item summed over the splits in order, and with it the row's
-    // l = sum_c w_c l_c in the same order
-    for (int e = ctid; e < items; e += MT) {
-      int t, d4, nc;
-      item_of(e, t, d4, nc);
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      float l = 0.f;
-      auto acc = [&](const float4& a, int c) {
-        const float w = wt[t * ATTN_SPLITS_MAX + c];
-        if (w != 0.f) {
-          o.x = fmaf(a.x, w, o.x);
-          o.y = fmaf(a.y, w, o.y);
-          o.z = fmaf(a.z, w, o.z);
-          o.w = fmaf(a.w, w, o.w);
-          l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
-        }
-      };
-      int c = 0;
-      if (e == ctid) {
+    // outputs four dims per item (a thread holds at most two), each summed
+    // over the splits in order; the last 16 threads, which hold one item
+    // when there are fewer than 2 MT, then take the rows' l = sum_c w_c l_c
+    // in split order, and the quotients wait for those
+    const int items = n * (DH / 4);
+    float4 o[2];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (k < nc) acc(pre[k], k);
-        c = 16;
-      }
+    for (int k = 0; k < 2; ++k) {
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int e = ctid + k * MT;
+      if (e >= items) continue;
+      const int t = e / (DH / 4), d4 = 4 * (e % (DH / 4));
+      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
 #pragma unroll 16
-      for (; c < nc; ++c) acc(__ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4)), c);
-      store_out4(gout + (size_t)(r0 + t) * H * DH + h * DH + d4, o, l);
+      for (int c = 0; c < nc; ++c) {
+        const float w = wt[t * ATTN_SPLITS_MAX + c];
+        const float4 oc = __ldcg(reinterpret_cast<const float4*>(po + ((size_t)c * NTOK + t) * DH + d4));
+        if (w != 0.f) {
+          o[k].x = fmaf(oc.x, w, o[k].x);
+          o[k].y = fmaf(oc.y, w, o[k].y);
+          o[k].z = fmaf(oc.z, w, o[k].z);
+          o[k].w = fmaf(oc.w, w, o[k].w);
+        }
+      }
+    }
+    if (ctid >= MT - 16 && ctid - (MT - 16) < n) {
+      const int t = ctid - (MT - 16);
+      const int nc = (int)(min(pos + t, ctx_max - 1) / span) + 1;
+      float l = 0.f;
+      for (int c = 0; c < nc; ++c) {
+        const float w = wt[t * ATTN_SPLITS_MAX + c];
+        if (w != 0.f) l = fmaf(lc[t * ATTN_SPLITS_MAX + c], w, l);
+      }
+      lt[t] = l;
+    }
+    math_sync<MT>();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = ctid + k * MT;
+      if (e >= items) continue;
+      const int t = e / (DH / 4), d4 = 4 * (e % (DH / 4));
+      store_out4(gout + (size_t)(r0 + t) * H * DH + h * DH + d4, o[k], lt[t]);
     }
     math_sync<MT>();  // the area is rewritten by the next fold
   }
