@@ -63,7 +63,7 @@ def parse():
     ap.add_argument("--cpu-one-thread-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--case", nargs="+", metavar=("KIND", "ARG"),
                     help="instead of the benchmark, launch one small profiler case and exit: "
-                         "gemm N K n | fir L d n | iir M d n | attn P n | stack L n | batch L B n")
+                         "gemm N K n | fir L d n | iir M d n | attn P n | stack L n | batch L B n | markov V k")
     ap.add_argument("--reps", type=int, default=4, help="repetitions of a --case launch")
     return ap.parse_args()
 
@@ -730,6 +730,8 @@ def run_case(args):
                    weight GEMM of a step once more, each launched alone
     batch L B n    the first L layers, B sequences of n rows verified in one
                    batched pass, each committing its block; --reps times
+    markov V k     the Markov head: 12 sampled draws of top-k over a V-entry
+                   trunk row plus a V x V Markov row, --reps times
     """
     import torch
 
@@ -737,7 +739,7 @@ def run_case(args):
     from hybrid_ssm_attention_gb300 import build as b
     b.build()
     kind, cargs = args.case[0], [int(x) for x in args.case[1:]]
-    if kind not in ("gemm", "fir", "iir", "attn", "stack", "batch"):
+    if kind not in ("gemm", "fir", "iir", "attn", "stack", "batch", "markov"):
         raise SystemExit(f"unknown case {kind}")
 
     class a:
@@ -776,6 +778,17 @@ def run_case(args):
         evs.evs_verify_block(st, toks, n, lg)
         evs.evs_commit(st, n)
         evs.evs_profile_gemms(st, n)
+    elif a.kind == "markov":
+        V, k = (a.args + [512, 4][len(a.args):])[:2]
+        gamma = 12
+        trunk = torch.randn(gamma, V, device=dev, generator=g) * 2
+        M = torch.randn(V, V, device=dev, generator=g) * 2
+        u = torch.rand(gamma, device=dev, generator=g)
+        prev = torch.tensor([3], dtype=torch.int32, device=dev)
+        d = torch.zeros(gamma, dtype=torch.int32, device=dev)
+        q = torch.empty(gamma, V, device=dev)
+        for _ in range(a.reps):
+            evs.evs_markov_draft(trunk, M, V, prev, u, gamma, 1.0, k, evs.EVS_SAMPLE, d, q)
     elif a.kind == "gemm":
         N, K, n = (a.args + [22016, 4096, 13][len(a.args):])[:3]
         W = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
