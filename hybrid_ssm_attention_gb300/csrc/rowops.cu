@@ -221,8 +221,11 @@ __global__ void mlp_act_kernel(const __grid_constant__ Src gu, int F, int il, T*
 }
 
 // Orderable key of a float: a larger value has a larger key; -0 and +0
-// share one key (they compare equal).
+// share one key (they compare equal); NaN has key 0, below every number, so
+// a NaN enters a top-k support only when fewer than k numbers exist (the
+// oracle's stable descending sort puts NaN last).
 __device__ __forceinline__ unsigned int ord_key(float x) {
+  if (x != x) return 0u;
   if (x == 0.f) x = 0.f;
   const unsigned int b = __float_as_uint(x);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
@@ -750,15 +753,13 @@ __global__ void __launch_bounds__(MK_THREADS) markov_draft_topk_kernel(
 
 // The top_k <= 8 chain by one warp when V <= 1024 and V % 4 == 0 (rows of
 // whole float4s): lane l owns the NPL contiguous entries from l * NPL.  An
-// entry's order is its orderable 32-bit key (NaN -> 0, never chosen), ties
+// entry's order is its orderable 32-bit key (NaN: key 0, never taken), ties
 // to the lower index; a support round is one warp max of the lanes' best
 // keys, a ballot for the lowest lane holding it (lowest lane = lowest
 // index), and a rescan by that lane alone.  The support then sits in every
 // lane's registers, and so do its softmax, the ladder draw and the next
 // draft: the next Markov row is requested before this slot's q is stored
 // (greedy: right after the first round, the draft being the argmax).
-__device__ __forceinline__ unsigned int mk_key(float x) { return x != x ? 0u : ord_key(x); }
-
 __device__ __forceinline__ float mk_val(unsigned int key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
@@ -816,7 +817,7 @@ __global__ void __launch_bounds__(32) markov_draft_warp_kernel(
     const float ui = u[i];
     unsigned int key[NPL];
 #pragma unroll
-    for (int e = 0; e < NPL; ++e) key[e] = e < nown ? mk_key(__fadd_rn(tr[e], x[e])) : 0u;
+    for (int e = 0; e < NPL; ++e) key[e] = e < nown ? ord_key(__fadd_rn(tr[e], x[e])) : 0u;
     unsigned int bk;
     int be;
     mk_lane_best<NPL>(key, bk, be);

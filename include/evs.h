@@ -281,8 +281,9 @@ int evs_verify_block_trace(evs_state* s, const int32_t* tokens_dev, int32_t n,
 
 /* Target distribution ([library]: T, top_k).  logits_dev [n][V] ->
  * p_dev [n][V]: softmax of logits / T over the top_k largest entries of each
- * row (ties to the lower index), zero elsewhere; top_k <= 0 or >= V keeps
- * all.  T > 0. */
+ * row (ties to the lower index; a NaN ranks below every number, so it enters
+ * the support only when a row holds fewer than top_k numbers), zero
+ * elsewhere; top_k <= 0 or >= V keeps all.  T > 0. */
 int evs_probs(const float* logits_dev, int32_t n, int32_t V, float T,
               int32_t top_k, float* p_dev, cudaStream_t stream);
 
@@ -319,8 +320,10 @@ int evs_accept(const float* p_dev, const float* q_dev, const int32_t* drafts_dev
  * q_dev [gamma][V]; draft i = sample(q_i, u_dev[i]) with the accept rule's
  * integer-ladder sampler (EVS_SAMPLE; a row without mass gives its argmax)
  * or the argmax of the logits, lowest index on ties (EVS_GREEDY, u_dev
- * unused, may be null), written to drafts_dev[i].  One CTA; V <= 8192,
- * 1 <= gamma <= 64, T > 0. */
+ * unused, may be null), written to drafts_dev[i].  A NaN logit ranks below
+ * every number (for 1 <= top_k <= 8 it never enters the support).  One CTA
+ * (one warp when 1 <= top_k <= 8, V <= 1024, V % 4 == 0 and the three
+ * float arrays are 16-byte aligned); V <= 8192, 1 <= gamma <= 64, T > 0. */
 int evs_markov_draft(const float* trunk_logits_dev, const float* markov_dev, int32_t V, const int32_t* prev_dev,
                      const float* u_dev, int32_t gamma, float T, int32_t top_k, int32_t mode,
                      int32_t* drafts_dev, float* q_dev, cudaStream_t stream);

@@ -132,6 +132,30 @@ def test_probs_topk_support_and_values():
 
 
 @pytest.mark.gpu
+def test_probs_nan_logits_rank_below_every_number():
+    # NaN entries stay out of a top-k support while the row holds k numbers
+    # (the oracle's stable descending sort puts them last)
+    import hybrid_ssm_attention_gb300 as evs
+    t = torch()
+    g = np.random.default_rng(29)
+    for V in (16, 512, 4096):
+        n = 4
+        L = (g.standard_normal((n, V)) * 3).astype(np.float32)
+        L[0, :3] = np.nan
+        L[1, g.choice(V, V // 4, replace=False)] = np.nan
+        L[2, V - 1] = np.nan
+        L[3, 1::2] = np.nan
+        for T, k in ((1.0, 4), (1.0, 1), (0.7, 5)):
+            p = t.empty((n, V), dtype=t.float32, device="cuda")
+            evs.evs_probs(up(L), n, V, T, k, p)
+            want = np.stack([topk_probs(r, T, k, dtype=np.float32) for r in L])
+            got = to_np(p)
+            assert not np.isnan(got).any()
+            assert np.array_equal(got > 0, want > 0), (V, T, k)
+            assert np.abs(got - want).max() <= 2e-6
+
+
+@pytest.mark.gpu
 def test_probs_topk_large_vocab_and_ties_at_the_cut():
     import hybrid_ssm_attention_gb300 as evs
     t = torch()

@@ -89,6 +89,32 @@ def test_markov_draft_ties_take_lower_indices(V):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("V", [16, 512, 1000, 2000])
+def test_markov_draft_nan_logits_stay_out_of_the_support(V):
+    # NaN trunk entries rank below every number: q and the sampled drafts
+    # match the oracle's rule on the same logits (top_k 1, 4, 8)
+    import hybrid_ssm_attention_gb300 as evs
+    g = np.random.default_rng(V + 7)
+    gamma = 12
+    M = (g.standard_normal((V, V)) * 2).astype(np.float32)
+    for k in (1, 4, 8):
+        trunk = (g.standard_normal((gamma, V)) * 2).astype(np.float32)
+        trunk[:, g.choice(V, V // 4, replace=False)] = np.nan
+        trunk[0, :2] = np.nan
+        prev = int(g.integers(0, V))
+        u = g.random(gamma).astype(np.float32)
+        d, q = _gpu(evs, trunk, M, prev, u, 1.0, k, SAMPLE)
+        assert not np.isnan(q).any()
+        p = prev
+        for i in range(gamma):
+            ref = topk_probs(trunk[i] + M[p], 1.0, k, dtype=np.float32)
+            assert np.array_equal(q[i] > 0, ref > 0), (k, i)
+            assert np.abs(q[i] - ref).max() <= 2e-6
+            assert d[i] == sample(q[i], u[i]), (k, i)
+            p = d[i]
+
+
+@pytest.mark.gpu
 def test_markov_draft_chain_and_bad_pending_token():
     import hybrid_ssm_attention_gb300 as evs
     V, gamma = 64, 10
