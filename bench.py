@@ -607,7 +607,10 @@ def drafter_rounds(evs, torch, dev, seed, prompt_len, rounds=16, warm=4):
     torch.cuda.synchronize()
     # the device sleeps while the host queues every timed round behind it,
     # so the events time the device, not the Python calls between them
-    torch.cuda._sleep(100_000_000)
+    # (without torch's sleep kernel the rounds run as queued; queued_ahead
+    # then reports false)
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(100_000_000)
     for r in range(rounds):
         one(warm + r, ev[r])
     queued_ahead = not ev[-1][2].query()
