@@ -966,25 +966,21 @@ def run_evs(args, rank, world, local):
                   "note": "host-driven: snapshot (FIR/IIR state + book), verify, accept, read keep, restore, "
                           "verify keep tokens, commit; identity drafter, so keep = 13"}
 
-    # end to end through the C ABI with host buffers (pinned), result read back every round
+    # end to end through the C ABI with the block and the result in host
+    # memory: evs_round_host copies the block in and the result out (both
+    # inside the round's graph) and returns once the result is on the host
     e2e = None
     if not args.no_e2e:
         snap.clone_into(st)
-        host_blocks = blocks.cpu().pin_memory()
-        acc_h = torch.zeros(1, dtype=torch.int32).pin_memory()
-        tok_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+        host_blocks = blocks.cpu().numpy()
         emitted_e2e = 0
         for r in range(rounds):
             if r == args.warmup:
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
-            tokens.copy_(host_blocks[r], non_blocking=True)
-            evs.evs_round(st, tokens, n, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY, acc, otok)
-            acc_h.copy_(acc, non_blocking=True)
-            tok_h.copy_(otok, non_blocking=True)
-            stream.synchronize()
+            a_r, _ = evs.evs_round_host(st, host_blocks[r], n, lg, None, None, None, 1.0, 0, evs.EVS_GREEDY)
             if r >= args.warmup:
-                emitted_e2e += int(acc_h.item()) + 1
+                emitted_e2e += a_r + 1
         dt = time.perf_counter() - t0
         e2e = {"value": reduce_sum(emitted_e2e, world) / reduce_max(dt, world), "unit": UNIT,
                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 8}

@@ -21,7 +21,7 @@ from ._abi import (EVS_BF16, EVS_ERR_ARG, EVS_ERR_CAPACITY, EVS_ERR_CUDA, EVS_ER
                    EVS_OPT_SWIGLU_EPILOGUE, EVS_SAMPLE, evs_book, evs_layer_view)
 
 __all__ = ["EvsError", "Model", "State", "lib", "evs_verify_block", "evs_verify_block_trace", "evs_probs", "evs_accept",
-           "evs_commit", "evs_commit_dev", "evs_markov_draft", "evs_round", "evs_round_batch", "evs_op_fir", "evs_op_iir",
+           "evs_commit", "evs_commit_dev", "evs_markov_draft", "evs_round", "evs_round_host", "evs_round_batch", "evs_op_fir", "evs_op_iir",
            "evs_op_attention", "evs_op_commit", "evs_op_gemm", "evs_op_gemm_static", "evs_verify_batch",
            "evs_kernel_launches"]
 
@@ -241,6 +241,19 @@ def evs_round(state: State, tokens, n: int, logits, p, q, u, T: float, top_k: in
     _check(lib().evs_round(state.handle, _ptr(tokens), int(n), _ptr(logits), _ptr(p), _ptr(q), _ptr(u),
                            float(T), int(top_k), int(mode), _ptr(out_accepted), _ptr(out_token),
                            _stream(stream)), "evs_round")
+
+
+def evs_round_host(state: State, tokens, n: int, logits, p, q, u, T: float, top_k: int, mode: int, stream=None):
+    """One round with the block in host memory (int32 numpy array or
+    sequence); returns (accepted, token) as Python ints."""
+    import numpy as _np
+    tok = _np.ascontiguousarray(_np.asarray(tokens, dtype=_np.int32)[:n])
+    acc = (C.c_int32 * 1)()
+    otok = (C.c_int32 * 1)()
+    _check(lib().evs_round_host(state.handle, tok.ctypes.data, int(n), _ptr(logits), _ptr(p), _ptr(q), _ptr(u),
+                                float(T), int(top_k), int(mode), C.cast(acc, C.c_void_p), C.cast(otok, C.c_void_p),
+                                _stream(stream)), "evs_round_host")
+    return int(acc[0]), int(otok[0])
 
 
 def evs_round_batch(states, tokens, ns, logits, p, q, u, T: float, top_k: int, mode: int, out_accepted, out_token,

@@ -79,6 +79,7 @@ PROTOTYPES = {
     "evs_commit": (i32, [vp, i32, vp]),
     "evs_commit_dev": (i32, [vp, vp, vp]),
     "evs_round": (i32, [vp, vp, i32, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
+    "evs_round_host": (i32, [vp, vp, i32, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
     "evs_round_batch": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp]),
     "evs_profile_gemm_chain": (i32, [vp, i32, i32, C.POINTER(C.c_float), C.POINTER(i64), C.POINTER(i32), vp]),
     "evs_op_fir": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),

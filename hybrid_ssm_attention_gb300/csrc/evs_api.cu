@@ -81,6 +81,7 @@ struct GraphEntry {
   float T;
   const void *tok, *logits, *p, *q, *u, *acc, *otok;
   bool round;
+  bool host_io;  // evs_round_host: the copies to and from the staging are in the graph
   // batched rounds: the sequences' states (by creation id, never reused)
   // and block lengths
   int nseq;
@@ -159,6 +160,10 @@ struct evs_state {
   float* ss;    // [tiles of d][ROWS_MAX] per-tile sums of squares
   int* cnt;     // [max tiles] GEMM arrival counters
   int cnt_len;
+  // evs_round_host: the block's tokens [NTOK] and the result (accepted,
+  // token) on the device, and their pinned host staging [NTOK + 2]
+  int32_t* io_dev = nullptr;
+  int32_t* io_pinned = nullptr;
   float* ws[2];
   void* attn_scratch;
   AttnBufs ab;
@@ -662,7 +667,7 @@ GraphEntry* find_graph(evs_state* s, const GraphEntry& key) {
   for (auto& g : s->graphs)
     if (g.round == key.round && g.n == key.n && g.tok == key.tok && g.logits == key.logits &&
         g.mode == key.mode && g.top_k == key.top_k && g.T == key.T && g.p == key.p && g.q == key.q &&
-        g.u == key.u && g.acc == key.acc && g.otok == key.otok && g.nseq == key.nseq &&
+        g.u == key.u && g.acc == key.acc && g.otok == key.otok && g.nseq == key.nseq && g.host_io == key.host_io &&
         std::equal(g.uid, g.uid + g.nseq, key.uid) && std::equal(g.ns, g.ns + g.nseq, key.ns))
       return &g;
   return nullptr;
@@ -920,6 +925,7 @@ static void state_free(evs_state* s) {
   for (auto& g : s->graphs) cudaGraphExecDestroy(g.exec);
   if (s->cap) cudaStreamDestroy(s->cap);
   for (void* p : s->allocs) cudaFree(p);
+  if (s->io_pinned) cudaFreeHost(s->io_pinned);
   delete s;
 }
 
@@ -964,6 +970,17 @@ extern "C" int evs_state_create(evs_model* m, int64_t ctx_max, evs_state** out) 
   ALLOC(s->ss, sizeof(float) * R * ((d + TILE_M - 1) / TILE_M));
   s->cnt_len = (std::max(3 * d, std::max(2 * F, c.vocab)) + TILE_M - 1) / TILE_M;
   ALLOC(s->cnt, sizeof(int) * s->cnt_len);
+  ALLOC(s->io_dev, sizeof(int32_t) * (NTOK + 2));
+  {
+    void* ph = nullptr;
+    cudaError_t e = cudaHostAlloc(&ph, sizeof(int32_t) * (NTOK + 2), cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      state_free(s);
+      return fail(EVS_ERR_OOM, "cudaHostAlloc(staging) failed: %s", cudaGetErrorString(e));
+    }
+    s->io_pinned = static_cast<int32_t*>(ph);
+  }
   size_t wsb = 0;
   wsb = m->ws_bytes;
   ALLOC(s->ws[0], wsb);
@@ -1356,6 +1373,48 @@ extern "C" int evs_round(evs_state* s, const int32_t* tokens, int32_t n, float* 
   EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) { return enqueue_round(s, tokens, n, logits, r, Lc); }));
   s->host_pos_known = false;
   s->host_pending = 0;
+  return EVS_OK;
+}
+
+extern "C" int evs_round_host(evs_state* s, const int32_t* tokens_host, int32_t n, float* logits, float* p,
+                              const float* q, const float* u, float T, int32_t top_k, int32_t mode,
+                              int32_t* accepted_host, int32_t* token_host, cudaStream_t stream) {
+  if (!s || !tokens_host || !logits || !accepted_host || !token_host) return fail(EVS_ERR_ARG, "null argument");
+  if (mode != EVS_GREEDY && mode != EVS_SAMPLE) return fail(EVS_ERR_ARG, "bad mode");
+  if (mode == EVS_SAMPLE && (!p || !u || (n > 1 && !q) || !(T > 0.f)))
+    return fail(EVS_ERR_ARG, "sample mode needs p, q, u and T > 0");
+  if (n < 1 || n > NTOK) return fail(EVS_ERR_ARG, "n must be in [1, %d]", NTOK);
+  EVS_TRY(check_block(s, n));
+  // the staging is free: every call returns after its graph has finished
+  memcpy(s->io_pinned, tokens_host, sizeof(int32_t) * n);
+  int32_t* tok_d = s->io_dev;
+  int32_t* res_d = s->io_dev + NTOK;  // accepted, token
+  RoundArgs r{p, q, tok_d + 1, u, T, top_k, mode, res_d, res_d + 1};
+  GraphEntry key{};
+  key.round = true;
+  key.host_io = true;
+  key.n = n;
+  key.tok = tok_d;
+  key.logits = logits;
+  key.p = p;
+  key.q = q;
+  key.u = u;
+  key.T = T;
+  key.top_k = top_k;
+  key.mode = mode;
+  key.acc = res_d;
+  key.otok = res_d + 1;
+  EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) -> int {
+    CUDA_TRY(cudaMemcpyAsync(tok_d, s->io_pinned, sizeof(int32_t) * n, cudaMemcpyHostToDevice, Lc.stream));
+    EVS_TRY(enqueue_round(s, tok_d, n, logits, r, Lc));
+    CUDA_TRY(cudaMemcpyAsync(s->io_pinned + NTOK, res_d, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, Lc.stream));
+    return EVS_OK;
+  }));
+  s->host_pos_known = false;
+  s->host_pending = 0;
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  accepted_host[0] = s->io_pinned[NTOK];
+  token_host[0] = s->io_pinned[NTOK + 1];
   return EVS_OK;
 }
 

@@ -348,6 +348,15 @@ int evs_round(evs_state* s, const int32_t* tokens_dev, int32_t n, float* logits_
               float* p_dev, const float* q_dev, const float* u_dev, float T, int32_t top_k,
               int32_t mode, int32_t* out_accepted_dev, int32_t* out_token_dev,
               cudaStream_t stream);
+/* The same round with the block and the result in host memory (any host
+ * buffers): copies tokens_host [n] in, runs the round (arguments as
+ * evs_round; n <= 16), and returns once accepted_host[0] and token_host[0]
+ * hold the result (the call synchronises the stream).  The two
+ * copies go through the state's pinned staging and are part of the round's
+ * graph, so a round costs one graph launch and one synchronisation. */
+int evs_round_host(evs_state* s, const int32_t* tokens_host, int32_t n, float* logits_dev,
+                   float* p_dev, const float* q_dev, const float* u_dev, float T, int32_t top_k,
+                   int32_t mode, int32_t* accepted_host, int32_t* token_host, cudaStream_t stream);
 /* Batched round ([systems] batched verification with ragged per-sequence
  * rollback, with the bookkeeping on the device): one graph launch doing
  * evs_verify_batch over the nseq sequences' blocks, then (EVS_SAMPLE) the
