@@ -439,7 +439,8 @@ def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, y, rounds=24,
     second for each (B, n)."""
     out = []
     V = shape.vocab
-    for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1), (2, 13), (4, 13), (8, 13), (16, 8)):
+    for B, n in ((1, 13), (2, 8), (4, 4), (8, 2), (16, 1), (2, 13), (4, 13), (8, 13), (16, 8), (1, 1), (2, 1),
+                 (4, 1), (8, 1)):
         states = [evs.State(model, ctx) for _ in range(B)]
         for st in states:
             post_prompt.clone_into(st)
@@ -465,6 +466,26 @@ def batched_sweep(evs, torch, model, shape, post_prompt, ctx, dev, y, rounds=24,
                     "all_accepted": all_acc})
         for st in states:
             st.close()
+    return out
+
+
+def crossover(sweep):
+    """Batched speculative verification against batched native decoding of
+    the same B sequences: native = one row per sequence per pass (B x 1);
+    speculative = the widest block pass per sequence measured (B x 13 up to
+    104 rows, 16 x 8 at B = 16).  A speculative round emits (accepted + 1)
+    tokens per sequence against one per native pass, so it wins once
+    accepted + 1 > spec_ms / native_ms (the break-even tokens per round);
+    at full acceptance the speedup is n * native_ms / spec_ms."""
+    ms = {(r["B"], r["n"]): r["ms_per_round"] for r in sweep}
+    out = []
+    for B in (1, 2, 4, 8, 16):
+        n = 13 if (B, 13) in ms else max(k[1] for k in ms if k[0] == B)
+        if (B, 1) not in ms or (B, n) not in ms or n == 1:
+            continue
+        out.append({"B": B, "native_ms": ms[(B, 1)], "spec_n": n, "spec_ms": ms[(B, n)],
+                    "break_even_tokens_per_round": ms[(B, n)] / ms[(B, 1)],
+                    "speedup_all_accepted": n * ms[(B, 1)] / ms[(B, n)]})
     return out
 
 
@@ -985,9 +1006,10 @@ def run_evs(args, rank, world, local):
         e2e = {"value": reduce_sum(emitted_e2e, world) / reduce_max(dt, world), "unit": UNIT,
                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 8}
 
-    batched = None
+    batched = cross = None
     if not args.no_batch:
         batched = batched_sweep(evs, torch, model, shape, snap, ctx, dev, y)
+        cross = crossover(batched)
 
     longgen = None
     if args.long_gen > 0:
@@ -1025,7 +1047,8 @@ def run_evs(args, rank, world, local):
             "step_hbm": {"bytes": sb, "achieved_gbs": sb / (ms_per_step / 1e3) / 1e9,
                          "frac": sb / (ms_per_step / 1e3) / 1e9 / peak},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "snapshot_replay": replay,
-            "long_generation": longgen, "batched_verify": batched, "sampled": sampled, "long_context": longctx,
+            "long_generation": longgen, "batched_verify": batched, "batched_crossover": cross, "sampled": sampled,
+            "long_context": longctx,
             "drafter": drafter,
             "gpu_launches": int(launches),
             "clocks": clk}
