@@ -822,6 +822,7 @@ __global__ void __launch_bounds__(AkLayout<DH, MW>::THREADS, MW == 8 ? 1 : 2)
     // over the splits in order; the last 16 threads, which hold one item
     // when there are fewer than 2 MT, then take the rows' l = sum_c w_c l_c
     // in split order, and the quotients wait for those
+    static_assert(!FUSED || 16 * (DH / 4) <= 2 * MT, "at most two output items per thread");
     const int items = n * (DH / 4);
     float4 o[2];
 #pragma unroll
