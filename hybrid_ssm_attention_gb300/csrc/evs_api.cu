@@ -639,8 +639,7 @@ int enqueue_round(evs_state* s, const int32_t* tokens, int n, float* logits, con
     CUDA_TRY(launch_probs(Lc, logits, n, V, r.T, r.top_k, r.p));
     P = r.p;
   }
-  CUDA_TRY(launch_accept(Lc, P, r.q, r.drafts, r.u, n, V, r.mode, r.acc, r.otok, s->book));
-  CUDA_TRY(launch_commit(Lc, s->book, 0, r.acc, 0));
+  CUDA_TRY(launch_accept(Lc, P, r.q, r.drafts, r.u, n, V, r.mode, r.acc, r.otok, s->book, true));
   return EVS_OK;
 }
 
@@ -658,8 +657,7 @@ int enqueue_round_batch(evs_state* const* states, const SeqRows& sr, const int32
   }
   SeqPtrs<evs_book*> books{};
   for (int b = 0; b < sr.nseq; ++b) books.p[b] = states[b]->book;
-  CUDA_TRY(launch_accept_batch(Lc, P, r.q, r.drafts, r.u, sr, V, r.mode, r.acc, r.otok, books));
-  CUDA_TRY(launch_commit_batch(Lc, books, sr.nseq, r.acc));
+  CUDA_TRY(launch_accept_batch(Lc, P, r.q, r.drafts, r.u, sr, V, r.mode, r.acc, r.otok, books, true));
   return EVS_OK;
 }
 

@@ -427,6 +427,22 @@ __device__ int ladder_find(const unsigned int* W, int V, unsigned long long thr,
   return *found;
 }
 
+__device__ void commit_one(evs_book* book, int keep, int n_explicit) {
+  const int n = n_explicit > 0 ? n_explicit : book->pending_n;
+  if (n <= 0 || keep < 0 || keep > n) {
+    set_status(book, EVS_DEV_BAD_KEEP);
+    book->pending_n = 0;
+    return;
+  }
+  // FIR windows follow pos (ring rows by absolute position)
+  if (keep > 0) {
+    book->iir_bank ^= 1;
+    book->iir_slot = keep - 1;
+  }
+  book->pos += keep;
+  book->pending_n = 0;
+}
+
 // One CTA per sequence b of sr: its rows r0 = sr.row0[b] .. + n - 1 of p,
 // q, drafts and u (row r0 + i of q / drafts: draft i + 1); results to
 // out_a[b], out_tok[b].
@@ -435,7 +451,7 @@ __device__ int ladder_find(const unsigned int* W, int V, unsigned long long thr,
 __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float* q, const int32_t* drafts,
                                                      const float* u, const __grid_constant__ SeqRows sr, int V,
                                                      int mode, int32_t* out_a, int32_t* out_tok,
-                                                     const __grid_constant__ SeqPtrs<evs_book*> books) {
+                                                     const __grid_constant__ SeqPtrs<evs_book*> books, int commit) {
   extern __shared__ unsigned int Wsm[];  // [V], then s_arg[n], s_ok[n]
   __shared__ unsigned long long us[256];
   __shared__ int found;
@@ -516,6 +532,8 @@ __global__ void __launch_bounds__(256) accept_kernel(const float* p, const float
   if (threadIdx.x == 0) {
     out_a[0] = a;
     out_tok[0] = token;
+    // a round's commit with keep = a + 1, here instead of one more launch
+    if (commit && books.p[b]) commit_one(books.p[b], a + 1, 0);
   }
 }
 
@@ -926,36 +944,11 @@ static cudaError_t launch_markov_topk(const LaunchCtx& L, const float* trunk, co
 
 // Commit: keep = *acc_dev + 1 when acc_dev is given, else keep_host.
 // n_explicit > 0 replaces book->pending_n (bare-book operator use).
-__device__ void commit_one(evs_book* book, int keep, int n_explicit) {
-  const int n = n_explicit > 0 ? n_explicit : book->pending_n;
-  if (n <= 0 || keep < 0 || keep > n) {
-    set_status(book, EVS_DEV_BAD_KEEP);
-    book->pending_n = 0;
-    return;
-  }
-  // FIR windows follow pos (ring rows by absolute position)
-  if (keep > 0) {
-    book->iir_bank ^= 1;
-    book->iir_slot = keep - 1;
-  }
-  book->pos += keep;
-  book->pending_n = 0;
-}
-
 __global__ void commit_kernel(evs_book* book, int keep_host, const int32_t* acc_dev, int n_explicit) {
   pdl_trigger();
   pdl_wait();
   if (threadIdx.x != 0) return;
   commit_one(book, acc_dev ? acc_dev[0] + 1 : keep_host, n_explicit);
-}
-
-// thread b: sequence b's commit with keep = acc_dev[b] + 1
-__global__ void commit_batch_kernel(const __grid_constant__ SeqPtrs<evs_book*> books, int nseq,
-                                    const int32_t* acc_dev) {
-  pdl_trigger();
-  pdl_wait();
-  const int b = threadIdx.x;
-  if (b < nseq) commit_one(books.p[b], acc_dev[b] + 1, 0);
 }
 
 // Fixed amount of arithmetic (no memory, no waits) that occupies the stream
@@ -1028,13 +1021,14 @@ cudaError_t launch_probs(const LaunchCtx& L, const float* logits, int n, int V, 
 }
 
 cudaError_t launch_accept(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
-                          const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok, evs_book* book) {
-  return launch_accept_batch(L, p, q, drafts, u, one_seq(n), V, mode, acc, tok, one_ptr(book));
+                          const float* u, int n, int V, int mode, int32_t* acc, int32_t* tok, evs_book* book,
+                          bool commit) {
+  return launch_accept_batch(L, p, q, drafts, u, one_seq(n), V, mode, acc, tok, one_ptr(book), commit);
 }
 
 cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float* q, const int32_t* drafts,
                                 const float* u, const SeqRows& sr, int V, int mode, int32_t* acc, int32_t* tok,
-                                const SeqPtrs<evs_book*>& books) {
+                                const SeqPtrs<evs_book*>& books, bool commit) {
   int nmax = 0;
   for (int b = 0; b < sr.nseq; ++b) nmax = std::max(nmax, sr.row0[b + 1] - sr.row0[b]);
   const size_t smem = sizeof(unsigned int) * V + 2 * sizeof(int) * nmax;
@@ -1043,7 +1037,8 @@ cudaError_t launch_accept_batch(const LaunchCtx& L, const float* p, const float*
     cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch(L, accept_kernel, dim3(sr.nseq), dim3(256), smem, p, q, drafts, u, sr, V, mode, acc, tok, books);
+  return launch(L, accept_kernel, dim3(sr.nseq), dim3(256), smem, p, q, drafts, u, sr, V, mode, acc, tok, books,
+                (int)commit);
 }
 
 cudaError_t launch_markov_draft(const LaunchCtx& L, const float* trunk, const float* M, int V, const int32_t* prev,
@@ -1060,10 +1055,6 @@ cudaError_t launch_markov_draft(const LaunchCtx& L, const float* trunk, const fl
   }
   return launch(L, markov_draft_kernel, dim3(1), dim3(256), smem, trunk, M, V, prev, u, gamma, T, top_k, mode, drafts,
                 q);
-}
-
-cudaError_t launch_commit_batch(const LaunchCtx& L, const SeqPtrs<evs_book*>& books, int nseq, const int32_t* acc) {
-  return launch(L, commit_batch_kernel, dim3(1), dim3(32), 0, books, nseq, acc);
 }
 
 cudaError_t launch_commit(const LaunchCtx& L, evs_book* book, int keep, const int32_t* acc_dev, int n_explicit) {
