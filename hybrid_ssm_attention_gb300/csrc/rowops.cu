@@ -838,7 +838,19 @@ __global__ void __launch_bounds__(32) markov_draft_warp_kernel(
     for (int e = 0; e < NPL; ++e) key[e] = e < nown ? ord_key(__fadd_rn(tr[e], x[e])) : 0u;
     unsigned int bk;
     int be;
+    // the lane's best and second-best entries (key 0: none); a lane whose
+    // best is taken promotes its second and rescans only when it wins again
     mk_lane_best<NPL>(key, bk, be);
+    unsigned int bk2;
+    int be2;
+    {
+      unsigned int rest[NPL];
+#pragma unroll
+      for (int e = 0; e < NPL; ++e) rest[e] = e == be ? 0u : key[e];
+      mk_lane_best<NPL>(rest, bk2, be2);
+    }
+    bool have2 = true;
+    unsigned int taken = 0;  // bit e: entry e is in the support
     unsigned int sk[KM];
     int si[KM];
     int d = -1;
@@ -852,12 +864,17 @@ __global__ void __launch_bounds__(32) markov_draft_warp_kernel(
           const int wl = __ffs(__ballot_sync(0xffffffffu, bk == mk)) - 1;
           sk[r] = mk;
           si[r] = wl * NPL + __shfl_sync(0xffffffffu, be, wl);
-          if (r + 1 < k) {
-            if (lane == wl) {
+          if (r + 1 < k && lane == wl) {
+            taken |= 1u << be;
+            if (have2) {
+              bk = bk2;
+              be = be2;
+              have2 = false;
+            } else {
+              unsigned int rest[NPL];
 #pragma unroll
-              for (int e = 0; e < NPL; ++e)
-                if (e == be) key[e] = 0u;
-              mk_lane_best<NPL>(key, bk, be);
+              for (int e = 0; e < NPL; ++e) rest[e] = (taken >> e) & 1u ? 0u : key[e];
+              mk_lane_best<NPL>(rest, bk, be);
             }
           }
         }
