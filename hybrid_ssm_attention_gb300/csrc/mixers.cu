@@ -629,11 +629,11 @@ cudaError_t launch_iir(const LaunchCtx& L, int dtype, MixSrc src, int d, const S
   return iir_dispatch<float>(L, sf, d, sr, M, lam, res, st0, st1, book, g);
 }
 
-// Key span of a split: max(chunk, 128) * 2^j, the smallest with at most
+// Key span of a split: max(chunk, 256) * 2^j, the smallest with at most
 // ATTN_SPLITS_MAX splits over ctx_max.  Fixed per cache, so the partition
 // of a query's keys never depends on the block size.
 long long attn_span(long long ctx_max, int chunk) {
-  long long span = std::max(chunk, 128);
+  long long span = std::max(chunk, 256);
   while ((ctx_max + span - 1) / span > ATTN_SPLITS_MAX) span *= 2;
   return span;
 }

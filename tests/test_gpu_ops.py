@@ -131,7 +131,7 @@ def test_attention_op_cache(H, Dh, P, chunk):
     # Dh 128 / 64: the tensor-map kernel, fused with rotary / append / fold
     # for caches above 8192 positions, between the rotary and combine kernels
     # at or below (Dh 64: one box per key row; the first block straddles a
-    # split boundary: 9216 at span 256, 3072 at span 128); Dh 32: the SIMT
+    # split boundary: 9216 and 3072, both at span 256); Dh 32: the SIMT
     # kernel on bf16 caches
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
