@@ -1402,12 +1402,18 @@ extern "C" int evs_round_host(evs_state* s, const int32_t* tokens_host, int32_t 
   key.mode = mode;
   key.acc = res_d;
   key.otok = res_d + 1;
-  EVS_TRY(run_captured(s, key, stream, [&](const LaunchCtx& Lc) -> int {
+  const int rc = run_captured(s, key, stream, [&](const LaunchCtx& Lc) -> int {
     CUDA_TRY(cudaMemcpyAsync(tok_d, s->io_pinned, sizeof(int32_t) * n, cudaMemcpyHostToDevice, Lc.stream));
     EVS_TRY(enqueue_round(s, tok_d, n, logits, r, Lc));
     CUDA_TRY(cudaMemcpyAsync(s->io_pinned + NTOK, res_d, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, Lc.stream));
     return EVS_OK;
-  }));
+  });
+  if (rc != EVS_OK) {
+    // without graphs the token copy may already be queued when a later step
+    // fails: wait for it, so the next call may rewrite the staging
+    cudaStreamSynchronize(stream);
+    return rc;
+  }
   s->host_pos_known = false;
   s->host_pending = 0;
   CUDA_TRY(cudaStreamSynchronize(stream));

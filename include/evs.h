@@ -321,7 +321,9 @@ int evs_accept(const float* p_dev, const float* q_dev, const int32_t* drafts_dev
  * integer-ladder sampler (EVS_SAMPLE; a row without mass gives its argmax)
  * or the argmax of the logits, lowest index on ties (EVS_GREEDY, u_dev
  * unused, may be null), written to drafts_dev[i].  A NaN logit ranks below
- * every number (for 1 <= top_k <= 8 it never enters the support).  One CTA
+ * every number (for 1 <= top_k <= 8 it never enters the support; a slot
+ * whose logits are all NaN then has an empty support: q_i all zero and
+ * draft 0).  One CTA
  * (one warp when 1 <= top_k <= 8, V <= 1024, V % 4 == 0 and the three
  * float arrays are 16-byte aligned); V <= 8192, 1 <= gamma <= 64, T > 0. */
 int evs_markov_draft(const float* trunk_logits_dev, const float* markov_dev, int32_t V, const int32_t* prev_dev,

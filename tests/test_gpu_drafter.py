@@ -8,7 +8,8 @@ the oracle's whole chain.  Vocab 16, 510, 512, 1000, 2000 and 8192; top_k
 0, 1, 4, 7 and V - 1 (top_k 1 .. 8: the one-warp kernel for V <= 1024 and
 V % 4 == 0, the merged-list kernel otherwise; other top_k: the radix
 select); T 1, 0.8 and 0.7; integer logits whose ties straddle the top-k cut;
-a one-hot Markov chain; a pending token outside the vocabulary.
+a one-hot Markov chain; a pending token outside the vocabulary; a slot whose
+logits are all NaN (empty support: q zero, draft 0).
 The drafter trunk stand-in (one attention layer at d_model 1024) scores the
 gamma slots in one verify pass whose rows feed the kernel.
 """
@@ -112,6 +113,34 @@ def test_markov_draft_nan_logits_stay_out_of_the_support(V):
             assert np.abs(q[i] - ref).max() <= 2e-6
             assert d[i] == sample(q[i], u[i]), (k, i)
             p = d[i]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("V", [16, 512, 1000, 2000])
+def test_markov_draft_row_without_a_number(V):
+    # a slot whose logits are all NaN has an empty support (top_k 1 .. 8):
+    # its q row is zero and its draft 0, so the next slot reads Markov row 0
+    import hybrid_ssm_attention_gb300 as evs
+    g = np.random.default_rng(V + 11)
+    gamma, bad = 6, 2
+    M = (g.standard_normal((V, V)) * 2).astype(np.float32)
+    for k in (1, 4, 8):
+        for mode in (GREEDY, SAMPLE):
+            trunk = (g.standard_normal((gamma, V)) * 2).astype(np.float32)
+            trunk[bad] = np.nan
+            u = g.random(gamma).astype(np.float32)
+            prev = int(g.integers(0, V))
+            d, q = _gpu(evs, trunk, M, prev, u, 1.0, k, mode)
+            assert d[bad] == 0 and not q[bad].any(), (k, mode)
+            p = prev
+            for i in range(gamma):
+                if i != bad:
+                    ref = topk_probs(trunk[i] + M[p], 1.0, k, dtype=np.float32)
+                    assert np.array_equal(q[i] > 0, ref > 0), (k, mode, i)
+                    assert np.abs(q[i] - ref).max() <= 2e-6
+                    want = sample(q[i], u[i]) if mode == SAMPLE else argmax_low(trunk[i] + M[p])
+                    assert d[i] == want, (k, mode, i)
+                p = d[i]
 
 
 @pytest.mark.gpu
