@@ -480,8 +480,11 @@ def crossover(sweep):
     ms = {(r["B"], r["n"]): r["ms_per_round"] for r in sweep}
     out = []
     for B in (1, 2, 4, 8, 16):
-        n = 13 if (B, 13) in ms else max(k[1] for k in ms if k[0] == B)
-        if (B, 1) not in ms or (B, n) not in ms or n == 1:
+        widths = [k[1] for k in ms if k[0] == B]
+        if not widths:
+            continue
+        n = 13 if (B, 13) in ms else max(widths)
+        if (B, 1) not in ms or n == 1:
             continue
         out.append({"B": B, "native_ms": ms[(B, 1)], "spec_n": n, "spec_ms": ms[(B, n)],
                     "break_even_tokens_per_round": ms[(B, n)] / ms[(B, 1)],

@@ -53,3 +53,20 @@ def test_step_bytes_counts_weights_once():
     w = 32 * (4 * 4096 * 4096 + 3 * 4096 * 11008) * 2
     assert w == 12952010752
     assert 13.0e9 < b < 13.3e9
+
+
+def test_crossover_break_even_and_full_acceptance_speedup():
+    # a speculative round of n rows emits accepted + 1 tokens per sequence
+    # against one per native pass: break-even = spec_ms / native_ms tokens per
+    # round, speedup at full acceptance = n * native_ms / spec_ms
+    import bench
+    sweep = [{"B": 1, "n": 1, "ms_per_round": 2.5}, {"B": 1, "n": 13, "ms_per_round": 2.75},
+             {"B": 16, "n": 1, "ms_per_round": 3.2}, {"B": 16, "n": 8, "ms_per_round": 6.4},
+             {"B": 4, "n": 13, "ms_per_round": 3.5}]  # B = 4 has no native pass: skipped
+    out = bench.crossover(sweep)
+    assert [r["B"] for r in out] == [1, 16]
+    b1, b16 = out
+    assert b1["spec_n"] == 13 and b1["break_even_tokens_per_round"] == 2.75 / 2.5
+    assert abs(b1["speedup_all_accepted"] - 13 * 2.5 / 2.75) < 1e-12
+    assert b16["spec_n"] == 8 and b16["break_even_tokens_per_round"] == 2.0
+    assert b16["speedup_all_accepted"] == 4.0
