@@ -70,3 +70,18 @@ def test_crossover_break_even_and_full_acceptance_speedup():
     assert abs(b1["speedup_all_accepted"] - 13 * 2.5 / 2.75) < 1e-12
     assert b16["spec_n"] == 8 and b16["break_even_tokens_per_round"] == 2.0
     assert b16["speedup_all_accepted"] == 4.0
+
+
+def test_clock_summary_of_nvidia_smi_lines():
+    # index, clocks.sm, clocks.max.sm, power.draw, reasons.active, then
+    # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    import bench
+    ok = "0, 2070, 2070, 912.40, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+    cap = "0, 1980, 2070, 1398.10, 0x0000000000000004, Not Active, Not Active, Not Active, Active"
+    hot = "0, 1500, 2070, 1200.00, 0x0000000000000040, Not Active, Active, Not Active, Not Active"
+    na = "0, 2070, [N/A], 900.00, 0x0, Not Active, Not Active, Not Active, Not Active"
+    s = bench.ClockSampler.summarize([ok, ok, cap, "garbage", na, ""])
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    s = bench.ClockSampler.summarize([ok, hot, cap])
+    assert s["sm_mhz"] == 1980.0 and s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler.summarize([])["sm_mhz"] is None
