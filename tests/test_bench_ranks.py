@@ -85,3 +85,14 @@ def test_clock_summary_of_nvidia_smi_lines():
     s = bench.ClockSampler.summarize([ok, hot, cap])
     assert s["sm_mhz"] == 1980.0 and s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     assert bench.ClockSampler.summarize([])["sm_mhz"] is None
+
+
+def test_peak_denominator_measured_else_fallback(tmp_path, monkeypatch):
+    import json
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks() == (bench.FALLBACK_HBM_GBS, "fallback")  # no file
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6743.6, "bf16_tflops": 1904.1}))
+    assert bench.load_peaks() == (6743.6, "measured")
+    (tmp_path / "MEASURED_PEAKS.json").write_text("{not json")
+    assert bench.load_peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
