@@ -283,7 +283,7 @@ def synth_state(shape: ModelShape, seed: int, P: int, ctx_max: Optional[int] = N
     """Random decoding state at committed length P.
 
     FIR windows [L-1][d] float32 ~ N(0, 1) (oldest first); IIR states [d][M]
-    complex64 with Re, Im ~ N(0, 2); KV caches [P][H][Dh] ~ N(0, 1) in the
+    complex64 with Re, Im ~ N(0, sqrt 2) (standard deviation sqrt 2); KV caches [P][H][Dh] ~ N(0, 1) in the
     storage dtype.  Layers are listed in model order; a field is None where
     the layer kind has no such state."""
     ss = np.random.SeedSequence([seed, 6])
