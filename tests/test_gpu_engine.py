@@ -6,9 +6,9 @@ GPU tests compare with the oracle.  Here two states of one model run the same
 prefill and rounds, one through the engine and one through the separate
 kernels: every verify's logits, every round's accepted count, output token
 and target distribution, the bookkeeping and the retained FIR windows, IIR
-states and KV rows must be identical bits.  Shapes: the small bf16 stack and
-a 7B-width stack with every layer kind (FIR 7, FIR 128, IIR 16, attention);
-ragged blocks n = 1 .. 13; greedy and sampled rounds.
+states and KV rows must be identical bits.  Shapes: the small bf16 stack (blocks
+of up to 13 and up to 16 rows) and a 7B-width stack with every layer kind
+(FIR 7, FIR 128, IIR 16, attention); ragged blocks; greedy and sampled rounds.
 """
 import numpy as np
 import pytest
@@ -17,10 +17,10 @@ import synth
 from gpu_util import to_np, torch, wrap
 
 
-def small_shape():
+def small_shape(gamma=12):
     return synth.ModelShape(name="small-bf16", vocab=128, d_model=256,
                             layers=[("SE", 7), ("MR", 128), ("LI", 16), ("SE", 7), ("MR", 32), ("ATT", 0)],
-                            n_heads=2, head_dim=128, d_ffn=512, gamma=12, dtype="bf16", attn_chunk=64)
+                            n_heads=2, head_dim=128, d_ffn=512, gamma=gamma, dtype="bf16", attn_chunk=64)
 
 
 def wide_shape():
@@ -53,11 +53,11 @@ def _state_bits(shape, st):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("which", ["small", "wide"])
+@pytest.mark.parametrize("which", ["small", "small16", "wide"])
 def test_engine_equals_separate_kernels_bitwise(which):
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
-    shape = small_shape() if which == "small" else wide_shape()
+    shape = {"small": small_shape(), "small16": small_shape(15), "wide": wide_shape()}[which]
     W = synth.make_weights(shape, 81)
     m = evs.Model(shape, W)
     V, nb = shape.vocab, shape.n_block

@@ -2,8 +2,9 @@
 graphs with programmatic dependent launch) against the fp32 oracle with
 bf16 storage points; tolerance 2e-2 of max |ref| on logits.
 
-* small 6-layer bf16 stack (d 256): prefill, block verify, commit; GPU
-  speculative == GPU native, bitwise, at every emitted position.
+* small 6-layer bf16 stack (d 256), blocks of 13 and of 16 rows (the
+  largest): prefill, block verify, commit; GPU speculative == GPU native,
+  bitwise, at every emitted position.
 * 7B-shaped stack (32 layers, d 4096, F 11008, vocab 512, gamma 12), at
   full size from a synthesised state at context 1024: every layer's update
   and retained state teacher-forced against the oracle (2e-2); free-running
@@ -23,10 +24,11 @@ from gpu_util import fir_ext, fir_set_window, noise_drafts, rel_err, to_np, torc
 TOL = 2e-2
 
 
-def small_shape():
+def small_shape(gamma=12):
+    # gamma 15: blocks of 16 rows, the largest a single-sequence verify takes
     return synth.ModelShape(name="small-bf16", vocab=128, d_model=256,
                             layers=[("SE", 7), ("MR", 128), ("LI", 16), ("SE", 7), ("MR", 32), ("ATT", 0)],
-                            n_heads=2, head_dim=128, d_ffn=512, gamma=12, dtype="bf16", attn_chunk=64)
+                            n_heads=2, head_dim=128, d_ffn=512, gamma=gamma, dtype="bf16", attn_chunk=64)
 
 
 def _verify(evs, st, toks, V):
@@ -38,14 +40,14 @@ def _verify(evs, st, toks, V):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("slots", ["1", "0"])
-def test_small_bf16_stack_matches_oracle(slots):
+@pytest.mark.parametrize("slots,gamma", [("1", 12), ("0", 12), ("1", 15)])
+def test_small_bf16_stack_matches_oracle(slots, gamma):
     # slots "1": GEMMs leave partial slots to the consuming kernels (default);
     # "0": every GEMM sums its own slots (cluster split-K out / down)
     import hybrid_ssm_attention_gb300 as evs
     from oracle.model import Model as OModel
     from oracle.numerics import Arith
-    shape = small_shape()
+    shape = small_shape(gamma)
     W = synth.make_weights(shape, 11)
     m = evs.Model(shape, W, options=0 if slots == "1" else evs.EVS_OPT_GEMM_SUMS_SLOTS)
     st = evs.State(m, 512)
@@ -67,11 +69,11 @@ def test_small_bf16_stack_matches_oracle(slots):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("graphs", [True, False])
-def test_small_bf16_spec_equals_native_bitwise(graphs):
+@pytest.mark.parametrize("graphs,gamma", [(True, 12), (False, 12), (True, 15)])
+def test_small_bf16_spec_equals_native_bitwise(graphs, gamma):
     import hybrid_ssm_attention_gb300 as evs
     t = torch()
-    shape = small_shape()
+    shape = small_shape(gamma)
     W = synth.make_weights(shape, 12)
     m = evs.Model(shape, W)
     prompt = [int(x) for x in synth.prompt(shape, 12, 40)]
