@@ -302,7 +302,7 @@ def oracle_round_tokens_per_s(shape, W, seed, P, rounds, native_steps, warm=0):
 def cpu_baseline(args, shape, W):
     """The oracle as the reported CPU baseline: all host cores, then one
     thread (a child process with one BLAS thread), on bounded samples."""
-    rounds, native = 4, 8  # about 20 s of host work with the drafts
+    rounds, native = 8, 16  # ~20 s timed on 16 cores (~35 s with the untimed drafts)
     tps, t_round, t_native = oracle_round_tokens_per_s(shape, W, args.seed, args.prompt, rounds, native)
     out = {"value": tps, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
            "cpu": cpu_model(), "host_cores": os.cpu_count(),
