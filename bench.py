@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-replay", action="store_true")
     ap.add_argument("--no-batch", action="store_true")
-    ap.add_argument("--long-gen", type=int, default=4096,
+    ap.add_argument("--long-gen", type=int, default=32768,
                     help="also generate this many tokens natively and speculatively (drafts with random "
                          "corrupted tails) and report whether the two sequences are identical (0: skip)")
     ap.add_argument("--no-sampled", action="store_true")
